@@ -1,0 +1,448 @@
+"""Pins of the oracle against what the pages and the mathematics fix (CPU only).
+
+Each test here checks the oracle against something other than itself: a
+value printed on the pages, a hand-worked case, a closed form, a textbook
+or library routine (scipy softmax, numpy searchsorted, torch's
+scaled_dot_product_attention), an invariant, or a statistical property
+(losslessness, the mean acceptance length).  A plausible slip in the oracle
+(a dropped term, a swapped P/Q, a wrong row, u <= alpha instead of u < alpha,
+an ignored temperature or scale, a wrong GQA head map, a mask that leaks
+across branches) fails at least one of them.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import scipy.stats
+import torch
+
+import oracle
+import workloads as W
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- N_async
+def test_n_async_printed_value():
+    g = json.load(open(os.path.join(GOLD, "n_async.json")))
+    assert oracle.n_async(g["B"], g["C"], g["F"]) == g["N_async"] == 384
+
+
+@pytest.mark.parametrize("C", [1, 2, 3, 4, 8, 12, 16])
+@pytest.mark.parametrize("F", [1, 2, 3, 5])
+def test_async_layout_fills_budget(C, F):
+    # the generator's branch layout has exactly the pages' budget of tokens,
+    # and one head per segment
+    segs = W.async_segments(16, C, F)
+    assert int(segs[:, 1].sum()) == oracle.n_async(16, C, F)
+    assert len(segs) == (C - 1) * F + 2
+    assert oracle.check_segments(segs, [0, int(segs[:, 1].sum())], [0, len(segs)]) == 0
+
+
+# ---------------------------------------------------------------- tau
+def test_tau_closed_forms():
+    B = 16
+    assert oracle.expected_tau(np.ones(B - 1)) == pytest.approx(B)
+    a = np.full(B - 1, 0.7)
+    a[0] = 0.0
+    assert oracle.expected_tau(a) == pytest.approx(1.0)
+    for c in (0.1, 0.5, 0.9):
+        closed = 1 + c * (1 - c ** (B - 1)) / (1 - c)
+        assert oracle.expected_tau(np.full(B - 1, c)) == pytest.approx(closed, rel=1e-12)
+    # hand-worked: V=2, P=(1/2,1/2), Q=(1,0) at every position => a_j = 1/2; B=4
+    assert oracle.expected_tau([0.5, 0.5, 0.5]) == pytest.approx(1.875)
+
+
+# ---------------------------------------------------------------- hand-worked verify cases
+def _case_inputs(c):
+    B, V = c["B"], c["V"]
+    return dict(target=np.array(c["target"], np.float32).reshape(1, B, V),
+                draft=np.array(c["draft"], np.float32).reshape(1, B - 1, V), dtype=W.DT_F32,
+                y=np.array(c["y"], np.int32).reshape(1, B - 1),
+                u_accept=np.array(c["u_accept"], np.float32).reshape(1, B - 1),
+                u_sample=np.array([c["u_sample"]], np.float32), R=1, B=B, V=V,
+                temperature=c["T"])
+
+
+@pytest.mark.parametrize("case", json.load(open(os.path.join(GOLD, "verify_hand.json")))["cases"],
+                         ids=lambda c: c["name"])
+def test_verify_hand_worked(case):
+    r = oracle.spec_verify(_case_inputs(case))
+    np.testing.assert_allclose(r["alpha"][0], case["alpha"], rtol=1e-6, atol=1e-7)
+    assert int(r["accept_len"][0]) == case["accept_len"]
+    n = case["accept_len"] + 1
+    assert int(r["num_tokens"][0]) == n
+    assert r["out_tokens"][0, :n].tolist() == case["tokens"]
+    assert (r["out_tokens"][0, n:] == -1).all()
+
+
+# ---------------------------------------------------------------- statistics helpers
+def _fixed_rows_inputs(x, z, T, R, seed):
+    """R trials of one fixed verification problem: target rows x [B, V], draft
+    rows z [B-1, V]; each trial draws its own draft tokens y_j ~ Q_j (scipy
+    softmax) and its own uniforms."""
+    B, V = x.shape
+    rng = np.random.default_rng(seed)
+    Qd = scipy.special.softmax(z.astype(np.float64) / T, axis=-1)
+    y = np.stack([rng.choice(V, size=R, p=Qd[j]) for j in range(B - 1)], axis=1).astype(np.int32)
+    u = W.uniform24(rng, (R, B))
+    return dict(target=np.broadcast_to(x, (R, B, V)).copy(), draft=np.broadcast_to(z, (R, B - 1, V)).copy(),
+                dtype=W.DT_F32, y=y, u_accept=np.ascontiguousarray(u[:, :B - 1]),
+                u_sample=np.ascontiguousarray(u[:, B - 1]), R=R, B=B, V=V, temperature=T)
+
+
+def _chi2_p(tokens, probs):
+    V = len(probs)
+    obs = np.bincount(tokens, minlength=V).astype(np.float64)
+    exp = probs * obs.sum()
+    keep = exp > 0
+    assert obs[~keep].sum() == 0, "token with zero target probability was emitted"
+    return scipy.stats.chisquare(obs[keep], exp[keep]).pvalue
+
+
+def _rows(V, B, seed, sigma=1.0, scale=1.5):
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((B, V)) * scale).astype(np.float32)
+    z = (x[: B - 1] + rng.standard_normal((B - 1, V)) * sigma).astype(np.float32)
+    return x, z
+
+
+# ---------------------------------------------------------------- mean acceptance length (MC)
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_tau_monte_carlo_matches_closed_form(T):
+    # a_j = sum_v min(P_j(v), Q_j(v)) is the per-position acceptance
+    # probability of speculative sampling (1 - total variation distance);
+    # the pages' MAT formula then gives E[a + 1].
+    V, B, R = 8, 5, 200_000
+    x, z = _rows(V, B, seed=11, sigma=1.2)
+    inp = _fixed_rows_inputs(x, z, T, R, seed=5)
+    r = oracle.spec_verify(inp)
+    P = scipy.special.softmax(x.astype(np.float64) / T, axis=-1)
+    Q = scipy.special.softmax(z.astype(np.float64) / T, axis=-1)
+    a = np.minimum(P[: B - 1], Q).sum(axis=-1)
+    tau = 1.0 + sum(np.prod(a[: k + 1]) for k in range(B - 1))
+    n = r["num_tokens"].astype(np.float64)
+    se = n.std() / np.sqrt(R)
+    assert abs(n.mean() - tau) < 5 * se, (n.mean(), tau, se)
+    # per-position survival as well (catches an index slip that keeps the mean)
+    for k in range(1, B):
+        s_emp = (r["accept_len"] >= k).mean()
+        s_true = np.prod(a[:k])
+        assert abs(s_emp - s_true) < 5 * np.sqrt(s_true * (1 - s_true) / R) + 1e-12
+
+
+# ---------------------------------------------------------------- losslessness (chi-square)
+@pytest.mark.slow
+@pytest.mark.parametrize("T", [1.0, 2.0])
+def test_lossless_chi_square(T):
+    # D3D/DScout "Background": the output distribution equals the target's.
+    # First emitted token ~ P_1; second emitted token given the first draft
+    # was accepted ~ P_2.  V <= 64, >= 10^6 trials, flag at p < 1e-4.
+    V, B = 16, 3
+    x, z = _rows(V, B, seed=3, sigma=1.0)
+    P = scipy.special.softmax(x.astype(np.float64) / T, axis=-1)
+    first, second = [], []
+    for chunk in range(5):
+        inp = _fixed_rows_inputs(x, z, T, 200_000, seed=100 + chunk)
+        r = oracle.spec_verify(inp)
+        first.append(r["out_tokens"][:, 0])
+        ok = r["accept_len"] >= 1
+        second.append(r["out_tokens"][ok, 1])
+    first, second = np.concatenate(first), np.concatenate(second)
+    assert len(first) == 1_000_000
+    assert _chi2_p(first, P[0]) > 1e-4
+    assert _chi2_p(second, P[1]) > 1e-4
+
+
+def test_lossless_detects_a_wrong_rule():
+    # the chi-square check has power: plain "accept if y == argmax" style
+    # outputs (here: always emitting the draft token) are not ~ P_1
+    V, B = 16, 2
+    x, z = _rows(V, B, seed=3, sigma=1.0)
+    P = scipy.special.softmax(x.astype(np.float64), axis=-1)
+    inp = _fixed_rows_inputs(x, z, 1.0, 200_000, seed=9)
+    assert _chi2_p(inp["y"][:, 0], P[0]) < 1e-4
+
+
+# ---------------------------------------------------------------- special cases
+def test_equal_distributions_always_accept_and_bonus_is_P_B():
+    V, B, R = 12, 4, 200_000
+    x, _ = _rows(V, B, seed=21)
+    inp = _fixed_rows_inputs(x, x[: B - 1].copy(), 1.0, R, seed=22)
+    r = oracle.spec_verify(inp)
+    assert (r["accept_len"] == B - 1).all()
+    assert (r["alpha"] == 1.0).all()
+    P = scipy.special.softmax(x.astype(np.float64), axis=-1)
+    assert _chi2_p(r["out_tokens"][:, B - 1], P[B - 1]) > 1e-4
+    np.testing.assert_array_equal(r["out_tokens"][:, : B - 1], inp["y"])
+
+
+def test_disjoint_support_always_rejects_first_and_samples_P1():
+    V, B, R = 16, 3, 200_000
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((B, V)).astype(np.float32)
+    z = rng.standard_normal((B - 1, V)).astype(np.float32)
+    x[0, 8:] = -10000.0   # P_1 lives on tokens 0..7
+    z[0, :8] = -10000.0   # Q_1 lives on tokens 8..15
+    inp = _fixed_rows_inputs(x, z, 1.0, R, seed=32)
+    r = oracle.spec_verify(inp)
+    assert (r["accept_len"] == 0).all()
+    assert (r["alpha"][:, 0] == 0.0).all()
+    P = scipy.special.softmax(x.astype(np.float64), axis=-1)
+    assert _chi2_p(r["out_tokens"][:, 0], P[0]) > 1e-4
+
+
+def test_rejection_never_emits_rejected_token():
+    V, B, R = 10, 6, 50_000
+    x, z = _rows(V, B, seed=41, sigma=2.0)
+    inp = _fixed_rows_inputs(x, z, 1.0, R, seed=42)
+    r = oracle.spec_verify(inp)
+    rej = np.nonzero(r["accept_len"] < B - 1)[0]
+    assert len(rej) > 1000
+    a = r["accept_len"][rej]
+    assert (r["out_tokens"][rej, a] != inp["y"][rej, a]).all()
+    assert not r["used_fallback"].any()
+
+
+def test_inverse_cdf_matches_searchsorted():
+    # Bonus path (P = Q in rows 1..B-1) and residual path with disjoint
+    # support (residual = P_1): the emitted token equals numpy's
+    # searchsorted over the cumulative target probabilities (scipy softmax).
+    rng = np.random.default_rng(51)
+    for trial in range(200):
+        V = int(rng.integers(2, 300))
+        B = int(rng.integers(2, 6))
+        x = (rng.standard_normal((B, V)) * 3).astype(np.float32)
+        if trial % 2 == 0:
+            z = x[: B - 1].copy()
+            row = B - 1
+        else:
+            z = rng.standard_normal((B - 1, V)).astype(np.float32)
+            cut = int(rng.integers(1, V)) if V > 1 else 1
+            x[0, cut:] = -10000.0
+            z[0, :cut] = -10000.0
+            row = 0
+        inp = _fixed_rows_inputs(x, z, 1.0, 64, seed=trial)
+        r = oracle.spec_verify(inp)
+        P = scipy.special.softmax(x[row].astype(np.float64))
+        c = np.cumsum(P)
+        ref = np.searchsorted(c, inp["u_sample"].astype(np.float64) * c[-1], side="right")
+        ref = np.minimum(ref, V - 1)
+        pos = r["accept_len"]
+        got = r["out_tokens"][np.arange(64), pos]
+        keep = r["margin_sample"] > 1e-9
+        assert keep.sum() > 50
+        np.testing.assert_array_equal(got[keep], ref[keep])
+
+
+def test_alpha_p_q_match_library_softmax():
+    inp = W.verify_inputs(**W.CONFIGS["tiny"], seed=3)
+    r = oracle.spec_verify(inp)
+    P = scipy.special.softmax(inp["target"].astype(np.float64), axis=-1)
+    Q = scipy.special.softmax(inp["draft"].astype(np.float64), axis=-1)
+    idx = np.arange(inp["B"] - 1)
+    p = P[0, idx, inp["y"][0]]
+    q = Q[0, idx, inp["y"][0]]
+    np.testing.assert_allclose(r["p"][0], p, rtol=1e-12)
+    np.testing.assert_allclose(r["q"][0], q, rtol=1e-12)
+    np.testing.assert_allclose(r["alpha"][0], np.minimum(1.0, p / q), rtol=1e-12)
+
+
+def test_bf16_logits_decode_exactly():
+    inp = W.verify_inputs(R=2, B=4, V=64, logits=W.DT_BF16, seed=4)
+    r16 = oracle.spec_verify(inp)
+    f32 = dict(inp, target=W.bf16_to_f32(inp["target"]), draft=W.bf16_to_f32(inp["draft"]), dtype=W.DT_F32)
+    r32 = oracle.spec_verify(f32)
+    for k in ("accept_len", "out_tokens", "alpha"):
+        np.testing.assert_array_equal(r16[k], r32[k])
+
+
+# ---------------------------------------------------------------- attention
+def _f64(bits):
+    return torch.from_numpy(W.bf16_to_f32(bits).astype(np.float64))
+
+
+def _sdpa(q, k, v, scale, causal=False):
+    """torch SDPA in fp64; q [n, H, d], k/v [m, Hkv, d] with GQA expansion."""
+    G = q.shape[1] // k.shape[1]
+    k = k.repeat_interleave(G, dim=1)
+    v = v.repeat_interleave(G, dim=1)
+    qt, kt, vt = (t.permute(1, 0, 2) for t in (q, k, v))
+    mask = None
+    if causal:
+        n, m = q.shape[0], k.shape[0]
+        mask = torch.ones(n, m, dtype=torch.bool).tril(diagonal=m - n)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
+    return o.permute(1, 0, 2).numpy()
+
+
+@pytest.mark.parametrize("B,C,F,L,Hq,Hkv,d,scale", [
+    (4, 3, 2, 8, 4, 2, 8, None), (4, 4, 1, 5, 2, 2, 16, 0.3), (3, 2, 3, 1, 8, 2, 4, None),
+    (6, 4, 2, 0, 4, 1, 8, None)])
+def test_packing_invariance_vs_sdpa(B, C, F, L, Hq, Hkv, d, scale):
+    """Each branch's rows equal an independent attention of that block over
+    [prefix | c_0 .. c_r | own block]; the current segment equals causal
+    attention over [prefix | current block] (torch SDPA, fp64, GQA by
+    repeat_interleave)."""
+    inp = W.attn_inputs(R=1, L=L, Hq=Hq, Hkv=Hkv, d=d, B=B, C=C, F=F, layout="async", seed=7)
+    if scale is not None:
+        inp["scale"] = scale
+    out = oracle.packed_attn(inp)
+    q, kp, vp, kn, vn = (_f64(inp[k]) for k in ("q", "kp", "vp", "kn", "vn"))
+    s = inp["scale"]
+    for g in inp["segs"]:
+        q0, n, mode, par, plen = (int(t) for t in g)
+        rows = slice(q0, q0 + n)
+        if par >= 0:
+            p0 = int(inp["segs"][par][0])
+            ks = torch.cat([kp, kn[p0:p0 + plen], kn[rows]])
+            vs = torch.cat([vp, vn[p0:p0 + plen], vn[rows]])
+        else:
+            ks, vs = torch.cat([kp, kn[rows]]), torch.cat([vp, vn[rows]])
+        ref = _sdpa(q[rows], ks, vs, s, causal=(mode == W.SEG_CAUSAL))
+        np.testing.assert_allclose(out[rows], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_single_block_is_noncausal_and_single_causal_is_textbook():
+    inp = W.attn_inputs(R=1, L=12, Hq=4, Hkv=2, d=8, B=8, layout="block", seed=8)
+    out = oracle.packed_attn(inp)
+    q, kp, vp, kn, vn = (_f64(inp[k]) for k in ("q", "kp", "vp", "kn", "vn"))
+    ref = _sdpa(q, torch.cat([kp, kn]), torch.cat([vp, vn]), inp["scale"])
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+    inp2 = W.attn_inputs(R=1, L=12, Hq=4, Hkv=2, d=8, B=8, seed=8,
+                         segs=np.array([[0, 8, W.SEG_CAUSAL, -1, 0]]))
+    out2 = oracle.packed_attn(inp2)
+    ref2 = _sdpa(q, torch.cat([kp, kn]), torch.cat([vp, vn]), inp2["scale"], causal=True)
+    np.testing.assert_allclose(out2, ref2, rtol=1e-10, atol=1e-12)
+
+
+def _random_segments(rng, n_seg):
+    rows, q = [], 0
+    causal = []
+    for s in range(n_seg):
+        ln = int(rng.integers(1, 6))
+        mode = int(rng.integers(0, 2))
+        par, plen = -1, 0
+        if causal and rng.random() < 0.7:
+            par = int(rng.choice(causal))
+            plen = int(rng.integers(0, rows[par][1] + 1))
+        rows.append([q, ln, mode, par, plen])
+        if mode == W.SEG_CAUSAL and par == -1:
+            causal.append(s)
+        q += ln
+    return np.array(rows, np.int32)
+
+
+def test_predicate_equals_dense_mask_random_tables():
+    rng = np.random.default_rng(61)
+    for t in range(40):
+        segs = _random_segments(rng, int(rng.integers(1, 9)))
+        N = int(segs[-1, 0] + segs[-1, 1])
+        L = int(rng.integers(0, 9))
+        inp = W.attn_inputs(R=1, L=L, Hq=2, Hkv=1, d=4, seed=t, segs=segs)
+        np.testing.assert_allclose(oracle.packed_attn(inp), oracle.dense_attn(inp), rtol=1e-12, atol=1e-14)
+        m = oracle.dense_mask(segs, L, N)
+        assert m[:, :L].all()
+        # no cross-branch leak: a row never sees a later segment's tokens
+        for g in segs:
+            q0, n = int(g[0]), int(g[1])
+            assert not m[q0:q0 + n, L + q0 + n:].any()
+
+
+def test_ragged_batch_equals_requests_alone():
+    segs = W.async_segments(4, 3, 2)
+    inp = W.attn_inputs(R=3, L=(0, 9), Hq=4, Hkv=2, d=8, seed=9, segs=segs)
+    out = oracle.packed_attn(inp)
+    for r in range(3):
+        p0, p1 = inp["cu_prefix"][r], inp["cu_prefix"][r + 1]
+        q0, q1 = inp["cu_q"][r], inp["cu_q"][r + 1]
+        one = dict(inp, R=1, q=inp["q"][q0:q1], kp=inp["kp"][p0:p1], vp=inp["vp"][p0:p1],
+                   kn=inp["kn"][q0:q1], vn=inp["vn"][q0:q1], segs=segs,
+                   cu_prefix=np.array([0, p1 - p0]), cu_q=np.array([0, q1 - q0]),
+                   cu_seg=np.array([0, len(segs)]))
+        np.testing.assert_array_equal(out[q0:q1], oracle.packed_attn(one))
+
+
+@pytest.mark.parametrize("bad", ["overlap", "gap", "later_parent", "bidir_parent", "long_parent",
+                                 "nested", "len_without_parent", "empty_seg", "short_total", "bad_mode"])
+def test_segment_checker_rejects(bad):
+    segs = W.async_segments(4, 3, 2).astype(np.int64)
+    N = int(segs[:, 1].sum())
+    cu_q = [0, N]
+    if bad == "overlap":
+        segs[2, 0] -= 1
+    elif bad == "gap":
+        segs[2:, 0] += 1
+        cu_q = [0, N + 1]
+    elif bad == "later_parent":
+        segs[1, 3] = 2
+    elif bad == "bidir_parent":
+        segs[2, 3] = 1
+    elif bad == "long_parent":
+        segs[1, 4] = 5
+    elif bad == "nested":
+        segs[1, 2] = W.SEG_CAUSAL
+        segs[2, 3] = 1
+        segs[2, 4] = 1
+    elif bad == "len_without_parent":
+        segs[0, 4] = 1
+    elif bad == "empty_seg":
+        segs[3, 1] = 0
+        segs[4:, 0] -= 4
+        cu_q = [0, N - 4]
+    elif bad == "short_total":
+        cu_q = [0, N + 3]
+    elif bad == "bad_mode":
+        segs[1, 2] = 7
+    assert oracle.check_segments(segs, cu_q, [0, len(segs)]) != 0
+
+
+# ---------------------------------------------------------------- branch match
+def _match_by_dict(inp):
+    """Independent formulation: the first head index for each exact prefix tuple."""
+    out = []
+    for r in range(inp["heads"].shape[0]):
+        table = {}
+        for k in range(inp["heads"].shape[1]):
+            n = int(inp["head_len"][r, k])
+            table.setdefault(tuple(inp["heads"][r, k, :n].tolist()), k)
+        v = tuple(inp["verified"][r, : int(inp["verified_len"][r])].tolist())
+        out.append(table.get(v, -1))
+    return np.array(out, np.int32)
+
+
+def test_match_against_dict_lookup():
+    inp = W.match_inputs(R=500, seed=71)
+    got = oracle.branch_match(inp)
+    np.testing.assert_array_equal(got, _match_by_dict(inp))
+    hits = (got >= 0).mean()
+    assert 0.5 < hits < 0.9
+
+
+def test_match_tiny_alphabet_brute_force():
+    # alphabet {0, 1}: many collisions, duplicate heads and ragged lengths
+    rng = np.random.default_rng(72)
+    R, M, B = 4000, 5, 3
+    inp = dict(verified=rng.integers(0, 2, (R, B)).astype(np.int32),
+               verified_len=rng.integers(0, B + 1, R).astype(np.int32),
+               heads=rng.integers(0, 2, (R, M, B)).astype(np.int32),
+               head_len=rng.integers(0, B + 1, (R, M)).astype(np.int32))
+    got = oracle.branch_match(inp)
+    np.testing.assert_array_equal(got, _match_by_dict(inp))
+    assert (got == -1).any() and (got > 0).any()
+
+
+def test_match_head0_never_hits_and_lowest_duplicate_wins():
+    y = np.arange(1, 16, dtype=np.int32)[None]
+    hb = W.branch_heads(y, 16, 12, 2, 1000, seed=1)
+    heads, hl = hb["heads"], hb["head_len"]
+    heads[0, 7] = heads[0, 3]
+    hl[0, 7] = hl[0, 3]
+    n = int(hl[0, 3])
+    verified = np.zeros((1, 16), np.int32)
+    verified[0, :n] = heads[0, 3, :n]
+    got = oracle.branch_match(dict(verified=verified, verified_len=np.array([n], np.int32),
+                                   heads=heads, head_len=hl))
+    assert got[0] == 3
