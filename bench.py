@@ -1,0 +1,502 @@
+#!/usr/bin/env python3
+"""Benchmark of the diffusion-drafted speculative decoding hot path on GB300.
+
+One step = one pass of the whole path over one round of synthetic input:
+packed drafting attention (one drafter layer, all heads) over the async
+packed sequence, batched speculative-sampling verification over the
+vocabulary, and the branch cache-hit match of the verified tokens.  The
+default workload is D3D's asynchronous packed pass at 8B-class shapes:
+1 request, prefix 2048, 32 query / 8 KV heads, head_dim 128, B=16, C=12,
+F=2 (N_async = 384 packed query tokens), verification of 16 positions over a
+151936-entry vocabulary, and a match against 24 branch heads.
+
+Timing: inputs resident in HBM; steps rotate over input sets whose total
+size exceeds twice the L2 cache, so no step finds its inputs in L2; each
+step is captured once in a CUDA graph and the K timed steps are graph
+replays, bracketed by a barrier and synchronisation, timed with CUDA events
+on the launching stream, max over ranks.  ``value`` is packed query tokens
+per second of whole steps, over all ranks (weak scaling: each rank runs its
+own request).  Per-part device times come from separate graph-replayed
+loops of each part alone over the same rotation.
+
+``--impl reference`` times the plain CPU oracle on this host instead (a
+bounded sample per step, scaled to the same unit).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "packed-draft query tokens/s + verified positions/s; % HBM/tensor roofline"
+UNIT = "packed-draft query tokens/s"
+# our kernel launches per call of each entry point
+LAUNCHES = {"attn": 1, "verify": 2, "match": 1}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="async8b", choices=["async8b", "long_block", "serve32b"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# Workload description (shapes and algorithmic work; no method arithmetic).
+# ----------------------------------------------------------------------------
+def workload(name: str) -> dict:
+    cfg = dict(W.CONFIGS[name])
+    segs = W.block_segments(cfg["B"]) if cfg["layout"] == "block" else W.async_segments(cfg["B"], cfg["C"], cfg["F"])
+    n_q = int(segs[:, 1].sum())
+    # visible packed keys per query token, from the segment rows
+    vis_packed = 0
+    for q0, ln, mode, par, plen in segs.tolist():
+        own = ln * ln if mode == W.SEG_BIDIR else ln * (ln + 1) // 2
+        vis_packed += own + ln * plen
+    R = cfg["R"]
+    L_mean = float(np.mean(cfg["L"])) if isinstance(cfg["L"], tuple) else float(cfg["L"])
+    Hq, Hkv, d, B, V = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["B"], cfg["V"]
+    flops = 4.0 * d * Hq * R * (n_q * L_mean + vis_packed)
+    attn_bytes = 2.0 * R * (2 * L_mean * Hkv * d + 2 * n_q * Hq * d + 2 * n_q * Hkv * d)
+    verify_bytes = 2.0 * R * ((2 * B - 1) * V + 2 * V)
+    return dict(cfg=cfg, segs=segs, n_q=n_q, R=R, flops=flops, attn_bytes=attn_bytes, verify_bytes=verify_bytes,
+                positions=R * B, vis_packed=vis_packed)
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="of measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="of fallback")
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling during the timed region.
+# ----------------------------------------------------------------------------
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.proc = None
+        cmd = ["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits", "-lms", "100"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out = self.proc.communicate(timeout=5)[0]
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out = self.proc.communicate()[0]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# Our arm.
+# ----------------------------------------------------------------------------
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__._build_module().build()
+    import diffusion_drafted_speculative_gb300 as d3d
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = workload(args.workload)
+    cfg = wl["cfg"]
+    R, B, V, Hq, Hkv, d = cfg["R"], cfg["B"], cfg["V"], cfg["Hq"], cfg["Hkv"], cfg["d"]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 << 20) or (126 << 20)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    def host_set(seed):
+        a = W.attn_inputs(**cfg, seed=seed)
+        v = W.verify_inputs(**cfg, seed=seed)
+        hb = W.branch_heads(v["y"], B, cfg.get("C", 1), cfg.get("F", 1), V, seed=seed) if cfg["layout"] == "async" \
+            else W.branch_heads(v["y"], B, 1, 1, V, seed=seed)
+        ins = dict(q=bf(a["q"]), kp=bf(a["kp"]), vp=bf(a["vp"]), kn=bf(a["kn"]), vn=bf(a["vn"]),
+                   segs=torch.from_numpy(a["segs"]), cu_prefix=torch.from_numpy(a["cu_prefix"]),
+                   cu_q=torch.from_numpy(a["cu_q"]), cu_seg=torch.from_numpy(a["cu_seg"]),
+                   target=bf(v["target"]), draft=bf(v["draft"]), y=torch.from_numpy(v["y"]),
+                   u_accept=torch.from_numpy(v["u_accept"]), u_sample=torch.from_numpy(v["u_sample"]),
+                   heads=torch.from_numpy(hb["heads"]), head_len=torch.from_numpy(hb["head_len"]))
+        return ins, a["max_q"], a["max_prefix"], a["scale"]
+
+    def outputs(NT):
+        return dict(out=torch.empty(NT, Hq, d, dtype=torch.bfloat16, device=dev),
+                    accept_len=torch.empty(R, dtype=torch.int32, device=dev),
+                    out_tokens=torch.empty(R, B, dtype=torch.int32, device=dev),
+                    num_tokens=torch.empty(R, dtype=torch.int32, device=dev),
+                    branch=torch.empty(R, dtype=torch.int32, device=dev))
+
+    first, max_q, max_prefix, scale = host_set(1000 * rank)
+    set_bytes = sum(t.numel() * t.element_size() for t in first.values()) + first["q"].numel() * 2
+    n_sets = max(2, math.ceil(2.2 * l2 / set_bytes))
+    sets = []
+    for s in range(n_sets):
+        hs = first if s == 0 else host_set(1000 * rank + s)[0]
+        dset = {k: t.to(dev) for k, t in hs.items()}
+        dset.update(outputs(hs["q"].shape[0]))
+        sets.append(dset)
+    ws_a = d3d.new_workspace(d3d.d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix), dev)
+    ws_v = d3d.new_workspace(d3d.d3d_spec_verify_workspace_size(R, B, V), dev)
+
+    def attn(s):
+        d3d.d3d_packed_draft_attn(s["q"], s["kp"], s["vp"], s["kn"], s["vn"], s["segs"], s["cu_prefix"], s["cu_q"],
+                                  s["cu_seg"], max_q, max_prefix, scale, s["out"], ws_a)
+
+    def verify(s):
+        d3d.d3d_spec_verify(s["target"], s["draft"], s["y"], s["u_accept"], s["u_sample"], 1.0, s["accept_len"],
+                            s["out_tokens"], s["num_tokens"], ws_v)
+
+    def match(s):
+        d3d.d3d_branch_match(s["out_tokens"], s["num_tokens"], s["heads"], s["head_len"], s["branch"])
+
+    def step(s):
+        attn(s)
+        verify(s)
+        match(s)
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def graphs(fn, n):
+        """Graphs that together run fn over exactly n consecutive rotation steps."""
+        full, tail = divmod(n, n_sets)
+        out = []
+        for count, reps in ((n_sets, full), (tail, 1)):
+            if count == 0 or reps == 0:
+                continue
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(count):
+                    fn(sets[i])
+            out.append((g, reps))
+        return out
+
+    def replay(gs):
+        for g, reps in gs:
+            for _ in range(reps):
+                g.replay()
+
+    def timed(fn, n):
+        gs = graphs(fn, n)
+        replay(gs)  # untimed pass of the same graphs
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            replay(gs)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    # eager warm-up (validates every call), then graph warm-up of W steps
+    with torch.cuda.stream(stream):
+        for i in range(min(args.warmup, n_sets)):
+            step(sets[i % n_sets])
+    torch.cuda.synchronize()
+    for w in (ws_a, ws_v):
+        st = d3d.d3d_workspace_status(w)
+        if st != 0:
+            raise RuntimeError("device status after warm-up: %s" % d3d.d3d_status_string(st))
+    g_warm = graphs(step, max(args.warmup, 1))
+    g_timed = graphs(step, args.steps)
+    replay(g_warm)
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid) if getattr(props, "uuid", None) is not None else None
+    except Exception:
+        uuid = None
+    clocks = Clocks(uuid)
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        replay(g_timed)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    ms_step = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    for w in (ws_a, ws_v):
+        st = d3d.d3d_workspace_status(w)
+        if st != 0:
+            raise RuntimeError("device status after timed region: %s" % d3d.d3d_status_string(st))
+
+    # per-part device time (each part alone, same rotation, graph replays)
+    n_part = max(n_sets, min(args.steps, 2000))
+    t_attn = timed(attn, n_part)
+    t_verify = timed(verify, n_part)
+    t_match = timed(match, n_part)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(torch, d3d, sets, n_sets, attn, verify, match, dev, stream, args, R, B, dist)
+
+    peaks = load_peaks()
+    achieved_tf = wl["flops"] / (t_attn * 1e-3) / 1e12
+    att_ai = wl["flops"] / wl["attn_bytes"]
+    ridge = peaks["bf16_sus"] * 1e12 / (peaks["hbm"] * 1e9)
+    if att_ai >= ridge:
+        roof = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
+                "frac": round(achieved_tf / peaks["bf16_sus"], 4)}
+    else:
+        gbs = wl["attn_bytes"] / (t_attn * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm"], 4)}
+    roof.update({"kernel": "packed draft attention", "traffic": None, "peak_source": peaks["source"] +
+                 (" (sustained bf16)" if roof["bound"] == "tensor" else " (copy bandwidth)"),
+                 "algorithmic": {"flops": wl["flops"], "bytes": wl["attn_bytes"]}})
+    verify_gbs = wl["verify_bytes"] / (t_verify * 1e-3) / 1e9
+
+    value = world * wl["n_q"] * R / (ms_step * 1e-3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy; random bf16 tensors and logits)",
+        "config": {"workload": "%s: R=%d, prefix %s, %d/%d heads, d=%d, B=%d%s, N_async=%d, V=%d, M=%d heads"
+                   % (args.workload, R, cfg["L"], Hq, Hkv, d, B,
+                      (", C=%d, F=%d" % (cfg["C"], cfg["F"])) if cfg["layout"] == "async" else " block",
+                      wl["n_q"], V, (cfg.get("C", 1) - 1) * cfg.get("F", 1) + 2),
+                   "l2": "inputs rotate over %d sets (%.0f MB > 2x L2 %.0f MB)" % (
+                       n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
+                   "timing": "CUDA graph replays, CUDA events on the launching stream"},
+        "verified_positions_per_s": round(world * wl["positions"] / (ms_step * 1e-3), 1),
+        "parts": {"attn_us": round(t_attn * 1e3, 3), "verify_us": round(t_verify * 1e3, 3),
+                  "match_us": round(t_match * 1e3, 3),
+                  "attn_query_tokens_per_s": round(wl["n_q"] * R / (t_attn * 1e-3), 1),
+                  "verify_positions_per_s": round(wl["positions"] / (t_verify * 1e-3), 1),
+                  "verify_hbm": {"achieved": round(verify_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                                 "frac": round(verify_gbs / peaks["hbm"], 4),
+                                 "bytes": wl["verify_bytes"]}},
+        "roofline": roof,
+        "gpu_launches": args.steps * (LAUNCHES["attn"] + LAUNCHES["verify"] + LAUNCHES["match"]),
+        "clocks": clk, "wall_s_timed_region": round(wall, 4),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(torch, d3d, sets, n_sets, attn, verify, match, dev, stream, args, R, B, dist):
+    """Same metric through the public API, inputs from pinned host memory and
+    results read back every step; copies inside the timed region."""
+    in_keys = ["q", "kp", "vp", "kn", "vn", "segs", "cu_prefix", "cu_q", "cu_seg", "target", "draft", "y",
+               "u_accept", "u_sample", "heads", "head_len"]
+    out_keys = ["out", "out_tokens", "num_tokens", "branch"]
+    host = [{k: s[k].cpu().pin_memory() for k in in_keys + out_keys} for s in sets]
+    h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in in_keys)
+    d2h = sum(host[0][k].numel() * host[0][k].element_size() for k in out_keys)
+    n = max(n_sets, min(args.steps, 2000))
+
+    def one(i):
+        s, h = sets[i % n_sets], host[i % n_sets]
+        for k in in_keys:
+            s[k].copy_(h[k], non_blocking=True)
+        attn(s)
+        verify(s)
+        match(s)
+        for k in out_keys:
+            h[k].copy_(s[k], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(n_sets):
+            one(i)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(n):
+            one(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    world = dist.get_world_size() if dist is not None else 1
+    n_q = sets[0]["q"].shape[0]
+    return {"value": round(world * n_q / (ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 5), "steps": n}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle baseline / reference arm.
+# ----------------------------------------------------------------------------
+class OracleSample:
+    """The oracle timed on a bounded sample of one round of the workload.
+
+    Inputs are generated once.  A sample is the attention of `tokens` packed
+    query tokens x `heads` query heads (fp64, every visible key), the
+    verification of the round over the first `vocab` vocabulary entries,
+    and the full branch match; each part's time is scaled by the fraction of
+    the round it covered, giving an estimate of one whole round."""
+
+    def __init__(self, wl_name: str, seed: int = 0):
+        import oracle
+
+        self.oracle = oracle
+        self.wl = workload(wl_name)
+        self.cfg = self.wl["cfg"]
+        self.attn = W.attn_inputs(**self.cfg, seed=seed)
+        self.seed = seed
+        self._verify = {}
+
+    def verify_inputs(self, vocab: int):
+        if vocab not in self._verify:
+            v = W.verify_inputs(**dict(self.cfg, V=vocab), seed=self.seed)
+            hb = W.branch_heads(v["y"], self.cfg["B"], self.cfg.get("C", 1), self.cfg.get("F", 1), vocab,
+                                seed=self.seed)
+            self._verify[vocab] = (v, hb)
+        return self._verify[vocab]
+
+    def run(self, tokens: int, heads: int, vocab: int):
+        NT = self.attn["q"].shape[0]
+        v, hb = self.verify_inputs(vocab)
+        t0 = time.perf_counter()
+        self.oracle.packed_attn(self.attn, heads=(0, heads), tokens=(0, tokens))
+        t1 = time.perf_counter()
+        r = self.oracle.spec_verify(v)
+        t2 = time.perf_counter()
+        self.oracle.branch_match(dict(verified=r["out_tokens"], verified_len=r["num_tokens"], heads=hb["heads"],
+                                      head_len=hb["head_len"]))
+        t3 = time.perf_counter()
+        sa = (NT / tokens) * (self.cfg["Hq"] / heads)
+        sv = self.cfg["V"] / vocab
+        est = (t1 - t0) * sa + (t2 - t1) * sv + (t3 - t2)
+        desc = ("plain C oracle, fp64, 1 thread: attention of %d of %d packed tokens x %d of %d query heads "
+                "(scaled x%.1f), verification over %d of %d vocabulary entries (scaled x%.1f), full match"
+                % (tokens, NT, heads, self.cfg["Hq"], sa, vocab, self.cfg["V"], sv))
+        return est, t3 - t0, desc
+
+
+def cpu_baseline(wl_name: str) -> dict:
+    """The oracle on one whole round (all tokens and heads, the full vocabulary)."""
+    s = OracleSample(wl_name)
+    est, actual, desc = s.run(s.attn["q"].shape[0], s.cfg["Hq"], s.cfg["V"])
+    return {"value": round(s.wl["n_q"] * s.wl["R"] / est, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": desc, "est_s_per_step": round(est, 3), "sample_s": round(actual, 3)}
+
+
+def run_reference(args, rank: int, world: int):
+    """The reference arm: the oracle on this host, one bounded sample per step."""
+    if rank != 0:
+        return
+    K, Wm = args.steps, args.warmup
+    budget = min(10.0, 150.0 / max(1, K + Wm))  # seconds per step: the run ends within minutes
+    s = OracleSample(args.workload)
+    NT, Hq, V = s.attn["q"].shape[0], s.cfg["Hq"], s.cfg["V"]
+    _, t_cal, _ = s.run(1, 1, 1024)  # calibration: one (token, head) row, 1024 vocabulary entries
+    rows = int(max(1, min(NT * Hq, budget / max(t_cal, 1e-6))))
+    heads = max(1, min(Hq, rows // NT))
+    tokens = NT if heads > 1 else max(1, min(NT, rows))
+    vocab = int(max(1024, min(V, V * (tokens * heads) / (NT * Hq))))
+    for _ in range(Wm):
+        s.run(tokens, heads, vocab)
+    ests, t0, desc = [], time.perf_counter(), ""
+    for _ in range(K):
+        e, _, desc = s.run(tokens, heads, vocab)
+        ests.append(e)
+    wall = time.perf_counter() - t0
+    ms = 1e3 * float(np.mean(ests))
+    value = s.wl["n_q"] * s.wl["R"] / (ms * 1e-3)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy)",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(wall, 2)}), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

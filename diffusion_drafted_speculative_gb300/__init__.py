@@ -1,0 +1,232 @@
+"""GB300 (sm_103a) hot path of diffusion-drafted speculative decoding.
+
+Thin Python binding of the C ABI in ``include/d3d.h`` (library
+``libd3d.so`` built from ``csrc/`` by :mod:`.build`).  The functions carry the
+C names and only marshal arguments: shapes, dtypes and devices are checked,
+sizes are read off the tensors, pointers and the current CUDA stream are
+passed through.  Every step runs in the library's kernels; there is no
+fallback of any kind.  If the library is missing, importing this package
+raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "D3DError", "lib", "d3d_status_string", "d3d_version", "d3d_validate_segments",
+    "d3d_packed_draft_attn", "d3d_packed_draft_attn_workspace_size", "d3d_spec_verify",
+    "d3d_spec_verify_workspace_size", "d3d_branch_match", "d3d_workspace_status",
+    "d3d_workspace_init", "new_workspace", "EXPORTED",
+    "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
+    "D3D_ERR_DEVICE_TIMEOUT", "D3D_ERR_DEVICE_INPUT", "D3D_DTYPE_F32", "D3D_DTYPE_BF16",
+    "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR",
+]
+
+D3D_OK = 0
+D3D_ERR_INVALID_ARG = -1
+D3D_ERR_UNSUPPORTED = -2
+D3D_ERR_WORKSPACE = -3
+D3D_ERR_CUDA = -4
+D3D_ERR_DEVICE_TIMEOUT = -5
+D3D_ERR_DEVICE_INPUT = -6
+D3D_DTYPE_F32 = 0
+D3D_DTYPE_BF16 = 1
+D3D_SEG_CAUSAL = 0
+D3D_SEG_BIDIR = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libd3d.so")
+
+_P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+# name -> (restype, argtypes): every symbol declared in include/d3d.h
+EXPORTED = {
+    "d3d_status_string": (ctypes.c_char_p, [_I]),
+    "d3d_version": (_I, []),
+    "d3d_workspace_init": (_I, [_P, _Z, _P]),
+    "d3d_workspace_status": (_I, [_P, _P, _I, _P]),
+    "d3d_validate_segments": (_I, [_P, _P, _P, _I]),
+    "d3d_packed_draft_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "d3d_packed_draft_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                   _F, _P, _P, _Z, _P]),
+    "d3d_spec_verify_workspace_size": (_Z, [_I, _I, _I]),
+    "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "d3d_branch_match": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
+}
+
+
+class D3DError(RuntimeError):
+    """A libd3d call returned a non-OK status."""
+
+    def __init__(self, name: str, rc: int):
+        super().__init__("%s failed: %s (%d)" % (name, d3d_status_string(rc), rc))
+        self.rc = rc
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libd3d.so is not built (expected at %s); run "
+                          "`python diffusion_drafted_speculative_gb300/build.py` (or __graft_entry__.build())" % LIB_PATH)
+    so = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in EXPORTED.items():
+        fn = getattr(so, name)
+        fn.restype, fn.argtypes = res, args
+    return so
+
+
+lib = _load()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, name, dtype, ndim=None, cuda=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims, got shape %s" % (name, ndim, tuple(t.shape)))
+    if cuda and not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _check(name, rc):
+    if rc != D3D_OK:
+        raise D3DError(name, rc)
+
+
+def d3d_status_string(rc: int) -> str:
+    return lib.d3d_status_string(int(rc)).decode()
+
+
+def d3d_version() -> int:
+    return lib.d3d_version()
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """Zero-filled uint8 device buffer for a workspace (torch allocations are 256-byte aligned)."""
+    ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+    assert ws.data_ptr() % 256 == 0
+    return ws
+
+
+def d3d_workspace_init(ws: torch.Tensor, stream=None) -> None:
+    _check("d3d_workspace_init", lib.d3d_workspace_init(_ptr(ws), ws.numel(), _stream(stream)))
+
+
+def d3d_workspace_status(ws: torch.Tensor, clear: bool = False, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    _check("d3d_workspace_status",
+           lib.d3d_workspace_status(_ptr(ws), ctypes.addressof(out), int(bool(clear)), _stream(stream)))
+    return out.value
+
+
+def d3d_validate_segments(segs: torch.Tensor, cu_q: torch.Tensor, cu_seg: torch.Tensor) -> int:
+    """Host-side check of a segment table (CPU int32 tensors); returns the status code."""
+    _need(segs, "segs", torch.int32, 2, cuda=False)
+    _need(cu_q, "cu_q", torch.int32, 1, cuda=False)
+    _need(cu_seg, "cu_seg", torch.int32, 1, cuda=False)
+    if segs.is_cuda or cu_q.is_cuda or cu_seg.is_cuda:
+        raise ValueError("d3d_validate_segments takes host (CPU) tensors")
+    if segs.numel() and segs.shape[1] != 5:
+        raise ValueError("segs must be [n, 5]")
+    return lib.d3d_validate_segments(_ptr(segs) if segs.numel() else None, _ptr(cu_q), _ptr(cu_seg),
+                                     cu_q.numel() - 1)
+
+
+def d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix) -> int:
+    return int(lib.d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix))
+
+
+def d3d_packed_draft_attn(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q, cu_seg,
+                          max_q: int, max_prefix: int, scale: float, out, ws, stream=None) -> None:
+    """Packed drafting attention; shapes as in include/d3d.h (bf16 tensors, int32 tables)."""
+    for t, n in ((q, "q"), (k_prefix, "k_prefix"), (v_prefix, "v_prefix"), (k_packed, "k_packed"),
+                 (v_packed, "v_packed"), (out, "out")):
+        _need(t, n, torch.bfloat16, 3)
+    _need(segs, "segs", torch.int32, 2)
+    for t, n in ((cu_prefix, "cu_prefix"), (cu_q, "cu_q"), (cu_seg, "cu_seg")):
+        _need(t, n, torch.int32, 1)
+    _need(ws, "ws", torch.uint8, 1)
+    NT, Hq, d = q.shape
+    LT, Hkv = k_prefix.shape[0], k_prefix.shape[1]
+    if (k_packed.shape != (NT, Hkv, d) or v_packed.shape != (NT, Hkv, d) or v_prefix.shape != k_prefix.shape
+            or k_prefix.shape[2] != d or out.shape != q.shape or segs.shape[1] != 5):
+        raise ValueError("inconsistent attention shapes")
+    R = cu_q.numel() - 1
+    if cu_prefix.numel() != R + 1 or cu_seg.numel() != R + 1:
+        raise ValueError("cu_prefix, cu_q and cu_seg must all have R+1 entries")
+    rc = lib.d3d_packed_draft_attn(
+        _ptr(q), _ptr(k_prefix), _ptr(v_prefix), _ptr(k_packed), _ptr(v_packed), _ptr(segs), _ptr(cu_prefix),
+        _ptr(cu_q), _ptr(cu_seg), R, Hq, Hkv, d, int(max_q), int(max_prefix), NT, LT, segs.shape[0],
+        float(scale), _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+    _check("d3d_packed_draft_attn", rc)
+
+
+def d3d_spec_verify_workspace_size(R, B, V) -> int:
+    return int(lib.d3d_spec_verify_workspace_size(R, B, V))
+
+
+def d3d_spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature: float,
+                    accept_len, out_tokens, num_tokens, ws, alpha=None, p_draft=None, q_draft=None,
+                    stream=None) -> None:
+    """Speculative-sampling verification; logits f32 or bf16 [R,B,V] / [R,B-1,V]."""
+    if target_logits.dtype == torch.bfloat16:
+        dt = D3D_DTYPE_BF16
+    elif target_logits.dtype == torch.float32:
+        dt = D3D_DTYPE_F32
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    _need(target_logits, "target_logits", target_logits.dtype, 3)
+    _need(draft_logits, "draft_logits", target_logits.dtype, 3)
+    R, B, V = target_logits.shape
+    if draft_logits.shape != (R, B - 1, V):
+        raise ValueError("draft_logits must be [R, B-1, V]")
+    _need(draft_tokens, "draft_tokens", torch.int32, 2)
+    _need(u_accept, "u_accept", torch.float32, 2)
+    _need(u_sample, "u_sample", torch.float32, 1)
+    for t, n, shp in ((accept_len, "accept_len", (R,)), (out_tokens, "out_tokens", (R, B)),
+                      (num_tokens, "num_tokens", (R,))):
+        _need(t, n, torch.int32, len(shp))
+        if tuple(t.shape) != shp:
+            raise ValueError("%s must be %s" % (n, shp))
+    for t, n in ((alpha, "alpha"), (p_draft, "p_draft"), (q_draft, "q_draft")):
+        if t is not None:
+            _need(t, n, torch.float32, 2)
+            if tuple(t.shape) != (R, B - 1):
+                raise ValueError("%s must be [R, B-1]" % n)
+    if draft_tokens.shape != (R, B - 1) or u_accept.shape != (R, B - 1) or u_sample.shape != (R,):
+        raise ValueError("draft_tokens/u_accept must be [R, B-1], u_sample [R]")
+    _need(ws, "ws", torch.uint8, 1)
+    rc = lib.d3d_spec_verify(
+        _ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), R, B, V,
+        float(temperature), _ptr(accept_len), _ptr(out_tokens), _ptr(num_tokens), _ptr(alpha), _ptr(p_draft),
+        _ptr(q_draft), _ptr(ws), ws.numel(), _stream(stream))
+    _check("d3d_spec_verify", rc)
+
+
+def d3d_branch_match(verified, verified_len, heads, head_len, branch, stream=None) -> None:
+    """Branch cache-hit match; int32 tensors as in include/d3d.h."""
+    _need(verified, "verified", torch.int32, 2)
+    _need(verified_len, "verified_len", torch.int32, 1)
+    _need(heads, "heads", torch.int32, 3)
+    _need(head_len, "head_len", torch.int32, 2)
+    _need(branch, "branch", torch.int32, 1)
+    R, M, B = heads.shape
+    if verified.shape != (R, B) or verified_len.shape != (R,) or head_len.shape != (R, M) or branch.shape != (R,):
+        raise ValueError("inconsistent match shapes")
+    rc = lib.d3d_branch_match(_ptr(verified), _ptr(verified_len), _ptr(heads), _ptr(head_len), R, M, B,
+                              _ptr(branch), _stream(stream))
+    _check("d3d_branch_match", rc)

@@ -1,0 +1,214 @@
+/*
+ * d3d.h — C ABI of the GB300 (sm_103a) hot path of diffusion-drafted
+ * speculative decoding: packed drafting attention, speculative-sampling
+ * verification, and the branch cache-hit match.
+ *
+ * Sources:
+ *   [D3D]    "D3D: Decoupled Diffusion Drafting for Asynchronous Speculative
+ *            Decoding" (paper summary page and arXiv abstract).
+ *   [DScout] "Factorization-Guided Training and Inference for
+ *            Diffusion-Drafted Speculative Decoding" (paper summary page).
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers to caller-owned memory, unless an
+ *     argument says "host".  The library never allocates device memory,
+ *     keeps no state between calls, and never frees anything.
+ *   - Work is enqueued on `stream`; the call returns once it is enqueued.
+ *     Outputs are valid after the stream reaches that point.
+ *   - Return value: D3D_OK, or a negative D3D_ERR_* code, in which case
+ *     nothing was enqueued.  Problems that can only be seen on the device
+ *     (a descriptor that lies, a bounded wait that expired) are recorded in
+ *     the status word at the start of the call's workspace; read it with
+ *     d3d_workspace_status().  Kernels never trap.
+ *   - Scratch ("workspace") is caller-allocated device memory of at least
+ *     the size the matching *_workspace_size() function returns, 256-byte
+ *     aligned, zero-filled once before its first use (d3d_workspace_init),
+ *     and not written by the caller between calls.  The kernels leave it
+ *     ready for the next call.  Calls that share one workspace must be
+ *     ordered on the device (same stream, or events).
+ *   - Layouts are row-major and dense (innermost dimension contiguous).
+ *     bf16 is IEEE bfloat16 stored as 16-bit words.
+ */
+#ifndef D3D_H_
+#define D3D_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+#define D3D_OK 0
+#define D3D_ERR_INVALID_ARG (-1)     /* a host-visible argument is invalid            */
+#define D3D_ERR_UNSUPPORTED (-2)     /* valid but not implemented (e.g. head_dim)    */
+#define D3D_ERR_WORKSPACE (-3)       /* workspace NULL, misaligned or too small      */
+#define D3D_ERR_CUDA (-4)            /* a CUDA runtime call failed at enqueue time   */
+#define D3D_ERR_DEVICE_TIMEOUT (-5)  /* device status: a bounded wait expired        */
+#define D3D_ERR_DEVICE_INPUT (-6)    /* device status: device-side data out of range */
+
+/* ---- enums -------------------------------------------------------------- */
+#define D3D_DTYPE_F32 0
+#define D3D_DTYPE_BF16 1
+
+#define D3D_SEG_CAUSAL 0 /* token i of the segment sees tokens 0..i of it      */
+#define D3D_SEG_BIDIR 1  /* every token of the segment sees the whole segment  */
+
+/*
+ * One segment of a request's packed query sequence ([D3D] "Background:
+ * asynchronous drafting and cache hits" and "Method steps", step 4: one
+ * packed forward drafts successor blocks for every rejection position and
+ * alternative anchor, plus the all-accept case).  Fields are local to the
+ * request: q_start is the first packed token of the segment, len its token
+ * count (>= 1); parent is the index (within the request) of an earlier
+ * causal segment without a parent whose first parent_len tokens this
+ * segment also sees, or -1 (then parent_len = 0).  Segments tile the
+ * request's packed tokens in order.
+ */
+typedef struct {
+    int32_t q_start;
+    int32_t len;
+    int32_t mode;
+    int32_t parent;
+    int32_t parent_len;
+} d3d_segment_t;
+
+/* Text for a status code (static storage; never NULL). */
+const char *d3d_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int d3d_version(void);
+
+/* Zero `bytes` of workspace on `stream` (first use, or after a device error). */
+int d3d_workspace_init(void *ws, size_t bytes, cudaStream_t stream);
+
+/* Copy the workspace status word to *status_host (synchronises `stream`) and,
+ * if `clear` is nonzero, reset it to D3D_OK.  Returns D3D_OK or D3D_ERR_CUDA. */
+int d3d_workspace_status(const void *ws, int32_t *status_host, int clear, cudaStream_t stream);
+
+/*
+ * Host-side check of a segment table (all pointers HOST): segments tile
+ * each request in order with no gap or overlap, len >= 1, mode is causal or
+ * bidirectional, a parent is an earlier causal segment of the same request
+ * with no parent of its own (one nesting level), 0 <= parent_len <=
+ * len(parent), parent_len = 0 without a parent, cu_q/cu_seg start at 0 and
+ * do not decrease.  Returns D3D_OK or D3D_ERR_INVALID_ARG.
+ */
+int d3d_validate_segments(const d3d_segment_t *segs, const int32_t *cu_q, const int32_t *cu_seg, int R);
+
+/* ========================================================================
+ * Packed drafting attention.
+ *
+ * [D3D] "Core method" and "Method steps" (steps 2 and 4): every draft block
+ * (anchor + mask tokens) attends to the shared prefix, causally to the
+ * hypothesised accepted tokens of its branch, and bidirectionally within
+ * itself; one packed pass covers N_async = B[(C-1)F+2] query tokens.
+ * [DScout] "Background: block-diffusion drafter": one forward predicts all
+ * mask positions of a block of the latest target token plus bs-1 masks.
+ *
+ * For request r, packed query token i (local) and query head h, with
+ * G = Hq/Hkv and kv head h/G:
+ *   out[i,h] = sum_k softmax_k(scale * <q[i,h], K[k]>) V[k]
+ * over the visible keys k: all prefix rows cu_prefix[r] .. cu_prefix[r+1]-1
+ * of k_prefix/v_prefix, and the packed rows j of k_packed/v_packed (rows
+ * cu_q[r] + j) that are in i's own segment (j <= i when causal) or among
+ * the first parent_len tokens of its parent segment.
+ *
+ *   q           [total_q, Hq, d] bf16      query rows (RoPE already applied)
+ *   k_prefix    [total_prefix, Hkv, d] bf16 cached keys of the shared prefix
+ *   v_prefix    [total_prefix, Hkv, d] bf16
+ *   k_packed    [total_q, Hkv, d] bf16     keys/values of the packed tokens
+ *   v_packed    [total_q, Hkv, d] bf16
+ *   segs        [total_segs] d3d_segment_t (device)
+ *   cu_prefix   [R+1] int32 (device) prefix row offsets, cu_prefix[R] = total_prefix
+ *   cu_q        [R+1] int32 (device) packed row offsets, cu_q[R] = total_q
+ *   cu_seg      [R+1] int32 (device) segment offsets, cu_seg[R] = total_segs
+ *   max_q, max_prefix  host upper bounds of any request's packed / prefix
+ *               length (they size the grid; a request beyond them is a
+ *               device input error)
+ *   d           64 or 128 (else D3D_ERR_UNSUPPORTED); Hq % Hkv == 0 and
+ *               128 % (Hq/Hkv) == 0
+ *   scale       softmax scale (normally 1/sqrt(d))
+ *   out         [total_q, Hq, d] bf16
+ *   ws          workspace, d3d_packed_draft_attn_workspace_size() bytes
+ * Device-side checks: offsets out of the totals' range or a segment table
+ * that breaks the rules of d3d_validate_segments set D3D_ERR_DEVICE_INPUT
+ * in the status word (the affected rows are written as zeros).
+ * ======================================================================== */
+size_t d3d_packed_draft_attn_workspace_size(int R, int Hq, int Hkv, int d, int max_q, int max_prefix);
+
+int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_prefix, const void *k_packed,
+                          const void *v_packed, const d3d_segment_t *segs, const int32_t *cu_prefix,
+                          const int32_t *cu_q, const int32_t *cu_seg, int R, int Hq, int Hkv, int d,
+                          int max_q, int max_prefix, int total_q, int total_prefix, int total_segs,
+                          float scale, void *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ========================================================================
+ * Speculative-sampling verification.
+ *
+ * [D3D] "Background: speculative decoding": accept the drafted prefix by
+ * rejection sampling and resample one token from the residual distribution
+ * at the first rejection, so the output follows the target exactly.
+ * [DScout] "Background: speculative decoding": accept the prefix before the
+ * first rejected token, add a replacement there, or a bonus token when all
+ * drafts are accepted.  [DScout] "Background: AWL and the acceptance rule":
+ * alpha_j = min(1, P_j(y_j) / Q_j(y_j)).
+ *
+ * Per request r (0-based rows: target row j is P_{j+1}, row B-1 is P_B):
+ *   P_j = softmax(target[r,j,:] / T), Q_j = softmax(draft[r,j,:] / T)
+ *   alpha_j = min(1, P_j(y_j) / Q_j(y_j))          (1 when Q_j(y_j) <= P_j(y_j))
+ *   a = number of leading j with u_accept[r,j] < alpha_j
+ *   if a < B-1: t = InvCDF(max(0, P_a - Q_a), u_sample[r])   (row a = P_{a+1})
+ *              (if that residual sums to 0 in fp32: InvCDF(P_a, u_sample[r]))
+ *   else:       t = InvCDF(P_{B-1}, u_sample[r])               (bonus, P_B)
+ *   InvCDF(w, u) = smallest v (ascending) with sum_{x<=v} w_x > u * sum(w)
+ *   out_tokens[r] = [y_0 .. y_{a-1}, t, -1, ...], num_tokens[r] = a + 1
+ *   (the round's tau: accepted drafts plus the target's own token).
+ *
+ *   target_logits [R, B, V], draft_logits [R, B-1, V]  f32 or bf16 (logits_dtype)
+ *   draft_tokens  [R, B-1] int32 in [0, V)
+ *   u_accept [R, B-1], u_sample [R]  float32 in [0, 1)
+ *   temperature   > 0 (else D3D_ERR_INVALID_ARG)
+ *   B >= 2, V >= 1
+ *   accept_len [R], out_tokens [R, B], num_tokens [R]  int32 outputs
+ *   alpha, p_draft, q_draft [R, B-1] float32 outputs, each may be NULL
+ *               (p_draft = P_j(y_j), q_draft = Q_j(y_j))
+ *   ws          workspace, d3d_spec_verify_workspace_size() bytes
+ * A draft token outside [0, V) sets D3D_ERR_DEVICE_INPUT in the status word
+ * and is treated as rejected (alpha = 0).
+ * ======================================================================== */
+size_t d3d_spec_verify_workspace_size(int R, int B, int V);
+
+int d3d_spec_verify(const void *target_logits, const void *draft_logits, int logits_dtype,
+                    const int32_t *draft_tokens, const float *u_accept, const float *u_sample, int R, int B,
+                    int V, float temperature, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
+                    float *alpha, float *p_draft, float *q_draft, void *ws, size_t ws_bytes,
+                    cudaStream_t stream);
+
+/* ========================================================================
+ * Branch cache-hit match.
+ *
+ * [D3D] "Background: asynchronous drafting and cache hits": in the next
+ * round, if the verified prefix equals the beginning of a pre-drafted
+ * branch exactly, that branch's remaining draft tokens are reused.
+ *
+ *   branch[r] = smallest k with head_len[r,k] == verified_len[r] and
+ *               heads[r,k,0:len] == verified[r,0:len]; -1 when none.
+ *   verified [R, B], verified_len [R]  int32 (the verified tokens of the
+ *               round, i.e. out_tokens/num_tokens of d3d_spec_verify)
+ *   heads [R, M, B], head_len [R, M]   int32 (tokens past a head's length
+ *               are ignored)
+ *   branch [R] int32 output
+ * A length outside [0, B] never matches.  No workspace.
+ * ======================================================================== */
+int d3d_branch_match(const int32_t *verified, const int32_t *verified_len, const int32_t *heads,
+                     const int32_t *head_len, int R, int M, int B, int32_t *branch, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* D3D_H_ */

@@ -46,7 +46,7 @@ def _load():
     with _lock:
         if _lib is None:
             _lib = ctypes.CDLL(build())
-            for name in ("oracle_packed_attn", "oracle_packed_attn_heads", "oracle_dense_attn",
+            for name in ("oracle_packed_attn", "oracle_packed_attn_sel", "oracle_dense_attn",
                          "oracle_dense_mask", "oracle_spec_verify", "oracle_branch_match",
                          "oracle_check_segments"):
                 getattr(_lib, name).restype = ctypes.c_int
@@ -97,23 +97,26 @@ def check_segments(segs, cu_q, cu_seg) -> int:
     return _load().oracle_check_segments(_p(segs), _p(cu_q), _p(cu_seg), ctypes.c_int(len(cu_q) - 1))
 
 
-def packed_attn(inp: dict, heads=None) -> np.ndarray:
+def packed_attn(inp: dict, heads=None, tokens=None) -> np.ndarray:
     """Packed drafting attention, visibility-predicate form, fp64 output [NT, Hq, d].
 
     D3D, "Core method" and "Method steps" step 2/4: each block attends to the
     shared prefix, to the hypothesised accepted tokens of its branch, and
     bidirectionally inside itself; the block under verification is causal.
-    ``heads=(lo, hi)`` computes only query heads lo..hi-1 (others stay 0).
+    ``heads=(lo, hi)`` / ``tokens=(lo, hi)`` compute only those query heads /
+    global packed rows (other outputs stay 0).
     """
     q, kp, vp, kn, vn = (_c(inp[k], np.uint16) for k in ("q", "kp", "vp", "kn", "vn"))
     segs, cu_p, cu_q, cu_s = (_c(inp[k], np.int32) for k in ("segs", "cu_prefix", "cu_q", "cu_seg"))
     NT, Hq, d = q.shape
     lo, hi = heads if heads is not None else (0, Hq)
+    tlo, thi = tokens if tokens is not None else (0, NT)
     out = np.zeros((NT, Hq, d), np.float64)
-    rc = _load().oracle_packed_attn_heads(
+    rc = _load().oracle_packed_attn_sel(
         _p(q), _p(kp), _p(vp), _p(kn), _p(vn), _p(segs), _p(cu_p), _p(cu_q), _p(cu_s),
         ctypes.c_int(inp["R"]), ctypes.c_int(Hq), ctypes.c_int(inp["Hkv"]), ctypes.c_int(d),
-        ctypes.c_double(inp["scale"]), ctypes.c_int(lo), ctypes.c_int(hi), _p(out))
+        ctypes.c_double(inp["scale"]), ctypes.c_int(lo), ctypes.c_int(hi), ctypes.c_int(tlo),
+        ctypes.c_int(thi), _p(out))
     if rc != OK:
         raise ValueError("oracle_packed_attn: invalid arguments (rc=%d)" % rc)
     return out

@@ -179,14 +179,16 @@ static void attend_row(const uint16_t *qrow, const uint16_t *const *krows, const
  * cu_seg[r+1].  out [NT, Hq, d] double:
  *   out[q,h] = sum_k softmax_k(scale <Q[q,h], K[k,h/G]>) V[k,h/G]
  * over the visible keys k (whole prefix, plus visible packed keys).
- * When heads_lo/heads_hi select a sub-range of query heads, only those heads
- * are computed (used to time a bounded sample).
+ * Only query heads [heads_lo, heads_hi) of packed rows [tok_lo, tok_hi)
+ * (global row indices) are computed; other outputs are left untouched.
+ * This selects which outputs to compute (to check or time a sample); it
+ * changes nothing in how each output is computed.
  * ---------------------------------------------------------------------- */
-int oracle_packed_attn_heads(const uint16_t *q, const uint16_t *kp, const uint16_t *vp,
-                             const uint16_t *kn, const uint16_t *vn, const int32_t *segs,
-                             const int32_t *cu_prefix, const int32_t *cu_q, const int32_t *cu_seg,
-                             int R, int Hq, int Hkv, int d, double scale, int heads_lo, int heads_hi,
-                             double *out)
+int oracle_packed_attn_sel(const uint16_t *q, const uint16_t *kp, const uint16_t *vp,
+                           const uint16_t *kn, const uint16_t *vn, const int32_t *segs,
+                           const int32_t *cu_prefix, const int32_t *cu_q, const int32_t *cu_seg,
+                           int R, int Hq, int Hkv, int d, double scale, int heads_lo, int heads_hi,
+                           int tok_lo, int tok_hi, double *out)
 {
     if (R < 0 || Hq < 1 || Hkv < 1 || d < 1 || Hq % Hkv)
         return OR_BAD_ARG;
@@ -217,6 +219,8 @@ int oracle_packed_attn_heads(const uint16_t *q, const uint16_t *kp, const uint16
         int nseg = cu_seg[r + 1] - cu_seg[r];
         for (int i = 0; i < N; ++i) {
             size_t qi = (size_t)cu_q[r] + i;
+            if ((long)qi < (long)tok_lo || (long)qi >= (long)tok_hi)
+                continue;
             for (int h = heads_lo; h < heads_hi; ++h) {
                 int hk = h / G;
                 int nk = 0;
@@ -250,8 +254,8 @@ int oracle_packed_attn(const uint16_t *q, const uint16_t *kp, const uint16_t *vp
                        const int32_t *cu_q, const int32_t *cu_seg, int R, int Hq, int Hkv, int d,
                        double scale, double *out)
 {
-    return oracle_packed_attn_heads(q, kp, vp, kn, vn, segs, cu_prefix, cu_q, cu_seg, R, Hq, Hkv, d,
-                                    scale, 0, Hq, out);
+    return oracle_packed_attn_sel(q, kp, vp, kn, vn, segs, cu_prefix, cu_q, cu_seg, R, Hq, Hkv, d, scale,
+                                  0, Hq, 0, cu_q[R], out);
 }
 
 /* ------------------------------------------------------------------------

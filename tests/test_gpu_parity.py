@@ -1,0 +1,248 @@
+"""CUDA path vs oracle, element by element, on seeded inputs (GB300 only).
+
+Sizes span several tiles and ragged tails; the full workloads of the
+benchmark shapes are checked on all tokens of sampled heads (attention) and
+on whole rows (verification)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_util import assert_attn_close, compare_verify, run_attn, run_match, run_verify
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def d3d():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import diffusion_drafted_speculative_gb300 as mod
+
+    return mod
+
+
+def _oracle_heads(a, heads):
+    ref = np.zeros((a["q"].shape[0], a["Hq"], a["d"]))
+    for h in heads:
+        ref[:, h] = oracle.packed_attn(a, heads=(h, h + 1))[:, h]
+    return ref
+
+
+# ------------------------------------------------------------------ attention
+@pytest.mark.parametrize("seed", [0, 1])
+def test_attn_tiny_config(d3d, seed):
+    a = W.attn_inputs(**W.CONFIGS["tiny"], seed=seed)
+    got, ws = run_attn(d3d, a)
+    assert_attn_close(got, oracle.packed_attn(a), "tiny")
+    assert d3d.d3d_workspace_status(ws) == 0
+
+
+@pytest.mark.parametrize("B,C,F,L,Hq,Hkv,d", [
+    (16, 12, 2, 300, 4, 1, 128),    # async layout, GQA 4, ragged prefix tail
+    (16, 4, 1, 129, 8, 2, 64),      # N = 80
+    (8, 3, 2, 0, 2, 2, 64),         # no prefix at all, G = 1
+    (16, 2, 2, 1000, 16, 2, 128),   # G = 8
+    (4, 5, 3, 77, 4, 4, 128),       # tiny blocks
+    (32, 1, 1, 513, 2, 1, 64),      # C = 1: current + all-accept only
+])
+def test_attn_async_layouts(d3d, B, C, F, L, Hq, Hkv, d):
+    a = W.attn_inputs(R=1, L=L, Hq=Hq, Hkv=Hkv, d=d, B=B, C=C, F=F, layout="async", seed=3)
+    got, _ = run_attn(d3d, a)
+    assert_attn_close(got, oracle.packed_attn(a), "async B%d C%d F%d" % (B, C, F))
+
+
+def test_attn_peaky_softmax(d3d):
+    a = W.attn_inputs(R=1, L=700, Hq=4, Hkv=2, d=128, B=16, C=3, F=2, layout="async", seed=4, k_scale=4.0)
+    got, _ = run_attn(d3d, a)
+    assert_attn_close(got, oracle.packed_attn(a), "k x 4")
+
+
+def test_attn_ragged_batch_with_empty_request(d3d):
+    segs = W.async_segments(8, 3, 2)
+    a = W.attn_inputs(R=3, L=(0, 400), Hq=8, Hkv=2, d=128, seed=5, segs=segs)
+    # make request 1 empty (no packed tokens, no segments)
+    n = int(segs[:, 1].sum())
+    keep_q = np.r_[0:n, 2 * n:3 * n]
+    a["q"], a["kn"], a["vn"] = a["q"][keep_q], a["kn"][keep_q], a["vn"][keep_q]
+    a["segs"] = np.concatenate([segs, segs]).astype(np.int32)
+    a["cu_q"] = np.array([0, n, n, 2 * n], np.int32)
+    a["cu_seg"] = np.array([0, len(segs), len(segs), 2 * len(segs)], np.int32)
+    got, ws = run_attn(d3d, a)
+    assert_attn_close(got, oracle.packed_attn(a), "ragged")
+    assert d3d.d3d_workspace_status(ws) == 0
+
+
+def test_attn_random_segment_tables(d3d):
+    rng = np.random.default_rng(6)
+    for t in range(6):
+        rows, q, causal = [], 0, []
+        for s in range(int(rng.integers(1, 12))):
+            ln = int(rng.integers(1, 40))
+            mode = int(rng.integers(0, 2))
+            par, plen = -1, 0
+            if causal and rng.random() < 0.7:
+                par = int(rng.choice(causal))
+                plen = int(rng.integers(0, rows[par][1] + 1))
+            rows.append([q, ln, mode, par, plen])
+            if mode == 0 and par == -1:
+                causal.append(s)
+            q += ln
+        a = W.attn_inputs(R=1, L=int(rng.integers(0, 300)), Hq=4, Hkv=2, d=64, seed=t,
+                          segs=np.array(rows, np.int32))
+        got, _ = run_attn(d3d, a)
+        assert_attn_close(got, oracle.packed_attn(a), "random table %d" % t)
+
+
+def test_attn_async8b_full_size_sampled_heads(d3d):
+    a = W.attn_inputs(**W.CONFIGS["async8b"], seed=0)
+    got, ws = run_attn(d3d, a)
+    heads = [0, 5, 31]
+    ref = _oracle_heads(a, heads)
+    assert_attn_close(got[:, heads], ref[:, heads], "async8b")
+    assert np.isfinite(got).all()
+    assert d3d.d3d_workspace_status(ws) == 0
+
+
+def test_attn_long_block_full_size_sampled_heads(d3d):
+    a = W.attn_inputs(**W.CONFIGS["long_block"], seed=1)
+    got, _ = run_attn(d3d, a)
+    heads = [0, 17]
+    assert_attn_close(got[:, heads], _oracle_heads(a, heads)[:, heads], "long_block")
+
+
+def test_attn_serve32b_full_size_sampled_head(d3d):
+    a = W.attn_inputs(**W.CONFIGS["serve32b"], seed=2)
+    got, _ = run_attn(d3d, a)
+    heads = [37]
+    assert_attn_close(got[:, heads], _oracle_heads(a, heads)[:, heads], "serve32b")
+    assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("C,F", [(4, 1), (16, 5)])
+def test_attn_sweep_full_size_sampled_head(d3d, C, F):
+    a = W.attn_inputs(**dict(W.CONFIGS["sweep"], C=C, F=F), seed=3)
+    assert a["q"].shape[0] == oracle.n_async(16, C, F)
+    got, _ = run_attn(d3d, a)
+    heads = [9]
+    assert_attn_close(got[:, heads], _oracle_heads(a, heads)[:, heads], "sweep C%d F%d" % (C, F))
+
+
+def test_attn_bad_device_descriptor_sets_status(d3d):
+    a = W.attn_inputs(R=1, L=64, Hq=2, Hkv=1, d=64, B=8, C=3, F=2, layout="async", seed=7)
+    a["segs"] = a["segs"].copy()
+    a["segs"][1, 4] = 99  # parent_len longer than the parent: only the device can see it
+    got, ws = run_attn(d3d, a)
+    assert d3d.d3d_workspace_status(ws, clear=True) == d3d.D3D_ERR_DEVICE_INPUT
+    assert d3d.d3d_workspace_status(ws) == d3d.D3D_OK
+    rows = slice(int(a["segs"][1, 0]), int(a["segs"][1, 0] + a["segs"][1, 1]))
+    assert (got[rows] == 0).all()
+
+
+# ------------------------------------------------------------------ verification
+@pytest.mark.parametrize("seed", range(3))
+def test_verify_tiny_config_batched(d3d, seed):
+    v = W.verify_inputs(**dict(W.CONFIGS["tiny"], R=256), seed=seed)
+    got, ws = run_verify(d3d, v)
+    compare_verify(got, oracle.spec_verify(v))
+    assert d3d.d3d_workspace_status(ws) == 0
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_verify_async8b_full_size(d3d, seed):
+    v = W.verify_inputs(**W.CONFIGS["async8b"], seed=seed)
+    got, _ = run_verify(d3d, v)
+    compare_verify(got, oracle.spec_verify(v), min_kept=0.0)
+
+
+def test_verify_serve32b_batch(d3d):
+    v = W.verify_inputs(**W.CONFIGS["serve32b"], seed=1)
+    got, _ = run_verify(d3d, v)
+    kept, excl = compare_verify(got, oracle.spec_verify(v), min_kept=0.8)
+    print("serve32b verify: %d compared, %d near ties excluded" % (kept, excl))
+
+
+@pytest.mark.parametrize("sigma", [0.25, 0.5, 1.0])
+def test_verify_long_block_sigma_sweep(d3d, sigma):
+    v = W.verify_inputs(**dict(W.CONFIGS["long_block"], R=4, sigma=sigma), seed=2)
+    got, _ = run_verify(d3d, v)
+    compare_verify(got, oracle.spec_verify(v), min_kept=0.5)
+
+
+@pytest.mark.parametrize("V", [1, 7, 1000, 8191, 8193, 12345, 16384])
+@pytest.mark.parametrize("dt", [W.DT_F32, W.DT_BF16])
+def test_verify_ragged_vocab(d3d, V, dt):
+    v = W.verify_inputs(R=64, B=5, V=V, logits=dt, seed=V)
+    got, _ = run_verify(d3d, v)
+    compare_verify(got, oracle.spec_verify(v), min_kept=0.8)
+
+
+@pytest.mark.parametrize("B,T", [(2, 1.0), (3, 0.7), (16, 2.0), (64, 1.0)])
+def test_verify_block_sizes_and_temperature(d3d, B, T):
+    v = W.verify_inputs(R=128, B=B, V=2048, logits=W.DT_BF16, seed=B, temperature=T)
+    got, _ = run_verify(d3d, v)
+    compare_verify(got, oracle.spec_verify(v), min_kept=0.8)
+
+
+def test_verify_high_acceptance_and_bonus_path(d3d):
+    # draft == target rows: every draft accepted, the bonus comes from P_B
+    v = W.verify_inputs(R=256, B=8, V=3000, logits=W.DT_F32, sigma=0.0, seed=9)
+    got, _ = run_verify(d3d, v)
+    ref = oracle.spec_verify(v)
+    assert (ref["accept_len"] == 7).all()
+    compare_verify(got, ref)
+
+
+def test_verify_workspace_reuse_and_many_requests(d3d):
+    v = W.verify_inputs(R=4096, B=4, V=64, logits=W.DT_F32, seed=10)
+    got1, ws = run_verify(d3d, v)
+    got2, _ = run_verify(d3d, v, ws=ws)
+    for k in got1:
+        np.testing.assert_array_equal(got1[k], got2[k])
+    compare_verify(got1, oracle.spec_verify(v))
+
+
+def test_verify_bad_draft_token_sets_status(d3d):
+    v = W.verify_inputs(R=2, B=4, V=100, seed=11)
+    v["y"] = v["y"].copy()
+    v["y"][1, 0] = 100
+    got, ws = run_verify(d3d, v)
+    assert d3d.d3d_workspace_status(ws, clear=True) == d3d.D3D_ERR_DEVICE_INPUT
+    assert got["alpha"][1, 0] == 0 and got["accept_len"][1] == 0
+    assert got["out_tokens"][1, 0] != 100
+
+
+# ------------------------------------------------------------------ branch match
+def test_match_planted_hits(d3d):
+    m = W.match_inputs(R=4096, seed=12)
+    got = run_match(d3d, m)
+    np.testing.assert_array_equal(got, oracle.branch_match(m))
+
+
+@pytest.mark.parametrize("M,B", [(5, 3), (70, 6), (33, 40), (0, 4)])
+def test_match_tiny_alphabet(d3d, M, B):
+    rng = np.random.default_rng(M * 100 + B)
+    R = 3000
+    m = dict(verified=rng.integers(0, 2, (R, B)).astype(np.int32),
+             verified_len=rng.integers(-1, B + 2, R).astype(np.int32),
+             heads=rng.integers(0, 2, (R, M, B)).astype(np.int32),
+             head_len=rng.integers(0, B + 1, (R, M)).astype(np.int32))
+    if M == 0:
+        m["heads"] = np.zeros((R, 0, B), np.int32)
+        m["head_len"] = np.zeros((R, 0), np.int32)
+    ref = np.where((m["verified_len"] < 0) | (m["verified_len"] > B), -1,
+                   oracle.branch_match(dict(m, verified_len=np.clip(m["verified_len"], 0, B))))
+    np.testing.assert_array_equal(run_match(d3d, m), ref)
+
+
+# ------------------------------------------------------------------ whole step
+def test_step_verify_then_match_async8b(d3d):
+    v = W.verify_inputs(**dict(W.CONFIGS["async8b"], R=8), seed=13)
+    got, _ = run_verify(d3d, v, want_probs=False)
+    hb = W.branch_heads(v["y"], 16, 12, 2, v["V"], seed=13)
+    m = dict(verified=got["out_tokens"], verified_len=got["num_tokens"], heads=hb["heads"], head_len=hb["head_len"])
+    np.testing.assert_array_equal(run_match(d3d, m), oracle.branch_match(m))
