@@ -19,7 +19,7 @@ __all__ = [
     "D3DError", "lib", "d3d_status_string", "d3d_version", "d3d_validate_segments",
     "d3d_packed_draft_attn", "d3d_packed_draft_attn_workspace_size", "d3d_spec_verify",
     "d3d_spec_verify_workspace_size", "d3d_branch_match", "d3d_workspace_status",
-    "d3d_workspace_init", "new_workspace", "EXPORTED",
+    "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
     "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
     "D3D_ERR_DEVICE_TIMEOUT", "D3D_ERR_DEVICE_INPUT", "D3D_DTYPE_F32", "D3D_DTYPE_BF16",
     "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR",
@@ -54,6 +54,7 @@ EXPORTED = {
     "d3d_spec_verify_workspace_size": (_Z, [_I, _I, _I]),
     "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "d3d_branch_match": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "d3d_debug_inject_fault": (None, [_I]),
 }
 
 
@@ -144,6 +145,11 @@ def d3d_validate_segments(segs: torch.Tensor, cu_q: torch.Tensor, cu_seg: torch.
         raise ValueError("segs must be [n, 5]")
     return lib.d3d_validate_segments(_ptr(segs) if segs.numel() else None, _ptr(cu_q), _ptr(cu_seg),
                                      cu_q.numel() - 1)
+
+
+def d3d_debug_inject_fault(mode: int) -> None:
+    """Failure-detection hook: 1 makes later attention launches time out on purpose, 0 restores."""
+    lib.d3d_debug_inject_fault(int(mode))
 
 
 def d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix) -> int:

@@ -89,8 +89,10 @@ template <> struct Logit<uint16_t> {
 
 template <typename T> __device__ inline bool aligned16(const T *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// Scaled logits x*c of one chunk [v0, v1) in a strided (coalesced) ownership;
-// positions past v1 read as -inf.  Used where only sums matter.
+// Scaled logits x*c of one chunk [v0, v1) in a strided (coalesced) ownership:
+// slot 8k+e of thread t holds position v0 + 2048k + 8t + e, whichever load
+// path a row takes, so two rows loaded this way line up slot by slot.
+// Positions past v1 read as -inf.
 template <typename T>
 __device__ inline void load_chunk_strided(const T *row, int v0, int v1, float c, float (&x)[kVPer])
 {
@@ -106,9 +108,12 @@ __device__ inline void load_chunk_strided(const T *row, int v0, int v1, float c,
         }
     } else {
 #pragma unroll
-        for (int k = 0; k < kVPer; ++k) {
-            const int v = v0 + k * kVThreads + tid;
-            x[k] = v < v1 ? Logit<T>::at(row, v) * c : -INFINITY;
+        for (int k = 0; k < kVPer / 8; ++k) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int v = v0 + k * kVThreads * 8 + tid * 8 + e;
+                x[k * 8 + e] = v < v1 ? Logit<T>::at(row, v) * c : -INFINITY;
+            }
         }
     }
 }

@@ -146,6 +146,17 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
                           int max_q, int max_prefix, int total_q, int total_prefix, int total_segs,
                           float scale, void *out, void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * Failure-detection hook (no counterpart on the pages).  mode 1 makes every
+ * later d3d_packed_draft_attn launch skip its first key-tile load, so the
+ * consumer's bounded wait expires: the kernel records D3D_ERR_DEVICE_TIMEOUT
+ * in the workspace status word, releases its resources and returns; the
+ * outputs of such a call are undefined and the workspace must be
+ * re-initialised.  mode 0 (the default) restores normal operation.  The
+ * setting is process-global and not thread-safe.
+ */
+void d3d_debug_inject_fault(int mode);
+
 /* ========================================================================
  * Speculative-sampling verification.
  *
