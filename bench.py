@@ -80,6 +80,30 @@ def workload(name: str) -> dict:
                 positions=R * B, vis_packed=vis_packed)
 
 
+# ----------------------------------------------------------------------------
+# Rank logic (weak scaling: every rank runs its own requests, no data exchange).
+# ----------------------------------------------------------------------------
+def rank_seed(rank: int, set_index: int) -> int:
+    """Seed of input set `set_index` on `rank`: ranks never share a request."""
+    return 1000 * rank + set_index
+
+
+def reduce_max(x: float, dist, device) -> float:
+    """Max over ranks of a host float (the slowest rank sets the job time)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms_per_step_max: float) -> float:
+    """Units all ranks processed per second, timed by the slowest rank."""
+    return world * units_per_rank / (ms_per_step_max * 1e-3)
+
+
 def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -184,12 +208,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                     num_tokens=torch.empty(R, dtype=torch.int32, device=dev),
                     branch=torch.empty(R, dtype=torch.int32, device=dev))
 
-    first, max_q, max_prefix, scale = host_set(1000 * rank)
+    first, max_q, max_prefix, scale = host_set(rank_seed(rank, 0))
     set_bytes = sum(t.numel() * t.element_size() for t in first.values()) + first["q"].numel() * 2
     n_sets = max(2, math.ceil(2.2 * l2 / set_bytes))
     sets = []
     for s in range(n_sets):
-        hs = first if s == 0 else host_set(1000 * rank + s)[0]
+        hs = first if s == 0 else host_set(rank_seed(rank, s))[0]
         dset = {k: t.to(dev) for k, t in hs.items()}
         dset.update(outputs(hs["q"].shape[0]))
         sets.append(dset)
@@ -282,10 +306,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     wall = time.perf_counter() - t_wall
     clk = clocks.stop()
     ms_step = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = reduce_max(ms_step, dist, dev)
     for w in (ws_a, ws_v):
         st = d3d.d3d_workspace_status(w)
         if st != 0:
@@ -318,7 +339,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                  "algorithmic": {"flops": wl["flops"], "bytes": wl["attn_bytes"]}})
     verify_gbs = wl["verify_bytes"] / (t_verify * 1e-3) / 1e9
 
-    value = world * wl["n_q"] * R / (ms_step * 1e-3)
+    value = whole_job_rate(wl["n_q"] * R, world, ms_step)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
@@ -387,13 +408,10 @@ def run_e2e(torch, d3d, sets, n_sets, attn, verify, match, dev, stream, args, R,
         e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / n
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(ms, dist, dev)
     world = dist.get_world_size() if dist is not None else 1
     n_q = sets[0]["q"].shape[0]
-    return {"value": round(world * n_q / (ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+    return {"value": round(whole_job_rate(n_q, world, ms), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 5), "steps": n}
 
 

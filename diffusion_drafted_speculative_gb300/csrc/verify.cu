@@ -28,6 +28,7 @@ constexpr int kVWarps = kVThreads / 32;
 constexpr int kVChunk = 8192;
 constexpr int kVPer = kVChunk / kVThreads;  // 32 logits per thread
 constexpr int kMaxB = 256;
+constexpr int kMaxChunks = 1024;  // vocabulary up to 8M entries
 constexpr unsigned kFull = 0xffffffffu;
 
 struct ReqInfo {
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kVThreads)
     __threadfence();
 
     // ---- last CTA of request r: row statistics, alpha, first-rejection scan
-    __shared__ float s_m[2 * kMaxB], s_z[2 * kMaxB], s_alpha[kMaxB];
+    __shared__ float s_m[2 * kMaxB], s_z[2 * kMaxB];
     __shared__ int s_a;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float2 *pr = part + (size_t)r * rows * L.nch;
@@ -289,8 +290,14 @@ __global__ void __launch_bounds__(kVThreads)
     }
     __syncthreads();
     int32_t *status = reinterpret_cast<int32_t *>(ws);
+    if (threadIdx.x == 0)
+        s_a = B - 1;
+    __syncthreads();
+    // alpha_j and the acceptance test of every position in parallel; the
+    // first rejection is the smallest rejected position
     for (int jj = threadIdx.x; jj < B - 1; jj += kVThreads) {
         const int yy = y[(size_t)r * (B - 1) + jj];
+        const float uj = u_acc[(size_t)r * (B - 1) + jj];
         float p = 0.f, q = 0.f, al = 0.f;
         if (yy < 0 || yy >= V) {
             record_status(status, D3D_ERR_DEVICE_INPUT);
@@ -301,7 +308,8 @@ __global__ void __launch_bounds__(kVThreads)
             q = exp2f(xd - s_m[B + jj]) / s_z[B + jj];
             al = (p >= q) ? 1.f : p / q;
         }
-        s_alpha[jj] = al;
+        if (!(uj < al))
+            atomicMin(&s_a, jj);
         const size_t o = (size_t)r * (B - 1) + jj;
         if (alpha_out)
             alpha_out[o] = al;
@@ -312,10 +320,7 @@ __global__ void __launch_bounds__(kVThreads)
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        int a = 0;
-        while (a < B - 1 && u_acc[(size_t)r * (B - 1) + a] < s_alpha[a])
-            ++a;
-        s_a = a;
+        const int a = s_a;
         ReqInfo inf;
         inf.a = a;
         inf.mode = (a < B - 1) ? 0 : 1;
@@ -392,13 +397,16 @@ __global__ void __launch_bounds__(kVThreads)
     // ---- last CTA: crossing chunk, then the ordered scan inside it
     __shared__ int s_kind, s_chunk, s_takelast, s_cand, s_lastpos;
     __shared__ float s_prefix, s_target;
+    __shared__ float2 s_sums[kMaxChunks];
     const float2 *pr = part + (size_t)r * L.nch;
+    for (int cc = threadIdx.x; cc < L.nch; cc += kVThreads)
+        s_sums[cc] = __ldcg(&pr[cc]);
+    __syncthreads();
     if (threadIdx.x == 0) {
         float S_res = 0.f, S_p = 0.f;
         for (int cc = 0; cc < L.nch; ++cc) {
-            const float2 t = __ldcg(&pr[cc]);
-            S_res += t.x;
-            S_p += t.y;
+            S_res += s_sums[cc].x;
+            S_p += s_sums[cc].y;
         }
         // residual unless it has no mass left in fp32 (then P at that row)
         const int kind = (inf.mode == 0 && S_res > 0.f) ? 0 : 1;
@@ -407,7 +415,7 @@ __global__ void __launch_bounds__(kVThreads)
         float run = 0.f;
         int ch = -1;
         for (int cc = 0; cc < L.nch; ++cc) {
-            const float2 t = __ldcg(&pr[cc]);
+            const float2 t = s_sums[cc];
             const float sc = kind == 0 ? t.x : t.y;
             if (run + sc > tgt) {
                 ch = cc;
@@ -419,7 +427,7 @@ __global__ void __launch_bounds__(kVThreads)
         if (ch < 0) {  // rounding left u*S at or past the end: last chunk with mass
             takelast = 1;
             for (int cc = L.nch - 1; cc >= 0 && ch < 0; --cc) {
-                const float2 t = __ldcg(&pr[cc]);
+                const float2 t = s_sums[cc];
                 if ((kind == 0 ? t.x : t.y) > 0.f)
                     ch = cc;
             }
@@ -505,7 +513,7 @@ extern "C" {
 
 size_t d3d_spec_verify_workspace_size(int R, int B, int V)
 {
-    if (R < 0 || B < 2 || V < 1 || B > d3d::kMaxB)
+    if (R < 0 || B < 2 || V < 1 || B > d3d::kMaxB || V > d3d::kMaxChunks * d3d::kVChunk)
         return 0;
     return d3d::verify_layout(R, B, V).total;
 }
@@ -520,7 +528,7 @@ int d3d_spec_verify(const void *target_logits, const void *draft_logits, int log
         return D3D_ERR_INVALID_ARG;
     if (logits_dtype != D3D_DTYPE_F32 && logits_dtype != D3D_DTYPE_BF16)
         return D3D_ERR_INVALID_ARG;
-    if (B > d3d::kMaxB)
+    if (B > d3d::kMaxB || V > d3d::kMaxChunks * d3d::kVChunk)
         return D3D_ERR_UNSUPPORTED;
     if (R == 0)
         return D3D_OK;
