@@ -18,7 +18,7 @@ import torch
 __all__ = [
     "D3DError", "lib", "d3d_status_string", "d3d_version", "d3d_validate_segments",
     "d3d_packed_draft_attn", "d3d_packed_draft_attn_workspace_size", "d3d_spec_verify",
-    "d3d_spec_verify_workspace_size", "d3d_branch_match", "d3d_workspace_status",
+    "d3d_spec_verify_workspace_size", "d3d_spec_verify_noalloc", "d3d_branch_match", "d3d_workspace_status",
     "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
     "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
     "D3D_ERR_DEVICE_TIMEOUT", "D3D_ERR_DEVICE_INPUT", "D3D_DTYPE_F32", "D3D_DTYPE_BF16",
@@ -55,6 +55,7 @@ EXPORTED = {
     "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "d3d_branch_match": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "d3d_debug_inject_fault": (None, [_I]),
+    "d3d_spec_verify_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 
@@ -221,6 +222,28 @@ def d3d_spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sampl
         float(temperature), _ptr(accept_len), _ptr(out_tokens), _ptr(num_tokens), _ptr(alpha), _ptr(p_draft),
         _ptr(q_draft), _ptr(ws), ws.numel(), _stream(stream))
     _check("d3d_spec_verify", rc)
+
+
+def d3d_spec_verify_noalloc(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature: float,
+                            accept_len, out_tokens, num_tokens, alpha=None, p_draft=None, q_draft=None,
+                            stream=None) -> None:
+    """d3d_spec_verify without a workspace: scratch lives inside the library (see include/d3d.h)."""
+    if target_logits.dtype == torch.bfloat16:
+        dt = D3D_DTYPE_BF16
+    elif target_logits.dtype == torch.float32:
+        dt = D3D_DTYPE_F32
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    R, B, V = target_logits.shape
+    for t, n in ((target_logits, "target_logits"), (draft_logits, "draft_logits"), (draft_tokens, "draft_tokens"),
+                 (u_accept, "u_accept"), (u_sample, "u_sample"), (accept_len, "accept_len"),
+                 (out_tokens, "out_tokens"), (num_tokens, "num_tokens")):
+        _need(t, n, t.dtype)
+    rc = lib.d3d_spec_verify_noalloc(
+        _ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), R, B, V,
+        float(temperature), _ptr(accept_len), _ptr(out_tokens), _ptr(num_tokens), _ptr(alpha), _ptr(p_draft),
+        _ptr(q_draft), _stream(stream))
+    _check("d3d_spec_verify_noalloc", rc)
 
 
 def d3d_branch_match(verified, verified_len, heads, head_len, branch, stream=None) -> None:

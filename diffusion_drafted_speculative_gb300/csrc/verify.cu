@@ -18,6 +18,8 @@
 // The second pass re-reads one row pair, normally still resident in L2.
 #include <math.h>
 
+#include <mutex>
+
 #include "d3d_common.cuh"
 
 namespace d3d {
@@ -548,3 +550,94 @@ int d3d_spec_verify(const void *target_logits, const void *draft_logits, int log
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Verification without a caller workspace.
+//
+// For callers that cannot allocate device memory, the scratch the two
+// verification kernels need lives in one fixed, file-scope device array.
+// Every device that loads this library holds it until the process exits.
+// ---------------------------------------------------------------------------
+namespace d3d {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;  // 2 MiB
+constexpr int kNoAllocMaxDevices = 64;
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kNoAllocMaxDevices];
+
+}  // namespace
+}  // namespace d3d
+
+static __device__ __align__(256) unsigned char d3d_noalloc_verify_scratch[d3d::kNoAllocScratchBytes];
+
+namespace d3d {
+namespace {
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device, with that device current, and cached.
+int noalloc_scratch(void **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return D3D_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return D3D_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, d3d_noalloc_verify_scratch);
+        if (e != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return D3D_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = ptr;
+    }
+    *out = g_noalloc_addr[dev];
+    return D3D_OK;
+}
+
+}  // namespace
+}  // namespace d3d
+
+extern "C" int d3d_spec_verify_noalloc(const void *target_logits, const void *draft_logits, int logits_dtype,
+                                       const int32_t *draft_tokens, const float *u_accept, const float *u_sample,
+                                       int R, int B, int V, float temperature, int32_t *accept_len,
+                                       int32_t *out_tokens, int32_t *num_tokens, float *alpha, float *p_draft,
+                                       float *q_draft, cudaStream_t stream)
+{
+    if (R < 0 || B < 2 || V < 1 || !(temperature > 0.f) || !isfinite(temperature))
+        return D3D_ERR_INVALID_ARG;
+    if (logits_dtype != D3D_DTYPE_F32 && logits_dtype != D3D_DTYPE_BF16)
+        return D3D_ERR_INVALID_ARG;
+    if (B > d3d::kMaxB || V > d3d::kMaxChunks * d3d::kVChunk)
+        return D3D_ERR_UNSUPPORTED;
+    if (R == 0)
+        return D3D_OK;
+    if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_sample || !accept_len ||
+        !out_tokens || !num_tokens)
+        return D3D_ERR_INVALID_ARG;
+    const d3d::VerifyLayout L = d3d::verify_layout(R, B, V);
+    if (L.total > d3d::kNoAllocScratchBytes)
+        return D3D_ERR_UNSUPPORTED;  // needs more scratch than the fixed array holds
+    void *scratch = nullptr;
+    const int rc = d3d::noalloc_scratch(&scratch);
+    if (rc != D3D_OK)
+        return rc;
+    // the array keeps the previous call's contents: zero the status word and
+    // the two per-request tickets, which must start at zero
+    if (cudaMemsetAsync(scratch, 0, L.part1, stream) != cudaSuccess)
+        return D3D_ERR_CUDA;
+    const float c = (float)(1.4426950408889634 / (double)temperature);
+    unsigned char *w = static_cast<unsigned char *>(scratch);
+    if (logits_dtype == D3D_DTYPE_BF16)
+        return d3d::launch_verify<uint16_t>(target_logits, draft_logits, draft_tokens, u_accept, u_sample, R, B, V,
+                                            c, accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w,
+                                            stream);
+    return d3d::launch_verify<float>(target_logits, draft_logits, draft_tokens, u_accept, u_sample, R, B, V, c,
+                                     accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w, stream);
+}

@@ -199,6 +199,36 @@ int d3d_spec_verify(const void *target_logits, const void *draft_logits, int log
                     float *alpha, float *p_draft, float *q_draft, void *ws, size_t ws_bytes,
                     cudaStream_t stream);
 
+/*
+ * Verification that allocates nothing (the pages have no counterpart: this
+ * is a calling convenience of this library).
+ *
+ * Some callers cannot allocate device memory at all: a serving process whose
+ * memory manager has already reserved the whole GPU for model weights and KV
+ * cache, code in a latency-critical loop that cannot afford the device-wide
+ * synchronisation cudaMalloc implies, or a caller behind a C interface with
+ * no allocator to hand.  This entry point computes exactly what
+ * d3d_spec_verify computes, with the same arguments minus the workspace; its
+ * scratch is a fixed 2 MiB array inside the library, which every device that
+ * loads the library holds until the process exits.
+ *
+ *   - Problems whose d3d_spec_verify_workspace_size(R, B, V) exceeds 2 MiB
+ *     are rejected with D3D_ERR_UNSUPPORTED (for B = 16 and V = 151936 that
+ *     is R above about 400 requests); use d3d_spec_verify for those.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call shares the one array per device: calls that overlap on the
+ *     GPU (different streams without ordering between them) race and give
+ *     wrong results.  Each call zeroes the parts that must start at zero.
+ *   - A draft token outside [0, V) is handled as in d3d_spec_verify but is
+ *     not reported back; call d3d_spec_verify when that status is needed.
+ * Returns D3D_OK, D3D_ERR_INVALID_ARG, D3D_ERR_UNSUPPORTED or D3D_ERR_CUDA.
+ */
+int d3d_spec_verify_noalloc(const void *target_logits, const void *draft_logits, int logits_dtype,
+                            const int32_t *draft_tokens, const float *u_accept, const float *u_sample, int R, int B,
+                            int V, float temperature, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
+                            float *alpha, float *p_draft, float *q_draft, cudaStream_t stream);
+
 /* ========================================================================
  * Branch cache-hit match.
  *
