@@ -3,27 +3,36 @@
 // [D3D] "Core method", "Method steps" steps 2 and 4; [DScout] "Background:
 // block-diffusion drafter".  See attn_common.cuh for the visibility rule.
 //
-// Work unit (one CTA): request r, KV head hk, a 128-row query tile and one
-// KV split.  The 128 rows are (packed token, query head of hk's group)
-// pairs, token-major, so one KV tile serves all G query heads of the group.
-// A unit's key list is every 128-key tile of the request's prefix followed
-// by the packed-key tiles that its rows can see (computed from the segment
-// table at CTA start); the list is cut into `S` contiguous splits.
+// Work unit (one CTA): request r, KV head hk, a pair of 128-row query tiles
+// and one KV split.  A query tile's 128 rows are (packed token, query head of
+// hk's group) pairs, token-major, so one K/V tile serves all G query heads
+// of the group and both query tiles of the pair.  A unit's key list is every
+// 128-key tile of the request's prefix followed by the packed-key tiles its
+// rows can see.  Splits cut the prefix tiles; the last split also takes the
+// packed tiles, so every other split knows its tiles without the visibility
+// mask and starts loading at once.
 //
-// Roles (192 threads):
-//   warps 0-3  softmax: thread i owns TMEM lane i = query row i.  Reads S
-//              from TMEM, applies the visibility mask, keeps the running max
-//              (rescaling O in TMEM only when the max grows by > 2^8) and the
-//              row sum, writes P (bf16) to shared memory in the 128-byte
-//              swizzled K-major layout, and finally normalises O.
-//   warp 4     TMA producer: Q once, then K and V tiles into 3- and 2-deep
-//              rings (3-D tensor maps over [rows, heads, head_dim]).
-//   warp 5     MMA issuer (one thread): S = Q K^T into one of two TMEM
-//              buffers, O += P V into TMEM; tcgen05.commit releases ring
-//              slots and signals the softmax warps.  Also owns TMEM.
-// With S > 1 splits each thread writes its row's partial (O, max, sum) to the
-// workspace; the thread that completes a row's last split (per-row atomic
-// ticket) merges the partials and writes the output row.
+// Roles (320 threads):
+//   warps 0-3 / 4-7  softmax warpgroup of query tile 0 / 1: thread i owns
+//              TMEM lane i = row i.  Reads S (one tcgen05.ld of 128 columns),
+//              masks it, keeps the running max (rescaling O in TMEM only when
+//              the max grows by more than 2^8) and the row sum, and writes P
+//              as bf16 pairs back over the first 64 columns of S.
+//   warp 8     TMA producer: Q tiles once, then K and V tiles into 3- and
+//              2-deep rings (3-D tensor maps, 128-byte swizzle).
+//   warp 9     MMA issuer (one thread), owner of TMEM.  Per key tile j it
+//              issues PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): O_t += P_t V_j
+//              with P read from TMEM, S_t = Q_t K^T into TMEM.  While one
+//              warpgroup computes its softmax the tensor core works for the
+//              other.  S_t(j+1) overwrites P_t(j) only after PV_t(j), which
+//              the tensor core executes first (MMAs of one thread run in
+//              issue order), and the commit that signals S_t(j+1) also
+//              guarantees PV_t(j) is complete, so O_t is stable for the
+//              softmax's rescale.
+// TMEM: tile t uses columns [256t, 256t+128) for S/P and [256t+128, +D) for O.
+// With several splits each thread writes its row's partial (O, max, sum) to
+// the workspace in a row-fastest layout; the thread completing a row's last
+// split (per-row atomic ticket) merges the partials and writes the output.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -41,11 +50,13 @@ using namespace sm100;
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per KV tile
+constexpr int kTiles = 2;  // query tiles per CTA
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
-constexpr int kThreads = 192;
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kSoftmaxThreads = kTiles * 128;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxPackedTiles = 64;  // packed keys per request <= 8192
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
@@ -54,15 +65,15 @@ constexpr uint32_t kBlockBytes = kBN * 128;  // one 128-row x 128-byte swizzled 
 // barrier indices
 enum {
     B_Q = 0,
-    B_KF = 1,                       // 3
-    B_KE = B_KF + kKStages,         // 3
-    B_VF = B_KE + kKStages,         // 2
-    B_VE = B_VF + kVStages,         // 2
-    B_SF = B_VE + kVStages,         // 2
-    B_SE = B_SF + 2,                // 2
-    B_PR = B_SE + 2,
-    B_PF = B_PR + 1,
-    B_DONE = B_PF + 1,
+    B_KF = 1,                   // kKStages
+    B_KE = B_KF + kKStages,     // kKStages
+    B_VF = B_KE + kKStages,     // kVStages
+    B_VE = B_VF + kVStages,     // kVStages
+    B_SF = B_VE + kVStages,     // kTiles: S_t(j) in TMEM
+    B_PR = B_SF + kTiles,       // kTiles: P_t(j) in TMEM (128 arrivals)
+    B_OD = B_PR + kTiles,       // kTiles: O_t final
+    B_MASK = B_OD + kTiles,     // visibility mask complete (256 arrivals)
+    B_DONE = B_MASK + 1,        // every MMA of the CTA complete
     B_COUNT = B_DONE + 1
 };
 
@@ -70,12 +81,10 @@ template <int D> struct Layout {
     static constexpr uint32_t kQBytes = kBM * D * 2;
     static constexpr uint32_t kKBytes = kBN * D * 2;
     static constexpr uint32_t kVBytes = kBN * D * 2;
-    static constexpr uint32_t kPBytes = kBM * kBN * 2;
     static constexpr uint32_t q = 0;
-    static constexpr uint32_t k = q + kQBytes;
+    static constexpr uint32_t k = q + kTiles * kQBytes;
     static constexpr uint32_t v = k + kKStages * kKBytes;
-    static constexpr uint32_t p = v + kVStages * kVBytes;
-    static constexpr uint32_t bars = p + kPBytes;
+    static constexpr uint32_t bars = v + kVStages * kVBytes;
     static constexpr uint32_t misc = bars + B_COUNT * 8;
     static constexpr uint32_t total = misc + 64;
     static constexpr uint32_t alloc = total + 1024;  // room to align the base to 1024 bytes
@@ -86,7 +95,7 @@ struct AttnParams {
     const int32_t *cu_prefix, *cu_q, *cu_seg;
     uint16_t *out;
     unsigned char *ws;
-    int Hq, Hkv, G, TQ, MT, S;
+    int Hq, Hkv, G, TQ, MT, MP, S, PK;
     int max_q, max_prefix, total_q, total_prefix, total_segs;
     float scale_log2;
     unsigned long long off_cnt, off_opart, off_ml;
@@ -104,12 +113,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
 }
 
 // k-th set bit (0-based) of the 64-bit mask (m0 | m1 << 32); k < popcount.
@@ -142,6 +145,16 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, int32_
     }
 }
 
+// First prefix tile of split sp: the prefix tiles are cut as if the packed
+// tiles (estimated PK of them) were part of the list, then clamped.
+__device__ __forceinline__ int split_prefix_begin(int sp, int S, int nP, int PK)
+{
+    if (sp >= S)
+        return nP;
+    const long long b = ((long long)(nP + PK) * sp) / S;
+    return (int)(b < nP ? b : nP);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
@@ -152,15 +165,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // ---- unit: ((r * Hkv + hk) * MT + mt) * S + sp
+    // ---- unit: ((r * Hkv + hk) * MP + mp) * S + sp
     unsigned u = blockIdx.x;
     const int sp = (int)(u % (unsigned)p.S);
     u /= (unsigned)p.S;
-    const int mt = (int)(u % (unsigned)p.MT);
-    u /= (unsigned)p.MT;
+    const int mp = (int)(u % (unsigned)p.MP);
+    u /= (unsigned)p.MP;
     const int hk = (int)(u % (unsigned)p.Hkv);
     const int r = (int)(u / (unsigned)p.Hkv);
-    const unsigned tile_id = blockIdx.x / (unsigned)p.S;  // (r, hk, mt)
+    const unsigned pair_id = blockIdx.x / (unsigned)p.S;  // (r, hk, mp)
     int32_t *status = reinterpret_cast<int32_t *>(p.ws);
 
     ReqBounds b;
@@ -170,20 +183,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             record_status(status, D3D_ERR_DEVICE_INPUT);
         return;
     }
-    const int tq0 = mt * p.TQ;
-    if (tq0 >= b.n_q)
+    bool tile_valid[kTiles];
+    for (int t = 0; t < kTiles; ++t)
+        tile_valid[t] = (2 * mp + t) < p.MT && (2 * mp + t) * p.TQ < b.n_q;
+    if (!tile_valid[0])
         return;
+    const int ntiles = tile_valid[1] ? 2 : 1;
+
+    // ---- this split's tiles: prefix tiles [pb, pe), then (last split only) packed tiles
+    const int nP = (b.L + kBN - 1) / kBN;
+    const int pb = split_prefix_begin(sp, p.S, nP, p.PK);
+    const int pe = (sp == p.S - 1) ? nP : split_prefix_begin(sp + 1, p.S, nP, p.PK);
+    const int n_pre = pe - pb;
+    const bool last_split = sp == p.S - 1;
 
     // ---- shared memory carve-up (1024-byte aligned base for the swizzled tiles)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (sbase - raw);
-    const uint32_t sQ = sbase + Lay::q, sK = sbase + Lay::k, sV = sbase + Lay::v, sP = sbase + Lay::p;
+    const uint32_t sQ = sbase + Lay::q, sK = sbase + Lay::k, sV = sbase + Lay::v;
     auto bar = [&](int i) -> uint32_t { return sbase + Lay::bars + 8u * (uint32_t)i; };
     uint32_t *misc = reinterpret_cast<uint32_t *>(gbase + Lay::misc);
     volatile uint32_t *tmem_slot = misc + 0;
     volatile uint32_t *abort_flag = misc + 1;
-    uint32_t *mask = misc + 2;  // 2 words: packed tiles visible to some row
+    uint32_t *mask = misc + 2;  // 2 words: packed tiles visible to some row of the pair
 
     if (tid == 0) {
         mbar_init(bar(B_Q), 1);
@@ -195,12 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_VF + i), 1);
             mbar_init(bar(B_VE + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_SF + i), 1);
-            mbar_init(bar(B_SE + i), 128);
+        for (int t = 0; t < kTiles; ++t) {
+            mbar_init(bar(B_SF + t), 1);
+            mbar_init(bar(B_PR + t), 128);
+            mbar_init(bar(B_OD + t), 1);
         }
-        mbar_init(bar(B_PR), 128);
-        mbar_init(bar(B_PF), 1);
+        mbar_init(bar(B_MASK), kSoftmaxThreads);
         mbar_init(bar(B_DONE), 1);
         *abort_flag = 0u;
         mask[0] = mask[1] = 0u;
@@ -217,93 +240,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
         tmem_relinquish();
     }
-    __syncthreads();
-
-    // ---- rows: visibility intervals and the packed tiles they need
-    RowVis vis;
-    vis.own_lo = vis.own_hi = vis.par_lo = vis.par_hi = 0;
-    bool row_valid = false, row_bad = false;
-    int token = 0;
-    if (warp < 4) {
-        token = tq0 + tid / p.G;
-        row_valid = token < b.n_q;
-        if (row_valid) {
-            if (!row_visibility(p.segs, b.s0, b.s1, b.n_q, token, vis)) {
-                row_bad = true;
-                vis.own_lo = vis.own_hi = vis.par_lo = vis.par_hi = 0;
-            }
-            auto mark = [&](int lo, int hi) {
-                if (lo >= hi)
-                    return;
-                for (int t = lo / kBN; t <= (hi - 1) / kBN && t < kMaxPackedTiles; ++t)
-                    atomicOr(&mask[t >> 5], 1u << (t & 31));
-            };
-            mark(vis.own_lo, vis.own_hi);
-            mark(vis.par_lo, vis.par_hi);
-        }
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t m0 = mask[0], m1 = mask[1];
-    const int nP = (b.L + kBN - 1) / kBN;
-    const int T = nP + __popc(m0) + __popc(m1);
-    const int t_begin = (int)(((long long)T * sp) / p.S);
-    const int n = (int)(((long long)T * (sp + 1)) / p.S) - t_begin;
-    // tile i of this split: prefix tile index, or packed tile index (is_prefix false)
-    auto tile_of = [&](int i, bool &is_prefix) -> int {
-        const int g = t_begin + i;
-        is_prefix = g < nP;
-        return is_prefix ? g : nth_set_bit(m0, m1, g - nP);
-    };
 
-    const uint32_t tS0 = tmem, tO = tmem + 256u;
+    // number of packed tiles of the pair; waits for the mask on first use
+    int npk_cache = -1;
+    uint32_t mk0 = 0, mk1 = 0;
+    auto npk = [&]() -> int {
+        if (npk_cache < 0) {
+            if (!wait_bar(bar(B_MASK), 0, abort_flag, status))
+                return -1;
+            mk0 = *(volatile uint32_t *)&mask[0];
+            mk1 = *(volatile uint32_t *)&mask[1];
+            npk_cache = __popc(mk0) + __popc(mk1);
+        }
+        return npk_cache;
+    };
+    // does tile j of this split exist (-1: gave up waiting)
+    auto exists = [&](int j) -> int {
+        if (j < n_pre)
+            return 1;
+        if (!last_split)
+            return 0;
+        const int c = npk();
+        return c < 0 ? -1 : (j - n_pre < c ? 1 : 0);
+    };
+    // global K/V row and map of tile j (call only when it exists)
+    auto tile_row = [&](int j, bool &pre) -> int {
+        pre = j < n_pre;
+        return pre ? b.p0 + (pb + j) * kBN : b.q0 + nth_set_bit(mk0, mk1, j - n_pre) * kBN;
+    };
 
     if (warp == kTmaWarp) {
         // =================== TMA producer ===================
-        if (lane == 0 && n > 0) {
+        if (lane == 0) {
             int k_cnt[kKStages] = {0, 0, 0}, v_cnt[kVStages] = {0, 0};
-            bool ok = true;
-            mbar_arrive_expect_tx(bar(B_Q), Lay::kQBytes);
-            for (int cb = 0; cb < D / 64; ++cb)
-                tma_load_3d(sQ + cb * kBlockBytes, &tm_q, bar(B_Q), cb * 64, hk * p.G, b.q0 + tq0);
-            auto issue_k = [&](int j) -> bool {
-                const int s = j % kKStages;
-                if (j >= kKStages && !wait_bar(bar(B_KE + s), ((j - kKStages) / kKStages) & 1, abort_flag, status))
+            mbar_arrive_expect_tx(bar(B_Q), Lay::kQBytes * ntiles);
+            for (int t = 0; t < ntiles; ++t)
+                for (int cb = 0; cb < D / 64; ++cb)
+                    tma_load_3d(sQ + t * Lay::kQBytes + cb * kBlockBytes, &tm_q, bar(B_Q), cb * 64, hk * p.G,
+                                b.q0 + (2 * mp + t) * p.TQ);
+            auto issue = [&](int j, bool is_k) -> bool {
+                const int ns = is_k ? kKStages : kVStages;
+                const int s = j % ns;
+                const int empty = is_k ? B_KE : B_VE, full = is_k ? B_KF : B_VF;
+                if (j >= ns && !wait_bar(bar(empty + s), ((j - ns) / ns) & 1, abort_flag, status))
                     return false;
-                if (p.fault == 1 && j == 0)
+                if (p.fault == 1 && is_k && j == 0)
                     return true;  // injected fault: this tile never arrives
                 bool pre;
-                const int t = tile_of(j, pre);
-                const CUtensorMap *m = pre ? &tm_kp : &tm_kn;
-                const int row = pre ? b.p0 + t * kBN : b.q0 + t * kBN;
-                mbar_arrive_expect_tx(bar(B_KF + s), Lay::kKBytes);
+                const int row = tile_row(j, pre);
+                const CUtensorMap *m = is_k ? (pre ? &tm_kp : &tm_kn) : (pre ? &tm_vp : &tm_vn);
+                const uint32_t dst = (is_k ? sK : sV) + s * Lay::kKBytes;
+                mbar_arrive_expect_tx(bar(full + s), Lay::kKBytes);
                 for (int cb = 0; cb < D / 64; ++cb)
-                    tma_load_3d(sK + s * Lay::kKBytes + cb * kBlockBytes, m, bar(B_KF + s), cb * 64, hk, row);
-                ++k_cnt[s];
+                    tma_load_3d(dst + cb * kBlockBytes, m, bar(full + s), cb * 64, hk, row);
+                ++(is_k ? k_cnt[s] : v_cnt[s]);
                 return true;
             };
-            auto issue_v = [&](int j) -> bool {
-                const int s = j % kVStages;
-                if (j >= kVStages && !wait_bar(bar(B_VE + s), ((j - kVStages) / kVStages) & 1, abort_flag, status))
-                    return false;
-                bool pre;
-                const int t = tile_of(j, pre);
-                const CUtensorMap *m = pre ? &tm_vp : &tm_vn;
-                const int row = pre ? b.p0 + t * kBN : b.q0 + t * kBN;
-                mbar_arrive_expect_tx(bar(B_VF + s), Lay::kVBytes);
-                for (int cb = 0; cb < D / 64; ++cb)
-                    tma_load_3d(sV + s * Lay::kVBytes + cb * kBlockBytes, m, bar(B_VF + s), cb * 64, hk, row);
-                ++v_cnt[s];
-                return true;
-            };
-            ok = issue_k(0);
-            for (int j = 0; j < n && ok; ++j) {
-                if (j + 1 < n)
-                    ok = issue_k(j + 1);
+            int more = exists(0);
+            bool ok = more >= 0;
+            if (more == 1)
+                ok = issue(0, true);
+            for (int j = 0; ok && more == 1; ++j) {
+                const int next = exists(j + 1);
+                if (next < 0)
+                    break;
+                if (next == 1)
+                    ok = issue(j + 1, true);
                 if (ok)
-                    ok = issue_v(j);
+                    ok = issue(j, false);
+                more = next;
             }
             // every copy this thread started must land before the CTA exits
             wait_drain(bar(B_Q), 0, status);
@@ -317,155 +326,184 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // =================== MMA issuer ===================
-        if (lane == 0 && n > 0) {
+        if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
             constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 0, 1);
-            auto pv = [&](int i) -> bool {
-                if (!wait_bar(bar(B_PR), i & 1, abort_flag, status))
-                    return false;
-                const int vs = i % kVStages;
-                if (!wait_bar(bar(B_VF + vs), (i / kVStages) & 1, abort_flag, status))
-                    return false;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    // A = P (K-major, 64 keys per swizzled block); B = V (MN-major:
-                    // 16 keys = two 8-row groups = 2048 bytes; next 64 d-columns +16 KB)
-                    const uint64_t a = sdesc_sw128(sP + (kk / 4) * kBlockBytes + (kk % 4) * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(sV + vs * Lay::kVBytes + kk * 2048, kBlockBytes, 1024);
-                    mma_bf16_ss(tO, a, bd, idO, (i > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(bar(B_VE + vs));
-                mma_commit(bar(B_PF));
-                return true;
-            };
-            bool ok = wait_bar(bar(B_Q), 0, abort_flag, status);
-            for (int j = 0; j < n && ok; ++j) {
+            auto issue_s = [&](int t, int j) {
                 const int ks = j % kKStages;
-                ok = wait_bar(bar(B_KF + ks), (j / kKStages) & 1, abort_flag, status);
-                if (ok && j >= 2)
-                    ok = wait_bar(bar(B_SE + (j & 1)), ((j - 2) / 2) & 1, abort_flag, status);
-                if (!ok)
-                    break;
-                tc_fence_after();
-                const uint32_t tS = tS0 + (uint32_t)(j & 1) * 128u;
+                const uint32_t tS = tmem + (uint32_t)t * 256u;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * kBlockBytes + (kk % 4) * 32;
-                    const uint64_t a = sdesc_sw128(sQ + off, 16, 1024);
+                    const uint64_t a = sdesc_sw128(sQ + t * Lay::kQBytes + off, 16, 1024);
                     const uint64_t bd = sdesc_sw128(sK + ks * Lay::kKBytes + off, 16, 1024);
                     mma_bf16_ss(tS, a, bd, idS, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(B_SF + (j & 1)));
-                mma_commit(bar(B_KE + ks));
-                if (j >= 1)
-                    ok = pv(j - 1);
+                mma_commit(bar(B_SF + t));
+            };
+            auto issue_pv = [&](int t, int j) {
+                const int vs = j % kVStages;
+                const uint32_t tP = tmem + (uint32_t)t * 256u, tO = tP + 128u;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    // A = P_t in TMEM (8 columns of bf16 pairs per 16 keys); B = V
+                    // MN-major: 16 keys = two 8-row groups = 2048 bytes, the next 64
+                    // head-dim columns are 16 KB further
+                    const uint64_t bd = sdesc_sw128(sV + vs * Lay::kVBytes + kk * 2048, kBlockBytes, 1024);
+                    mma_bf16_ts(tO, tP + kk * 8, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
+            int more = exists(0);
+            bool ok = more >= 0 && wait_bar(bar(B_Q), 0, abort_flag, status);
+            if (ok && more == 1) {
+                ok = wait_bar(bar(B_KF), 0, abort_flag, status);
+                if (ok) {
+                    tc_fence_after();
+                    for (int t = 0; t < ntiles; ++t)
+                        issue_s(t, 0);
+                    mma_commit(bar(B_KE));
+                }
             }
-            if (ok)
-                pv(n - 1);
+            for (int j = 0; ok && more == 1; ++j) {
+                const int next = exists(j + 1);
+                if (next < 0)
+                    break;
+                ok = wait_bar(bar(B_VF + j % kVStages), (j / kVStages) & 1, abort_flag, status);
+                if (ok && next == 1)
+                    ok = wait_bar(bar(B_KF + (j + 1) % kKStages), ((j + 1) / kKStages) & 1, abort_flag, status);
+                for (int t = 0; ok && t < ntiles; ++t) {
+                    ok = wait_bar(bar(B_PR + t), j & 1, abort_flag, status);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    issue_pv(t, j);
+                    if (next == 1)
+                        issue_s(t, j + 1);
+                    else
+                        mma_commit(bar(B_OD + t));
+                }
+                if (!ok)
+                    break;
+                mma_commit(bar(B_VE + j % kVStages));
+                if (next == 1)
+                    mma_commit(bar(B_KE + (j + 1) % kKStages));
+                more = next;
+            }
             // all MMAs this thread issued must finish before TMEM is released
             mma_commit(bar(B_DONE));
             wait_drain(bar(B_DONE), 0, status);
         }
         __syncwarp();
     } else {
-        // =================== softmax warps ===================
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const int row = tid;
+        // =================== softmax warpgroups ===================
+        const int t = warp >> 2;  // query tile of this warpgroup
+        const int row = tid & 127;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + (uint32_t)t * 256u + lane_off, tO = tS + 128u;
+        const int token = (2 * mp + t) * p.TQ + row / p.G;
+        const bool row_valid = tile_valid[t] && token < b.n_q;
+        bool row_bad = false;
+        RowVis vis;
+        vis.own_lo = vis.own_hi = vis.par_lo = vis.par_hi = 0;
+        if (row_valid) {
+            if (!row_visibility(p.segs, b.s0, b.s1, b.n_q, token, vis)) {
+                row_bad = true;
+                vis.own_lo = vis.own_hi = vis.par_lo = vis.par_hi = 0;
+            }
+            auto mark = [&](int lo, int hi) {
+                if (lo >= hi)
+                    return;
+                for (int k = lo / kBN; k <= (hi - 1) / kBN && k < kMaxPackedTiles; ++k)
+                    atomicOr(&mask[k >> 5], 1u << (k & 31));
+            };
+            mark(vis.own_lo, vis.own_hi);
+            mark(vis.par_lo, vis.par_hi);
+        }
+        mbar_arrive(bar(B_MASK));
+
         float m_ref = -INFINITY, l = 0.f;
         bool aborted = false;
-        for (int j = 0; j < n; ++j) {
-            bool ok = wait_bar(bar(B_SF + (j & 1)), (j / 2) & 1, abort_flag, status);
-            if (!__all_sync(0xffffffffu, ok)) {
-                aborted = true;
-                break;
-            }
-            tc_fence_after();
-            float s[kBN];
-            const uint32_t tS = tS0 + (uint32_t)(j & 1) * 128u + lane_off;
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c)
-                tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(&s[c * 32]));
-            tc_fence_before();
-            mbar_arrive(bar(B_SE + (j & 1)));
-
-            bool pre;
-            const int t = tile_of(j, pre);
-            if (pre) {
-                const int valid = b.L - t * kBN;
-                if (valid < kBN) {
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c)
-                        if (c >= valid)
-                            s[c] = -INFINITY;
+        int n_done = 0;
+        if (tile_valid[t]) {
+            for (int j = 0;; ++j) {
+                const int ex = exists(j);
+                if (!__all_sync(0xffffffffu, ex >= 0)) {
+                    aborted = true;
+                    break;
                 }
-            } else {
-                const int kb = t * kBN;
-#pragma unroll
-                for (int c = 0; c < kBN; ++c)
-                    if (!vis_has(vis, kb + c))
-                        s[c] = -INFINITY;
-            }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kBN; ++c)
-                mx = fmaxf(mx, s[c]);
-            mx *= p.scale_log2;
-            float factor = 1.f;
-            if (mx > m_ref + kRescaleLog2) {
-                factor = ex2(m_ref - mx);  // 0 when m_ref = -inf
-                m_ref = mx;
-            }
-            const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float rs = 0.f;
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                s[c] = ex2(fmaf(s[c], p.scale_log2, -msub));
-                rs += s[c];
-            }
-            l = l * factor + rs;
-
-            if (j >= 1) {  // P buffer free and O final for the previous tile
-                ok = wait_bar(bar(B_PF), (j - 1) & 1, abort_flag, status);
+                if (ex == 0)
+                    break;
+                bool ok = wait_bar(bar(B_SF + t), j & 1, abort_flag, status);
                 if (!__all_sync(0xffffffffu, ok)) {
                     aborted = true;
                     break;
                 }
-                if (__any_sync(0xffffffffu, factor != 1.f)) {
-                    tc_fence_after();
+                tc_fence_after();
+                float s[kBN];
+                tmem_ld128(tS, s);
+                bool pre;
+                const int krow = tile_row(j, pre);
+                if (pre) {
+                    const int valid = b.L - (pb + j) * kBN;
+                    if (valid < kBN) {
+#pragma unroll
+                        for (int c = 0; c < kBN; ++c)
+                            if (c >= valid)
+                                s[c] = -INFINITY;
+                    }
+                } else {
+                    const int kb = krow - b.q0;
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c)
+                        if (!vis_has(vis, kb + c))
+                            s[c] = -INFINITY;
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kBN; ++c)
+                    mx = fmaxf(mx, s[c]);
+                mx *= p.scale_log2;
+                float factor = 1.f;
+                if (mx > m_ref + kRescaleLog2) {
+                    factor = ex2(m_ref - mx);  // 0 when m_ref = -inf
+                    m_ref = mx;
+                }
+                const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
+                float rs = 0.f;
+                uint32_t pk[kBN / 2];
+#pragma unroll
+                for (int c = 0; c < kBN / 2; ++c) {
+                    const float e0 = ex2(fmaf(s[2 * c], p.scale_log2, -msub));
+                    const float e1 = ex2(fmaf(s[2 * c + 1], p.scale_log2, -msub));
+                    rs += e0 + e1;
+                    pk[c] = pack_bf16x2(e0, e1);
+                }
+                l = l * factor + rs;
+                // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled
+                if (j > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         float o[32];
-                        tmem_ld32(tO + lane_off + c * 32, o);
+                        tmem_ld32(tO + c * 32, o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             o[e] *= factor;
-                        tmem_st32(tO + lane_off + c * 32, o);
+                        tmem_st32(tO + c * 32, o);
                     }
-                    tmem_wait_st();
                 }
+                tmem_st64(tS, pk);  // P over the first 64 columns of S
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(B_PR + t));
+                n_done = j + 1;
             }
-            // P row -> shared memory, 128-byte swizzle: chunk ch of row i at (ch ^ (i & 7))
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const float *q8 = &s[cb * 64 + ch * 8];
-                    const uint32_t addr = sP + cb * kBlockBytes + row * 128 + (((uint32_t)ch ^ (row & 7)) << 4);
-                    st_shared_v4(addr, pack_bf16x2(q8[0], q8[1]), pack_bf16x2(q8[2], q8[3]),
-                                 pack_bf16x2(q8[4], q8[5]), pack_bf16x2(q8[6], q8[7]));
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(B_PR));
         }
 
         // ---- epilogue
-        if (!aborted) {
-            bool have_o = n > 0;
+        if (tile_valid[t] && !aborted) {
+            const bool have_o = n_done > 0;
             if (have_o) {
-                const bool ok = wait_bar(bar(B_PF), (n - 1) & 1, abort_flag, status);
+                const bool ok = wait_bar(bar(B_OD + t), 0, abort_flag, status);
                 if (!__all_sync(0xffffffffu, ok))
                     aborted = true;
             }
@@ -473,91 +511,92 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 uint16_t *orow = p.out + ((size_t)(b.q0 + token) * p.Hq + hk * p.G + (row % p.G)) * D;
                 if (p.S == 1) {
-                    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+                    const float inv = (l > 0.f && !row_bad) ? 1.f / l : 0.f;
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         float o[32];
-                        tmem_ld32(tO + lane_off + c * 32, o);
+                        tmem_ld32(tO + c * 32, o);
                         if (row_valid) {
                             uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
                             for (int q4 = 0; q4 < 4; ++q4) {
                                 uint4 w;
-                                const float sc = row_bad ? 0.f : inv;
-                                w.x = pack_bf16x2(o[q4 * 8 + 0] * sc, o[q4 * 8 + 1] * sc);
-                                w.y = pack_bf16x2(o[q4 * 8 + 2] * sc, o[q4 * 8 + 3] * sc);
-                                w.z = pack_bf16x2(o[q4 * 8 + 4] * sc, o[q4 * 8 + 5] * sc);
-                                w.w = pack_bf16x2(o[q4 * 8 + 6] * sc, o[q4 * 8 + 7] * sc);
+                                w.x = pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+                                w.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+                                w.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+                                w.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
                                 dst[q4] = w;
                             }
                         }
                     }
                 } else {
-                    // partial of this split, then the per-row ticket
-                    const size_t pidx = (size_t)tile_id * p.S + sp;
-                    float *opart = reinterpret_cast<float *>(p.ws + p.off_opart) + (pidx * kBM + row) * D;
-                    float2 *ml = reinterpret_cast<float2 *>(p.ws + p.off_ml) + pidx * kBM + row;
+                    // partial of this split in a row-fastest layout: float4 chunk c4 of
+                    // row i of partial q lives at ((q * D/4 + c4) * 128 + i)
+                    const size_t tile_id = (size_t)pair_id * kTiles + t;
+                    const size_t pidx = tile_id * p.S + sp;
+                    float4 *opart = reinterpret_cast<float4 *>(p.ws + p.off_opart);
+                    float2 *mls = reinterpret_cast<float2 *>(p.ws + p.off_ml);
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         float o[32];
                         if (have_o) {
-                            tmem_ld32(tO + lane_off + c * 32, o);
+                            tmem_ld32(tO + c * 32, o);
                         } else {
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
                                 o[e] = 0.f;
                         }
-                        float4 *dst = reinterpret_cast<float4 *>(opart + c * 32);
 #pragma unroll
                         for (int q4 = 0; q4 < 8; ++q4)
-                            dst[q4] = make_float4(o[q4 * 4], o[q4 * 4 + 1], o[q4 * 4 + 2], o[q4 * 4 + 3]);
+                            opart[(pidx * (D / 4) + c * 8 + q4) * kBM + row] =
+                                make_float4(o[q4 * 4], o[q4 * 4 + 1], o[q4 * 4 + 2], o[q4 * 4 + 3]);
                     }
-                    *ml = make_float2(m_ref, l);
+                    mls[pidx * kBM + row] = make_float2(m_ref, l);
                     __threadfence();
-                    int *cnt = reinterpret_cast<int *>(p.ws + p.off_cnt) + (size_t)tile_id * kBM + row;
-                    const int prev = atomicAdd(cnt, 1);
-                    if (prev == p.S - 1) {
+                    int *cnt = reinterpret_cast<int *>(p.ws + p.off_cnt) + tile_id * kBM + row;
+                    if (atomicAdd(cnt, 1) == p.S - 1) {
                         __threadfence();
                         *cnt = 0;  // ready for the next call
                         float M = -INFINITY;
                         for (int s2 = 0; s2 < p.S; ++s2)
-                            M = fmaxf(M, __ldcg(reinterpret_cast<float2 *>(p.ws + p.off_ml) +
-                                                ((size_t)tile_id * p.S + s2) * kBM + row)
-                                             .x);
+                            M = fmaxf(M, __ldcg(mls + (tile_id * p.S + s2) * kBM + row).x);
                         float Lsum = 0.f;
-                        float acc[D];
-#pragma unroll
-                        for (int e = 0; e < D; ++e)
-                            acc[e] = 0.f;
-                        if (M != -INFINITY) {
+                        if (M != -INFINITY)
                             for (int s2 = 0; s2 < p.S; ++s2) {
-                                const size_t q2 = ((size_t)tile_id * p.S + s2) * kBM + row;
-                                const float2 mls = __ldcg(reinterpret_cast<float2 *>(p.ws + p.off_ml) + q2);
-                                const float wgt = ex2(mls.x - M);
-                                Lsum += mls.y * wgt;
-                                const float4 *src = reinterpret_cast<const float4 *>(
-                                    reinterpret_cast<float *>(p.ws + p.off_opart) + q2 * D);
+                                const float2 v = __ldcg(mls + (tile_id * p.S + s2) * kBM + row);
+                                Lsum += v.y * ex2(v.x - M);
+                            }
+                        const float sc = (row_bad || !(Lsum > 0.f) || M == -INFINITY) ? 0.f : 1.f / Lsum;
+                        for (int c = 0; c < D / 32; ++c) {
+                            float acc[32];
 #pragma unroll
-                                for (int e4 = 0; e4 < D / 4; ++e4) {
-                                    const float4 v = __ldcg(src + e4);
-                                    acc[e4 * 4 + 0] += wgt * v.x;
-                                    acc[e4 * 4 + 1] += wgt * v.y;
-                                    acc[e4 * 4 + 2] += wgt * v.z;
-                                    acc[e4 * 4 + 3] += wgt * v.w;
+                            for (int e = 0; e < 32; ++e)
+                                acc[e] = 0.f;
+                            if (sc != 0.f) {
+                                for (int s2 = 0; s2 < p.S; ++s2) {
+                                    const size_t q2 = tile_id * p.S + s2;
+                                    const float wgt = ex2(__ldcg(mls + q2 * kBM + row).x - M);
+#pragma unroll
+                                    for (int q4 = 0; q4 < 8; ++q4) {
+                                        const float4 v = __ldcg(opart + (q2 * (D / 4) + c * 8 + q4) * kBM + row);
+                                        acc[q4 * 4 + 0] += wgt * v.x;
+                                        acc[q4 * 4 + 1] += wgt * v.y;
+                                        acc[q4 * 4 + 2] += wgt * v.z;
+                                        acc[q4 * 4 + 3] += wgt * v.w;
+                                    }
                                 }
                             }
-                        }
-                        if (row_valid) {
-                            const float sc = (row_bad || !(Lsum > 0.f)) ? 0.f : 1.f / Lsum;
-                            uint4 *dst = reinterpret_cast<uint4 *>(orow);
+                            if (row_valid) {
+                                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
-                            for (int q8 = 0; q8 < D / 8; ++q8) {
-                                uint4 w;
-                                w.x = pack_bf16x2(acc[q8 * 8 + 0] * sc, acc[q8 * 8 + 1] * sc);
-                                w.y = pack_bf16x2(acc[q8 * 8 + 2] * sc, acc[q8 * 8 + 3] * sc);
-                                w.z = pack_bf16x2(acc[q8 * 8 + 4] * sc, acc[q8 * 8 + 5] * sc);
-                                w.w = pack_bf16x2(acc[q8 * 8 + 6] * sc, acc[q8 * 8 + 7] * sc);
-                                dst[q8] = w;
+                                for (int q4 = 0; q4 < 4; ++q4) {
+                                    uint4 w;
+                                    w.x = pack_bf16x2(acc[q4 * 8 + 0] * sc, acc[q4 * 8 + 1] * sc);
+                                    w.y = pack_bf16x2(acc[q4 * 8 + 2] * sc, acc[q4 * 8 + 3] * sc);
+                                    w.z = pack_bf16x2(acc[q4 * 8 + 4] * sc, acc[q4 * 8 + 5] * sc);
+                                    w.w = pack_bf16x2(acc[q4 * 8 + 6] * sc, acc[q4 * 8 + 7] * sc);
+                                    dst[q4] = w;
+                                }
                             }
                         }
                     }
@@ -581,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Host side
 // ---------------------------------------------------------------------------
 struct AttnPlan {
-    int G, TQ, MT, S;
+    int G, TQ, MT, MP, S, PK;
     long long units;
     size_t off_cnt, off_opart, off_ml, total;
 };
@@ -598,35 +637,38 @@ int num_sms()
 }
 
 // Split count: minimise (waves of one-CTA-per-SM units) x (tiles per unit +
-// a fixed per-unit cost), where the per-unit cost covers the prologue, the
-// pipeline fill and, with splits, the merge.
+// a fixed per-unit cost for the prologue and pipeline fill, one more for the
+// merge when splitting).
 AttnPlan make_plan(int R, int Hq, int Hkv, int d, int max_q, int max_prefix, int nsm)
 {
     AttnPlan pl{};
     pl.G = Hq / Hkv;
     pl.TQ = kBM / pl.G;
     pl.MT = (max_q + pl.TQ - 1) / pl.TQ;
-    const long long base = (long long)R * Hkv * pl.MT;
-    const int tiles = (max_prefix + kBN - 1) / kBN + 2;
+    pl.MP = (pl.MT + kTiles - 1) / kTiles;
+    pl.PK = (max_q + kBN - 1) / kBN < 2 ? (max_q + kBN - 1) / kBN : 2;
+    const long long base = (long long)R * Hkv * pl.MP;
+    const int tiles = (max_prefix + kBN - 1) / kBN + pl.PK;
     double best = 1e300;
     pl.S = 1;
     for (int S = 1; S <= 32 && S <= tiles; ++S) {
         const double waves = (double)((base * S + nsm - 1) / nsm);
-        const double cost = waves * (double)((tiles + S - 1) / S + 2 + (S > 1 ? 1 : 0));
+        const double cost = waves * (double)((tiles + S - 1) / S + 3 + (S > 1 ? 1 : 0));
         if (cost < best - 1e-9) {
             best = cost;
             pl.S = S;
         }
     }
     pl.units = base * pl.S;
+    const size_t rows = (size_t)base * kTiles * kBM;
     size_t o = sizeof(WsHeader);
     pl.off_cnt = o;
     if (pl.S > 1) {
-        o = align_up(o + sizeof(int) * (size_t)base * kBM, kWsAlign);
+        o = align_up(o + sizeof(int) * rows, kWsAlign);
         pl.off_opart = o;
-        o = align_up(o + sizeof(float) * (size_t)base * pl.S * kBM * d, kWsAlign);
+        o = align_up(o + sizeof(float) * rows * pl.S * d, kWsAlign);
         pl.off_ml = o;
-        o = align_up(o + sizeof(float2) * (size_t)base * pl.S * kBM, kWsAlign);
+        o = align_up(o + sizeof(float2) * rows * pl.S, kWsAlign);
     } else {
         pl.off_opart = pl.off_ml = o;
     }
@@ -730,12 +772,11 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
         return D3D_ERR_UNSUPPORTED;
 
     CUtensorMap maps[5];
-    const bool have_prefix = total_prefix > 0;
     if (!d3d::make_map(&maps[0], q, d, Hq, total_q, pl.G, pl.TQ) ||
         !d3d::make_map(&maps[3], k_packed, d, Hkv, total_q, 1, d3d::kBN) ||
         !d3d::make_map(&maps[4], v_packed, d, Hkv, total_q, 1, d3d::kBN))
         return D3D_ERR_CUDA;
-    if (have_prefix) {
+    if (total_prefix > 0) {
         if (!d3d::make_map(&maps[1], k_prefix, d, Hkv, total_prefix, 1, d3d::kBN) ||
             !d3d::make_map(&maps[2], v_prefix, d, Hkv, total_prefix, 1, d3d::kBN))
             return D3D_ERR_CUDA;
@@ -756,7 +797,9 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
     prm.G = pl.G;
     prm.TQ = pl.TQ;
     prm.MT = pl.MT;
+    prm.MP = pl.MP;
     prm.S = pl.S;
+    prm.PK = pl.PK;
     prm.max_q = max_q;
     prm.max_prefix = max_prefix;
     prm.total_q = total_q;

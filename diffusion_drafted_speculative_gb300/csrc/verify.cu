@@ -38,7 +38,7 @@ struct ReqInfo {
     int32_t mode;  // 0: residual at target/draft row a; 1: bonus from target row B-1
     int32_t row;   // target row the sample uses (and draft row when mode == 0)
     int32_t pad;
-    float mP, ZP, mQ, ZQ;  // log2-domain row max and normaliser of that target / draft row
+    float mP, rZP, mQ, rZQ;  // log2-domain row max and 1 / normaliser of that target / draft row
 };
 
 struct VerifyLayout {
@@ -145,6 +145,15 @@ __device__ inline void load_chunk_contig(const T *row, int v0, int v1, float c, 
     }
 }
 
+// 2^x with the hardware approximation (relative error about 2^-22, far
+// inside the 1e-5 tolerance on probabilities); -inf gives 0.
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // (max, sum of exp2(x - max)) merge; an empty side has max = -inf, sum = 0.
 __device__ inline void ms_merge(float &m, float &z, float m2, float z2)
 {
@@ -154,7 +163,7 @@ __device__ inline void ms_merge(float &m, float &z, float m2, float z2)
         z = 0.f;
         return;
     }
-    z = z * exp2f(m - M) + z2 * exp2f(m2 - M);
+    z = z * fast_exp2(m - M) + z2 * fast_exp2(m2 - M);
     m = M;
 }
 
@@ -250,7 +259,7 @@ __global__ void __launch_bounds__(kVThreads)
     if (m != -INFINITY) {
 #pragma unroll
         for (int k = 0; k < kVPer; ++k)
-            z += exp2f(x[k] - m);
+            z += fast_exp2(x[k] - m);
     }
     __shared__ float red[2 * kVWarps];
     __shared__ int s_last;
@@ -306,8 +315,8 @@ __global__ void __launch_bounds__(kVThreads)
         } else {
             const float xt = Logit<T>::at(target + ((size_t)r * B + jj) * V, yy) * c;
             const float xd = Logit<T>::at(draft + ((size_t)r * (B - 1) + jj) * V, yy) * c;
-            p = exp2f(xt - s_m[jj]) / s_z[jj];
-            q = exp2f(xd - s_m[B + jj]) / s_z[B + jj];
+            p = fast_exp2(xt - s_m[jj]) / s_z[jj];
+            q = fast_exp2(xd - s_m[B + jj]) / s_z[B + jj];
             al = (p >= q) ? 1.f : p / q;
         }
         if (!(uj < al))
@@ -329,9 +338,9 @@ __global__ void __launch_bounds__(kVThreads)
         inf.row = (a < B - 1) ? a : B - 1;
         inf.pad = 0;
         inf.mP = s_m[inf.row];
-        inf.ZP = s_z[inf.row];
+        inf.rZP = __frcp_rn(s_z[inf.row]);
         inf.mQ = (a < B - 1) ? s_m[B + a] : 0.f;
-        inf.ZQ = (a < B - 1) ? s_z[B + a] : 1.f;
+        inf.rZQ = (a < B - 1) ? __frcp_rn(s_z[B + a]) : 1.f;
         reinterpret_cast<ReqInfo *>(ws + L.info)[r] = inf;
         accept_len[r] = a;
         num_tokens[r] = a + 1;
@@ -348,10 +357,10 @@ __global__ void __launch_bounds__(kVThreads)
 // max(0, P - Q) (kind 0) or P itself (kind 1); xp/xq are scaled logits.
 __device__ inline float sample_mass(int kind, float xp, float xq, const ReqInfo &inf)
 {
-    const float P = exp2f(xp - inf.mP) / inf.ZP;
+    const float P = fast_exp2(xp - inf.mP) * inf.rZP;
     if (kind != 0)
         return P;
-    const float Q = exp2f(xq - inf.mQ) / inf.ZQ;
+    const float Q = fast_exp2(xq - inf.mQ) * inf.rZQ;
     return fmaxf(P - Q, 0.f);
 }
 
@@ -376,9 +385,9 @@ __global__ void __launch_bounds__(kVThreads)
     float s_res = 0.f, s_p = 0.f;
 #pragma unroll
     for (int k = 0; k < kVPer; ++k) {
-        const float P = exp2f(xp[k] - inf.mP) / inf.ZP;
+        const float P = fast_exp2(xp[k] - inf.mP) * inf.rZP;
         s_p += P;
-        s_res += (inf.mode == 0) ? fmaxf(P - exp2f(xq[k] - inf.mQ) / inf.ZQ, 0.f) : P;
+        s_res += (inf.mode == 0) ? fmaxf(P - fast_exp2(xq[k] - inf.mQ) * inf.rZQ, 0.f) : P;
     }
     __shared__ float red[2 * kVWarps];
     __shared__ int s_last;
