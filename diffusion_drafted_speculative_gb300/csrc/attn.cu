@@ -30,9 +30,11 @@
 //              guarantees PV_t(j) is complete, so O_t is stable for the
 //              softmax's rescale.
 // TMEM: tile t uses columns [256t, 256t+128) for S/P and [256t+128, +D) for O.
-// With several splits each thread writes its row's partial (O, max, sum) to
-// the workspace in a row-fastest layout; the thread completing a row's last
-// split (per-row atomic ticket) merges the partials and writes the output.
+// With several splits, a warpgroup takes a per-tile ticket when it has
+// finished its key tiles; all but the last write their partial (O divided by
+// its row sum, bf16, row-fastest layout, plus max and sum) to the workspace,
+// and the last waits for those stores and merges them with its own O, which
+// is still in TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -61,6 +63,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxPackedTiles = 64;  // packed keys per request <= 8192
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
 constexpr uint32_t kBlockBytes = kBN * 128;  // one 128-row x 128-byte swizzled block (16 KB)
+constexpr int kStagedSegs = 80;  // segment rows staged in shared memory (more: searched in global memory)
+constexpr int kMergeUnroll = 3;  // other splits' partial loads issued together in the merge
+constexpr int kMaxSplits = 32;
 
 // barrier indices
 enum {
@@ -72,7 +77,9 @@ enum {
     B_SF = B_VE + kVStages,     // kTiles: S_t(j) in TMEM
     B_PR = B_SF + kTiles,       // kTiles: P_t(j) in TMEM (128 arrivals)
     B_OD = B_PR + kTiles,       // kTiles: O_t final
-    B_MASK = B_OD + kTiles,     // visibility mask complete (256 arrivals)
+    B_TK = B_OD + kTiles,       // kTiles: split ticket of the tile taken
+    B_RDY = B_TK + kTiles,      // kTiles: merger saw every other split's partial
+    B_MASK = B_RDY + kTiles,    // visibility mask complete (256 arrivals)
     B_DONE = B_MASK + 1,        // every MMA of the CTA complete
     B_COUNT = B_DONE + 1
 };
@@ -86,7 +93,8 @@ template <int D> struct Layout {
     static constexpr uint32_t v = k + kKStages * kKBytes;
     static constexpr uint32_t bars = v + kVStages * kVBytes;
     static constexpr uint32_t misc = bars + B_COUNT * 8;
-    static constexpr uint32_t total = misc + 64;
+    static constexpr uint32_t segs = misc + 64;  // staged segment table of the request
+    static constexpr uint32_t total = segs + kStagedSegs * sizeof(d3d_segment_t);
     static constexpr uint32_t alloc = total + 1024;  // room to align the base to 1024 bytes
 };
 
@@ -129,6 +137,17 @@ __device__ __forceinline__ int nth_set_bit(uint32_t m0, uint32_t m1, int k)
     for (int i = 0; i < k; ++i)
         m &= m - 1;
     return off + __ffs(m) - 1;
+}
+
+// Bits [lo, hi) of a 32-bit word, clipped to [0, 32).
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi)
+{
+    lo = max(lo, 0);
+    hi = min(hi, 32);
+    if (lo >= hi)
+        return 0u;
+    const uint32_t upto_hi = (hi == 32) ? 0xffffffffu : ((1u << hi) - 1u);
+    return upto_hi & ~((1u << lo) - 1u);
 }
 
 // Wait that ignores the abort flag (used to drain in-flight copies / MMAs).
@@ -207,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *tmem_slot = misc + 0;
     volatile uint32_t *abort_flag = misc + 1;
     uint32_t *mask = misc + 2;  // 2 words: packed tiles visible to some row of the pair
+    volatile int *ticket = reinterpret_cast<volatile int *>(misc + 4);  // 2 words: split tickets
+    volatile int *ready_flag = reinterpret_cast<volatile int *>(misc + 6);  // 2 words: merger may go
 
     if (tid == 0) {
         mbar_init(bar(B_Q), 1);
@@ -222,6 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_SF + t), 1);
             mbar_init(bar(B_PR + t), 128);
             mbar_init(bar(B_OD + t), 1);
+        }
+        for (int t = 0; t < kTiles; ++t) {
+            mbar_init(bar(B_TK + t), 1);
+            mbar_init(bar(B_RDY + t), 1);
         }
         mbar_init(bar(B_MASK), kSoftmaxThreads);
         mbar_init(bar(B_DONE), 1);
@@ -405,8 +430,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool row_bad = false;
         RowVis vis;
         vis.own_lo = vis.own_hi = vis.par_lo = vis.par_hi = 0;
-        if (row_valid) {
-            if (!row_visibility(p.segs, b.s0, b.s1, b.n_q, token, vis)) {
+        // only the last split visits packed keys; it searches a shared-memory copy of
+        // the request's segment table when the table is small enough
+        const d3d_segment_t *seg_base = p.segs;
+        int seg_lo = b.s0, seg_hi = b.s1;
+        const int n_seg = b.s1 - b.s0;
+        if (last_split && n_seg <= kStagedSegs) {
+            d3d_segment_t *staged = reinterpret_cast<d3d_segment_t *>(gbase + Lay::segs);
+            const int32_t *src = reinterpret_cast<const int32_t *>(p.segs + b.s0);
+            int32_t *dst = reinterpret_cast<int32_t *>(staged);
+            for (int i = tid; i < n_seg * 5; i += kSoftmaxThreads)
+                dst[i] = src[i];
+            asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+            seg_base = staged;
+            seg_lo = 0;
+            seg_hi = n_seg;
+        }
+        if (row_valid && last_split) {
+            if (!row_visibility(seg_base, seg_lo, seg_hi, b.n_q, token, vis)) {
                 row_bad = true;
                 vis.own_lo = vis.own_hi = vis.par_lo = vis.par_hi = 0;
             }
@@ -421,6 +462,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive(bar(B_MASK));
 
+        // split ticket of this query tile, taken before the last key tile so the
+        // atomic's round trip overlaps that tile's work
+        const size_t tile_id = (size_t)pair_id * kTiles + t;
+        const size_t n_tiles = (size_t)(gridDim.x / p.S) * kTiles;
+        int *tk_cnt = reinterpret_cast<int *>(p.ws + p.off_cnt) + tile_id;
+        int *wr_cnt = reinterpret_cast<int *>(p.ws + p.off_cnt) + n_tiles + tile_id;
+        int my_ticket = -1;
         float m_ref = -INFINITY, l = 0.f;
         bool aborted = false;
         int n_done = 0;
@@ -433,6 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (ex == 0)
                     break;
+                if (p.S > 1 && row == 0 && my_ticket < 0 && exists(j + 1) == 0)
+                    my_ticket = atomicAdd(tk_cnt, 1);
                 bool ok = wait_bar(bar(B_SF + t), j & 1, abort_flag, status);
                 if (!__all_sync(0xffffffffu, ok)) {
                     aborted = true;
@@ -452,11 +502,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 s[c] = -INFINITY;
                     }
                 } else {
+                    // this row's visible keys in the tile as a 128-bit mask: two
+                    // half-open intervals cut into four 32-key words
                     const int kb = krow - b.q0;
+                    uint32_t wbits[4];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int base = kb + 32 * w;
+                        wbits[w] = range_bits(vis.own_lo - base, vis.own_hi - base) |
+                                   range_bits(vis.par_lo - base, vis.par_hi - base);
+                    }
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
-                        if (!vis_has(vis, kb + c))
-                            s[c] = -INFINITY;
+                        s[c] = ((wbits[c >> 5] >> (c & 31)) & 1u) ? s[c] : -INFINITY;
                 }
                 float mx = -INFINITY;
 #pragma unroll
@@ -530,72 +588,220 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 } else {
-                    // partial of this split in a row-fastest layout: float4 chunk c4 of
-                    // row i of partial q lives at ((q * D/4 + c4) * 128 + i)
-                    const size_t tile_id = (size_t)pair_id * kTiles + t;
-                    const size_t pidx = tile_id * p.S + sp;
-                    float4 *opart = reinterpret_cast<float4 *>(p.ws + p.off_opart);
+                    // Ticket first: the warpgroup that finishes this query tile's key
+                    // tiles last merges; the others write their partial normalised by
+                    // its row sum, as bf16 (16-byte chunk c8 of row i of partial q at
+                    // ((q * D/8 + c8) * 128 + i)), with (max, sum) beside it.
+                    uint4 *opart = reinterpret_cast<uint4 *>(p.ws + p.off_opart);
                     float2 *mls = reinterpret_cast<float2 *>(p.ws + p.off_ml);
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        if (have_o) {
-                            tmem_ld32(tO + c * 32, o);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                o[e] = 0.f;
-                        }
-#pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4)
-                            opart[(pidx * (D / 4) + c * 8 + q4) * kBM + row] =
-                                make_float4(o[q4 * 4], o[q4 * 4 + 1], o[q4 * 4 + 2], o[q4 * 4 + 3]);
+                    if (row == 0) {
+                        ticket[t] = (my_ticket >= 0) ? my_ticket : atomicAdd(tk_cnt, 1);
+                        mbar_arrive(bar(B_TK + t));
                     }
-                    mls[pidx * kBM + row] = make_float2(m_ref, l);
-                    __threadfence();
-                    int *cnt = reinterpret_cast<int *>(p.ws + p.off_cnt) + tile_id * kBM + row;
-                    if (atomicAdd(cnt, 1) == p.S - 1) {
-                        __threadfence();
-                        *cnt = 0;  // ready for the next call
-                        float M = -INFINITY;
-                        for (int s2 = 0; s2 < p.S; ++s2)
-                            M = fmaxf(M, __ldcg(mls + (tile_id * p.S + s2) * kBM + row).x);
-                        float Lsum = 0.f;
-                        if (M != -INFINITY)
-                            for (int s2 = 0; s2 < p.S; ++s2) {
-                                const float2 v = __ldcg(mls + (tile_id * p.S + s2) * kBM + row);
-                                Lsum += v.y * ex2(v.x - M);
-                            }
-                        const float sc = (row_bad || !(Lsum > 0.f) || M == -INFINITY) ? 0.f : 1.f / Lsum;
-                        for (int c = 0; c < D / 32; ++c) {
-                            float acc[32];
+                    const bool got = wait_bar(bar(B_TK + t), 0, abort_flag, status);
+                    if (__all_sync(0xffffffffu, got)) {
+                        const bool is_last = ticket[t] == p.S - 1;
+                        if (!is_last) {
+                            const size_t pidx = tile_id * p.S + sp;
+                            const float inv = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                acc[e] = 0.f;
-                            if (sc != 0.f) {
-                                for (int s2 = 0; s2 < p.S; ++s2) {
-                                    const size_t q2 = tile_id * p.S + s2;
-                                    const float wgt = ex2(__ldcg(mls + q2 * kBM + row).x - M);
+                            for (int c = 0; c < D / 32; ++c) {
+                                float o[32];
+                                if (have_o) {
+                                    tmem_ld32(tO + c * 32, o);
+                                } else {
 #pragma unroll
-                                    for (int q4 = 0; q4 < 8; ++q4) {
-                                        const float4 v = __ldcg(opart + (q2 * (D / 4) + c * 8 + q4) * kBM + row);
-                                        acc[q4 * 4 + 0] += wgt * v.x;
-                                        acc[q4 * 4 + 1] += wgt * v.y;
-                                        acc[q4 * 4 + 2] += wgt * v.z;
-                                        acc[q4 * 4 + 3] += wgt * v.w;
-                                    }
+                                    for (int e = 0; e < 32; ++e)
+                                        o[e] = 0.f;
                                 }
-                            }
-                            if (row_valid) {
-                                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
                                 for (int q4 = 0; q4 < 4; ++q4) {
                                     uint4 w;
-                                    w.x = pack_bf16x2(acc[q4 * 8 + 0] * sc, acc[q4 * 8 + 1] * sc);
-                                    w.y = pack_bf16x2(acc[q4 * 8 + 2] * sc, acc[q4 * 8 + 3] * sc);
-                                    w.z = pack_bf16x2(acc[q4 * 8 + 4] * sc, acc[q4 * 8 + 5] * sc);
-                                    w.w = pack_bf16x2(acc[q4 * 8 + 6] * sc, acc[q4 * 8 + 7] * sc);
-                                    dst[q4] = w;
+                                    w.x = pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+                                    w.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+                                    w.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+                                    w.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
+                                    opart[(pidx * (D / 8) + c * 4 + q4) * kBM + row] = w;
+                                }
+                            }
+                            // a negative sum marks a row whose descriptors failed the
+                            // check (only the last split, which visits packed keys, checks)
+                            mls[pidx * kBM + row] = make_float2(m_ref, row_bad ? -1.f : l);
+                            __threadfence();
+                            __syncwarp();
+                            if (lane == 0)
+                                atomicAdd(wr_cnt, 32);
+                        } else {
+                            // every other split holds a ticket, so it is past its key
+                            // tiles and only has stores left: wait (bounded) for them
+                            if (row == 0) {
+                                // one poller; it also resets both counters for the next call
+                                const int need = (p.S - 1) * kBM;
+                                const uint64_t t0 = global_ns();
+                                int ok_all = 1;
+                                while (*reinterpret_cast<volatile int *>(wr_cnt) < need) {
+                                    if (global_ns() - t0 > kWaitTimeoutNs) {
+                                        record_status(status, D3D_ERR_DEVICE_TIMEOUT);
+                                        ok_all = 0;
+                                        break;
+                                    }
+                                }
+                                if (ok_all) {
+                                    *wr_cnt = 0;
+                                    *tk_cnt = 0;
+                                }
+                                ready_flag[t] = ok_all;
+                                mbar_arrive(bar(B_RDY + t));
+                            }
+                            const bool rel = wait_bar(bar(B_RDY + t), 0, abort_flag, status);
+                            const int ready = __all_sync(0xffffffffu, rel) ? ready_flag[t] : 0;
+                            if (ready) {
+                                __threadfence();
+                                float2 mlv[kMaxSplits];
+                                float M = m_ref;
+                                for (int s2 = 0; s2 < p.S; ++s2) {
+                                    mlv[s2] = (s2 == sp) ? make_float2(m_ref, l)
+                                                         : __ldcg(mls + (tile_id * p.S + s2) * kBM + row);
+                                    M = fmaxf(M, mlv[s2].x);
+                                }
+                                float Lsum = 0.f;
+                                bool bad = row_bad;
+                                for (int s2 = 0; s2 < p.S; ++s2) {
+                                    bad = bad || mlv[s2].y < 0.f;
+                                    const float w = (M == -INFINITY) ? 0.f : ex2(mlv[s2].x - M);
+                                    Lsum += w * fmaxf(mlv[s2].y, 0.f);
+                                    // own O is unnormalised; the others were divided by their sum
+                                    mlv[s2].x = (s2 == sp) ? w : w * fmaxf(mlv[s2].y, 0.f);
+                                }
+                                const float sc = (bad || !(Lsum > 0.f)) ? 0.f : 1.f / Lsum;
+                                const uint4 *pa = nullptr, *pb = nullptr;  // the other splits (fast path)
+                                float wa = 0.f, wb = 0.f;
+                                if (p.S <= 3) {
+                                    // the other splits: (1, 2), (0, 2) or (0, 1); only one when S = 2
+                                    const int oa = (sp == 0) ? 1 : 0, ob = (p.S < 3) ? -1 : ((sp == 2) ? 1 : 2);
+                                    pa = opart + ((tile_id * p.S + oa) * (D / 8)) * kBM + row;
+                                    wa = mlv[oa].x;
+                                    if (ob >= 0) {
+                                        pb = opart + ((tile_id * p.S + ob) * (D / 8)) * kBM + row;
+                                        wb = mlv[ob].x;
+                                    }
+                                }
+                                if (p.S <= 3 && sc != 0.f) {
+                                    // software-pipelined: chunk c+1's loads are in flight while
+                                    // chunk c is accumulated
+                                    uint4 cur[2][4], nxt[2][4];
+#pragma unroll
+                                    for (int q4 = 0; q4 < 4; ++q4) {
+                                        cur[0][q4] = __ldcg(pa + (size_t)q4 * kBM);
+                                        cur[1][q4] = pb ? __ldcg(pb + (size_t)q4 * kBM) : make_uint4(0, 0, 0, 0);
+                                    }
+#pragma unroll
+                                    for (int c = 0; c < D / 32; ++c) {
+                                        if (c + 1 < D / 32) {
+#pragma unroll
+                                            for (int q4 = 0; q4 < 4; ++q4) {
+                                                nxt[0][q4] = __ldcg(pa + (size_t)((c + 1) * 4 + q4) * kBM);
+                                                nxt[1][q4] = pb ? __ldcg(pb + (size_t)((c + 1) * 4 + q4) * kBM)
+                                                                : make_uint4(0, 0, 0, 0);
+                                            }
+                                        }
+                                        float acc[32];
+                                        if (have_o) {
+                                            tmem_ld32(tO + c * 32, acc);
+                                        } else {
+#pragma unroll
+                                            for (int e = 0; e < 32; ++e)
+                                                acc[e] = 0.f;
+                                        }
+                                        const float wown = mlv[sp].x;
+#pragma unroll
+                                        for (int q4 = 0; q4 < 4; ++q4) {
+                                            const uint32_t da[4] = {cur[0][q4].x, cur[0][q4].y, cur[0][q4].z, cur[0][q4].w};
+                                            const uint32_t db[4] = {cur[1][q4].x, cur[1][q4].y, cur[1][q4].z, cur[1][q4].w};
+#pragma unroll
+                                            for (int e = 0; e < 4; ++e) {
+                                                float &lo = acc[q4 * 8 + 2 * e], &hi = acc[q4 * 8 + 2 * e + 1];
+                                                lo = lo * wown + wa * __uint_as_float(da[e] << 16) +
+                                                     wb * __uint_as_float(db[e] << 16);
+                                                hi = hi * wown + wa * __uint_as_float(da[e] & 0xffff0000u) +
+                                                     wb * __uint_as_float(db[e] & 0xffff0000u);
+                                            }
+                                        }
+                                        if (row_valid) {
+                                            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                                            for (int q4 = 0; q4 < 4; ++q4) {
+                                                uint4 w;
+                                                w.x = pack_bf16x2(acc[q4 * 8 + 0] * sc, acc[q4 * 8 + 1] * sc);
+                                                w.y = pack_bf16x2(acc[q4 * 8 + 2] * sc, acc[q4 * 8 + 3] * sc);
+                                                w.z = pack_bf16x2(acc[q4 * 8 + 4] * sc, acc[q4 * 8 + 5] * sc);
+                                                w.w = pack_bf16x2(acc[q4 * 8 + 6] * sc, acc[q4 * 8 + 7] * sc);
+                                                dst[q4] = w;
+                                            }
+                                        }
+#pragma unroll
+                                        for (int q4 = 0; q4 < 4; ++q4) {
+                                            cur[0][q4] = nxt[0][q4];
+                                            cur[1][q4] = nxt[1][q4];
+                                        }
+                                    }
+                                } else
+                                {
+                                for (int c = 0; c < D / 32; ++c) {
+                                    float acc[32];
+                                    if (have_o) {
+                                        tmem_ld32(tO + c * 32, acc);
+                                    } else {
+#pragma unroll
+                                        for (int e = 0; e < 32; ++e)
+                                            acc[e] = 0.f;
+                                    }
+                                    const float wown = mlv[sp].x;
+#pragma unroll
+                                    for (int e = 0; e < 32; ++e)
+                                        acc[e] *= wown;
+                                    for (int s0 = 0; sc != 0.f && s0 < p.S; s0 += kMergeUnroll) {
+                                        uint4 v[kMergeUnroll][4];
+#pragma unroll
+                                        for (int u = 0; u < kMergeUnroll; ++u) {
+                                            const int s2 = s0 + u;
+                                            if (s2 < p.S && s2 != sp) {
+                                                const size_t q2 = tile_id * p.S + s2;
+#pragma unroll
+                                                for (int q4 = 0; q4 < 4; ++q4)
+                                                    v[u][q4] = __ldcg(opart + (q2 * (D / 8) + c * 4 + q4) * kBM + row);
+                                            }
+                                        }
+#pragma unroll
+                                        for (int u = 0; u < kMergeUnroll; ++u) {
+                                            const int s2 = s0 + u;
+                                            if (s2 < p.S && s2 != sp) {
+                                                const float wgt = mlv[s2].x;
+#pragma unroll
+                                                for (int q4 = 0; q4 < 4; ++q4) {
+                                                    const uint32_t wd[4] = {v[u][q4].x, v[u][q4].y, v[u][q4].z, v[u][q4].w};
+#pragma unroll
+                                                    for (int e = 0; e < 4; ++e) {
+                                                        acc[q4 * 8 + 2 * e] += wgt * __uint_as_float(wd[e] << 16);
+                                                        acc[q4 * 8 + 2 * e + 1] += wgt * __uint_as_float(wd[e] & 0xffff0000u);
+                                                    }
+                                                }
+                                            }
+                                        }
+                                    }
+                                    if (row_valid) {
+                                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                                        for (int q4 = 0; q4 < 4; ++q4) {
+                                            uint4 w;
+                                            w.x = pack_bf16x2(acc[q4 * 8 + 0] * sc, acc[q4 * 8 + 1] * sc);
+                                            w.y = pack_bf16x2(acc[q4 * 8 + 2] * sc, acc[q4 * 8 + 3] * sc);
+                                            w.z = pack_bf16x2(acc[q4 * 8 + 4] * sc, acc[q4 * 8 + 5] * sc);
+                                            w.w = pack_bf16x2(acc[q4 * 8 + 6] * sc, acc[q4 * 8 + 7] * sc);
+                                            dst[q4] = w;
+                                        }
+                                    }
+                                }
                                 }
                             }
                         }
@@ -651,7 +857,7 @@ AttnPlan make_plan(int R, int Hq, int Hkv, int d, int max_q, int max_prefix, int
     const int tiles = (max_prefix + kBN - 1) / kBN + pl.PK;
     double best = 1e300;
     pl.S = 1;
-    for (int S = 1; S <= 32 && S <= tiles; ++S) {
+    for (int S = 1; S <= kMaxSplits && S <= tiles; ++S) {
         const double waves = (double)((base * S + nsm - 1) / nsm);
         const double cost = waves * (double)((tiles + S - 1) / S + 3 + (S > 1 ? 1 : 0));
         if (cost < best - 1e-9) {
@@ -664,9 +870,10 @@ AttnPlan make_plan(int R, int Hq, int Hkv, int d, int max_q, int max_prefix, int
     size_t o = sizeof(WsHeader);
     pl.off_cnt = o;
     if (pl.S > 1) {
-        o = align_up(o + sizeof(int) * rows, kWsAlign);
+        const size_t tiles_total = (size_t)base * kTiles;
+        o = align_up(o + sizeof(int) * 2 * tiles_total, kWsAlign);  // split tickets, rows written
         pl.off_opart = o;
-        o = align_up(o + sizeof(float) * rows * pl.S * d, kWsAlign);
+        o = align_up(o + sizeof(uint16_t) * rows * pl.S * d, kWsAlign);  // bf16 partials
         pl.off_ml = o;
         o = align_up(o + sizeof(float2) * rows * pl.S, kWsAlign);
     } else {

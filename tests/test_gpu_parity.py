@@ -143,6 +143,25 @@ def test_attn_bad_device_descriptor_sets_status(d3d):
     assert (got[rows] == 0).all()
 
 
+def test_attn_many_splits_and_bad_descriptor(d3d):
+    # one query-tile pair over a long prefix: the planner cuts the key list
+    # into many splits, so the merge path runs with a large split count
+    a = W.attn_inputs(R=1, L=4096, Hq=4, Hkv=1, d=128, B=8, C=3, F=2, layout="async", seed=8)
+    got, ws = run_attn(d3d, a)
+    assert_attn_close(got, oracle.packed_attn(a), "many splits")
+    assert d3d.d3d_workspace_status(ws) == 0
+    # the same with a descriptor only the device can see is wrong: the rows of
+    # that segment come out as zeros, every other row is still correct
+    bad = dict(a, segs=a["segs"].copy())
+    bad["segs"][2, 4] = 99
+    got2, ws2 = run_attn(d3d, bad)
+    assert d3d.d3d_workspace_status(ws2, clear=True) == d3d.D3D_ERR_DEVICE_INPUT
+    rows = np.zeros(got2.shape[0], bool)
+    rows[int(bad["segs"][2, 0]):int(bad["segs"][2, 0] + bad["segs"][2, 1])] = True
+    assert (got2[rows] == 0).all()
+    assert_attn_close(got2[~rows], oracle.packed_attn(a)[~rows], "other rows")
+
+
 # ------------------------------------------------------------------ verification
 @pytest.mark.parametrize("seed", range(3))
 def test_verify_tiny_config_batched(d3d, seed):
