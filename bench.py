@@ -44,6 +44,33 @@ METRIC = "packed-draft query tokens/s + verified positions/s; % HBM/tensor roofl
 UNIT = "packed-draft query tokens/s"
 # our kernel launches per call of each entry point
 LAUNCHES = {"attn": 1, "verify": 1, "match": 1}
+CSRC = os.path.join(ROOT, "diffusion_drafted_speculative_gb300", "csrc")
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of this bench's workload, keyed by a hash of the sources the
+# kernel is built from: reported only while those sources are unchanged.
+NCU_TRAFFIC = {
+    ("async8b", "attn"): {"sources": ("attn.cu", "attn_common.cuh", "sm100_ptx.cuh", "d3d_common.cuh"),
+                          "sha": "f93ee60f6ec46a75", "bytes": 13359616},
+    ("async8b", "verify"): {"sources": ("verify.cu", "d3d_common.cuh"),
+                            "sha": "3465a241d1d59d30", "bytes": 9506304},
+}
+
+
+def sources_sha(names) -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(CSRC, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(wl_name: str, part: str):
+    t = NCU_TRAFFIC.get((wl_name, part))
+    if t is None or sources_sha(t["sources"]) != t["sha"]:
+        return None
+    return t["bytes"]
 
 
 def parse_args():
@@ -323,19 +350,21 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if not args.no_e2e:
         e2e = run_e2e(torch, d3d, sets, n_sets, attn, verify, match, dev, stream, args, R, B, dist)
 
+    # attention and verification are each timed alone in a short loop: the
+    # burst peaks apply (sustained is for a kernel inside a seconds-long step)
     peaks = load_peaks()
     achieved_tf = wl["flops"] / (t_attn * 1e-3) / 1e12
     att_ai = wl["flops"] / wl["attn_bytes"]
-    ridge = peaks["bf16_sus"] * 1e12 / (peaks["hbm"] * 1e9)
+    ridge = peaks["bf16"] * 1e12 / (peaks["hbm"] * 1e9)
     if att_ai >= ridge:
-        roof = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
-                "frac": round(achieved_tf / peaks["bf16_sus"], 4)}
+        roof = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": round(achieved_tf / peaks["bf16"], 4)}
     else:
         gbs = wl["attn_bytes"] / (t_attn * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": round(gbs / peaks["hbm"], 4)}
-    roof.update({"kernel": "packed draft attention", "traffic": None, "peak_source": peaks["source"] +
-                 (" (sustained bf16)" if roof["bound"] == "tensor" else " (copy bandwidth)"),
+    roof.update({"kernel": "packed draft attention", "traffic": ncu_traffic(args.workload, "attn"),
+                 "peak_source": peaks["source"] + (" (burst bf16)" if roof["bound"] == "tensor" else " (copy bandwidth)"),
                  "algorithmic": {"flops": wl["flops"], "bytes": wl["attn_bytes"]}})
     verify_gbs = wl["verify_bytes"] / (t_verify * 1e-3) / 1e9
 
@@ -358,7 +387,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                   "verify_positions_per_s": round(wl["positions"] / (t_verify * 1e-3), 1),
                   "verify_hbm": {"achieved": round(verify_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
                                  "frac": round(verify_gbs / peaks["hbm"], 4),
-                                 "bytes": wl["verify_bytes"]}},
+                                 "bytes": wl["verify_bytes"], "traffic": ncu_traffic(args.workload, "verify")}},
         "roofline": roof,
         "gpu_launches": args.steps * (LAUNCHES["attn"] + LAUNCHES["verify"] + LAUNCHES["match"]),
         "clocks": clk, "wall_s_timed_region": round(wall, 4),
