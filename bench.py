@@ -8,7 +8,10 @@ vocabulary, and the branch cache-hit match of the verified tokens.  The
 default workload is D3D's asynchronous packed pass at 8B-class shapes:
 1 request, prefix 2048, 32 query / 8 KV heads, head_dim 128, B=16, C=12,
 F=2 (N_async = 384 packed query tokens), verification of 16 positions over a
-151936-entry vocabulary, and a match against 24 branch heads.
+151936-entry vocabulary, and a match against 24 branch heads.  Within a
+round the packed drafting pass and the verification are independent (the
+drafter prepares the successor blocks while the current block is verified),
+so they run concurrently on two streams; the match runs after both.
 
 Timing: inputs resident in HBM; steps rotate over input sets whose total
 size exceeds twice the L2 cache, so no step finds its inputs in L2; each
@@ -258,12 +261,21 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     def match(s):
         d3d.d3d_branch_match(s["out_tokens"], s["num_tokens"], s["heads"], s["head_len"], s["branch"])
 
+    stream = torch.cuda.Stream(device=dev)
+    side = torch.cuda.Stream(device=dev)
+
     def step(s):
+        # the asynchronous round: the packed drafting pass and the verification
+        # of the current block are independent and run concurrently (the
+        # verification on a second stream); the branch match needs both
+        cur = torch.cuda.current_stream()
+        side.wait_stream(cur)
         attn(s)
-        verify(s)
+        with torch.cuda.stream(side):
+            verify(s)
+        cur.wait_stream(side)
         match(s)
 
-    stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
 
     def graphs(fn, n):
@@ -348,7 +360,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(torch, d3d, sets, n_sets, attn, verify, match, dev, stream, args, R, B, dist)
+        e2e = run_e2e(torch, d3d, sets, n_sets, step, dev, stream, args, R, B, dist)
 
     # attention and verification are each timed alone in a short loop: the
     # burst peaks apply (sustained is for a kernel inside a seconds-long step)
@@ -402,7 +414,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         dist.destroy_process_group()
 
 
-def run_e2e(torch, d3d, sets, n_sets, attn, verify, match, dev, stream, args, R, B, dist):
+def run_e2e(torch, d3d, sets, n_sets, step, dev, stream, args, R, B, dist):
     """Same metric through the public API, inputs from pinned host memory and
     results read back every step; copies inside the timed region."""
     in_keys = ["q", "kp", "vp", "kn", "vn", "segs", "cu_prefix", "cu_q", "cu_seg", "target", "draft", "y",
@@ -417,9 +429,7 @@ def run_e2e(torch, d3d, sets, n_sets, attn, verify, match, dev, stream, args, R,
         s, h = sets[i % n_sets], host[i % n_sets]
         for k in in_keys:
             s[k].copy_(h[k], non_blocking=True)
-        attn(s)
-        verify(s)
-        match(s)
+        step(s)
         for k in out_keys:
             h[k].copy_(s[k], non_blocking=True)
 

@@ -10,19 +10,22 @@
 // three phases.  A phase waits only for the previous phase of the same
 // request, through per-request counters (bounded spins); phase A waits for
 // nothing, so every wait ends even when CTAs loop over several items:
-//   A. one work item per (logit row, 8192-entry chunk): 16-byte vector loads,
-//      the chunk's softmax statistics (max and sum of exp2, log2 domain) and,
-//      for rows that are evaluated at a draft token, that token's logit when
-//      it lies in the chunk.  One record per item.
-//   B+C. one item per (request, chunk): the CTA combines its request's records
-//      in shared memory (every such CTA does, which costs L2 reads instead of
-//      a barrier), forms p_j, q_j, alpha_j, runs the first-rejection scan,
-//      picks the row pair the sample needs, and computes its chunk's residual
-//      max(0, P - Q) (or P_B) mass, keeping the per-entry masses in registers.
-//      The chunk-0 CTA writes the per-request outputs.
-//   D. every item reads its request's chunk sums; the one chunk holding the
-//      crossing C(v) > u*S scans its registers in vocabulary order and writes
-//      the sampled token.  The request's last phase-D item resets its counters.
+//   A. one work item per (request, position j, 8192-entry chunk): the chunk of
+//      target row j and, for j < B-1, of draft row j, with 16-byte vector
+//      loads; the chunk's softmax statistics of both rows (max and sum of
+//      exp2, log2 domain) and the two logits at the draft token y_j when it
+//      lies in the chunk.  One record per item.
+//   B. every CTA that goes on combines its request's records in shared memory
+//      (each does it redundantly, which costs L2 reads instead of a hand-off),
+//      forms p_j, q_j, alpha_j, runs the first-rejection scan and picks the
+//      row pair the sample uses.  One CTA writes the per-request outputs.
+//   C. the items of that row pair compute their chunk's residual max(0, P - Q)
+//      (or P_B) mass.  When every item has its own CTA, phase A's
+//      exponentials are still in registers and a per-thread scale turns them
+//      into probabilities: no reload and no exponential.  Otherwise the
+//      chunk is reloaded.
+//   D. the chunk holding the crossing C(v) > u*S scans its masses in
+//      vocabulary order and writes the sampled token.
 #include <math.h>
 
 #include <mutex>
@@ -35,36 +38,49 @@ namespace {
 constexpr int kVThreads = 256;
 constexpr int kVWarps = kVThreads / 32;
 constexpr int kVChunk = 8192;
-constexpr int kVPer = kVChunk / kVThreads;  // 32 logits per thread
+constexpr int kVPer = kVChunk / kVThreads;  // 32 logits per thread and row
+constexpr int kVGroup = kVThreads * 8;      // positions covered by one 8-wide slot group
 constexpr int kMaxB = 256;
 constexpr int kMaxChunks = 1024;  // vocabulary up to 8M entries
-constexpr int kVBlocksPerSm = 2;  // register budget for four resident CTAs per SM
+constexpr int kVBlocksPerSm = 2;
 constexpr uint64_t kBarrierTimeoutNs = 250ull * 1000ull * 1000ull;
-constexpr int kStagedRecords = 2048;  // chunk records the finalising CTA stages in shared memory (32 KB)
+constexpr int kStagedRecords = 1024;  // item records staged in shared memory (32 KB)
 constexpr unsigned kFull = 0xffffffffu;
+
+// Statistics of one (request, position, chunk) item.  Target row: mP, zP and
+// the scaled logit at the draft token xP; draft row likewise.  An absent row
+// (the bonus row has no draft row) has m = -inf, z = 0.
+struct Rec {
+    float mP, zP, mQ, zQ;
+    float xP, xQ, pad0, pad1;
+};
 
 // What the sample of one request uses.
 struct Sel {
     int32_t a;     // accepted drafts
     int32_t mode;  // 0: residual at target/draft row a; 1: bonus from target row B-1
-    int32_t row;   // target row the sample uses (and draft row when mode == 0)
+    int32_t row;   // position whose rows the sample uses
     float mP, rZP, mQ, rZQ;  // log2-domain row max and 1 / normaliser of that target / draft row
 };
 
 struct VerifyLayout {
-    size_t bar, part1, part2, total;  // bar: per-request counters
+    size_t bar, rec, part2, total;
     int nch;
 };
+
+// Per-request counters: phase-A items done, waiters that passed the phase-A
+// wait, phase-C items done, phase-D items done.
+constexpr int kBarInts = 4;
 
 __host__ __device__ inline VerifyLayout verify_layout(int R, int B, int V)
 {
     VerifyLayout L;
     L.nch = (V + kVChunk - 1) / kVChunk;
     size_t o = sizeof(WsHeader);
-    L.bar = o;  // per request: phase-A items done, phase-C items done, phase-D items done
-    o = align_up(o + 3 * sizeof(int) * (size_t)R, kWsAlign);
-    L.part1 = o;  // per (row, chunk): max, sum, scaled logit of the row's draft token if in the chunk
-    o = align_up(o + sizeof(float4) * (size_t)R * (size_t)(2 * B - 1) * (size_t)L.nch, kWsAlign);
+    L.bar = o;
+    o = align_up(o + kBarInts * sizeof(int) * (size_t)R, kWsAlign);
+    L.rec = o;  // per (request, position, chunk)
+    o = align_up(o + sizeof(Rec) * (size_t)R * (size_t)B * (size_t)L.nch, kWsAlign);
     L.part2 = o;  // per (request, chunk): residual mass, P mass
     o = align_up(o + sizeof(float2) * (size_t)R * (size_t)L.nch, kWsAlign);
     L.total = o;
@@ -98,55 +114,30 @@ template <> struct Logit<uint16_t> {
 
 template <typename T> __device__ inline bool aligned16(const T *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// Scaled logits x*c of one chunk [v0, v1) in a strided (coalesced) ownership:
-// slot 8k+e of thread t holds position v0 + 2048k + 8t + e, whichever load
-// path a row takes, so two rows loaded this way line up slot by slot.
-// Positions past v1 read as -inf.
+// Vocabulary position of slot i (0..kVPer) of this thread in chunk v0: slot
+// 8g+e holds v0 + g*kVGroup + 8*tid + e, so each 8-slot group is one
+// coalesced 16-byte load per thread.
+__device__ __forceinline__ int slot_pos(int v0, int i) { return v0 + (i >> 3) * kVGroup + (int)threadIdx.x * 8 + (i & 7); }
+
+// Scaled logits x*c of one chunk [v0, v1) in slot order; positions past v1
+// read as -inf.
 template <typename T>
-__device__ inline void load_chunk_strided(const T *row, int v0, int v1, float c, float (&x)[kVPer])
+__device__ inline void load_chunk(const T *row, int v0, int v1, float c, float (&x)[kVPer])
 {
-    const int tid = threadIdx.x;
     if (v1 - v0 == kVChunk && aligned16(row + v0)) {
 #pragma unroll
-        for (int k = 0; k < kVPer / 8; ++k) {
+        for (int g = 0; g < kVPer / 8; ++g) {
             float t[8];
-            Logit<T>::load8(row + v0 + k * kVThreads * 8 + tid * 8, t);
+            Logit<T>::load8(row + slot_pos(v0, 8 * g), t);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                x[k * 8 + e] = t[e] * c;
+                x[8 * g + e] = t[e] * c;
         }
     } else {
 #pragma unroll
-        for (int k = 0; k < kVPer / 8; ++k) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int v = v0 + k * kVThreads * 8 + tid * 8 + e;
-                x[k * 8 + e] = v < v1 ? Logit<T>::at(row, v) * c : -INFINITY;
-            }
-        }
-    }
-}
-
-// Scaled logits of thread-contiguous positions v0 + tid*kVPer + k (vocabulary
-// order inside a thread), -inf past v1.  Used for the ordered scan.
-template <typename T>
-__device__ inline void load_chunk_contig(const T *row, int v0, int v1, float c, float (&x)[kVPer])
-{
-    const int base = v0 + threadIdx.x * kVPer;
-    if (base + kVPer <= v1 && aligned16(row + base)) {
-#pragma unroll
-        for (int k = 0; k < kVPer / 8; ++k) {
-            float t[8];
-            Logit<T>::load8(row + base + k * 8, t);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                x[k * 8 + e] = t[e] * c;
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < kVPer; ++k) {
-            const int v = base + k;
-            x[k] = v < v1 ? Logit<T>::at(row, v) * c : -INFINITY;
+        for (int i = 0; i < kVPer; ++i) {
+            const int v = slot_pos(v0, i);
+            x[i] = v < v1 ? Logit<T>::at(row, v) * c : -INFINITY;
         }
     }
 }
@@ -173,25 +164,47 @@ __device__ inline void ms_merge(float &m, float &z, float m2, float z2)
     m = M;
 }
 
-// Block-wide (max, sum) merge; the result is valid in thread 0.
-__device__ inline void block_ms(float &m, float &z, float *red)
+// Per-thread max and exponentials of one row chunk, in place: x[i] becomes
+// exp2(x[i] - m) with m this thread's max (0 everywhere when m = -inf).
+__device__ inline void thread_exp(float (&x)[kVPer], float &m, float &z)
+{
+    m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kVPer; ++i)
+        m = fmaxf(m, x[i]);
+    z = 0.f;
+    const float mm = (m == -INFINITY) ? 0.f : m;
+#pragma unroll
+    for (int i = 0; i < kVPer; ++i) {
+        x[i] = fast_exp2(x[i] - mm);
+        z += x[i];
+    }
+}
+
+// Block-wide merge of two (max, sum) pairs; the result is valid in thread 0.
+__device__ inline void block_ms2(float &m1, float &z1, float &m2, float &z2, float *red)
 {
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
-        const float m2 = __shfl_xor_sync(kFull, m, o), z2 = __shfl_xor_sync(kFull, z, o);
-        ms_merge(m, z, m2, z2);
+        const float a = __shfl_xor_sync(kFull, m1, o), b = __shfl_xor_sync(kFull, z1, o);
+        const float c = __shfl_xor_sync(kFull, m2, o), d = __shfl_xor_sync(kFull, z2, o);
+        ms_merge(m1, z1, a, b);
+        ms_merge(m2, z2, c, d);
     }
     const int w = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) {
-        red[w] = m;
-        red[kVWarps + w] = z;
+        red[4 * w + 0] = m1;
+        red[4 * w + 1] = z1;
+        red[4 * w + 2] = m2;
+        red[4 * w + 3] = z2;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        m = red[0];
-        z = red[kVWarps];
-        for (int i = 1; i < kVWarps; ++i)
-            ms_merge(m, z, red[i], red[kVWarps + i]);
+        m1 = red[0], z1 = red[1], m2 = red[2], z2 = red[3];
+        for (int i = 1; i < kVWarps; ++i) {
+            ms_merge(m1, z1, red[4 * i + 0], red[4 * i + 1]);
+            ms_merge(m2, z2, red[4 * i + 2], red[4 * i + 3]);
+        }
     }
 }
 
@@ -205,53 +218,78 @@ __device__ inline void block_sum2(float &a, float &b, float *red)
     }
     const int w = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) {
-        red[w] = a;
-        red[kVWarps + w] = b;
+        red[2 * w] = a;
+        red[2 * w + 1] = b;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         a = red[0];
-        b = red[kVWarps];
+        b = red[1];
         for (int i = 1; i < kVWarps; ++i) {
-            a += red[i];
-            b += red[kVWarps + i];
+            a += red[2 * i];
+            b += red[2 * i + 1];
         }
     }
 }
 
-// Block-wide exclusive scan of one value per thread, in thread order.
-__device__ inline float block_exclusive_scan(float v, float *red)
+// Block-wide exclusive scan of the four per-thread group sums g[0..3] in
+// vocabulary order (group-major, then thread): returns each group's prefix.
+__device__ inline float4 block_group_scan(float4 g, float *red)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    float inc = v;
+    float4 inc = g;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const float t = __shfl_up_sync(kFull, inc, o);
+        const float a = __shfl_up_sync(kFull, inc.x, o), b = __shfl_up_sync(kFull, inc.y, o);
+        const float c = __shfl_up_sync(kFull, inc.z, o), d = __shfl_up_sync(kFull, inc.w, o);
         if (lane >= o)
-            inc += t;
+            inc.x += a, inc.y += b, inc.z += c, inc.w += d;
     }
-    if (lane == 31)
-        red[w] = inc;
+    if (lane == 31) {
+        red[4 * w + 0] = inc.x;
+        red[4 * w + 1] = inc.y;
+        red[4 * w + 2] = inc.z;
+        red[4 * w + 3] = inc.w;
+    }
     __syncthreads();
-    float base = 0.f;
-    for (int i = 0; i < w; ++i)
-        base += red[i];
-    return base + inc - v;
+    float tot[4] = {0.f, 0.f, 0.f, 0.f}, before[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < kVWarps; ++i) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float t = red[4 * i + q];
+            tot[q] += t;
+            if (i < w)
+                before[q] += t;
+        }
+    }
+    float4 r;
+    r.x = before[0] + inc.x - g.x;
+    r.y = tot[0] + before[1] + inc.y - g.y;
+    r.z = tot[0] + tot[1] + before[2] + inc.z - g.z;
+    r.w = tot[0] + tot[1] + tot[2] + before[3] + inc.w - g.w;
+    return r;
 }
 
-// Wait (thread 0 spins, bounded) until *cnt reaches `target`, then make the
-// producers' writes visible to the whole CTA.  Returns false if the wait ran
-// out (the status word is then set).
+__device__ __forceinline__ int load_acquire(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait (thread 0 spins with acquire loads, bounded) until *cnt reaches
+// `target`; the barrier after it passes the producers' writes on to the whole
+// CTA.  Returns false if the wait ran out (the status word is then set).
 __device__ bool wait_count(const int *cnt, int target, int32_t *status)
 {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
-        if (*reinterpret_cast<const volatile int *>(cnt) < target) {
+        if (load_acquire(cnt) < target) {
             uint64_t t0;
             asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-            while (*reinterpret_cast<const volatile int *>(cnt) < target) {
+            while (load_acquire(cnt) < target) {
                 uint64_t t1;
                 asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
                 if (t1 - t0 > kBarrierTimeoutNs) {
@@ -261,96 +299,116 @@ __device__ bool wait_count(const int *cnt, int target, int32_t *status)
                 }
             }
         }
-        __threadfence();
         s_ok = ok;
     }
     __syncthreads();
     return s_ok != 0;
 }
 
-// Signal one finished item: its writes first, then the count (no return value).
+// Signal one finished item (no return value).  The release orders the
+// calling thread's earlier writes (the item's record) before the count.
 __device__ inline void signal_count(int *cnt)
 {
-    __threadfence();
     asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(cnt) : "memory");
 }
 
-// Phase B for request r, done by one CTA: combine the records, alpha_j, the
-// first rejection, the sample's row pair.  With write_outputs the CTA also
-// writes accept_len, num_tokens, alpha/p/q and the accepted tokens.
-template <typename T>
-__device__ void select_request(int r, int B, int V, int nch, const float4 *__restrict__ part1,
-                               const int32_t *__restrict__ y, const float *__restrict__ u_acc, bool write_outputs,
+// Draft tokens, acceptance uniforms and the sample uniform of request r into
+// shared memory (issued before the selection's wait, which they do not
+// depend on).
+__device__ inline void load_request_inputs(int r, int B, const int32_t *__restrict__ y,
+                                           const float *__restrict__ u_acc, const float *__restrict__ u_s,
+                                           int32_t *s_y, float *s_u, float *s_us)
+{
+    for (int jj = threadIdx.x; jj < B - 1; jj += kVThreads) {
+        s_y[jj] = __ldg(y + (size_t)r * (B - 1) + jj);
+        s_u[jj] = __ldg(u_acc + (size_t)r * (B - 1) + jj);
+    }
+    if (threadIdx.x == 0)
+        *s_us = __ldg(u_s + r);
+}
+
+// Phase B for request r: combine the records, alpha_j, the first rejection,
+// the sample's row pair.  s_y / s_u hold the request's draft tokens and
+// uniforms.  With write_outputs the CTA also writes accept_len, num_tokens,
+// alpha/p/q and the accepted tokens.
+__device__ void select_request(int r, int B, int V, int nch, const Rec *__restrict__ rec,
+                               const int32_t *s_y, const float *s_u, bool write_outputs,
                                int32_t *__restrict__ accept_len, int32_t *__restrict__ out_tokens,
                                int32_t *__restrict__ num_tokens, float *__restrict__ alpha_out,
                                float *__restrict__ p_out, float *__restrict__ q_out, int32_t *status, Sel &sel,
-                               float4 *s_part)
+                               Rec *s_rec)
 {
-    __shared__ float s_m[2 * kMaxB], s_z[2 * kMaxB], s_u[kMaxB];
-    __shared__ int s_y[kMaxB], s_a;
-    const int rows = 2 * B - 1;
+    __shared__ float s_mp[kMaxB], s_zp[kMaxB], s_mq[kMaxB], s_zq[kMaxB];
+    __shared__ int s_a;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float4 *pr = part1 + (size_t)r * rows * nch;
-    const int nrec = rows * nch;
+    const Rec *pr = rec + (size_t)r * B * nch;
+    const int nrec = B * nch;
     const bool staged = nrec <= kStagedRecords;
-    if (staged)
-        for (int i = threadIdx.x; i < nrec; i += kVThreads)
-            s_part[i] = __ldcg(&pr[i]);
-    for (int jj = threadIdx.x; jj < B - 1; jj += kVThreads) {
-        s_y[jj] = y[(size_t)r * (B - 1) + jj];
-        s_u[jj] = u_acc[(size_t)r * (B - 1) + jj];
+    if (staged) {
+        const float4 *src = reinterpret_cast<const float4 *>(pr);
+        float4 *dst = reinterpret_cast<float4 *>(s_rec);
+        for (int i = threadIdx.x; i < 2 * nrec; i += kVThreads)
+            dst[i] = __ldcg(src + i);
     }
     if (threadIdx.x == 0)
         s_a = B - 1;
     __syncthreads();
-    for (int jj = warp; jj < rows; jj += kVWarps) {
-        // row max over the chunk records, then the rescaled sums
-        float mm = -INFINITY, zz = 0.f;
+    // records written by other CTAs of this launch: L2 reads when not staged
+    auto rec_at = [&](int i) -> Rec {
+        if (staged)
+            return s_rec[i];
+        const float4 a = __ldcg(reinterpret_cast<const float4 *>(pr + i));
+        const float4 b = __ldcg(reinterpret_cast<const float4 *>(pr + i) + 1);
+        return Rec{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    };
+    // one warp per position: the row statistics over the chunk records, then
+    // p_j, q_j, alpha_j and the acceptance test
+    for (int jj = warp; jj < B; jj += kVWarps) {
+        float mp = -INFINITY, zp = 0.f, mq = -INFINITY, zq = 0.f;
         for (int cc = lane; cc < nch; cc += 32) {
-            const float4 t = staged ? s_part[jj * nch + cc] : __ldcg(&pr[(size_t)jj * nch + cc]);
-            ms_merge(mm, zz, t.x, t.y);
+            const Rec t = rec_at(jj * nch + cc);
+            ms_merge(mp, zp, t.mP, t.zP);
+            ms_merge(mq, zq, t.mQ, t.zQ);
         }
-        float M = mm;
+        float MP = mp, MQ = mq;
 #pragma unroll
-        for (int o = 16; o; o >>= 1)
-            M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-        float zs = (mm == -INFINITY) ? 0.f : zz * fast_exp2(mm - M);
+        for (int o = 16; o; o >>= 1) {
+            MP = fmaxf(MP, __shfl_xor_sync(kFull, MP, o));
+            MQ = fmaxf(MQ, __shfl_xor_sync(kFull, MQ, o));
+        }
+        float sp = (mp == -INFINITY) ? 0.f : zp * fast_exp2(mp - MP);
+        float sq = (mq == -INFINITY) ? 0.f : zq * fast_exp2(mq - MQ);
 #pragma unroll
-        for (int o = 16; o; o >>= 1)
-            zs += __shfl_xor_sync(kFull, zs, o);
+        for (int o = 16; o; o >>= 1) {
+            sp += __shfl_xor_sync(kFull, sp, o);
+            sq += __shfl_xor_sync(kFull, sq, o);
+        }
         if (lane == 0) {
-            s_m[jj] = M;
-            s_z[jj] = zs;
-        }
-    }
-    __syncthreads();
-    // alpha_j and the acceptance test of every position in parallel; the first
-    // rejection is the smallest rejected position
-    for (int jj = threadIdx.x; jj < B - 1; jj += kVThreads) {
-        const int yv = s_y[jj];
-        float p = 0.f, q = 0.f, al = 0.f;
-        if (yv < 0 || yv >= V) {
-            if (write_outputs)
-                record_status(status, D3D_ERR_DEVICE_INPUT);
-        } else {
-            const int ch = yv / kVChunk;
-            const size_t it = (size_t)jj * nch + ch, id = (size_t)(B + jj) * nch + ch;
-            const float xt = staged ? s_part[it].z : __ldcg(&pr[it]).z;
-            const float xd = staged ? s_part[id].z : __ldcg(&pr[id]).z;
-            p = fast_exp2(xt - s_m[jj]) / s_z[jj];
-            q = fast_exp2(xd - s_m[B + jj]) / s_z[B + jj];
-            al = (p >= q) ? 1.f : p / q;
-        }
-        if (!(s_u[jj] < al))
-            atomicMin(&s_a, jj);
-        if (write_outputs) {
-            const size_t o = (size_t)r * (B - 1) + jj;
-            if (alpha_out)
-                alpha_out[o] = al;
-            if (p_out)
-                p_out[o] = p;
-            if (q_out)
-                q_out[o] = q;
+            s_mp[jj] = MP, s_zp[jj] = sp, s_mq[jj] = MQ, s_zq[jj] = sq;
+            if (jj < B - 1) {
+                const int yv = s_y[jj];
+                float p = 0.f, q = 0.f, al = 0.f;
+                if (yv < 0 || yv >= V) {
+                    if (write_outputs)
+                        record_status(status, D3D_ERR_DEVICE_INPUT);
+                } else {
+                    const Rec t = rec_at(jj * nch + yv / kVChunk);
+                    p = fast_exp2(t.xP - MP) / sp;
+                    q = fast_exp2(t.xQ - MQ) / sq;
+                    al = (p >= q) ? 1.f : p / q;
+                }
+                if (!(s_u[jj] < al))
+                    atomicMin(&s_a, jj);
+                if (write_outputs) {
+                    const size_t o = (size_t)r * (B - 1) + jj;
+                    if (alpha_out)
+                        alpha_out[o] = al;
+                    if (p_out)
+                        p_out[o] = p;
+                    if (q_out)
+                        q_out[o] = q;
+                }
+            }
         }
     }
     __syncthreads();
@@ -358,10 +416,10 @@ __device__ void select_request(int r, int B, int V, int nch, const float4 *__res
     sel.a = a;
     sel.mode = (a < B - 1) ? 0 : 1;
     sel.row = (a < B - 1) ? a : B - 1;
-    sel.mP = s_m[sel.row];
-    sel.rZP = __frcp_rn(s_z[sel.row]);
-    sel.mQ = (a < B - 1) ? s_m[B + a] : 0.f;
-    sel.rZQ = (a < B - 1) ? __frcp_rn(s_z[B + a]) : 1.f;
+    sel.mP = s_mp[sel.row];
+    sel.rZP = __frcp_rn(s_zp[sel.row]);
+    sel.mQ = (a < B - 1) ? s_mq[a] : 0.f;
+    sel.rZQ = (a < B - 1) ? __frcp_rn(s_zq[a]) : 1.f;
     if (write_outputs) {
         if (threadIdx.x == 0) {
             accept_len[r] = a;
@@ -374,37 +432,104 @@ __device__ void select_request(int r, int B, int V, int nch, const float4 *__res
     __syncthreads();  // the shared arrays are reused by the next call
 }
 
-// Mass of position v of the sampled distribution: the residual
-// max(0, P - Q) (kind 0) or P itself (kind 1); xp/xq are scaled logits.
-__device__ inline float sample_mass(int kind, float xp, float xq, const Sel &sel)
-{
-    const float P = fast_exp2(xp - sel.mP) * sel.rZP;
-    if (kind != 0)
-        return P;
-    const float Q = fast_exp2(xq - sel.mQ) * sel.rZQ;
-    return fmaxf(P - Q, 0.f);
-}
-
-// Per-entry masses of one chunk [c0, c1) in thread-contiguous order
-// (positions c0 + tid*kVPer + k), and their sums.
+// Per-slot masses w of the sampled distribution in chunk [c0, c1): the
+// residual max(0, P - Q) (kind 0) or P (kind 1), reloading the chunk; and
+// the sums of w and of P.
 template <typename T>
 __device__ inline void chunk_masses(const T *prow, const T *qrow, int kind, int c0, int c1, float c,
                                     const Sel &sel, float (&w)[kVPer], float &s_kind, float &s_p)
 {
-    float xp[kVPer], xq[kVPer];
-    load_chunk_contig<T>(prow, c0, c1, c, xp);
+    float xp[kVPer];
+    load_chunk<T>(prow, c0, c1, c, xp);
     if (kind == 0)
-        load_chunk_contig<T>(qrow, c0, c1, c, xq);
+        load_chunk<T>(qrow, c0, c1, c, w);
     s_kind = 0.f;
     s_p = 0.f;
 #pragma unroll
-    for (int k = 0; k < kVPer; ++k) {
-        const bool in = c0 + (int)threadIdx.x * kVPer + k < c1;
-        const float P = in ? fast_exp2(xp[k] - sel.mP) * sel.rZP : 0.f;
-        w[k] = in ? (kind == 0 ? fmaxf(P - fast_exp2(xq[k] - sel.mQ) * sel.rZQ, 0.f) : P) : 0.f;
-        s_kind += w[k];
+    for (int i = 0; i < kVPer; ++i) {
+        const float P = fast_exp2(xp[i] - sel.mP) * sel.rZP;
+        w[i] = (kind == 0) ? fmaxf(P - fast_exp2(w[i] - sel.mQ) * sel.rZQ, 0.f) : P;
+        s_kind += w[i];
         s_p += P;
     }
+}
+
+// The same from exponentials kept since phase A: eP/eQ = exp2(x - m_t) with
+// m_t this thread's max of the row chunk; w may alias eQ.
+__device__ inline void kept_masses(int kind, const float (&eP)[kVPer], float (&eQ)[kVPer], float mtP, float mtQ,
+                                   const Sel &sel, float &s_kind, float &s_p)
+{
+    const float sP = (mtP == -INFINITY) ? 0.f : fast_exp2(mtP - sel.mP) * sel.rZP;
+    const float sQ = (kind != 0 || mtQ == -INFINITY) ? 0.f : fast_exp2(mtQ - sel.mQ) * sel.rZQ;
+    s_kind = 0.f;
+    s_p = 0.f;
+#pragma unroll
+    for (int i = 0; i < kVPer; ++i) {
+        const float P = eP[i] * sP;
+        eQ[i] = fmaxf(P - eQ[i] * sQ, 0.f);
+        s_kind += eQ[i];
+        s_p += P;
+    }
+}
+
+// Phase D of request r in the chunk [c0, c1) that holds the crossing: the
+// ordered scan of the slot masses w (slot order is group-major vocabulary
+// order); writes the sampled token.
+__device__ void scan_owner(const float (&w)[kVPer], int c0, float prefix, float target, bool takelast,
+                           int32_t *out_tok, float *red)
+{
+    __shared__ int s_cand, s_lastpos;
+    if (threadIdx.x == 0) {
+        s_cand = 0x7fffffff;
+        s_lastpos = -1;
+    }
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+    int lastpos = -1;
+#pragma unroll
+    for (int i = 0; i < kVPer; ++i) {
+        const int q = i >> 3;
+        if (q == 0) g.x += w[i];
+        else if (q == 1) g.y += w[i];
+        else if (q == 2) g.z += w[i];
+        else g.w += w[i];
+        if (w[i] > 0.f)
+            lastpos = max(lastpos, slot_pos(c0, i));
+    }
+    const float4 ex = block_group_scan(g, red);  // has a __syncthreads (s_cand initialised)
+    const float gs[4] = {g.x, g.y, g.z, g.w}, bs[4] = {ex.x, ex.y, ex.z, ex.w};
+    if (!takelast) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (prefix + bs[q] + gs[q] > target) {
+                atomicMin(&s_cand, q * kVThreads + (int)threadIdx.x);
+                break;
+            }
+    }
+    atomicMax(&s_lastpos, lastpos);
+    __syncthreads();
+    const int cand = s_cand;
+    if (!takelast && cand != 0x7fffffff && (cand % kVThreads) == (int)threadIdx.x) {
+        const int q = cand / kVThreads;
+        int tok = -1, last = -1;
+        float cum = prefix + bs[q];
+#pragma unroll
+        for (int i = 0; i < kVPer; ++i) {
+            if ((i >> 3) == q && tok < 0) {
+                cum += w[i];
+                if (w[i] > 0.f)
+                    last = slot_pos(c0, i);
+                if (cum > target)
+                    tok = slot_pos(c0, i);
+            }
+        }
+        // rounding between the two summation orders: the group's last position with mass
+        if (tok < 0)
+            tok = last >= 0 ? last : s_lastpos;
+        *out_tok = tok;
+    }
+    if ((takelast || cand == 0x7fffffff) && threadIdx.x == 0)
+        *out_tok = s_lastpos;
+    __syncthreads();
 }
 
 template <typename T>
@@ -415,136 +540,92 @@ __global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
                   int32_t *__restrict__ num_tokens, float *__restrict__ alpha_out, float *__restrict__ p_out,
                   float *__restrict__ q_out, unsigned char *__restrict__ ws)
 {
-    extern __shared__ float4 s_part[];  // request records when staged; chunk sums in phase D
-    __shared__ float red[2 * kVWarps];
-    __shared__ float s_xy;
+    extern __shared__ float4 s_dyn[];  // request records when staged; chunk sums in phase D
+    __shared__ float red[4 * kVWarps];
+    __shared__ float s_xy[2];
+    __shared__ int32_t s_y[kMaxB];
+    __shared__ float s_u[kMaxB], s_us;
     const VerifyLayout L = verify_layout(R, B, V);
-    const int rows = 2 * B - 1, nch = L.nch;
-    const long long nA = (long long)R * rows * nch;
+    const int nch = L.nch;
+    const long long nA = (long long)R * B * nch;
     const int nC = R * nch;
-    float4 *part1 = reinterpret_cast<float4 *>(ws + L.part1);
+    Rec *rec = reinterpret_cast<Rec *>(ws + L.rec);
     float2 *part2 = reinterpret_cast<float2 *>(ws + L.part2);
     int *bar = reinterpret_cast<int *>(ws + L.bar);
     int32_t *status = reinterpret_cast<int32_t *>(ws);
+    Rec *s_rec = reinterpret_cast<Rec *>(s_dyn);
+    // one phase-A item per CTA: its exponentials stay in registers for phase C
+    const bool keep = nA <= (long long)gridDim.x;
 
-    // ---- phase A: per (row, chunk) statistics; the next item's loads are in
-    // flight while the current item is reduced
-    auto item_row = [&](long long item, int &v0, int &v1, int &yy) -> const T * {
+    // ---- phase A: per (request, position, chunk) statistics of the row pair
+    float eP[kVPer], eQ[kVPer];
+    float mtP = -INFINITY, mtQ = -INFINITY;
+    for (long long item = blockIdx.x; item < nA; item += gridDim.x) {
         const int chunk = (int)(item % nch);
-        const int rowg = (int)(item / nch);
-        const int r = rowg / rows, j = rowg % rows;
-        v0 = chunk * kVChunk;
-        v1 = min(V, v0 + kVChunk);
-        // the draft token this row is evaluated at (none for the bonus row P_B)
-        const int yj = (j < B - 1) ? j : (j >= B ? j - B : -1);
-        yy = (yj >= 0) ? __ldg(y + (size_t)r * (B - 1) + yj) : -1;
-        return (j < B) ? target + ((size_t)r * B + j) * V : draft + ((size_t)r * (B - 1) + (j - B)) * V;
-    };
-    float xc[kVPer];
-    int v0c = 0, v1c = 0, yyc = -1;
-    long long item = blockIdx.x;
-    if (item < nA)
-        load_chunk_strided<T>(item_row(item, v0c, v1c, yyc), v0c, v1c, c, xc);
-    while (item < nA) {
-        const long long next = item + gridDim.x;
-        float xn[kVPer];
-        int v0n = 0, v1n = 0, yyn = -1;
-        if (next < nA)
-            load_chunk_strided<T>(item_row(next, v0n, v1n, yyn), v0n, v1n, c, xn);
-        const int r = (int)(item / nch) / rows;
-        if (yyc >= v0c && yyc < v1c) {  // the thread holding x[yy] keeps it for the record
-            const int rel = yyc - v0c;
-            if ((int)threadIdx.x == (rel % (kVThreads * 8)) / 8) {
-                const int slot = (rel / (kVThreads * 8)) * 8 + rel % 8;
-                float xv = 0.f;
+        const int rj = (int)(item / nch);
+        const int r = rj / B, j = rj % B;
+        const int v0 = chunk * kVChunk, v1 = min(V, v0 + kVChunk);
+        const int yv = (j < B - 1) ? __ldg(y + (size_t)r * (B - 1) + j) : -1;
+        load_chunk<T>(target + ((size_t)r * B + j) * V, v0, v1, c, eP);
+        if (j < B - 1) {
+            load_chunk<T>(draft + ((size_t)r * (B - 1) + j) * V, v0, v1, c, eQ);
+        } else {
 #pragma unroll
-                for (int k = 0; k < kVPer; ++k)
-                    xv = (k == slot) ? xc[k] : xv;
-                s_xy = xv;
+            for (int i = 0; i < kVPer; ++i)
+                eQ[i] = -INFINITY;
+        }
+        if (yv >= v0 && yv < v1) {  // the thread holding position y keeps both logits for the record
+            const int rel = yv - v0;
+            if ((int)threadIdx.x == (rel % kVGroup) / 8) {
+                const int slot = (rel / kVGroup) * 8 + rel % 8;
+                float xp = 0.f, xq = 0.f;
+#pragma unroll
+                for (int i = 0; i < kVPer; ++i) {
+                    xp = (i == slot) ? eP[i] : xp;
+                    xq = (i == slot) ? eQ[i] : xq;
+                }
+                s_xy[0] = xp;
+                s_xy[1] = xq;
             }
         }
-        float m = -INFINITY, z = 0.f;
-#pragma unroll
-        for (int k = 0; k < kVPer; ++k)
-            m = fmaxf(m, xc[k]);
-        if (m != -INFINITY) {
-#pragma unroll
-            for (int k = 0; k < kVPer; ++k)
-                z += fast_exp2(xc[k] - m);
-        }
-        block_ms(m, z, red);  // has a __syncthreads: s_xy is visible to thread 0 after it
+        float zP, zQ;
+        thread_exp(eP, mtP, zP);
+        thread_exp(eQ, mtQ, zQ);
+        float m1 = mtP, z1 = zP, m2 = mtQ, z2 = zQ;
+        block_ms2(m1, z1, m2, z2, red);  // has a __syncthreads: s_xy is visible to thread 0 after it
         if (threadIdx.x == 0) {
-            part1[item] = make_float4(m, z, (yyc >= v0c && yyc < v1c) ? s_xy : 0.f, 0.f);
-            signal_count(bar + 3 * r);
+            const bool has = yv >= v0 && yv < v1;
+            float4 *dst = reinterpret_cast<float4 *>(rec + item);
+            dst[0] = make_float4(m1, z1, m2, z2);
+            dst[1] = make_float4(has ? s_xy[0] : 0.f, has ? s_xy[1] : 0.f, 0.f, 0.f);
+            signal_count(bar + kBarInts * r);
         }
         __syncthreads();  // red and s_xy are reused by the next item
-        if (next < nA) {
-#pragma unroll
-            for (int k = 0; k < kVPer; ++k)
-                xc[k] = xn[k];
-        }
-        v0c = v0n, v1c = v1n, yyc = yyn;
-        item = next;
     }
 
-    // ---- phase B+C: the request's selection, then this chunk's masses
-    const bool keep = nC <= (int)gridDim.x;  // at most one item per CTA: masses stay in registers
-    float w[kVPer];
-    Sel sel;
-#pragma unroll
-    for (int k = 0; k < kVPer; ++k)
-        w[k] = 0.f;
-    sel.a = 0, sel.mode = 1, sel.row = 0, sel.mP = 0.f, sel.rZP = 0.f, sel.mQ = 0.f, sel.rZQ = 0.f;
-    for (int item = blockIdx.x; item < nC; item += gridDim.x) {
-        const int r = item / nch, chunk = item % nch;
-        if (!wait_count(bar + 3 * r, rows * nch, status))
-            return;
-        select_request<T>(r, B, V, nch, part1, y, u_acc, chunk == 0, accept_len, out_tokens, num_tokens, alpha_out,
-                          p_out, q_out, status, sel, s_part);
-        const T *prow = target + ((size_t)r * B + sel.row) * V;
-        const T *qrow = draft + ((size_t)r * (B - 1) + (sel.mode == 0 ? sel.row : 0)) * V;
-        const int c0 = chunk * kVChunk, c1 = min(V, c0 + kVChunk);
-        float s_kind, s_p;
-        chunk_masses<T>(prow, qrow, sel.mode == 0 ? 0 : 1, c0, c1, c, sel, w, s_kind, s_p);
-        block_sum2(s_kind, s_p, red);
-        if (threadIdx.x == 0) {
-            part2[item] = make_float2(s_kind, s_p);
-            signal_count(bar + 3 * r + 1);
-        }
-        __syncthreads();
-    }
-
-    // ---- phase D: the chunk holding the crossing scans its masses
-    __shared__ int s_kind_used, s_owner, s_takelast, s_cand, s_lastpos;
+    __shared__ int s_kind_used, s_owner, s_takelast;
     __shared__ float s_prefix, s_target;
-    for (int item = blockIdx.x; item < nC; item += gridDim.x) {
-        const int r = item / nch, chunk = item % nch;
-        if (!wait_count(bar + 3 * r + 1, nch, status))
-            return;
-        if (!keep)  // every phase-C item of r waited for r's phase A, so the records are complete
-            select_request<T>(r, B, V, nch, part1, y, u_acc, false, accept_len, out_tokens, num_tokens, alpha_out,
-                              p_out, q_out, status, sel, s_part);
-        float2 *s_sums = reinterpret_cast<float2 *>(s_part);  // the records are no longer needed
+    // Phase D decision for request r from its chunk sums (thread 0 computes,
+    // everyone reads the shared results after the call).
+    auto decide = [&](int r, const Sel &sel) {
+        float2 *s_sums = reinterpret_cast<float2 *>(s_dyn);  // the records are no longer needed
         for (int cc = threadIdx.x; cc < nch; cc += kVThreads)
             s_sums[cc] = __ldcg(part2 + (size_t)r * nch + cc);
         __syncthreads();
         if (threadIdx.x == 0) {
-            const float2 *pr = s_sums;
             float S_res = 0.f, S_p = 0.f;
             for (int cc = 0; cc < nch; ++cc) {
-                const float2 t = pr[cc];
-                S_res += t.x;
-                S_p += t.y;
+                S_res += s_sums[cc].x;
+                S_p += s_sums[cc].y;
             }
             // residual unless it has no mass left in fp32 (then P at that row)
             const int kind = (sel.mode == 0 && S_res > 0.f) ? 0 : 1;
             const float S = kind == 0 ? S_res : S_p;
-            const float tgt = u_s[r] * S;
+            const float tgt = s_us * S;
             float run = 0.f;
             int owner = -1;
             for (int cc = 0; cc < nch; ++cc) {
-                const float2 t = pr[cc];
-                const float sc = kind == 0 ? t.x : t.y;
+                const float sc = kind == 0 ? s_sums[cc].x : s_sums[cc].y;
                 if (run + sc > tgt) {
                     owner = cc;
                     break;
@@ -554,73 +635,125 @@ __global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
             int takelast = 0;
             if (owner < 0) {  // rounding left u*S at or past the end: last chunk with mass
                 takelast = 1;
-                for (int cc = nch - 1; cc >= 0 && owner < 0; --cc) {
-                    const float2 t = pr[cc];
-                    if ((kind == 0 ? t.x : t.y) > 0.f)
+                for (int cc = nch - 1; cc >= 0 && owner < 0; --cc)
+                    if ((kind == 0 ? s_sums[cc].x : s_sums[cc].y) > 0.f)
                         owner = cc;
-                }
             }
             s_kind_used = kind;
             s_owner = owner;
             s_takelast = takelast;
             s_prefix = run;
             s_target = tgt;
-            s_cand = kVThreads;
-            s_lastpos = -1;
         }
         __syncthreads();
-        const int owner = s_owner;
-        if (owner == chunk) {
-            const int kind = s_kind_used;
-            const int c0 = chunk * kVChunk, c1 = min(V, c0 + kVChunk);
-            if (!keep || kind != (sel.mode == 0 ? 0 : 1)) {  // masses not in registers (or the fallback kind)
-                const T *prow = target + ((size_t)r * B + sel.row) * V;
-                const T *qrow = draft + ((size_t)r * (B - 1) + (sel.mode == 0 ? sel.row : 0)) * V;
+    };
+    // The request's last phase-D item resets the phase-C/D counters (every
+    // phase-C signal has arrived and every phase-D waiter has passed).
+    auto finish_d = [&](int r) {
+        if (threadIdx.x == 0 && atomicAdd(bar + kBarInts * r + 3, 1) == nch - 1) {
+            bar[kBarInts * r + 2] = 0;
+            bar[kBarInts * r + 3] = 0;
+        }
+    };
+    // Count a waiter past the phase-A wait; the last one resets the phase-A
+    // counters (no waiter reads them any more).
+    auto passed_a = [&](int r, int waiters) {
+        if (threadIdx.x == 0 && atomicAdd(bar + kBarInts * r + 1, 1) == waiters - 1) {
+            bar[kBarInts * r + 0] = 0;
+            bar[kBarInts * r + 1] = 0;
+        }
+    };
+
+    Sel sel;
+    if (keep) {
+        // ---- B, C, D on the CTA's own item
+        if ((long long)blockIdx.x >= nA)
+            return;
+        const int item = blockIdx.x;
+        const int chunk = item % nch, rj = item / nch;
+        const int r = rj / B, j = rj % B;
+        load_request_inputs(r, B, y, u_acc, u_s, s_y, s_u, &s_us);
+        if (!wait_count(bar + kBarInts * r, B * nch, status))
+            return;
+        select_request(r, B, V, nch, rec, s_y, s_u, j == 0 && chunk == 0, accept_len, out_tokens, num_tokens,
+                       alpha_out, p_out, q_out, status, sel, s_rec);
+        if (j != sel.row) {
+            passed_a(r, B * nch);  // counted once the CTA's work is done: off the critical path
+            return;
+        }
+        const int c0 = chunk * kVChunk;
+        float s_kind, s_p;
+        kept_masses(sel.mode == 0 ? 0 : 1, eP, eQ, mtP, mtQ, sel, s_kind, s_p);  // eQ now holds the masses
+        block_sum2(s_kind, s_p, red);
+        if (threadIdx.x == 0) {
+            part2[(size_t)r * nch + chunk] = make_float2(s_kind, s_p);
+            signal_count(bar + kBarInts * r + 2);
+        }
+        if (!wait_count(bar + kBarInts * r + 2, nch, status))
+            return;
+        decide(r, sel);
+        if (s_owner == chunk) {
+            if (s_kind_used != sel.mode) {  // residual without mass in fp32: P at that row
                 float a1, a2;
-                chunk_masses<T>(prow, qrow, kind, c0, c1, c, sel, w, a1, a2);
+                kept_masses(1, eP, eQ, mtP, mtQ, sel, a1, a2);
             }
-            float tot = 0.f;
-            int lastpos = -1;
-#pragma unroll
-            for (int k = 0; k < kVPer; ++k) {
-                tot += w[k];
-                if (w[k] > 0.f)
-                    lastpos = c0 + threadIdx.x * kVPer + k;
-            }
-            const float excl = block_exclusive_scan(tot, red);
-            const float base = s_prefix + excl;
-            if (!s_takelast && base + tot > s_target)
-                atomicMin(&s_cand, (int)threadIdx.x);
-            atomicMax(&s_lastpos, lastpos);
-            __syncthreads();
-            if (!s_takelast && (int)threadIdx.x == s_cand) {
-                int tok = -1;
-                float cum = base;
-                for (int k = 0; k < kVPer; ++k) {
-                    cum += w[k];
-                    if (cum > s_target) {
-                        tok = c0 + threadIdx.x * kVPer + k;
-                        break;
-                    }
-                }
-                if (tok < 0)
-                    tok = lastpos;  // rounding between the two summation orders
-                out_tokens[(size_t)r * B + sel.a] = tok;
-            }
-            if ((s_takelast || s_cand == kVThreads) && threadIdx.x == 0)
-                out_tokens[(size_t)r * B + sel.a] = s_lastpos;
-        } else if (owner < 0 && chunk == 0 && threadIdx.x == 0) {
+            scan_owner(eQ, c0, s_prefix, s_target, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
+        } else if (s_owner < 0 && chunk == 0 && threadIdx.x == 0) {
             // no mass anywhere: cannot happen for a finite softmax row
             record_status(status, D3D_ERR_DEVICE_INPUT);
             out_tokens[(size_t)r * B + sel.a] = 0;
         }
-        // the request's last phase-D item resets its counters for the next call
-        // (every phase-A and phase-C signal of the request has arrived by now)
-        if (threadIdx.x == 0 && atomicAdd(bar + 3 * r + 2, 1) == nch - 1) {
-            bar[3 * r] = 0;
-            bar[3 * r + 1] = 0;
-            bar[3 * r + 2] = 0;
+        finish_d(r);
+        passed_a(r, B * nch);
+        return;
+    }
+
+    // ---- phase C (several items per CTA): the request's selection, then this
+    // chunk's masses from a reload
+    float w[kVPer];
+    for (int item = blockIdx.x; item < nC; item += gridDim.x) {
+        const int r = item / nch, chunk = item % nch;
+        load_request_inputs(r, B, y, u_acc, u_s, s_y, s_u, &s_us);
+        if (!wait_count(bar + kBarInts * r, B * nch, status))
+            return;
+        passed_a(r, nch);
+        select_request(r, B, V, nch, rec, s_y, s_u, chunk == 0, accept_len, out_tokens, num_tokens, alpha_out,
+                       p_out, q_out, status, sel, s_rec);
+        const T *prow = target + ((size_t)r * B + sel.row) * V;
+        const T *qrow = draft + ((size_t)r * (B - 1) + (sel.mode == 0 ? sel.row : 0)) * V;
+        const int c0 = chunk * kVChunk, c1 = min(V, c0 + kVChunk);
+        float s_kind, s_p;
+        chunk_masses<T>(prow, qrow, sel.mode == 0 ? 0 : 1, c0, c1, c, sel, w, s_kind, s_p);
+        block_sum2(s_kind, s_p, red);
+        if (threadIdx.x == 0) {
+            part2[item] = make_float2(s_kind, s_p);
+            signal_count(bar + kBarInts * r + 2);
         }
+        __syncthreads();
+    }
+
+    // ---- phase D: the chunk holding the crossing reloads its masses and scans
+    for (int item = blockIdx.x; item < nC; item += gridDim.x) {
+        const int r = item / nch, chunk = item % nch;
+        load_request_inputs(r, B, y, u_acc, u_s, s_y, s_u, &s_us);
+        if (!wait_count(bar + kBarInts * r + 2, nch, status))
+            return;
+        // every phase-C item of r waited for r's phase A, so the records are complete
+        select_request(r, B, V, nch, rec, s_y, s_u, false, accept_len, out_tokens, num_tokens, alpha_out, p_out,
+                       q_out, status, sel, s_rec);
+        decide(r, sel);
+        if (s_owner == chunk) {
+            const int c0 = chunk * kVChunk, c1 = min(V, c0 + kVChunk);
+            const T *prow = target + ((size_t)r * B + sel.row) * V;
+            const T *qrow = draft + ((size_t)r * (B - 1) + (sel.mode == 0 ? sel.row : 0)) * V;
+            float a1, a2;
+            chunk_masses<T>(prow, qrow, s_kind_used, c0, c1, c, sel, w, a1, a2);
+            scan_owner(w, c0, s_prefix, s_target, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
+        } else if (s_owner < 0 && chunk == 0 && threadIdx.x == 0) {
+            record_status(status, D3D_ERR_DEVICE_INPUT);
+            out_tokens[(size_t)r * B + sel.a] = 0;
+        }
+        finish_d(r);
         __syncthreads();
     }
 }
@@ -631,17 +764,17 @@ int launch_verify(const void *target, const void *draft, const int32_t *y, const
                   float *alpha, float *p, float *q, unsigned char *ws, cudaStream_t stream)
 {
     const VerifyLayout L = verify_layout(R, B, V);
-    const long long nA = (long long)R * (2 * B - 1) * L.nch;
+    const long long nA = (long long)R * B * L.nch;
     if (nA > 0x7fffffffLL)
         return D3D_ERR_UNSUPPORTED;
-    const int nrec = (2 * B - 1) * L.nch;
+    const int nrec = B * L.nch;
     // dynamic shared memory: the request's records when they are staged, and
     // at least the request's chunk sums (phase D)
-    size_t dyn = nrec <= kStagedRecords ? sizeof(float4) * (size_t)nrec : 0;
+    size_t dyn = nrec <= kStagedRecords ? sizeof(Rec) * (size_t)nrec : 0;
     if (dyn < sizeof(float2) * (size_t)L.nch)
         dyn = sizeof(float2) * (size_t)L.nch;
-    // every CTA must be resident (grid-wide barriers): at most the occupancy
-    // limit, and no more than there are phase-A items
+    // every CTA must be resident (CTAs wait on one another): at most the
+    // occupancy limit, and no more than there are phase-A items
     int dev = 0, nsm = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -712,8 +845,8 @@ int d3d_spec_verify(const void *target_logits, const void *draft_logits, int log
 // ---------------------------------------------------------------------------
 // Verification without a caller workspace.
 //
-// For callers that cannot allocate device memory, the scratch the two
-// verification kernels need lives in one fixed, file-scope device array.
+// For callers that cannot allocate device memory, the scratch the
+// verification kernel needs lives in one fixed, file-scope device array.
 // Every device that loads this library holds it until the process exits.
 // ---------------------------------------------------------------------------
 namespace d3d {
@@ -787,8 +920,8 @@ extern "C" int d3d_spec_verify_noalloc(const void *target_logits, const void *dr
     if (rc != D3D_OK)
         return rc;
     // the array keeps the previous call's contents: zero the status word and
-    // the two per-request tickets, which must start at zero
-    if (cudaMemsetAsync(scratch, 0, L.part1, stream) != cudaSuccess)
+    // the per-request counters, which must start at zero
+    if (cudaMemsetAsync(scratch, 0, L.rec, stream) != cudaSuccess)
         return D3D_ERR_CUDA;
     const float c = (float)(1.4426950408889634 / (double)temperature);
     unsigned char *w = static_cast<unsigned char *>(scratch);

@@ -218,6 +218,23 @@ def test_verify_high_acceptance_and_bonus_path(d3d):
     compare_verify(got, ref)
 
 
+@pytest.mark.parametrize("R,B,V,dt,sigma", [(1, 16, 151936, W.DT_BF16, 0.5), (2, 5, 12345, W.DT_F32, 0.5),
+                                             (2, 16, 70001, W.DT_BF16, 1.0), (3, 2, 8193, W.DT_F32, 0.5),
+                                             (1, 64, 16384, W.DT_BF16, 0.25), (5, 7, 9, W.DT_F32, 0.5),
+                                             (2, 8, 3000, W.DT_F32, 0.0)])
+def test_verify_one_item_per_cta(d3d, R, B, V, dt, sigma):
+    # few requests: every (request, position, chunk) item has a CTA of its own,
+    # and the sample reuses phase A's exponentials from registers
+    for seed in range(3):
+        v = W.verify_inputs(R=R, B=B, V=V, logits=dt, sigma=sigma, seed=seed + 31 * B)
+        got, ws = run_verify(d3d, v)
+        ref = oracle.spec_verify(v)
+        if sigma == 0.0:
+            assert (ref["accept_len"] == B - 1).all()
+        compare_verify(got, ref, min_kept=0.0 if V > 50000 else 0.5)
+        assert d3d.d3d_workspace_status(ws) == 0
+
+
 def test_verify_workspace_reuse_and_many_requests(d3d):
     v = W.verify_inputs(R=4096, B=4, V=64, logits=W.DT_F32, seed=10)
     got1, ws = run_verify(d3d, v)
