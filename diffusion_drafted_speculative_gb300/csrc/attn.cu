@@ -3,38 +3,47 @@
 // [D3D] "Core method", "Method steps" steps 2 and 4; [DScout] "Background:
 // block-diffusion drafter".  See attn_common.cuh for the visibility rule.
 //
-// Work unit (one CTA): request r, KV head hk, a pair of 128-row query tiles
-// and one KV split.  A query tile's 128 rows are (packed token, query head of
-// hk's group) pairs, token-major, so one K/V tile serves all G query heads
-// of the group and both query tiles of the pair.  A unit's key list is every
-// 128-key tile of the request's prefix followed by the packed-key tiles its
-// rows can see.  Splits cut the prefix tiles; the last split also takes the
-// packed tiles, so every other split knows its tiles without the visibility
-// mask and starts loading at once.
+// Work unit (one CTA): request r, KV head hk, one 128-row query tile and one
+// key split.  A query tile's 128 rows are (packed token, query head of hk's
+// group) pairs, token-major, so one K/V tile serves all G query heads of the
+// group.  A unit's key list is every 128-key tile of the request's prefix
+// followed by the packed-key tiles its rows can see.  Splits cut the prefix
+// tiles; the last split also takes the packed tiles, so every other split
+// knows its tiles without the visibility mask and starts loading at once.
 //
 // Roles (320 threads):
-//   warps 0-3 / 4-7  softmax warpgroup of query tile 0 / 1: thread i owns
-//              TMEM lane i = row i.  Reads S (one tcgen05.ld of 128 columns),
-//              masks it, keeps the running max (rescaling O in TMEM only when
-//              the max grows by more than 2^8) and the row sum, and writes P
-//              as bf16 pairs back over the first 64 columns of S.
-//   warp 8     TMA producer: Q tiles once, then K and V tiles into 3- and
-//              2-deep rings (3-D tensor maps, 128-byte swizzle).
-//   warp 9     MMA issuer (one thread), owner of TMEM.  Per key tile j it
-//              issues PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): O_t += P_t V_j
-//              with P read from TMEM, S_t = Q_t K^T into TMEM.  While one
-//              warpgroup computes its softmax the tensor core works for the
-//              other.  S_t(j+1) overwrites P_t(j) only after PV_t(j), which
-//              the tensor core executes first (MMAs of one thread run in
-//              issue order), and the commit that signals S_t(j+1) also
-//              guarantees PV_t(j) is complete, so O_t is stable for the
+//   warps 0-3 / 4-7  softmax warpgroup w = 0 / 1: the two warpgroups take the
+//              key tiles of the list alternately (w takes tiles w, w+2, ...),
+//              each with its own S/P and O in TMEM.  Thread i of either
+//              warpgroup owns TMEM lane i = query row i.  Reads S (one
+//              tcgen05.ld of 128 columns), masks it, keeps the running max
+//              (rescaling O in TMEM only when the max grows by more than 2^8)
+//              and the row sum, and writes P as bf16 pairs back over the
+//              first 64 columns of S.
+//   warp 8     TMA producer: the Q tile once, then K and V tiles into two
+//              3-deep rings (3-D tensor maps, 128-byte swizzle).
+//   warp 9     MMA issuer (one thread), owner of TMEM.  Per pair of key tiles
+//              (2i, 2i+1) it issues PV_0(2i), S_0(2i+2), PV_1(2i+1), S_1(2i+3):
+//              O_w += P_w V, with P read from TMEM, and S_w = Q K^T into TMEM.
+//              While one warpgroup computes its softmax the tensor core works
+//              for the other.  S_w(k+2) overwrites P_w(k) only after PV_w(k),
+//              which the tensor core executes first (MMAs of one thread run in
+//              issue order), and the commit that signals S_w(k+2) also
+//              guarantees PV_w(k) is complete, so O_w is stable for the
 //              softmax's rescale.
-// TMEM: tile t uses columns [256t, 256t+128) for S/P and [256t+128, +D) for O.
-// With several splits, a warpgroup takes a per-tile ticket when it has
-// finished its key tiles; all but the last write their partial (O divided by
-// its row sum, bf16, row-fastest layout, plus max and sum) to the workspace,
-// and the last waits for those stores and merges them with its own O, which
-// is still in TMEM.
+// TMEM: warpgroup w uses columns [256w, 256w+128) for S/P and [256w+128, +D)
+// for O_w.  Both warpgroups' O rows sit in the same TMEM lanes, so at the end
+// each thread combines O_0 and O_1 of its row for half of the head dimension
+// (the two (max, sum) pairs are exchanged through shared memory).
+//
+// With S > 1 splits the S CTAs of a query tile run as one thread-block
+// cluster.  Each CTA writes its combined partial (O divided by its row sum,
+// bf16) into its own shared memory, in the K ring that nothing reads any
+// more, with the rows' (max, sum).  After a cluster barrier every CTA
+// combines its share of the head-dim columns (8-column unit u goes to split
+// u mod S) from all splits through distributed shared memory, in a fixed
+// order; a second cluster barrier keeps every CTA resident until its shared
+// memory has been read.  No global scratch is used.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -52,10 +61,11 @@ using namespace sm100;
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per KV tile
-constexpr int kTiles = 2;  // query tiles per CTA
+constexpr int kWG = 2;    // softmax warpgroups: each takes half of every key tile's columns
+constexpr int kHalf = kBN / kWG;  // 64 keys per softmax thread and tile
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
-constexpr int kSoftmaxThreads = kTiles * 128;
+constexpr int kSoftmaxThreads = kWG * 128;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
@@ -64,8 +74,7 @@ constexpr int kMaxPackedTiles = 64;  // packed keys per request <= 8192
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
 constexpr uint32_t kBlockBytes = kBN * 128;  // one 128-row x 128-byte swizzled block (16 KB)
 constexpr int kStagedSegs = 80;  // segment rows staged in shared memory (more: searched in global memory)
-constexpr int kMergeUnroll = 3;  // other splits' partial loads issued together in the merge
-constexpr int kMaxSplits = 32;
+constexpr int kMaxSplits = 8;  // key splits of a query tile: one thread-block cluster
 
 // barrier indices
 enum {
@@ -74,12 +83,11 @@ enum {
     B_KE = B_KF + kKStages,     // kKStages
     B_VF = B_KE + kKStages,     // kVStages
     B_VE = B_VF + kVStages,     // kVStages
-    B_SF = B_VE + kVStages,     // kTiles: S_t(j) in TMEM
-    B_PR = B_SF + kTiles,       // kTiles: P_t(j) in TMEM (128 arrivals)
-    B_OD = B_PR + kTiles,       // kTiles: O_t final
-    B_TK = B_OD + kTiles,       // kTiles: split ticket of the tile taken
-    B_RDY = B_TK + kTiles,      // kTiles: merger saw every other split's partial
-    B_MASK = B_RDY + kTiles,    // visibility mask complete (256 arrivals)
+    B_SF = B_VE + kVStages,     // 2: S(k) in TMEM buffer k % 2
+    B_PR = B_SF + 2,            // 2: P(k) in TMEM buffer k % 2 (one arrival per softmax warp)
+    B_MX = B_PR + 2,            // 2: both halves' row maxima of tile k published (one per softmax warp)
+    B_OW = B_MX + 2,            // one completion per PV (O written)
+    B_MASK = B_OW + 1,          // visibility mask complete (256 arrivals)
     B_DONE = B_MASK + 1,        // every MMA of the CTA complete
     B_COUNT = B_DONE + 1
 };
@@ -89,11 +97,13 @@ template <int D> struct Layout {
     static constexpr uint32_t kKBytes = kBN * D * 2;
     static constexpr uint32_t kVBytes = kBN * D * 2;
     static constexpr uint32_t q = 0;
-    static constexpr uint32_t k = q + kTiles * kQBytes;
+    static constexpr uint32_t k = q + kQBytes;
     static constexpr uint32_t v = k + kKStages * kKBytes;
     static constexpr uint32_t bars = v + kVStages * kVBytes;
     static constexpr uint32_t misc = bars + B_COUNT * 8;
-    static constexpr uint32_t segs = misc + 64;  // staged segment table of the request
+    static constexpr uint32_t mx = misc + 64;  // [2 buffers][kWG][kBM] row maxima of a tile's column halves
+    static constexpr uint32_t ml = q;  // per warpgroup and row: (max, sum), over Q after the last MMA
+    static constexpr uint32_t segs = mx + 2 * kWG * kBM * 4;  // staged segment table of the request
     static constexpr uint32_t total = segs + kStagedSegs * sizeof(d3d_segment_t);
     static constexpr uint32_t alloc = total + 1024;  // room to align the base to 1024 bytes
 };
@@ -103,10 +113,9 @@ struct AttnParams {
     const int32_t *cu_prefix, *cu_q, *cu_seg;
     uint16_t *out;
     unsigned char *ws;
-    int Hq, Hkv, G, TQ, MT, MP, S, PK;
+    int Hq, Hkv, G, TQ, MT, S, PK;
     int max_q, max_prefix, total_q, total_prefix, total_segs;
     float scale_log2;
-    unsigned long long off_cnt, off_opart, off_ml;
     int fault;
 };
 
@@ -156,7 +165,7 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, int32_
     if (mbar_try_wait(bar, parity))
         return;
     const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity)) {
         if (global_ns() - t0 > kWaitTimeoutNs) {
             record_status(status, D3D_ERR_DEVICE_TIMEOUT);
             return;
@@ -174,6 +183,92 @@ __device__ __forceinline__ int split_prefix_begin(int sp, int S, int nP, int PK)
     return (int)(b < nP ? b : nP);
 }
 
+// Shared-memory exchange area of the split combine (in the K ring, free once
+// every MMA is done): the CTA's partial O normalised by its row sum as bf16,
+// 16-byte unit u (head-dim columns 8u..8u+7) of row i at (u * 128 + i) * 16,
+// then (max, sum) per row.
+template <int D> struct Xchg {
+    static constexpr uint32_t kPartBytes = (D / 8) * kBM * 16;
+    static __device__ uint32_t part(uint32_t sK) { return sK; }
+    static __device__ uint32_t ml(uint32_t sK) { return sK + kPartBytes; }
+};
+static_assert(Xchg<128>::kPartBytes + kBM * 8 <= kKStages * kBN * 128 * 2, "exchange fits the K ring");
+static_assert(Xchg<64>::kPartBytes + kBM * 8 <= kKStages * kBN * 64 * 2, "exchange fits the K ring");
+
+__device__ __forceinline__ uint4 pack8(const float *a, float sc)
+{
+    uint4 w;
+    w.x = pack_bf16x2(a[0] * sc, a[1] * sc);
+    w.y = pack_bf16x2(a[2] * sc, a[3] * sc);
+    w.z = pack_bf16x2(a[4] * sc, a[5] * sc);
+    w.w = pack_bf16x2(a[6] * sc, a[7] * sc);
+    return w;
+}
+
+// Split combine of one query row over the S CTAs of the cluster: the
+// (max, sum) of every split and the units of this thread, u = sp + S*(2k+w)
+// (CTA sp takes units u mod S = sp, its two warpgroups alternate), read
+// through distributed shared memory in split order; writes those output units.
+template <int D, int S>
+__device__ __forceinline__ void cluster_merge(int sp, int w, uint32_t part, uint32_t ml, int row, bool row_valid,
+                                              uint16_t *orow)
+{
+    constexpr int kUnits = D / 8;
+    constexpr int kMine = (kUnits + 2 * S - 1) / (2 * S);
+    float ms[S], ls[S];
+#pragma unroll
+    for (int s2 = 0; s2 < S; ++s2) {
+        const float2 v = dsmem_ld_f2(dsmem_addr(ml + (uint32_t)row * 8u, (uint32_t)s2));
+        ms[s2] = v.x;
+        ls[s2] = v.y;
+    }
+    float M = -INFINITY;
+    bool bad = false;
+#pragma unroll
+    for (int s2 = 0; s2 < S; ++s2) {
+        M = fmaxf(M, ms[s2]);
+        bad = bad || ls[s2] < 0.f;
+    }
+    float coef[S], Lsum = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < S; ++s2) {
+        const float wt = (M == -INFINITY) ? 0.f : ex2(ms[s2] - M);
+        coef[s2] = wt * fmaxf(ls[s2], 0.f);  // every partial was divided by its own sum
+        Lsum += coef[s2];
+    }
+    const float sc = (bad || !(Lsum > 0.f)) ? 0.f : 1.f / Lsum;
+    uint4 rem[kMine][S];
+#pragma unroll
+    for (int k = 0; k < kMine; ++k) {
+        const int u = sp + S * (2 * k + w);
+#pragma unroll
+        for (int s2 = 0; s2 < S; ++s2) {
+            rem[k][s2] = make_uint4(0, 0, 0, 0);
+            if (u < kUnits && coef[s2] != 0.f && sc != 0.f)
+                rem[k][s2] = dsmem_ld_v4(dsmem_addr(part + ((uint32_t)u * kBM + (uint32_t)row) * 16u, (uint32_t)s2));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kMine; ++k) {
+        const int u = sp + S * (2 * k + w);
+        if (u >= kUnits)
+            break;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s2 = 0; s2 < S; ++s2) {
+            const float cw = coef[s2];
+            const uint32_t wd[4] = {rem[k][s2].x, rem[k][s2].y, rem[k][s2].z, rem[k][s2].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[2 * e] += cw * __uint_as_float(wd[e] << 16);
+                acc[2 * e + 1] += cw * __uint_as_float(wd[e] & 0xffff0000u);
+            }
+        }
+        if (row_valid)
+            *reinterpret_cast<uint4 *>(orow + 8 * u) = pack8(acc, sc);
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
@@ -184,32 +279,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // ---- unit: ((r * Hkv + hk) * MP + mp) * S + sp
+    // ---- unit: ((r * Hkv + hk) * MT + mt) * S + sp
     unsigned u = blockIdx.x;
     const int sp = (int)(u % (unsigned)p.S);
     u /= (unsigned)p.S;
-    const int mp = (int)(u % (unsigned)p.MP);
-    u /= (unsigned)p.MP;
+    const int mt = (int)(u % (unsigned)p.MT);
+    u /= (unsigned)p.MT;
     const int hk = (int)(u % (unsigned)p.Hkv);
     const int r = (int)(u / (unsigned)p.Hkv);
-    const unsigned pair_id = blockIdx.x / (unsigned)p.S;  // (r, hk, mp)
     int32_t *status = reinterpret_cast<int32_t *>(p.ws);
 
+    // early exits are uniform over the CTAs of a cluster (same r and tile)
     ReqBounds b;
     if (!request_bounds(p.cu_prefix, p.cu_q, p.cu_seg, r, p.max_q, p.max_prefix, p.total_q, p.total_prefix,
                         p.total_segs, b)) {
-        if (tid == 0)
+        if (tid == 0 && sp == 0)
             record_status(status, D3D_ERR_DEVICE_INPUT);
         return;
     }
-    bool tile_valid[kTiles];
-    for (int t = 0; t < kTiles; ++t)
-        tile_valid[t] = (2 * mp + t) < p.MT && (2 * mp + t) * p.TQ < b.n_q;
-    if (!tile_valid[0])
+    if (mt * p.TQ >= b.n_q)
         return;
-    const int ntiles = tile_valid[1] ? 2 : 1;
 
-    // ---- this split's tiles: prefix tiles [pb, pe), then (last split only) packed tiles
+    // ---- this split's key list: prefix tiles [pb, pe), then (last split only) packed tiles
     const int nP = (b.L + kBN - 1) / kBN;
     const int pb = split_prefix_begin(sp, p.S, nP, p.PK);
     const int pe = (sp == p.S - 1) ? nP : split_prefix_begin(sp + 1, p.S, nP, p.PK);
@@ -225,9 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *misc = reinterpret_cast<uint32_t *>(gbase + Lay::misc);
     volatile uint32_t *tmem_slot = misc + 0;
     volatile uint32_t *abort_flag = misc + 1;
-    uint32_t *mask = misc + 2;  // 2 words: packed tiles visible to some row of the pair
-    volatile int *ticket = reinterpret_cast<volatile int *>(misc + 4);  // 2 words: split tickets
-    volatile int *ready_flag = reinterpret_cast<volatile int *>(misc + 6);  // 2 words: merger may go
+    uint32_t *mask = misc + 2;  // 2 words: packed tiles visible to some row of the tile
+    float2 *s_ml = reinterpret_cast<float2 *>(gbase + Lay::ml);  // [kWG][kBM]: max, sum
+    float *s_mx = reinterpret_cast<float *>(gbase + Lay::mx);     // [2][kWG][kBM]
 
     if (tid == 0) {
         mbar_init(bar(B_Q), 1);
@@ -239,15 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_VF + i), 1);
             mbar_init(bar(B_VE + i), 1);
         }
-        for (int t = 0; t < kTiles; ++t) {
-            mbar_init(bar(B_SF + t), 1);
-            mbar_init(bar(B_PR + t), 128);
-            mbar_init(bar(B_OD + t), 1);
+        for (int b2 = 0; b2 < 2; ++b2) {
+            mbar_init(bar(B_SF + b2), 1);
+            mbar_init(bar(B_PR + b2), kSoftmaxThreads / 32);
+            mbar_init(bar(B_MX + b2), kSoftmaxThreads / 32);
         }
-        for (int t = 0; t < kTiles; ++t) {
-            mbar_init(bar(B_TK + t), 1);
-            mbar_init(bar(B_RDY + t), 1);
-        }
+        mbar_init(bar(B_OW), 1);
         mbar_init(bar(B_MASK), kSoftmaxThreads);
         mbar_init(bar(B_DONE), 1);
         *abort_flag = 0u;
@@ -270,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // number of packed tiles of the pair; waits for the mask on first use
+    // number of packed tiles of the query tile; waits for the mask on first use
     int npk_cache = -1;
     uint32_t mk0 = 0, mk1 = 0;
     auto npk = [&]() -> int {
@@ -283,40 +371,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return npk_cache;
     };
-    // does tile j of this split exist (-1: gave up waiting)
-    auto exists = [&](int j) -> int {
-        if (j < n_pre)
+    // does list tile k of this split exist (-1: gave up waiting)
+    auto exists = [&](int k) -> int {
+        if (k < n_pre)
             return 1;
         if (!last_split)
             return 0;
         const int c = npk();
-        return c < 0 ? -1 : (j - n_pre < c ? 1 : 0);
+        return c < 0 ? -1 : (k - n_pre < c ? 1 : 0);
     };
-    // global K/V row and map of tile j (call only when it exists)
-    auto tile_row = [&](int j, bool &pre) -> int {
-        pre = j < n_pre;
-        return pre ? b.p0 + (pb + j) * kBN : b.q0 + nth_set_bit(mk0, mk1, j - n_pre) * kBN;
+    // global K/V row of list tile k (call only when it exists)
+    auto tile_row = [&](int k, bool &pre) -> int {
+        pre = k < n_pre;
+        return pre ? b.p0 + (pb + k) * kBN : b.q0 + nth_set_bit(mk0, mk1, k - n_pre) * kBN;
     };
+
+    // what a softmax thread hands to the split combine after the role code
+    bool mg_on = false, mg_valid = false;
+    uint16_t *mg_orow = nullptr;
 
     if (warp == kTmaWarp) {
         // =================== TMA producer ===================
+        // issue order = the tensor core's consumption order: K0, K1, then
+        // V(k), K(k+2) for k = 0, 1, ...
         if (lane == 0) {
-            int k_cnt[kKStages] = {0, 0, 0}, v_cnt[kVStages] = {0, 0};
-            mbar_arrive_expect_tx(bar(B_Q), Lay::kQBytes * ntiles);
-            for (int t = 0; t < ntiles; ++t)
-                for (int cb = 0; cb < D / 64; ++cb)
-                    tma_load_3d(sQ + t * Lay::kQBytes + cb * kBlockBytes, &tm_q, bar(B_Q), cb * 64, hk * p.G,
-                                b.q0 + (2 * mp + t) * p.TQ);
-            auto issue = [&](int j, bool is_k) -> bool {
+            int k_cnt[kKStages] = {}, v_cnt[kVStages] = {};
+            mbar_arrive_expect_tx(bar(B_Q), Lay::kQBytes);
+            for (int cb = 0; cb < D / 64; ++cb)
+                tma_load_3d(sQ + cb * kBlockBytes, &tm_q, bar(B_Q), cb * 64, hk * p.G, b.q0 + mt * p.TQ);
+            auto issue = [&](int k, bool is_k) -> bool {
                 const int ns = is_k ? kKStages : kVStages;
-                const int s = j % ns;
+                const int s = k % ns;
                 const int empty = is_k ? B_KE : B_VE, full = is_k ? B_KF : B_VF;
-                if (j >= ns && !wait_bar(bar(empty + s), ((j - ns) / ns) & 1, abort_flag, status))
+                if (k >= ns && !wait_bar(bar(empty + s), ((k - ns) / ns) & 1, abort_flag, status))
                     return false;
-                if (p.fault == 1 && is_k && j == 0)
+                if (p.fault == 1 && is_k && k == 0)
                     return true;  // injected fault: this tile never arrives
                 bool pre;
-                const int row = tile_row(j, pre);
+                const int row = tile_row(k, pre);
                 const CUtensorMap *m = is_k ? (pre ? &tm_kp : &tm_kn) : (pre ? &tm_vp : &tm_vn);
                 const uint32_t dst = (is_k ? sK : sV) + s * Lay::kKBytes;
                 mbar_arrive_expect_tx(bar(full + s), Lay::kKBytes);
@@ -325,19 +417,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++(is_k ? k_cnt[s] : v_cnt[s]);
                 return true;
             };
-            int more = exists(0);
-            bool ok = more >= 0;
-            if (more == 1)
-                ok = issue(0, true);
-            for (int j = 0; ok && more == 1; ++j) {
-                const int next = exists(j + 1);
-                if (next < 0)
+            bool ok = true;
+            for (int k = 0; ok && k < 2; ++k) {
+                const int e = exists(k);
+                ok = e >= 0;
+                if (e == 1)
+                    ok = issue(k, true);
+            }
+            for (int k = 0; ok; ++k) {
+                const int e = exists(k);
+                if (e != 1)
                     break;
-                if (next == 1)
-                    ok = issue(j + 1, true);
-                if (ok)
-                    ok = issue(j, false);
-                more = next;
+                ok = issue(k, false);
+                const int e2 = ok ? exists(k + 2) : -1;
+                if (e2 < 0)
+                    break;
+                if (e2 == 1)
+                    ok = issue(k + 2, true);
             }
             // every copy this thread started must land before the CTA exits
             wait_drain(bar(B_Q), 0, status);
@@ -354,79 +450,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
             constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 0, 1);
-            auto issue_s = [&](int t, int j) {
-                const int ks = j % kKStages;
-                const uint32_t tS = tmem + (uint32_t)t * 256u;
+            // S(k) = Q K_k^T into TMEM buffer k % 2, then release the K stage
+            auto issue_s = [&](int k) {
+                const int ks = k % kKStages;
+                const uint32_t tS = tmem + (uint32_t)(k & 1) * kBN;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * kBlockBytes + (kk % 4) * 32;
-                    const uint64_t a = sdesc_sw128(sQ + t * Lay::kQBytes + off, 16, 1024);
+                    const uint64_t a = sdesc_sw128(sQ + off, 16, 1024);
                     const uint64_t bd = sdesc_sw128(sK + ks * Lay::kKBytes + off, 16, 1024);
                     mma_bf16_ss(tS, a, bd, idS, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(B_SF + t));
+                mma_commit(bar(B_SF + (k & 1)));
+                mma_commit(bar(B_KE + ks));
             };
-            auto issue_pv = [&](int t, int j) {
-                const int vs = j % kVStages;
-                const uint32_t tP = tmem + (uint32_t)t * 256u, tO = tP + 128u;
+            // O += P(k) V_k with P read from buffer k % 2, then release the V stage
+            auto issue_pv = [&](int k) {
+                const int vs = k % kVStages;
+                const uint32_t tP = tmem + (uint32_t)(k & 1) * kBN, tO = tmem + 2u * kBN;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
-                    // A = P_t in TMEM (8 columns of bf16 pairs per 16 keys); B = V
+                    // A = P in TMEM (8 columns of bf16 pairs per 16 keys); B = V
                     // MN-major: 16 keys = two 8-row groups = 2048 bytes, the next 64
                     // head-dim columns are 16 KB further
                     const uint64_t bd = sdesc_sw128(sV + vs * Lay::kVBytes + kk * 2048, kBlockBytes, 1024);
-                    mma_bf16_ts(tO, tP + kk * 8, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16_ts(tO, tP + kk * 8, bd, idO, (k > 0 || kk > 0) ? 1u : 0u);
                 }
+                mma_commit(bar(B_OW));
+                mma_commit(bar(B_VE + vs));
             };
-            int more = exists(0);
-            bool ok = more >= 0 && wait_bar(bar(B_Q), 0, abort_flag, status);
-            if (ok && more == 1) {
-                ok = wait_bar(bar(B_KF), 0, abort_flag, status);
-                if (ok) {
-                    tc_fence_after();
-                    for (int t = 0; t < ntiles; ++t)
-                        issue_s(t, 0);
-                    mma_commit(bar(B_KE));
+            bool ok = wait_bar(bar(B_Q), 0, abort_flag, status);
+            for (int k = 0; ok && k < 2; ++k) {
+                const int e = exists(k);
+                ok = e >= 0;
+                if (e == 1) {
+                    ok = wait_bar(bar(B_KF + k % kKStages), (k / kKStages) & 1, abort_flag, status);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_s(k);
+                    }
                 }
             }
-            for (int j = 0; ok && more == 1; ++j) {
-                const int next = exists(j + 1);
-                if (next < 0)
+            // per tile k: PV(k) once P(k) is written, then S(k+2) into the buffer PV(k)
+            // has just read; the tensor core computes these while the softmax
+            // works on tile k+1
+            for (int k = 0; ok; ++k) {
+                const int e = exists(k);
+                if (e != 1) {
+                    ok = e >= 0;
                     break;
-                ok = wait_bar(bar(B_VF + j % kVStages), (j / kVStages) & 1, abort_flag, status);
-                if (ok && next == 1)
-                    ok = wait_bar(bar(B_KF + (j + 1) % kKStages), ((j + 1) / kKStages) & 1, abort_flag, status);
-                for (int t = 0; ok && t < ntiles; ++t) {
-                    ok = wait_bar(bar(B_PR + t), j & 1, abort_flag, status);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    issue_pv(t, j);
-                    if (next == 1)
-                        issue_s(t, j + 1);
-                    else
-                        mma_commit(bar(B_OD + t));
                 }
+                ok = wait_bar(bar(B_VF + k % kVStages), (k / kVStages) & 1, abort_flag, status) &&
+                     wait_bar(bar(B_PR + (k & 1)), (k >> 1) & 1, abort_flag, status);
                 if (!ok)
                     break;
-                mma_commit(bar(B_VE + j % kVStages));
-                if (next == 1)
-                    mma_commit(bar(B_KE + (j + 1) % kKStages));
-                more = next;
+                tc_fence_after();
+                issue_pv(k);
+                const int e2 = exists(k + 2);
+                ok = e2 >= 0;
+                if (e2 == 1) {
+                    ok = wait_bar(bar(B_KF + (k + 2) % kKStages), ((k + 2) / kKStages) & 1, abort_flag, status);
+                    if (ok)
+                        issue_s(k + 2);
+                }
             }
-            // all MMAs this thread issued must finish before TMEM is released
+            // every MMA is complete when B_DONE fires: O_0, O_1 final, and the
+            // Q and K/V buffers free; TMEM is released only after it
             mma_commit(bar(B_DONE));
             wait_drain(bar(B_DONE), 0, status);
         }
         __syncwarp();
     } else {
         // =================== softmax warpgroups ===================
-        const int t = warp >> 2;  // query tile of this warpgroup
+        const int w = warp >> 2;  // warpgroup: key columns [64w, 64w + 64) of every tile
         const int row = tid & 127;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + (uint32_t)t * 256u + lane_off, tO = tS + 128u;
-        const int token = (2 * mp + t) * p.TQ + row / p.G;
-        const bool row_valid = tile_valid[t] && token < b.n_q;
+        const uint32_t tS0 = tmem + lane_off, tO = tmem + 2u * kBN + lane_off;
+        const int token = mt * p.TQ + row / p.G;
+        const bool row_valid = token < b.n_q;
         bool row_bad = false;
         RowVis vis;
         vis.own_lo = vis.own_hi = vis.par_lo = vis.par_hi = 0;
@@ -451,371 +552,210 @@ __global__ void __launch_bounds__(kThreads, 1)
                 row_bad = true;
                 vis.own_lo = vis.own_hi = vis.par_lo = vis.par_hi = 0;
             }
-            auto mark = [&](int lo, int hi) {
-                if (lo >= hi)
-                    return;
-                for (int k = lo / kBN; k <= (hi - 1) / kBN && k < kMaxPackedTiles; ++k)
-                    atomicOr(&mask[k >> 5], 1u << (k & 31));
-            };
-            mark(vis.own_lo, vis.own_hi);
-            mark(vis.par_lo, vis.par_hi);
+            if (w == 0) {
+                auto mark = [&](int lo, int hi) {
+                    if (lo >= hi)
+                        return;
+                    for (int k = lo / kBN; k <= (hi - 1) / kBN && k < kMaxPackedTiles; ++k)
+                        atomicOr(&mask[k >> 5], 1u << (k & 31));
+                };
+                mark(vis.own_lo, vis.own_hi);
+                mark(vis.par_lo, vis.par_hi);
+            }
         }
         mbar_arrive(bar(B_MASK));
 
-        // split ticket of this query tile, taken before the last key tile so the
-        // atomic's round trip overlaps that tile's work
-        const size_t tile_id = (size_t)pair_id * kTiles + t;
-        const size_t n_tiles = (size_t)(gridDim.x / p.S) * kTiles;
-        int *tk_cnt = reinterpret_cast<int *>(p.ws + p.off_cnt) + tile_id;
-        int *wr_cnt = reinterpret_cast<int *>(p.ws + p.off_cnt) + n_tiles + tile_id;
-        int my_ticket = -1;
-        float m_ref = -INFINITY, l = 0.f;
+        float m_ref = -INFINITY, l = 0.f;  // l: this thread's column half of the row sum
         bool aborted = false;
         int n_done = 0;
-        if (tile_valid[t]) {
-            for (int j = 0;; ++j) {
-                const int ex = exists(j);
-                if (!__all_sync(0xffffffffu, ex >= 0)) {
-                    aborted = true;
-                    break;
+        for (int k = 0;; ++k) {
+            const int ex = exists(k);
+            if (!__all_sync(0xffffffffu, ex >= 0)) {
+                aborted = true;
+                break;
+            }
+            if (ex == 0)
+                break;
+            const int bf = k & 1;
+            const uint32_t tS = tS0 + (uint32_t)bf * kBN;
+            bool ok = wait_bar(bar(B_SF + bf), (k >> 1) & 1, abort_flag, status);
+            if (!__all_sync(0xffffffffu, ok)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            float s[kHalf];
+            tmem_ld64(tS + (uint32_t)(w * kHalf), s);
+            bool pre;
+            const int krow = tile_row(k, pre);
+            if (pre) {
+                const int valid = b.L - (pb + k) * kBN - w * kHalf;
+                if (valid < kHalf) {
+#pragma unroll
+                    for (int e = 0; e < kHalf; ++e)
+                        if (e >= valid)
+                            s[e] = -INFINITY;
                 }
-                if (ex == 0)
-                    break;
-                if (p.S > 1 && row == 0 && my_ticket < 0 && exists(j + 1) == 0)
-                    my_ticket = atomicAdd(tk_cnt, 1);
-                bool ok = wait_bar(bar(B_SF + t), j & 1, abort_flag, status);
+            } else {
+                // this row's visible keys among the 64 as a mask: two half-open
+                // intervals cut into two 32-key words
+                const int kb = krow - b.q0 + w * kHalf;
+                uint32_t wbits[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int base = kb + 32 * q;
+                    wbits[q] = range_bits(vis.own_lo - base, vis.own_hi - base) |
+                               range_bits(vis.par_lo - base, vis.par_hi - base);
+                }
+#pragma unroll
+                for (int e = 0; e < kHalf; ++e)
+                    s[e] = ((wbits[e >> 5] >> (e & 31)) & 1u) ? s[e] : -INFINITY;
+            }
+            // max of this half with eight independent chains, then the row max
+            // from both halves (published in shared memory, bounded wait)
+            float m8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                m8[e] = s[e];
+#pragma unroll
+            for (int e0 = 8; e0 < kHalf; e0 += 8)
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    m8[e] = fmaxf(m8[e], s[e0 + e]);
+            const float mloc = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            s_mx[(bf * kWG + w) * kBM + row] = mloc;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(B_MX + bf));
+            ok = wait_bar(bar(B_MX + bf), (k >> 1) & 1, abort_flag, status);
+            if (!__all_sync(0xffffffffu, ok)) {
+                aborted = true;
+                break;
+            }
+            // both halves of the S buffer are in registers by now: P may overwrite it
+            const float mx = fmaxf(mloc, s_mx[(bf * kWG + 1 - w) * kBM + row]) * p.scale_log2;
+            float factor = 1.f;
+            if (mx > m_ref + kRescaleLog2) {
+                factor = ex2(m_ref - mx);  // 0 when m_ref = -inf
+                m_ref = mx;
+            }
+            const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
+            float r4[4] = {0.f, 0.f, 0.f, 0.f};  // row sum in four chains
+            uint32_t pk[kHalf / 2];
+#pragma unroll
+            for (int e = 0; e < kHalf / 2; ++e) {
+                const float e0 = ex2(fmaf(s[2 * e], p.scale_log2, -msub));
+                const float e1 = ex2(fmaf(s[2 * e + 1], p.scale_log2, -msub));
+                r4[e & 3] += e0 + e1;
+                pk[e] = pack_bf16x2(e0, e1);
+            }
+            l = l * factor + (r4[0] + r4[1]) + (r4[2] + r4[3]);
+            // rescale this thread's half of O once PV(k-1) has landed (rare: only
+            // when the max grows by more than 2^8)
+            if (k > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+                ok = wait_bar(bar(B_OW), (k - 1) & 1, abort_flag, status);
                 if (!__all_sync(0xffffffffu, ok)) {
                     aborted = true;
                     break;
                 }
                 tc_fence_after();
-                float s[kBN];
-                tmem_ld128(tS, s);
-                bool pre;
-                const int krow = tile_row(j, pre);
-                if (pre) {
-                    const int valid = b.L - (pb + j) * kBN;
-                    if (valid < kBN) {
 #pragma unroll
-                        for (int c = 0; c < kBN; ++c)
-                            if (c >= valid)
-                                s[c] = -INFINITY;
-                    }
-                } else {
-                    // this row's visible keys in the tile as a 128-bit mask: two
-                    // half-open intervals cut into four 32-key words
-                    const int kb = krow - b.q0;
-                    uint32_t wbits[4];
+                for (int q = 0; q < D / 64; ++q) {
+                    float o[32];
+                    const uint32_t col = (uint32_t)(w * (D / 2) + q * 32);
+                    tmem_ld32(tO + col, o);
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const int base = kb + 32 * w;
-                        wbits[w] = range_bits(vis.own_lo - base, vis.own_hi - base) |
-                                   range_bits(vis.par_lo - base, vis.par_hi - base);
-                    }
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c)
-                        s[c] = ((wbits[c >> 5] >> (c & 31)) & 1u) ? s[c] : -INFINITY;
+                    for (int e = 0; e < 32; ++e)
+                        o[e] *= factor;
+                    tmem_st32(tO + col, o);
                 }
-                float mx = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < kBN; ++c)
-                    mx = fmaxf(mx, s[c]);
-                mx *= p.scale_log2;
-                float factor = 1.f;
-                if (mx > m_ref + kRescaleLog2) {
-                    factor = ex2(m_ref - mx);  // 0 when m_ref = -inf
-                    m_ref = mx;
-                }
-                const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
-                float rs = 0.f;
-                uint32_t pk[kBN / 2];
-#pragma unroll
-                for (int c = 0; c < kBN / 2; ++c) {
-                    const float e0 = ex2(fmaf(s[2 * c], p.scale_log2, -msub));
-                    const float e1 = ex2(fmaf(s[2 * c + 1], p.scale_log2, -msub));
-                    rs += e0 + e1;
-                    pk[c] = pack_bf16x2(e0, e1);
-                }
-                l = l * factor + rs;
-                // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled
-                if (j > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(tO + c * 32, o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            o[e] *= factor;
-                        tmem_st32(tO + c * 32, o);
-                    }
-                }
-                tmem_st64(tS, pk);  // P over the first 64 columns of S
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(bar(B_PR + t));
-                n_done = j + 1;
             }
+            tmem_st32u(tS + (uint32_t)(w * (kHalf / 2)), pk);  // P of keys 64w.. over columns 32w..
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(B_PR + bf));
+            n_done = k + 1;
         }
 
-        // ---- epilogue
-        if (tile_valid[t] && !aborted) {
-            const bool have_o = n_done > 0;
-            if (have_o) {
-                const bool ok = wait_bar(bar(B_OD + t), 0, abort_flag, status);
-                if (!__all_sync(0xffffffffu, ok))
-                    aborted = true;
+        // ---- epilogue: every MMA done, then the two warpgroups combine
+        wait_drain(bar(B_DONE), 0, status);
+        // (max, column-half sum, tiles done) of this thread's row; a negative sum
+        // marks a void row (failed descriptor check or an abandoned wait)
+        float4 *s_ml4 = reinterpret_cast<float4 *>(s_ml);
+        s_ml4[w * kBM + row] = make_float4(m_ref, (aborted || row_bad) ? -1.f : l, (float)n_done, 0.f);
+        tc_fence_before();
+        asm volatile("bar.sync 2, %0;" ::"n"(kSoftmaxThreads) : "memory");
+        tc_fence_after();
+        const float4 mine = s_ml4[w * kBM + row], other = s_ml4[(1 - w) * kBM + row];
+        const bool void_row = mine.y < 0.f || other.y < 0.f;
+        const float M = fmaxf(mine.x, other.x);  // both halves keep the same running max
+        const float L = fmaxf(mine.y, 0.f) + fmaxf(other.y, 0.f);
+        const bool have = fminf(mine.z, other.z) > 0.f;  // uniform over each warp
+        const float inv = (void_row || !(L > 0.f)) ? 0.f : 1.f / L;
+        // this thread's half of the head dimension: columns [w*D/2, (w+1)*D/2)
+        uint16_t *orow = p.out + ((size_t)(b.q0 + token) * p.Hq + hk * p.G + (row % p.G)) * D + w * (D / 2);
+        const uint32_t part = Xchg<D>::part(sK);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            float x0[32];
+            if (have) {
+                tmem_ld32(tO + (uint32_t)(w * (D / 2) + c * 32), x0);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    x0[e] = 0.f;
             }
-            if (!aborted) {
-                tc_fence_after();
-                uint16_t *orow = p.out + ((size_t)(b.q0 + token) * p.Hq + hk * p.G + (row % p.G)) * D;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 v = pack8(x0 + 8 * q, inv);
                 if (p.S == 1) {
-                    const float inv = (l > 0.f && !row_bad) ? 1.f / l : 0.f;
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(tO + c * 32, o);
-                        if (row_valid) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
-                                uint4 w;
-                                w.x = pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
-                                w.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
-                                w.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
-                                w.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
-                                dst[q4] = w;
-                            }
-                        }
-                    }
+                    if (row_valid)
+                        *reinterpret_cast<uint4 *>(orow + c * 32 + q * 8) = v;
                 } else {
-                    // Ticket first: the warpgroup that finishes this query tile's key
-                    // tiles last merges; the others write their partial normalised by
-                    // its row sum, as bf16 (16-byte chunk c8 of row i of partial q at
-                    // ((q * D/8 + c8) * 128 + i)), with (max, sum) beside it.
-                    uint4 *opart = reinterpret_cast<uint4 *>(p.ws + p.off_opart);
-                    float2 *mls = reinterpret_cast<float2 *>(p.ws + p.off_ml);
-                    if (row == 0) {
-                        ticket[t] = (my_ticket >= 0) ? my_ticket : atomicAdd(tk_cnt, 1);
-                        mbar_arrive(bar(B_TK + t));
-                    }
-                    const bool got = wait_bar(bar(B_TK + t), 0, abort_flag, status);
-                    if (__all_sync(0xffffffffu, got)) {
-                        const bool is_last = ticket[t] == p.S - 1;
-                        if (!is_last) {
-                            const size_t pidx = tile_id * p.S + sp;
-                            const float inv = (l > 0.f) ? 1.f / l : 0.f;
-#pragma unroll
-                            for (int c = 0; c < D / 32; ++c) {
-                                float o[32];
-                                if (have_o) {
-                                    tmem_ld32(tO + c * 32, o);
-                                } else {
-#pragma unroll
-                                    for (int e = 0; e < 32; ++e)
-                                        o[e] = 0.f;
-                                }
-#pragma unroll
-                                for (int q4 = 0; q4 < 4; ++q4) {
-                                    uint4 w;
-                                    w.x = pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
-                                    w.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
-                                    w.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
-                                    w.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
-                                    opart[(pidx * (D / 8) + c * 4 + q4) * kBM + row] = w;
-                                }
-                            }
-                            // a negative sum marks a row whose descriptors failed the
-                            // check (only the last split, which visits packed keys, checks)
-                            mls[pidx * kBM + row] = make_float2(m_ref, row_bad ? -1.f : l);
-                            __threadfence();
-                            __syncwarp();
-                            if (lane == 0)
-                                atomicAdd(wr_cnt, 32);
-                        } else {
-                            // every other split holds a ticket, so it is past its key
-                            // tiles and only has stores left: wait (bounded) for them
-                            if (row == 0) {
-                                // one poller; it also resets both counters for the next call
-                                const int need = (p.S - 1) * kBM;
-                                const uint64_t t0 = global_ns();
-                                int ok_all = 1;
-                                while (*reinterpret_cast<volatile int *>(wr_cnt) < need) {
-                                    if (global_ns() - t0 > kWaitTimeoutNs) {
-                                        record_status(status, D3D_ERR_DEVICE_TIMEOUT);
-                                        ok_all = 0;
-                                        break;
-                                    }
-                                }
-                                if (ok_all) {
-                                    *wr_cnt = 0;
-                                    *tk_cnt = 0;
-                                }
-                                ready_flag[t] = ok_all;
-                                mbar_arrive(bar(B_RDY + t));
-                            }
-                            const bool rel = wait_bar(bar(B_RDY + t), 0, abort_flag, status);
-                            const int ready = __all_sync(0xffffffffu, rel) ? ready_flag[t] : 0;
-                            if (ready) {
-                                __threadfence();
-                                float2 mlv[kMaxSplits];
-                                float M = m_ref;
-                                for (int s2 = 0; s2 < p.S; ++s2) {
-                                    mlv[s2] = (s2 == sp) ? make_float2(m_ref, l)
-                                                         : __ldcg(mls + (tile_id * p.S + s2) * kBM + row);
-                                    M = fmaxf(M, mlv[s2].x);
-                                }
-                                float Lsum = 0.f;
-                                bool bad = row_bad;
-                                for (int s2 = 0; s2 < p.S; ++s2) {
-                                    bad = bad || mlv[s2].y < 0.f;
-                                    const float w = (M == -INFINITY) ? 0.f : ex2(mlv[s2].x - M);
-                                    Lsum += w * fmaxf(mlv[s2].y, 0.f);
-                                    // own O is unnormalised; the others were divided by their sum
-                                    mlv[s2].x = (s2 == sp) ? w : w * fmaxf(mlv[s2].y, 0.f);
-                                }
-                                const float sc = (bad || !(Lsum > 0.f)) ? 0.f : 1.f / Lsum;
-                                const uint4 *pa = nullptr, *pb = nullptr;  // the other splits (fast path)
-                                float wa = 0.f, wb = 0.f;
-                                if (p.S <= 3) {
-                                    // the other splits: (1, 2), (0, 2) or (0, 1); only one when S = 2
-                                    const int oa = (sp == 0) ? 1 : 0, ob = (p.S < 3) ? -1 : ((sp == 2) ? 1 : 2);
-                                    pa = opart + ((tile_id * p.S + oa) * (D / 8)) * kBM + row;
-                                    wa = mlv[oa].x;
-                                    if (ob >= 0) {
-                                        pb = opart + ((tile_id * p.S + ob) * (D / 8)) * kBM + row;
-                                        wb = mlv[ob].x;
-                                    }
-                                }
-                                if (p.S <= 3 && sc != 0.f) {
-                                    // software-pipelined: chunk c+1's loads are in flight while
-                                    // chunk c is accumulated
-                                    uint4 cur[2][4], nxt[2][4];
-#pragma unroll
-                                    for (int q4 = 0; q4 < 4; ++q4) {
-                                        cur[0][q4] = __ldcg(pa + (size_t)q4 * kBM);
-                                        cur[1][q4] = pb ? __ldcg(pb + (size_t)q4 * kBM) : make_uint4(0, 0, 0, 0);
-                                    }
-#pragma unroll
-                                    for (int c = 0; c < D / 32; ++c) {
-                                        if (c + 1 < D / 32) {
-#pragma unroll
-                                            for (int q4 = 0; q4 < 4; ++q4) {
-                                                nxt[0][q4] = __ldcg(pa + (size_t)((c + 1) * 4 + q4) * kBM);
-                                                nxt[1][q4] = pb ? __ldcg(pb + (size_t)((c + 1) * 4 + q4) * kBM)
-                                                                : make_uint4(0, 0, 0, 0);
-                                            }
-                                        }
-                                        float acc[32];
-                                        if (have_o) {
-                                            tmem_ld32(tO + c * 32, acc);
-                                        } else {
-#pragma unroll
-                                            for (int e = 0; e < 32; ++e)
-                                                acc[e] = 0.f;
-                                        }
-                                        const float wown = mlv[sp].x;
-#pragma unroll
-                                        for (int q4 = 0; q4 < 4; ++q4) {
-                                            const uint32_t da[4] = {cur[0][q4].x, cur[0][q4].y, cur[0][q4].z, cur[0][q4].w};
-                                            const uint32_t db[4] = {cur[1][q4].x, cur[1][q4].y, cur[1][q4].z, cur[1][q4].w};
-#pragma unroll
-                                            for (int e = 0; e < 4; ++e) {
-                                                float &lo = acc[q4 * 8 + 2 * e], &hi = acc[q4 * 8 + 2 * e + 1];
-                                                lo = lo * wown + wa * __uint_as_float(da[e] << 16) +
-                                                     wb * __uint_as_float(db[e] << 16);
-                                                hi = hi * wown + wa * __uint_as_float(da[e] & 0xffff0000u) +
-                                                     wb * __uint_as_float(db[e] & 0xffff0000u);
-                                            }
-                                        }
-                                        if (row_valid) {
-                                            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                                            for (int q4 = 0; q4 < 4; ++q4) {
-                                                uint4 w;
-                                                w.x = pack_bf16x2(acc[q4 * 8 + 0] * sc, acc[q4 * 8 + 1] * sc);
-                                                w.y = pack_bf16x2(acc[q4 * 8 + 2] * sc, acc[q4 * 8 + 3] * sc);
-                                                w.z = pack_bf16x2(acc[q4 * 8 + 4] * sc, acc[q4 * 8 + 5] * sc);
-                                                w.w = pack_bf16x2(acc[q4 * 8 + 6] * sc, acc[q4 * 8 + 7] * sc);
-                                                dst[q4] = w;
-                                            }
-                                        }
-#pragma unroll
-                                        for (int q4 = 0; q4 < 4; ++q4) {
-                                            cur[0][q4] = nxt[0][q4];
-                                            cur[1][q4] = nxt[1][q4];
-                                        }
-                                    }
-                                } else
-                                {
-                                for (int c = 0; c < D / 32; ++c) {
-                                    float acc[32];
-                                    if (have_o) {
-                                        tmem_ld32(tO + c * 32, acc);
-                                    } else {
-#pragma unroll
-                                        for (int e = 0; e < 32; ++e)
-                                            acc[e] = 0.f;
-                                    }
-                                    const float wown = mlv[sp].x;
-#pragma unroll
-                                    for (int e = 0; e < 32; ++e)
-                                        acc[e] *= wown;
-                                    for (int s0 = 0; sc != 0.f && s0 < p.S; s0 += kMergeUnroll) {
-                                        uint4 v[kMergeUnroll][4];
-#pragma unroll
-                                        for (int u = 0; u < kMergeUnroll; ++u) {
-                                            const int s2 = s0 + u;
-                                            if (s2 < p.S && s2 != sp) {
-                                                const size_t q2 = tile_id * p.S + s2;
-#pragma unroll
-                                                for (int q4 = 0; q4 < 4; ++q4)
-                                                    v[u][q4] = __ldcg(opart + (q2 * (D / 8) + c * 4 + q4) * kBM + row);
-                                            }
-                                        }
-#pragma unroll
-                                        for (int u = 0; u < kMergeUnroll; ++u) {
-                                            const int s2 = s0 + u;
-                                            if (s2 < p.S && s2 != sp) {
-                                                const float wgt = mlv[s2].x;
-#pragma unroll
-                                                for (int q4 = 0; q4 < 4; ++q4) {
-                                                    const uint32_t wd[4] = {v[u][q4].x, v[u][q4].y, v[u][q4].z, v[u][q4].w};
-#pragma unroll
-                                                    for (int e = 0; e < 4; ++e) {
-                                                        acc[q4 * 8 + 2 * e] += wgt * __uint_as_float(wd[e] << 16);
-                                                        acc[q4 * 8 + 2 * e + 1] += wgt * __uint_as_float(wd[e] & 0xffff0000u);
-                                                    }
-                                                }
-                                            }
-                                        }
-                                    }
-                                    if (row_valid) {
-                                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                                        for (int q4 = 0; q4 < 4; ++q4) {
-                                            uint4 w;
-                                            w.x = pack_bf16x2(acc[q4 * 8 + 0] * sc, acc[q4 * 8 + 1] * sc);
-                                            w.y = pack_bf16x2(acc[q4 * 8 + 2] * sc, acc[q4 * 8 + 3] * sc);
-                                            w.z = pack_bf16x2(acc[q4 * 8 + 4] * sc, acc[q4 * 8 + 5] * sc);
-                                            w.w = pack_bf16x2(acc[q4 * 8 + 6] * sc, acc[q4 * 8 + 7] * sc);
-                                            dst[q4] = w;
-                                        }
-                                    }
-                                }
-                                }
-                            }
-                        }
-                    }
+                    // the CTA's partial for the cluster's combine (every MMA is done)
+                    const uint32_t unit = (uint32_t)(w * (D / 16) + c * 4 + q);
+                    smem_st_v4(part + (unit * kBM + (uint32_t)row) * 16u, v);
                 }
-                if (row_valid && row_bad)
-                    record_status(status, D3D_ERR_DEVICE_INPUT);
             }
         }
+        if (p.S > 1 && w == 0)
+            smem_st_f2(Xchg<D>::ml(sK) + (uint32_t)row * 8u, make_float2(M, void_row ? -1.f : L));
+        if (!aborted && row_valid && row_bad && w == 0)
+            record_status(status, D3D_ERR_DEVICE_INPUT);
+        mg_on = true;
+        mg_valid = row_valid;
+        mg_orow = p.out + ((size_t)(b.q0 + token) * p.Hq + hk * p.G + (row % p.G)) * D;
     }
 
-    // ---- teardown: every role is done (all waits are bounded); release TMEM
+    // ---- every role is done (all waits are bounded, copies and MMAs drained)
     tc_fence_before();
     __syncthreads();
+    if (p.S > 1) {
+        // split combine across the cluster: every thread of every CTA passes
+        // both cluster barriers exactly once
+        cluster_arrive();
+        cluster_wait();
+        if (mg_on) {
+            const int w = warp >> 2, row = tid & 127;
+            const uint32_t part = Xchg<D>::part(sK), ml = Xchg<D>::ml(sK);
+            switch (p.S) {
+            case 2: cluster_merge<D, 2>(sp, w, part, ml, row, mg_valid, mg_orow); break;
+            case 3: cluster_merge<D, 3>(sp, w, part, ml, row, mg_valid, mg_orow); break;
+            case 4: cluster_merge<D, 4>(sp, w, part, ml, row, mg_valid, mg_orow); break;
+            case 5: cluster_merge<D, 5>(sp, w, part, ml, row, mg_valid, mg_orow); break;
+            case 6: cluster_merge<D, 6>(sp, w, part, ml, row, mg_valid, mg_orow); break;
+            case 7: cluster_merge<D, 7>(sp, w, part, ml, row, mg_valid, mg_orow); break;
+            default: cluster_merge<D, 8>(sp, w, part, ml, row, mg_valid, mg_orow); break;
+            }
+        }
+        // no CTA leaves while another may still read its shared memory
+        cluster_arrive();
+        cluster_wait();
+    }
+    // release TMEM
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -826,9 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Host side
 // ---------------------------------------------------------------------------
 struct AttnPlan {
-    int G, TQ, MT, MP, S, PK;
+    int G, TQ, MT, S, PK;
     long long units;
-    size_t off_cnt, off_opart, off_ml, total;
 };
 
 int num_sms()
@@ -842,44 +781,85 @@ int num_sms()
     return n;
 }
 
-// Split count: minimise (waves of one-CTA-per-SM units) x (tiles per unit +
-// a fixed per-unit cost for the prologue and pipeline fill, one more for the
-// merge when splitting).
-AttnPlan make_plan(int R, int Hq, int Hkv, int d, int max_q, int max_prefix, int nsm)
+template <int D> cudaError_t set_smem_attr()
+{
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)Layout<D>::alloc);
+    });
+    return err;
+}
+
+// CTAs of the attention kernel resident at once when launched in clusters of
+// S (one CTA per SM; a cluster needs S free SMs of one GPC).  Cached per
+// device and S; 0 when the query fails.
+template <int D> int cluster_capacity(int S)
+{
+    constexpr int kDev = 64;
+    static std::mutex mu;
+    static int cache[kDev][kMaxSplits + 1];
+    static bool have[kDev][kMaxSplits + 1];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDev) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev][S]) {
+        int n = 0;
+        if (set_smem_attr<D>() == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(S * 64));
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = Layout<D>::alloc;
+            cudaLaunchAttribute a[1];
+            a[0].id = cudaLaunchAttributeClusterDimension;
+            a[0].val.clusterDim.x = (unsigned)S;
+            a[0].val.clusterDim.y = 1;
+            a[0].val.clusterDim.z = 1;
+            cfg.attrs = a;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<D>, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+        }
+        cache[dev][S] = n * S;
+        have[dev][S] = true;
+    }
+    return cache[dev][S];
+}
+
+// Split count S (a cluster of S CTAs per query tile): minimise (waves of
+// resident CTAs) x (key-tile steps per CTA, two tiles per step, + a fixed
+// per-CTA cost for the prologue, pipeline fill and epilogue, three more for
+// the cluster combine when splitting).
+template <int D> AttnPlan make_plan(int R, int Hq, int Hkv, int max_q, int max_prefix)
 {
     AttnPlan pl{};
     pl.G = Hq / Hkv;
     pl.TQ = kBM / pl.G;
     pl.MT = (max_q + pl.TQ - 1) / pl.TQ;
-    pl.MP = (pl.MT + kTiles - 1) / kTiles;
     pl.PK = (max_q + kBN - 1) / kBN < 2 ? (max_q + kBN - 1) / kBN : 2;
-    const long long base = (long long)R * Hkv * pl.MP;
+    const long long base = (long long)R * Hkv * pl.MT;
     const int tiles = (max_prefix + kBN - 1) / kBN + pl.PK;
     double best = 1e300;
     pl.S = 1;
     for (int S = 1; S <= kMaxSplits && S <= tiles; ++S) {
-        const double waves = (double)((base * S + nsm - 1) / nsm);
-        const double cost = waves * (double)((tiles + S - 1) / S + 3 + (S > 1 ? 1 : 0));
+        const int cap = S == 1 ? num_sms() : cluster_capacity<D>(S);
+        if (cap < S)
+            continue;
+        const double waves = (double)((base * S + cap - 1) / cap);
+        const int per_split = (tiles + S - 1) / S;
+        const double cost = waves * (double)((per_split + 1) / 2 + 2 + (S > 1 ? 3 : 0));
         if (cost < best - 1e-9) {
             best = cost;
             pl.S = S;
         }
     }
     pl.units = base * pl.S;
-    const size_t rows = (size_t)base * kTiles * kBM;
-    size_t o = sizeof(WsHeader);
-    pl.off_cnt = o;
-    if (pl.S > 1) {
-        const size_t tiles_total = (size_t)base * kTiles;
-        o = align_up(o + sizeof(int) * 2 * tiles_total, kWsAlign);  // split tickets, rows written
-        pl.off_opart = o;
-        o = align_up(o + sizeof(uint16_t) * rows * pl.S * d, kWsAlign);  // bf16 partials
-        pl.off_ml = o;
-        o = align_up(o + sizeof(float2) * rows * pl.S, kWsAlign);
-    } else {
-        pl.off_opart = pl.off_ml = o;
-    }
-    pl.total = o;
     return pl;
 }
 
@@ -920,17 +900,23 @@ int g_fault_mode = 0;
 template <int D>
 int launch_attn(const CUtensorMap (&maps)[5], const AttnParams &prm, long long units, cudaStream_t stream)
 {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)Layout<D>::alloc);
-    });
-    if (attr_err != cudaSuccess)
+    if (set_smem_attr<D>() != cudaSuccess)
         return D3D_ERR_CUDA;
-    attn_tc_kernel<D><<<(unsigned)units, kThreads, Layout<D>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3],
-                                                                               maps[4], prm);
-    return cuda_status(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)units);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Layout<D>::alloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute a[1];
+    if (prm.S > 1) {  // the splits of one query-tile pair form a cluster (consecutive CTAs)
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = (unsigned)prm.S;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        cfg.attrs = a;
+        cfg.numAttrs = 1;
+    }
+    return cuda_status(cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, maps[0], maps[1], maps[2], maps[3], maps[4], prm));
 }
 
 }  // namespace
@@ -943,7 +929,7 @@ size_t d3d_packed_draft_attn_workspace_size(int R, int Hq, int Hkv, int d, int m
     if (R < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_q < 0 || max_prefix < 0 || (d != 64 && d != 128) ||
         d3d::kBM % (Hq / Hkv) != 0)
         return 0;
-    return d3d::make_plan(R, Hq, Hkv, d, max_q, max_prefix, d3d::num_sms()).total;
+    return sizeof(d3d::WsHeader);  // the status word: the split combine needs no global scratch
 }
 
 void d3d_debug_inject_fault(int mode) { d3d::g_fault_mode = mode; }
@@ -972,9 +958,10 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
             return D3D_ERR_INVALID_ARG;
     if (total_prefix > 0 && (reinterpret_cast<uintptr_t>(k_prefix) % 16 || reinterpret_cast<uintptr_t>(v_prefix) % 16))
         return D3D_ERR_INVALID_ARG;
-    const d3d::AttnPlan pl = d3d::make_plan(R, Hq, Hkv, d, max_q, max_prefix, d3d::num_sms());
-    if (!d3d::ws_ok(ws, ws_bytes, pl.total))
+    if (!d3d::ws_ok(ws, ws_bytes, sizeof(d3d::WsHeader)))
         return D3D_ERR_WORKSPACE;
+    const d3d::AttnPlan pl = d == 64 ? d3d::make_plan<64>(R, Hq, Hkv, max_q, max_prefix)
+                                     : d3d::make_plan<128>(R, Hq, Hkv, max_q, max_prefix);
     if (pl.units > 0x7fffffffLL)
         return D3D_ERR_UNSUPPORTED;
 
@@ -1004,7 +991,6 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
     prm.G = pl.G;
     prm.TQ = pl.TQ;
     prm.MT = pl.MT;
-    prm.MP = pl.MP;
     prm.S = pl.S;
     prm.PK = pl.PK;
     prm.max_q = max_q;
@@ -1013,9 +999,6 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
     prm.total_prefix = total_prefix;
     prm.total_segs = total_segs;
     prm.scale_log2 = scale * 1.4426950408889634f;
-    prm.off_cnt = pl.off_cnt;
-    prm.off_opart = pl.off_opart;
-    prm.off_ml = pl.off_ml;
     prm.fault = d3d::g_fault_mode;
     if (d == 64)
         return d3d::launch_attn<64>(maps, prm, pl.units, stream);

@@ -133,7 +133,10 @@ int d3d_validate_segments(const d3d_segment_t *segs, const int32_t *cu_q, const 
  *               128 % (Hq/Hkv) == 0
  *   scale       softmax scale (normally 1/sqrt(d))
  *   out         [total_q, Hq, d] bf16
- *   ws          workspace, d3d_packed_draft_attn_workspace_size() bytes
+ *   ws          workspace, d3d_packed_draft_attn_workspace_size() bytes (the
+ *               status word only: the key splits of a query tile combine
+ *               their partial results through distributed shared memory of
+ *               a thread-block cluster, not through global scratch)
  * Device-side checks: offsets out of the totals' range or a segment table
  * that breaks the rules of d3d_validate_segments set D3D_ERR_DEVICE_INPUT
  * in the status word (the affected rows are written as zeros).
