@@ -249,14 +249,19 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         sets.append(dset)
     ws_a = d3d.new_workspace(d3d.d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix), dev)
     ws_v = d3d.new_workspace(d3d.d3d_spec_verify_workspace_size(R, B, V), dev)
+    # the attention holds one SM per CTA; the verification that runs beside it
+    # takes the SMs it leaves (0: the attention fills the GPU, no limit)
+    attn_ctas = d3d.d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix)
+    side_sms = props.multi_processor_count - attn_ctas
+    verify_sms = side_sms if 0 < attn_ctas and side_sms > 0 else 0
 
     def attn(s):
         d3d.d3d_packed_draft_attn(s["q"], s["kp"], s["vp"], s["kn"], s["vn"], s["segs"], s["cu_prefix"], s["cu_q"],
                                   s["cu_seg"], max_q, max_prefix, scale, s["out"], ws_a)
 
-    def verify(s):
+    def verify(s, sm_limit=0):
         d3d.d3d_spec_verify(s["target"], s["draft"], s["y"], s["u_accept"], s["u_sample"], 1.0, s["accept_len"],
-                            s["out_tokens"], s["num_tokens"], ws_v)
+                            s["out_tokens"], s["num_tokens"], ws_v, sm_limit=sm_limit)
 
     def match(s):
         d3d.d3d_branch_match(s["out_tokens"], s["num_tokens"], s["heads"], s["head_len"], s["branch"])
@@ -272,7 +277,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         side.wait_stream(cur)
         attn(s)
         with torch.cuda.stream(side):
-            verify(s)
+            verify(s, verify_sms)
         cur.wait_stream(side)
         match(s)
 
@@ -355,6 +360,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     n_part = max(n_sets, min(args.steps, 2000))
     t_attn = timed(attn, n_part)
     t_verify = timed(verify, n_part)
+    t_verify_side = timed(lambda s: verify(s, verify_sms), n_part) if verify_sms else t_verify
     t_match = timed(match, n_part)
 
     # end to end through the public API with host buffers
@@ -394,6 +400,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "timing": "CUDA graph replays, CUDA events on the launching stream"},
         "verified_positions_per_s": round(world * wl["positions"] / (ms_step * 1e-3), 1),
         "parts": {"attn_us": round(t_attn * 1e3, 3), "verify_us": round(t_verify * 1e3, 3),
+                  "attn_ctas": attn_ctas, "verify_side_sms": verify_sms,
+                  "verify_side_us": round(t_verify_side * 1e3, 3),
                   "match_us": round(t_match * 1e3, 3),
                   "attn_query_tokens_per_s": round(wl["n_q"] * R / (t_attn * 1e-3), 1),
                   "verify_positions_per_s": round(wl["positions"] / (t_verify * 1e-3), 1),

@@ -17,7 +17,8 @@ import torch
 
 __all__ = [
     "D3DError", "lib", "d3d_status_string", "d3d_version", "d3d_validate_segments",
-    "d3d_packed_draft_attn", "d3d_packed_draft_attn_workspace_size", "d3d_spec_verify",
+    "d3d_packed_draft_attn", "d3d_packed_draft_attn_workspace_size", "d3d_packed_draft_attn_ctas",
+    "d3d_spec_verify",
     "d3d_spec_verify_workspace_size", "d3d_spec_verify_noalloc", "d3d_branch_match", "d3d_workspace_status",
     "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
     "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
@@ -52,7 +53,8 @@ EXPORTED = {
     "d3d_packed_draft_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                                    _F, _P, _P, _Z, _P]),
     "d3d_spec_verify_workspace_size": (_Z, [_I, _I, _I]),
-    "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "d3d_packed_draft_attn_ctas": (_I, [_I, _I, _I, _I, _I, _I]),
+    "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _Z, _I, _P]),
     "d3d_branch_match": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "d3d_debug_inject_fault": (None, [_I]),
     "d3d_spec_verify_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P]),
@@ -157,6 +159,14 @@ def d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix) -> in
     return int(lib.d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix))
 
 
+def d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix) -> int:
+    """CTAs (one SM each) the attention launch uses on the current device."""
+    n = int(lib.d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix))
+    if n < 0:
+        _check("d3d_packed_draft_attn_ctas", n)
+    return n
+
+
 def d3d_packed_draft_attn(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q, cu_seg,
                           max_q: int, max_prefix: int, scale: float, out, ws, stream=None) -> None:
     """Packed drafting attention; shapes as in include/d3d.h (bf16 tensors, int32 tables)."""
@@ -188,7 +198,7 @@ def d3d_spec_verify_workspace_size(R, B, V) -> int:
 
 def d3d_spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature: float,
                     accept_len, out_tokens, num_tokens, ws, alpha=None, p_draft=None, q_draft=None,
-                    stream=None) -> None:
+                    sm_limit: int = 0, stream=None) -> None:
     """Speculative-sampling verification; logits f32 or bf16 [R,B,V] / [R,B-1,V]."""
     if target_logits.dtype == torch.bfloat16:
         dt = D3D_DTYPE_BF16
@@ -220,7 +230,7 @@ def d3d_spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sampl
     rc = lib.d3d_spec_verify(
         _ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), R, B, V,
         float(temperature), _ptr(accept_len), _ptr(out_tokens), _ptr(num_tokens), _ptr(alpha), _ptr(p_draft),
-        _ptr(q_draft), _ptr(ws), ws.numel(), _stream(stream))
+        _ptr(q_draft), _ptr(ws), ws.numel(), int(sm_limit), _stream(stream))
     _check("d3d_spec_verify", rc)
 
 

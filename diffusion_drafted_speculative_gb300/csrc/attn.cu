@@ -932,6 +932,21 @@ size_t d3d_packed_draft_attn_workspace_size(int R, int Hq, int Hkv, int d, int m
     return sizeof(d3d::WsHeader);  // the status word: the split combine needs no global scratch
 }
 
+int d3d_packed_draft_attn_ctas(int R, int Hq, int Hkv, int d, int max_q, int max_prefix)
+{
+    if (R < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_q < 0 || max_prefix < 0)
+        return D3D_ERR_INVALID_ARG;
+    if (d != 64 && d != 128)
+        return D3D_ERR_UNSUPPORTED;
+    if (d3d::kBM % (Hq / Hkv) != 0 || max_q > d3d::kMaxPackedTiles * d3d::kBN)
+        return D3D_ERR_UNSUPPORTED;
+    if (R == 0 || max_q == 0)
+        return 0;
+    const d3d::AttnPlan pl = d == 64 ? d3d::make_plan<64>(R, Hq, Hkv, max_q, max_prefix)
+                                     : d3d::make_plan<128>(R, Hq, Hkv, max_q, max_prefix);
+    return pl.units > 0x7fffffffLL ? D3D_ERR_UNSUPPORTED : (int)pl.units;
+}
+
 void d3d_debug_inject_fault(int mode) { d3d::g_fault_mode = mode; }
 
 int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_prefix, const void *k_packed,

@@ -35,14 +35,20 @@
 namespace d3d {
 namespace {
 
-constexpr int kVThreads = 256;
-constexpr int kVWarps = kVThreads / 32;
-constexpr int kVChunk = 8192;
-constexpr int kVPer = kVChunk / kVThreads;  // 32 logits per thread and row
-constexpr int kVGroup = kVThreads * 8;      // positions covered by one 8-wide slot group
+constexpr int kVPer = 32;  // logits per thread and row of an item
+// Thread count NT of a CTA: 256 for a launch over the whole device (two CTAs
+// per SM), 512 when the launch is limited to some SMs (one CTA fills an SM).
+// A chunk is NT * 32 vocabulary entries.
+template <int NT> struct VCfg {
+    static constexpr int kWarps = NT / 32;
+    static constexpr int kChunk = NT * kVPer;
+    static constexpr int kGroup = NT * 8;  // positions covered by one 8-wide slot group
+};
+constexpr int kNTDevice = 256;
+constexpr int kNTLimited = 512;
+constexpr int kVChunkMin = kNTDevice * kVPer;  // the workspace is sized for the smaller chunk
 constexpr int kMaxB = 256;
-constexpr int kMaxChunks = 1024;  // vocabulary up to 8M entries
-constexpr int kVBlocksPerSm = 2;
+constexpr int kMaxChunks = 1024;  // vocabulary up to 8M entries (in the smaller chunks)
 constexpr uint64_t kBarrierTimeoutNs = 250ull * 1000ull * 1000ull;
 constexpr int kStagedRecords = 1024;  // item records staged in shared memory (32 KB)
 constexpr unsigned kFull = 0xffffffffu;
@@ -72,10 +78,10 @@ struct VerifyLayout {
 // wait, phase-C items done, phase-D items done.
 constexpr int kBarInts = 4;
 
-__host__ __device__ inline VerifyLayout verify_layout(int R, int B, int V)
+__host__ __device__ inline VerifyLayout verify_layout(int R, int B, int V, int chunk)
 {
     VerifyLayout L;
-    L.nch = (V + kVChunk - 1) / kVChunk;
+    L.nch = (V + chunk - 1) / chunk;
     size_t o = sizeof(WsHeader);
     L.bar = o;
     o = align_up(o + kBarInts * sizeof(int) * (size_t)R, kWsAlign);
@@ -115,20 +121,24 @@ template <> struct Logit<uint16_t> {
 template <typename T> __device__ inline bool aligned16(const T *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 // Vocabulary position of slot i (0..kVPer) of this thread in chunk v0: slot
-// 8g+e holds v0 + g*kVGroup + 8*tid + e, so each 8-slot group is one
+// 8g+e holds v0 + g*(8 NT) + 8*tid + e, so each 8-slot group is one
 // coalesced 16-byte load per thread.
-__device__ __forceinline__ int slot_pos(int v0, int i) { return v0 + (i >> 3) * kVGroup + (int)threadIdx.x * 8 + (i & 7); }
+template <int NT>
+__device__ __forceinline__ int slot_pos(int v0, int i)
+{
+    return v0 + (i >> 3) * VCfg<NT>::kGroup + (int)threadIdx.x * 8 + (i & 7);
+}
 
 // Scaled logits x*c of one chunk [v0, v1) in slot order; positions past v1
 // read as -inf.
-template <typename T>
+template <typename T, int NT>
 __device__ inline void load_chunk(const T *row, int v0, int v1, float c, float (&x)[kVPer])
 {
-    if (v1 - v0 == kVChunk && aligned16(row + v0)) {
+    if (v1 - v0 == VCfg<NT>::kChunk && aligned16(row + v0)) {
 #pragma unroll
         for (int g = 0; g < kVPer / 8; ++g) {
             float t[8];
-            Logit<T>::load8(row + slot_pos(v0, 8 * g), t);
+            Logit<T>::load8(row + slot_pos<NT>(v0, 8 * g), t);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 x[8 * g + e] = t[e] * c;
@@ -136,7 +146,7 @@ __device__ inline void load_chunk(const T *row, int v0, int v1, float c, float (
     } else {
 #pragma unroll
         for (int i = 0; i < kVPer; ++i) {
-            const int v = slot_pos(v0, i);
+            const int v = slot_pos<NT>(v0, i);
             x[i] = v < v1 ? Logit<T>::at(row, v) * c : -INFINITY;
         }
     }
@@ -182,6 +192,7 @@ __device__ inline void thread_exp(float (&x)[kVPer], float &m, float &z)
 }
 
 // Block-wide merge of two (max, sum) pairs; the result is valid in thread 0.
+template <int NT>
 __device__ inline void block_ms2(float &m1, float &z1, float &m2, float &z2, float *red)
 {
 #pragma unroll
@@ -201,7 +212,7 @@ __device__ inline void block_ms2(float &m1, float &z1, float &m2, float &z2, flo
     __syncthreads();
     if (threadIdx.x == 0) {
         m1 = red[0], z1 = red[1], m2 = red[2], z2 = red[3];
-        for (int i = 1; i < kVWarps; ++i) {
+        for (int i = 1; i < VCfg<NT>::kWarps; ++i) {
             ms_merge(m1, z1, red[4 * i + 0], red[4 * i + 1]);
             ms_merge(m2, z2, red[4 * i + 2], red[4 * i + 3]);
         }
@@ -209,6 +220,7 @@ __device__ inline void block_ms2(float &m1, float &z1, float &m2, float &z2, flo
 }
 
 // Block-wide sums of two values; the result is valid in thread 0.
+template <int NT>
 __device__ inline void block_sum2(float &a, float &b, float *red)
 {
 #pragma unroll
@@ -225,7 +237,7 @@ __device__ inline void block_sum2(float &a, float &b, float *red)
     if (threadIdx.x == 0) {
         a = red[0];
         b = red[1];
-        for (int i = 1; i < kVWarps; ++i) {
+        for (int i = 1; i < VCfg<NT>::kWarps; ++i) {
             a += red[2 * i];
             b += red[2 * i + 1];
         }
@@ -234,6 +246,7 @@ __device__ inline void block_sum2(float &a, float &b, float *red)
 
 // Block-wide exclusive scan of the four per-thread group sums g[0..3] in
 // vocabulary order (group-major, then thread): returns each group's prefix.
+template <int NT>
 __device__ inline float4 block_group_scan(float4 g, float *red)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -253,7 +266,7 @@ __device__ inline float4 block_group_scan(float4 g, float *red)
     }
     __syncthreads();
     float tot[4] = {0.f, 0.f, 0.f, 0.f}, before[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = 0; i < kVWarps; ++i) {
+    for (int i = 0; i < VCfg<NT>::kWarps; ++i) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float t = red[4 * i + q];
@@ -315,11 +328,12 @@ __device__ inline void signal_count(int *cnt)
 // Draft tokens, acceptance uniforms and the sample uniform of request r into
 // shared memory (issued before the selection's wait, which they do not
 // depend on).
+template <int NT>
 __device__ inline void load_request_inputs(int r, int B, const int32_t *__restrict__ y,
                                            const float *__restrict__ u_acc, const float *__restrict__ u_s,
                                            int32_t *s_y, float *s_u, float *s_us)
 {
-    for (int jj = threadIdx.x; jj < B - 1; jj += kVThreads) {
+    for (int jj = threadIdx.x; jj < B - 1; jj += NT) {
         s_y[jj] = __ldg(y + (size_t)r * (B - 1) + jj);
         s_u[jj] = __ldg(u_acc + (size_t)r * (B - 1) + jj);
     }
@@ -331,6 +345,7 @@ __device__ inline void load_request_inputs(int r, int B, const int32_t *__restri
 // the sample's row pair.  s_y / s_u hold the request's draft tokens and
 // uniforms.  With write_outputs the CTA also writes accept_len, num_tokens,
 // alpha/p/q and the accepted tokens.
+template <int NT>
 __device__ void select_request(int r, int B, int V, int nch, const Rec *__restrict__ rec,
                                const int32_t *s_y, const float *s_u, bool write_outputs,
                                int32_t *__restrict__ accept_len, int32_t *__restrict__ out_tokens,
@@ -347,7 +362,7 @@ __device__ void select_request(int r, int B, int V, int nch, const Rec *__restri
     if (staged) {
         const float4 *src = reinterpret_cast<const float4 *>(pr);
         float4 *dst = reinterpret_cast<float4 *>(s_rec);
-        for (int i = threadIdx.x; i < 2 * nrec; i += kVThreads)
+        for (int i = threadIdx.x; i < 2 * nrec; i += NT)
             dst[i] = __ldcg(src + i);
     }
     if (threadIdx.x == 0)
@@ -363,7 +378,7 @@ __device__ void select_request(int r, int B, int V, int nch, const Rec *__restri
     };
     // one warp per position: the row statistics over the chunk records, then
     // p_j, q_j, alpha_j and the acceptance test
-    for (int jj = warp; jj < B; jj += kVWarps) {
+    for (int jj = warp; jj < B; jj += VCfg<NT>::kWarps) {
         float mp = -INFINITY, zp = 0.f, mq = -INFINITY, zq = 0.f;
         for (int cc = lane; cc < nch; cc += 32) {
             const Rec t = rec_at(jj * nch + cc);
@@ -392,7 +407,7 @@ __device__ void select_request(int r, int B, int V, int nch, const Rec *__restri
                     if (write_outputs)
                         record_status(status, D3D_ERR_DEVICE_INPUT);
                 } else {
-                    const Rec t = rec_at(jj * nch + yv / kVChunk);
+                    const Rec t = rec_at(jj * nch + yv / VCfg<NT>::kChunk);
                     p = fast_exp2(t.xP - MP) / sp;
                     q = fast_exp2(t.xQ - MQ) / sq;
                     al = (p >= q) ? 1.f : p / q;
@@ -425,7 +440,7 @@ __device__ void select_request(int r, int B, int V, int nch, const Rec *__restri
             accept_len[r] = a;
             num_tokens[r] = a + 1;
         }
-        for (int jj = threadIdx.x; jj < B; jj += kVThreads)
+        for (int jj = threadIdx.x; jj < B; jj += NT)
             if (jj != a)
                 out_tokens[(size_t)r * B + jj] = (jj < a) ? s_y[jj] : -1;
     }
@@ -435,14 +450,14 @@ __device__ void select_request(int r, int B, int V, int nch, const Rec *__restri
 // Per-slot masses w of the sampled distribution in chunk [c0, c1): the
 // residual max(0, P - Q) (kind 0) or P (kind 1), reloading the chunk; and
 // the sums of w and of P.
-template <typename T>
+template <typename T, int NT>
 __device__ inline void chunk_masses(const T *prow, const T *qrow, int kind, int c0, int c1, float c,
                                     const Sel &sel, float (&w)[kVPer], float &s_kind, float &s_p)
 {
     float xp[kVPer];
-    load_chunk<T>(prow, c0, c1, c, xp);
+    load_chunk<T, NT>(prow, c0, c1, c, xp);
     if (kind == 0)
-        load_chunk<T>(qrow, c0, c1, c, w);
+        load_chunk<T, NT>(qrow, c0, c1, c, w);
     s_kind = 0.f;
     s_p = 0.f;
 #pragma unroll
@@ -475,6 +490,7 @@ __device__ inline void kept_masses(int kind, const float (&eP)[kVPer], float (&e
 // Phase D of request r in the chunk [c0, c1) that holds the crossing: the
 // ordered scan of the slot masses w (slot order is group-major vocabulary
 // order); writes the sampled token.
+template <int NT>
 __device__ void scan_owner(const float (&w)[kVPer], int c0, float prefix, float target, bool takelast,
                            int32_t *out_tok, float *red)
 {
@@ -493,23 +509,23 @@ __device__ void scan_owner(const float (&w)[kVPer], int c0, float prefix, float 
         else if (q == 2) g.z += w[i];
         else g.w += w[i];
         if (w[i] > 0.f)
-            lastpos = max(lastpos, slot_pos(c0, i));
+            lastpos = max(lastpos, slot_pos<NT>(c0, i));
     }
-    const float4 ex = block_group_scan(g, red);  // has a __syncthreads (s_cand initialised)
+    const float4 ex = block_group_scan<NT>(g, red);  // has a __syncthreads (s_cand initialised)
     const float gs[4] = {g.x, g.y, g.z, g.w}, bs[4] = {ex.x, ex.y, ex.z, ex.w};
     if (!takelast) {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
             if (prefix + bs[q] + gs[q] > target) {
-                atomicMin(&s_cand, q * kVThreads + (int)threadIdx.x);
+                atomicMin(&s_cand, q * NT + (int)threadIdx.x);
                 break;
             }
     }
     atomicMax(&s_lastpos, lastpos);
     __syncthreads();
     const int cand = s_cand;
-    if (!takelast && cand != 0x7fffffff && (cand % kVThreads) == (int)threadIdx.x) {
-        const int q = cand / kVThreads;
+    if (!takelast && cand != 0x7fffffff && (cand % NT) == (int)threadIdx.x) {
+        const int q = cand / NT;
         int tok = -1, last = -1;
         float cum = prefix + bs[q];
 #pragma unroll
@@ -517,9 +533,9 @@ __device__ void scan_owner(const float (&w)[kVPer], int c0, float prefix, float 
             if ((i >> 3) == q && tok < 0) {
                 cum += w[i];
                 if (w[i] > 0.f)
-                    last = slot_pos(c0, i);
+                    last = slot_pos<NT>(c0, i);
                 if (cum > target)
-                    tok = slot_pos(c0, i);
+                    tok = slot_pos<NT>(c0, i);
             }
         }
         // rounding between the two summation orders: the group's last position with mass
@@ -532,8 +548,8 @@ __device__ void scan_owner(const float (&w)[kVPer], int c0, float prefix, float 
     __syncthreads();
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT, NT == kNTDevice ? 2 : 1)
     verify_kernel(const T *__restrict__ target, const T *__restrict__ draft, const int32_t *__restrict__ y,
                   const float *__restrict__ u_acc, const float *__restrict__ u_s, int R, int B, int V, float c,
                   int32_t *__restrict__ accept_len, int32_t *__restrict__ out_tokens,
@@ -541,11 +557,12 @@ __global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
                   float *__restrict__ q_out, unsigned char *__restrict__ ws)
 {
     extern __shared__ float4 s_dyn[];  // request records when staged; chunk sums in phase D
-    __shared__ float red[4 * kVWarps];
+    using C = VCfg<NT>;
+    __shared__ float red[4 * C::kWarps];
     __shared__ float s_xy[2];
     __shared__ int32_t s_y[kMaxB];
     __shared__ float s_u[kMaxB], s_us;
-    const VerifyLayout L = verify_layout(R, B, V);
+    const VerifyLayout L = verify_layout(R, B, V, C::kChunk);
     const int nch = L.nch;
     const long long nA = (long long)R * B * nch;
     const int nC = R * nch;
@@ -564,11 +581,11 @@ __global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
         const int chunk = (int)(item % nch);
         const int rj = (int)(item / nch);
         const int r = rj / B, j = rj % B;
-        const int v0 = chunk * kVChunk, v1 = min(V, v0 + kVChunk);
+        const int v0 = chunk * C::kChunk, v1 = min(V, v0 + C::kChunk);
         const int yv = (j < B - 1) ? __ldg(y + (size_t)r * (B - 1) + j) : -1;
-        load_chunk<T>(target + ((size_t)r * B + j) * V, v0, v1, c, eP);
+        load_chunk<T, NT>(target + ((size_t)r * B + j) * V, v0, v1, c, eP);
         if (j < B - 1) {
-            load_chunk<T>(draft + ((size_t)r * (B - 1) + j) * V, v0, v1, c, eQ);
+            load_chunk<T, NT>(draft + ((size_t)r * (B - 1) + j) * V, v0, v1, c, eQ);
         } else {
 #pragma unroll
             for (int i = 0; i < kVPer; ++i)
@@ -576,8 +593,8 @@ __global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
         }
         if (yv >= v0 && yv < v1) {  // the thread holding position y keeps both logits for the record
             const int rel = yv - v0;
-            if ((int)threadIdx.x == (rel % kVGroup) / 8) {
-                const int slot = (rel / kVGroup) * 8 + rel % 8;
+            if ((int)threadIdx.x == (rel % C::kGroup) / 8) {
+                const int slot = (rel / C::kGroup) * 8 + rel % 8;
                 float xp = 0.f, xq = 0.f;
 #pragma unroll
                 for (int i = 0; i < kVPer; ++i) {
@@ -592,7 +609,7 @@ __global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
         thread_exp(eP, mtP, zP);
         thread_exp(eQ, mtQ, zQ);
         float m1 = mtP, z1 = zP, m2 = mtQ, z2 = zQ;
-        block_ms2(m1, z1, m2, z2, red);  // has a __syncthreads: s_xy is visible to thread 0 after it
+        block_ms2<NT>(m1, z1, m2, z2, red);  // has a __syncthreads: s_xy is visible to thread 0 after it
         if (threadIdx.x == 0) {
             const bool has = yv >= v0 && yv < v1;
             float4 *dst = reinterpret_cast<float4 *>(rec + item);
@@ -609,7 +626,7 @@ __global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
     // everyone reads the shared results after the call).
     auto decide = [&](int r, const Sel &sel) {
         float2 *s_sums = reinterpret_cast<float2 *>(s_dyn);  // the records are no longer needed
-        for (int cc = threadIdx.x; cc < nch; cc += kVThreads)
+        for (int cc = threadIdx.x; cc < nch; cc += NT)
             s_sums[cc] = __ldcg(part2 + (size_t)r * nch + cc);
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -672,19 +689,19 @@ __global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
         const int item = blockIdx.x;
         const int chunk = item % nch, rj = item / nch;
         const int r = rj / B, j = rj % B;
-        load_request_inputs(r, B, y, u_acc, u_s, s_y, s_u, &s_us);
+        load_request_inputs<NT>(r, B, y, u_acc, u_s, s_y, s_u, &s_us);
         if (!wait_count(bar + kBarInts * r, B * nch, status))
             return;
-        select_request(r, B, V, nch, rec, s_y, s_u, j == 0 && chunk == 0, accept_len, out_tokens, num_tokens,
+        select_request<NT>(r, B, V, nch, rec, s_y, s_u, j == 0 && chunk == 0, accept_len, out_tokens, num_tokens,
                        alpha_out, p_out, q_out, status, sel, s_rec);
         if (j != sel.row) {
             passed_a(r, B * nch);  // counted once the CTA's work is done: off the critical path
             return;
         }
-        const int c0 = chunk * kVChunk;
+        const int c0 = chunk * C::kChunk;
         float s_kind, s_p;
         kept_masses(sel.mode == 0 ? 0 : 1, eP, eQ, mtP, mtQ, sel, s_kind, s_p);  // eQ now holds the masses
-        block_sum2(s_kind, s_p, red);
+        block_sum2<NT>(s_kind, s_p, red);
         if (threadIdx.x == 0) {
             part2[(size_t)r * nch + chunk] = make_float2(s_kind, s_p);
             signal_count(bar + kBarInts * r + 2);
@@ -697,7 +714,7 @@ __global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
                 float a1, a2;
                 kept_masses(1, eP, eQ, mtP, mtQ, sel, a1, a2);
             }
-            scan_owner(eQ, c0, s_prefix, s_target, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
+            scan_owner<NT>(eQ, c0, s_prefix, s_target, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
         } else if (s_owner < 0 && chunk == 0 && threadIdx.x == 0) {
             // no mass anywhere: cannot happen for a finite softmax row
             record_status(status, D3D_ERR_DEVICE_INPUT);
@@ -713,18 +730,18 @@ __global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
     float w[kVPer];
     for (int item = blockIdx.x; item < nC; item += gridDim.x) {
         const int r = item / nch, chunk = item % nch;
-        load_request_inputs(r, B, y, u_acc, u_s, s_y, s_u, &s_us);
+        load_request_inputs<NT>(r, B, y, u_acc, u_s, s_y, s_u, &s_us);
         if (!wait_count(bar + kBarInts * r, B * nch, status))
             return;
         passed_a(r, nch);
-        select_request(r, B, V, nch, rec, s_y, s_u, chunk == 0, accept_len, out_tokens, num_tokens, alpha_out,
+        select_request<NT>(r, B, V, nch, rec, s_y, s_u, chunk == 0, accept_len, out_tokens, num_tokens, alpha_out,
                        p_out, q_out, status, sel, s_rec);
         const T *prow = target + ((size_t)r * B + sel.row) * V;
         const T *qrow = draft + ((size_t)r * (B - 1) + (sel.mode == 0 ? sel.row : 0)) * V;
-        const int c0 = chunk * kVChunk, c1 = min(V, c0 + kVChunk);
+        const int c0 = chunk * C::kChunk, c1 = min(V, c0 + C::kChunk);
         float s_kind, s_p;
-        chunk_masses<T>(prow, qrow, sel.mode == 0 ? 0 : 1, c0, c1, c, sel, w, s_kind, s_p);
-        block_sum2(s_kind, s_p, red);
+        chunk_masses<T, NT>(prow, qrow, sel.mode == 0 ? 0 : 1, c0, c1, c, sel, w, s_kind, s_p);
+        block_sum2<NT>(s_kind, s_p, red);
         if (threadIdx.x == 0) {
             part2[item] = make_float2(s_kind, s_p);
             signal_count(bar + kBarInts * r + 2);
@@ -735,20 +752,20 @@ __global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
     // ---- phase D: the chunk holding the crossing reloads its masses and scans
     for (int item = blockIdx.x; item < nC; item += gridDim.x) {
         const int r = item / nch, chunk = item % nch;
-        load_request_inputs(r, B, y, u_acc, u_s, s_y, s_u, &s_us);
+        load_request_inputs<NT>(r, B, y, u_acc, u_s, s_y, s_u, &s_us);
         if (!wait_count(bar + kBarInts * r + 2, nch, status))
             return;
         // every phase-C item of r waited for r's phase A, so the records are complete
-        select_request(r, B, V, nch, rec, s_y, s_u, false, accept_len, out_tokens, num_tokens, alpha_out, p_out,
+        select_request<NT>(r, B, V, nch, rec, s_y, s_u, false, accept_len, out_tokens, num_tokens, alpha_out, p_out,
                        q_out, status, sel, s_rec);
         decide(r, sel);
         if (s_owner == chunk) {
-            const int c0 = chunk * kVChunk, c1 = min(V, c0 + kVChunk);
+            const int c0 = chunk * C::kChunk, c1 = min(V, c0 + C::kChunk);
             const T *prow = target + ((size_t)r * B + sel.row) * V;
             const T *qrow = draft + ((size_t)r * (B - 1) + (sel.mode == 0 ? sel.row : 0)) * V;
             float a1, a2;
-            chunk_masses<T>(prow, qrow, s_kind_used, c0, c1, c, sel, w, a1, a2);
-            scan_owner(w, c0, s_prefix, s_target, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
+            chunk_masses<T, NT>(prow, qrow, s_kind_used, c0, c1, c, sel, w, a1, a2);
+            scan_owner<NT>(w, c0, s_prefix, s_target, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
         } else if (s_owner < 0 && chunk == 0 && threadIdx.x == 0) {
             record_status(status, D3D_ERR_DEVICE_INPUT);
             out_tokens[(size_t)r * B + sel.a] = 0;
@@ -758,12 +775,12 @@ __global__ void __launch_bounds__(kVThreads, kVBlocksPerSm)
     }
 }
 
-template <typename T>
-int launch_verify(const void *target, const void *draft, const int32_t *y, const float *u_acc, const float *u_s,
-                  int R, int B, int V, float c, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
-                  float *alpha, float *p, float *q, unsigned char *ws, cudaStream_t stream)
+template <typename T, int NT>
+int launch_verify_nt(const void *target, const void *draft, const int32_t *y, const float *u_acc, const float *u_s,
+                     int R, int B, int V, float c, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
+                     float *alpha, float *p, float *q, unsigned char *ws, int sm_limit, cudaStream_t stream)
 {
-    const VerifyLayout L = verify_layout(R, B, V);
+    const VerifyLayout L = verify_layout(R, B, V, VCfg<NT>::kChunk);
     const long long nA = (long long)R * B * L.nch;
     if (nA > 0x7fffffffLL)
         return D3D_ERR_UNSUPPORTED;
@@ -774,18 +791,20 @@ int launch_verify(const void *target, const void *draft, const int32_t *y, const
     if (dyn < sizeof(float2) * (size_t)L.nch)
         dyn = sizeof(float2) * (size_t)L.nch;
     // every CTA must be resident (CTAs wait on one another): at most the
-    // occupancy limit, and no more than there are phase-A items
+    // occupancy limit (and the SM limit), and no more than there are phase-A items
     int dev = 0, nsm = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<T>, kVThreads, dyn) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<T, NT>, NT, dyn) != cudaSuccess ||
         per_sm < 1)
         return D3D_ERR_CUDA;
-    const long long cap = (long long)nsm * per_sm;
+    long long cap = (long long)nsm * per_sm;
+    if (sm_limit > 0 && (long long)sm_limit * per_sm < cap)
+        cap = (long long)sm_limit * per_sm;
     const unsigned grid = (unsigned)(nA < cap ? nA : cap);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kVThreads);
+    cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = dyn;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -793,10 +812,24 @@ int launch_verify(const void *target, const void *draft, const int32_t *y, const
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, verify_kernel<T>, static_cast<const T *>(target),
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, verify_kernel<T, NT>, static_cast<const T *>(target),
                                              static_cast<const T *>(draft), y, u_acc, u_s, R, B, V, c, accept_len,
                                              out_tokens, num_tokens, alpha, p, q, ws);
     return cuda_status(e);
+}
+
+// With an SM limit the CTAs are 512 threads, one per SM (the register file
+// holds one): a launch beside another kernel takes at most sm_limit SMs.
+template <typename T>
+int launch_verify(const void *target, const void *draft, const int32_t *y, const float *u_acc, const float *u_s,
+                  int R, int B, int V, float c, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
+                  float *alpha, float *p, float *q, unsigned char *ws, int sm_limit, cudaStream_t stream)
+{
+    if (sm_limit > 0)
+        return launch_verify_nt<T, kNTLimited>(target, draft, y, u_acc, u_s, R, B, V, c, accept_len, out_tokens,
+                                               num_tokens, alpha, p, q, ws, sm_limit, stream);
+    return launch_verify_nt<T, kNTDevice>(target, draft, y, u_acc, u_s, R, B, V, c, accept_len, out_tokens,
+                                          num_tokens, alpha, p, q, ws, 0, stream);
 }
 
 }  // namespace
@@ -806,38 +839,40 @@ extern "C" {
 
 size_t d3d_spec_verify_workspace_size(int R, int B, int V)
 {
-    if (R < 0 || B < 2 || V < 1 || B > d3d::kMaxB || V > d3d::kMaxChunks * d3d::kVChunk)
+    if (R < 0 || B < 2 || V < 1 || B > d3d::kMaxB || V > d3d::kMaxChunks * d3d::kVChunkMin)
         return 0;
-    return d3d::verify_layout(R, B, V).total;
+    // the smaller chunk has the most records: the workspace fits both launches
+    return d3d::verify_layout(R, B, V, d3d::kVChunkMin).total;
 }
 
 int d3d_spec_verify(const void *target_logits, const void *draft_logits, int logits_dtype,
                     const int32_t *draft_tokens, const float *u_accept, const float *u_sample, int R, int B,
                     int V, float temperature, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
-                    float *alpha, float *p_draft, float *q_draft, void *ws, size_t ws_bytes,
+                    float *alpha, float *p_draft, float *q_draft, void *ws, size_t ws_bytes, int sm_limit,
                     cudaStream_t stream)
 {
-    if (R < 0 || B < 2 || V < 1 || !(temperature > 0.f) || !isfinite(temperature))
+    if (R < 0 || B < 2 || V < 1 || !(temperature > 0.f) || !isfinite(temperature) || sm_limit < 0)
         return D3D_ERR_INVALID_ARG;
     if (logits_dtype != D3D_DTYPE_F32 && logits_dtype != D3D_DTYPE_BF16)
         return D3D_ERR_INVALID_ARG;
-    if (B > d3d::kMaxB || V > d3d::kMaxChunks * d3d::kVChunk)
+    if (B > d3d::kMaxB || V > d3d::kMaxChunks * d3d::kVChunkMin)
         return D3D_ERR_UNSUPPORTED;
     if (R == 0)
         return D3D_OK;
     if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_sample || !accept_len ||
         !out_tokens || !num_tokens)
         return D3D_ERR_INVALID_ARG;
-    if (!d3d::ws_ok(ws, ws_bytes, d3d::verify_layout(R, B, V).total))
+    if (!d3d::ws_ok(ws, ws_bytes, d3d::verify_layout(R, B, V, d3d::kVChunkMin).total))
         return D3D_ERR_WORKSPACE;
     const float c = (float)(1.4426950408889634 / (double)temperature);  // log2(e) / T
     unsigned char *w = static_cast<unsigned char *>(ws);
     if (logits_dtype == D3D_DTYPE_BF16)
         return d3d::launch_verify<uint16_t>(target_logits, draft_logits, draft_tokens, u_accept, u_sample, R, B, V,
                                             c, accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w,
-                                            stream);
+                                            sm_limit, stream);
     return d3d::launch_verify<float>(target_logits, draft_logits, draft_tokens, u_accept, u_sample, R, B, V, c,
-                                     accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w, stream);
+                                     accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w, sm_limit,
+                                     stream);
 }
 
 }  // extern "C"
@@ -905,14 +940,14 @@ extern "C" int d3d_spec_verify_noalloc(const void *target_logits, const void *dr
         return D3D_ERR_INVALID_ARG;
     if (logits_dtype != D3D_DTYPE_F32 && logits_dtype != D3D_DTYPE_BF16)
         return D3D_ERR_INVALID_ARG;
-    if (B > d3d::kMaxB || V > d3d::kMaxChunks * d3d::kVChunk)
+    if (B > d3d::kMaxB || V > d3d::kMaxChunks * d3d::kVChunkMin)
         return D3D_ERR_UNSUPPORTED;
     if (R == 0)
         return D3D_OK;
     if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_sample || !accept_len ||
         !out_tokens || !num_tokens)
         return D3D_ERR_INVALID_ARG;
-    const d3d::VerifyLayout L = d3d::verify_layout(R, B, V);
+    const d3d::VerifyLayout L = d3d::verify_layout(R, B, V, d3d::kVChunkMin);
     if (L.total > d3d::kNoAllocScratchBytes)
         return D3D_ERR_UNSUPPORTED;  // needs more scratch than the fixed array holds
     void *scratch = nullptr;
@@ -927,8 +962,8 @@ extern "C" int d3d_spec_verify_noalloc(const void *target_logits, const void *dr
     unsigned char *w = static_cast<unsigned char *>(scratch);
     if (logits_dtype == D3D_DTYPE_BF16)
         return d3d::launch_verify<uint16_t>(target_logits, draft_logits, draft_tokens, u_accept, u_sample, R, B, V,
-                                            c, accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w,
+                                            c, accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w, 0,
                                             stream);
     return d3d::launch_verify<float>(target_logits, draft_logits, draft_tokens, u_accept, u_sample, R, B, V, c,
-                                     accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w, stream);
+                                     accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w, 0, stream);
 }

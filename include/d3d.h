@@ -143,6 +143,15 @@ int d3d_validate_segments(const d3d_segment_t *segs, const int32_t *cu_q, const 
  * ======================================================================== */
 size_t d3d_packed_draft_attn_workspace_size(int R, int Hq, int Hkv, int d, int max_q, int max_prefix);
 
+/* Number of CTAs the d3d_packed_draft_attn launch for these sizes uses on the
+ * current device; each holds one SM from its start to its end (they all fit
+ * in one wave when the count is at most the SM count).  A caller that runs
+ * another kernel beside the attention can give it the remaining SMs (see
+ * d3d_spec_verify's sm_limit).  Returns the count, or a negative status for
+ * arguments d3d_packed_draft_attn would reject (D3D_ERR_INVALID_ARG,
+ * D3D_ERR_UNSUPPORTED); 0 when there is nothing to compute. */
+int d3d_packed_draft_attn_ctas(int R, int Hq, int Hkv, int d, int max_q, int max_prefix);
+
 int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_prefix, const void *k_packed,
                           const void *v_packed, const d3d_segment_t *segs, const int32_t *cu_prefix,
                           const int32_t *cu_q, const int32_t *cu_seg, int R, int Hq, int Hkv, int d,
@@ -191,6 +200,11 @@ void d3d_debug_inject_fault(int mode);
  *   alpha, p_draft, q_draft [R, B-1] float32 outputs, each may be NULL
  *               (p_draft = P_j(y_j), q_draft = Q_j(y_j))
  *   ws          workspace, d3d_spec_verify_workspace_size() bytes
+ *   sm_limit    0: the kernel may use every SM.  n > 0: at most n CTAs, each
+ *               holding a whole SM, so that a kernel launched beside it on
+ *               another stream (the drafting attention of the same round)
+ *               keeps the remaining SMs whichever starts first.  Results do
+ *               not depend on it.  Negative: D3D_ERR_INVALID_ARG.
  * A draft token outside [0, V) sets D3D_ERR_DEVICE_INPUT in the status word
  * and is treated as rejected (alpha = 0).
  * ======================================================================== */
@@ -199,7 +213,7 @@ size_t d3d_spec_verify_workspace_size(int R, int B, int V);
 int d3d_spec_verify(const void *target_logits, const void *draft_logits, int logits_dtype,
                     const int32_t *draft_tokens, const float *u_accept, const float *u_sample, int R, int B,
                     int V, float temperature, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
-                    float *alpha, float *p_draft, float *q_draft, void *ws, size_t ws_bytes,
+                    float *alpha, float *p_draft, float *q_draft, void *ws, size_t ws_bytes, int sm_limit,
                     cudaStream_t stream);
 
 /*

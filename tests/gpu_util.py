@@ -42,7 +42,7 @@ def assert_attn_close(got, ref, what=""):
                                                                                                   excess.shape))
 
 
-def run_verify(d3d, v, ws=None, want_probs=True):
+def run_verify(d3d, v, ws=None, want_probs=True, sm_limit=0):
     dev = "cuda"
     R, B = v["R"], v["B"]
     if v["dtype"] == 1:
@@ -57,7 +57,7 @@ def run_verify(d3d, v, ws=None, want_probs=True):
         ws = d3d.new_workspace(d3d.d3d_spec_verify_workspace_size(R, B, v["V"]), dev)
     d3d.d3d_spec_verify(tgt, dr, i32(v["y"]), f32(v["u_accept"]), f32(v["u_sample"]), v.get("temperature", 1.0),
                         out["accept_len"], out["out_tokens"], out["num_tokens"], ws, alpha=probs.get("alpha"),
-                        p_draft=probs.get("p"), q_draft=probs.get("q"))
+                        p_draft=probs.get("p"), q_draft=probs.get("q"), sm_limit=sm_limit)
     torch.cuda.synchronize()
     res = {k: t.cpu().numpy() for k, t in {**out, **probs}.items()}
     return res, ws

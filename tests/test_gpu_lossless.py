@@ -35,8 +35,9 @@ def _chi2_p(tokens, probs):
     return scipy.stats.chisquare(obs[keep], probs[keep] * obs.sum()).pvalue
 
 
-@pytest.mark.parametrize("T,dt", [(1.0, W.DT_F32), (1.0, W.DT_BF16), (0.5, W.DT_F32)])
-def test_gpu_lossless_chi_square(d3d, T, dt):
+@pytest.mark.parametrize("T,dt,sm_limit", [(1.0, W.DT_F32, 0), (1.0, W.DT_BF16, 0), (0.5, W.DT_F32, 0),
+                                            (1.0, W.DT_BF16, 56)])
+def test_gpu_lossless_chi_square(d3d, T, dt, sm_limit):
     V, B, R = 16, 3, 65536
     rng = np.random.default_rng(77)
     x = (rng.standard_normal((B, V)) * 1.5).astype(np.float32)
@@ -58,7 +59,7 @@ def test_gpu_lossless_chi_square(d3d, T, dt):
         v = dict(target=np.ascontiguousarray(tg), draft=np.ascontiguousarray(dr), dtype=dt, y=y,
                  u_accept=np.ascontiguousarray(u[:, : B - 1]), u_sample=np.ascontiguousarray(u[:, B - 1]),
                  R=R, B=B, V=V, temperature=T)
-        got, ws = run_verify(d3d, v, ws=ws, want_probs=False)
+        got, ws = run_verify(d3d, v, ws=ws, want_probs=False, sm_limit=sm_limit)
         first.append(got["out_tokens"][:, 0])
         second.append(got["out_tokens"][got["accept_len"] >= 1, 1])
     first, second = np.concatenate(first), np.concatenate(second)

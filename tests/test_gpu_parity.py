@@ -235,6 +235,31 @@ def test_verify_one_item_per_cta(d3d, R, B, V, dt, sigma):
         assert d3d.d3d_workspace_status(ws) == 0
 
 
+@pytest.mark.parametrize("sm_limit", [1, 7, 56, 151])
+def test_verify_sm_limit_same_results(d3d, sm_limit):
+    # an SM limit changes how the work is spread: 512-thread CTAs over
+    # 16384-entry chunks, one CTA per SM.  Probabilities may differ from the
+    # unlimited launch in the last bit (another summation order); both meet
+    # the oracle under the same tolerances
+    for v in (W.verify_inputs(**W.CONFIGS["async8b"], seed=3),
+              W.verify_inputs(R=40, B=6, V=9000, logits=W.DT_F32, seed=4)):
+        ref = oracle.spec_verify(v)
+        free, ws = run_verify(d3d, v)
+        lim, ws2 = run_verify(d3d, v, sm_limit=sm_limit)
+        compare_verify(free, ref, min_kept=0.0)
+        compare_verify(lim, ref, min_kept=0.0)
+        for k in ("alpha", "p", "q"):
+            np.testing.assert_allclose(lim[k], free[k], rtol=1e-6, atol=1e-30, err_msg=k)
+        assert d3d.d3d_workspace_status(ws2) == 0
+
+
+def test_attention_cta_count_matches_plan(d3d):
+    # one CTA per query tile and key split, all in one wave on this GPU
+    n = d3d.d3d_packed_draft_attn_ctas(1, 32, 8, 128, 384, 2048)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert 0 < n <= sms
+
+
 def test_verify_workspace_reuse_and_many_requests(d3d):
     v = W.verify_inputs(R=4096, B=4, V=64, logits=W.DT_F32, seed=10)
     got1, ws = run_verify(d3d, v)
