@@ -3,38 +3,37 @@
 // [D3D] "Core method", "Method steps" steps 2 and 4; [DScout] "Background:
 // block-diffusion drafter".  See attn_common.cuh for the visibility rule.
 //
-// Work unit (one CTA): request r, KV head hk, one 128-row query tile and one
-// key split.  A query tile's 128 rows are (packed token, query head of hk's
-// group) pairs, token-major, so one K/V tile serves all G query heads of the
-// group.  A unit's key list is every 128-key tile of the request's prefix
+// Work unit (one CTA, which holds one SM): request r, KV head hk, one 128-row
+// query tile and one key split.  A query tile's 128 rows are (packed token,
+// query head of hk's group) pairs, token-major, so one K/V tile serves all G
+// query heads of the group.  A unit's key list is every 128-key tile of the request's prefix
 // followed by the packed-key tiles its rows can see.  Splits cut the prefix
 // tiles; the last split also takes the packed tiles, so every other split
 // knows its tiles without the visibility mask and starts loading at once.
 //
-// Roles (320 threads):
-//   warps 0-3 / 4-7  softmax warpgroup w = 0 / 1: the two warpgroups take the
-//              key tiles of the list alternately (w takes tiles w, w+2, ...),
-//              each with its own S/P and O in TMEM.  Thread i of either
-//              warpgroup owns TMEM lane i = query row i.  Reads S (one
-//              tcgen05.ld of 128 columns), masks it, keeps the running max
-//              (rescaling O in TMEM only when the max grows by more than 2^8)
-//              and the row sum, and writes P as bf16 pairs back over the
-//              first 64 columns of S.
-//   warp 8     TMA producer: the Q tile once, then K and V tiles into two
-//              3-deep rings (3-D tensor maps, 128-byte swizzle).
-//   warp 9     MMA issuer (one thread), owner of TMEM.  Per pair of key tiles
-//              (2i, 2i+1) it issues PV_0(2i), S_0(2i+2), PV_1(2i+1), S_1(2i+3):
-//              O_w += P_w V, with P read from TMEM, and S_w = Q K^T into TMEM.
-//              While one warpgroup computes its softmax the tensor core works
-//              for the other.  S_w(k+2) overwrites P_w(k) only after PV_w(k),
-//              which the tensor core executes first (MMAs of one thread run in
-//              issue order), and the commit that signals S_w(k+2) also
-//              guarantees PV_w(k) is complete, so O_w is stable for the
-//              softmax's rescale.
-// TMEM: warpgroup w uses columns [256w, 256w+128) for S/P and [256w+128, +D)
-// for O_w.  Both warpgroups' O rows sit in the same TMEM lanes, so at the end
-// each thread combines O_0 and O_1 of its row for half of the head dimension
-// (the two (max, sum) pairs are exchanged through shared memory).
+// Roles (320 threads with two softmax warpgroups; the count kWG is a build
+// option, 2 or 4):
+//   warps 0..4kWG-1  softmax warpgroups: warpgroup w takes key columns
+//              [w*128/kWG, (w+1)*128/kWG) of every key tile; thread i of any
+//              warpgroup owns TMEM lane i = query row i.  Per tile: one
+//              tcgen05.ld of its S columns, the mask, its part of the row max,
+//              published in shared memory (mbarrier, bounded wait) to form the
+//              row max, a rescale of its part of O in TMEM only when the max
+//              grows by more than 2^8, the exponentials (arguments and sums in
+//              packed f32x2 arithmetic), its part of the row sum, and P as
+//              bf16 pairs written over the first half of the S buffer.
+//   warp 4kWG  TMA producer: the Q tile once, then K and V tiles into 3- and
+//              2-deep rings (3-D tensor maps, 128-byte swizzle), in the order
+//              the tensor core consumes them.
+//   warp 4kWG+1  MMA issuer (one thread), owner of TMEM.  S(k) = Q K_k^T goes to
+//              TMEM buffer k % 2; once P(k) is written it issues O += P(k) V_k
+//              (P read from TMEM) and S(k+2) into the buffer P(k) came from.
+//              The tensor core thus computes PV(k-1) and S(k+1) while the
+//              softmax works on tile k; MMAs of one thread run in issue order,
+//              so S(k+2) never overwrites P(k) before PV(k) has read it.
+// TMEM: S buffers in columns [0, 128) and [128, 256), O in [256, 256 + D).
+// At the end the parts' row sums add up (every part keeps the same running
+// max) and each thread normalises and stores its D/kWG columns of the row.
 //
 // With S > 1 splits the S CTAs of a query tile run as one thread-block
 // cluster.  Each CTA writes its combined partial (O divided by its row sum,
@@ -61,14 +60,18 @@ using namespace sm100;
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per KV tile
-constexpr int kWG = 2;    // softmax warpgroups: each takes half of every key tile's columns
-constexpr int kHalf = kBN / kWG;  // 64 keys per softmax thread and tile
+#ifndef D3D_ATTN_WG
+#define D3D_ATTN_WG 2
+#endif
+static_assert(D3D_ATTN_WG == 2 || D3D_ATTN_WG == 4, "two or four softmax warpgroups");
+constexpr int kWG = D3D_ATTN_WG;  // softmax warpgroups: each takes 1/kWG of every key tile's columns
+constexpr int kPart = kBN / kWG;  // 32 keys per softmax thread and tile
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 constexpr int kSoftmaxThreads = kWG * 128;
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kTmaWarp = kWG * 4;
+constexpr int kMmaWarp = kTmaWarp + 1;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxPackedTiles = 64;  // packed keys per request <= 8192
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
@@ -101,8 +104,8 @@ template <int D> struct Layout {
     static constexpr uint32_t v = k + kKStages * kKBytes;
     static constexpr uint32_t bars = v + kVStages * kVBytes;
     static constexpr uint32_t misc = bars + B_COUNT * 8;
-    static constexpr uint32_t mx = misc + 64;  // [2 buffers][kWG][kBM] row maxima of a tile's column halves
-    static constexpr uint32_t ml = q;  // per warpgroup and row: (max, sum), over Q after the last MMA
+    static constexpr uint32_t mx = misc + 64;  // [2 buffers][kWG][kBM] row maxima of a tile's column parts
+    static constexpr uint32_t ml = q;  // per warpgroup and row: (max, sum, tiles done), over Q after the last MMA
     static constexpr uint32_t segs = mx + 2 * kWG * kBM * 4;  // staged segment table of the request
     static constexpr uint32_t total = segs + kStagedSegs * sizeof(d3d_segment_t);
     static constexpr uint32_t alloc = total + 1024;  // room to align the base to 1024 bytes
@@ -206,15 +209,15 @@ __device__ __forceinline__ uint4 pack8(const float *a, float sc)
 }
 
 // Split combine of one query row over the S CTAs of the cluster: the
-// (max, sum) of every split and the units of this thread, u = sp + S*(2k+w)
-// (CTA sp takes units u mod S = sp, its two warpgroups alternate), read
-// through distributed shared memory in split order; writes those output units.
+// (max, sum) of every split and the units of this thread, u = sp + S*(kWG*k+w)
+// (CTA sp takes units u mod S = sp, its warpgroups take turns), read through
+// distributed shared memory in split order; writes those output units.
 template <int D, int S>
 __device__ __forceinline__ void cluster_merge(int sp, int w, uint32_t part, uint32_t ml, int row, bool row_valid,
                                               uint16_t *orow)
 {
     constexpr int kUnits = D / 8;
-    constexpr int kMine = (kUnits + 2 * S - 1) / (2 * S);
+    constexpr int kMine = (kUnits + kWG * S - 1) / (kWG * S);
     float ms[S], ls[S];
 #pragma unroll
     for (int s2 = 0; s2 < S; ++s2) {
@@ -240,7 +243,7 @@ __device__ __forceinline__ void cluster_merge(int sp, int w, uint32_t part, uint
     uint4 rem[kMine][S];
 #pragma unroll
     for (int k = 0; k < kMine; ++k) {
-        const int u = sp + S * (2 * k + w);
+        const int u = sp + S * (kWG * k + w);
 #pragma unroll
         for (int s2 = 0; s2 < S; ++s2) {
             rem[k][s2] = make_uint4(0, 0, 0, 0);
@@ -250,7 +253,7 @@ __device__ __forceinline__ void cluster_merge(int sp, int w, uint32_t part, uint
     }
 #pragma unroll
     for (int k = 0; k < kMine; ++k) {
-        const int u = sp + S * (2 * k + w);
+        const int u = sp + S * (kWG * k + w);
         if (u >= kUnits)
             break;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *tmem_slot = misc + 0;
     volatile uint32_t *abort_flag = misc + 1;
     uint32_t *mask = misc + 2;  // 2 words: packed tiles visible to some row of the tile
-    float2 *s_ml = reinterpret_cast<float2 *>(gbase + Lay::ml);  // [kWG][kBM]: max, sum
+    float4 *s_ml = reinterpret_cast<float4 *>(gbase + Lay::ml);  // [kWG][kBM]: max, sum, tiles done
     float *s_mx = reinterpret_cast<float *>(gbase + Lay::mx);     // [2][kWG][kBM]
 
     if (tid == 0) {
@@ -522,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // =================== softmax warpgroups ===================
-        const int w = warp >> 2;  // warpgroup: key columns [64w, 64w + 64) of every tile
+        const int w = warp >> 2;  // warpgroup: key columns [32w, 32w + 32) of every tile
         const int row = tid & 127;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS0 = tmem + lane_off, tO = tmem + 2u * kBN + lane_off;
@@ -565,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive(bar(B_MASK));
 
-        float m_ref = -INFINITY, l = 0.f;  // l: this thread's column half of the row sum
+        float m_ref = -INFINITY, l = 0.f;  // l: this thread's column part of the row sum
         bool aborted = false;
         int n_done = 0;
         for (int k = 0;; ++k) {
@@ -584,41 +587,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            float s[kHalf];
-            tmem_ld64(tS + (uint32_t)(w * kHalf), s);
+            float s[kPart];
+#if D3D_ATTN_WG == 2
+            tmem_ld64(tS + (uint32_t)(w * kPart), s);
+#else
+            tmem_ld32(tS + (uint32_t)(w * kPart), s);
+#endif
             bool pre;
             const int krow = tile_row(k, pre);
             if (pre) {
-                const int valid = b.L - (pb + k) * kBN - w * kHalf;
-                if (valid < kHalf) {
+                const int valid = b.L - (pb + k) * kBN - w * kPart;
+                if (valid < kPart) {
 #pragma unroll
-                    for (int e = 0; e < kHalf; ++e)
+                    for (int e = 0; e < kPart; ++e)
                         if (e >= valid)
                             s[e] = -INFINITY;
                 }
             } else {
-                // this row's visible keys among the 64 as a mask: two half-open
-                // intervals cut into two 32-key words
-                const int kb = krow - b.q0 + w * kHalf;
-                uint32_t wbits[2];
+                // this row's visible keys of the part as a mask: two half-open
+                // intervals cut into 32-key words
+                uint32_t wbits[kPart / 32];
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int base = kb + 32 * q;
+                for (int q = 0; q < kPart / 32; ++q) {
+                    const int base = krow - b.q0 + w * kPart + 32 * q;
                     wbits[q] = range_bits(vis.own_lo - base, vis.own_hi - base) |
                                range_bits(vis.par_lo - base, vis.par_hi - base);
                 }
 #pragma unroll
-                for (int e = 0; e < kHalf; ++e)
+                for (int e = 0; e < kPart; ++e)
                     s[e] = ((wbits[e >> 5] >> (e & 31)) & 1u) ? s[e] : -INFINITY;
             }
-            // max of this half with eight independent chains, then the row max
-            // from both halves (published in shared memory, bounded wait)
+            // max of this part with eight independent chains, then the row max
+            // from all parts (published in shared memory, bounded wait)
             float m8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 m8[e] = s[e];
 #pragma unroll
-            for (int e0 = 8; e0 < kHalf; e0 += 8)
+            for (int e0 = 8; e0 < kPart; e0 += 8)
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     m8[e] = fmaxf(m8[e], s[e0 + e]);
@@ -633,25 +639,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 aborted = true;
                 break;
             }
-            // both halves of the S buffer are in registers by now: P may overwrite it
-            const float mx = fmaxf(mloc, s_mx[(bf * kWG + 1 - w) * kBM + row]) * p.scale_log2;
+            // every part of the S buffer is in registers by now: P may overwrite it
+            float mrow = mloc;
+#pragma unroll
+            for (int w2 = 0; w2 < kWG; ++w2)
+                mrow = fmaxf(mrow, s_mx[(bf * kWG + w2) * kBM + row]);
+            const float mx = mrow * p.scale_log2;
             float factor = 1.f;
             if (mx > m_ref + kRescaleLog2) {
                 factor = ex2(m_ref - mx);  // 0 when m_ref = -inf
                 m_ref = mx;
             }
             const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float r4[4] = {0.f, 0.f, 0.f, 0.f};  // row sum in four chains
-            uint32_t pk[kHalf / 2];
+            // exponent arguments and the row sum in packed pairs (two sum chains of
+            // two lanes each)
+            float r4[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[kPart / 2];
 #pragma unroll
-            for (int e = 0; e < kHalf / 2; ++e) {
-                const float e0 = ex2(fmaf(s[2 * e], p.scale_log2, -msub));
-                const float e1 = ex2(fmaf(s[2 * e + 1], p.scale_log2, -msub));
-                r4[e & 3] += e0 + e1;
+            for (int e = 0; e < kPart / 2; ++e) {
+                float x0, x1;
+                ffma2(x0, x1, s[2 * e], s[2 * e + 1], p.scale_log2, p.scale_log2, -msub, -msub);
+                const float e0 = ex2(x0), e1 = ex2(x1);
+                float &ra = r4[2 * (e & 1)], &rb = r4[2 * (e & 1) + 1];
+                fadd2(ra, rb, ra, rb, e0, e1);
                 pk[e] = pack_bf16x2(e0, e1);
             }
             l = l * factor + (r4[0] + r4[1]) + (r4[2] + r4[3]);
-            // rescale this thread's half of O once PV(k-1) has landed (rare: only
+            // rescale this thread's part of O once PV(k-1) has landed (rare: only
             // when the max grows by more than 2^8)
             if (k > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
                 ok = wait_bar(bar(B_OW), (k - 1) & 1, abort_flag, status);
@@ -661,17 +675,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int q = 0; q < D / 64; ++q) {
-                    float o[32];
-                    const uint32_t col = (uint32_t)(w * (D / 2) + q * 32);
-                    tmem_ld32(tO + col, o);
+                for (int q = 0; q < D / kWG / 8; ++q) {
+                    float o[8];
+                    const uint32_t col = (uint32_t)(w * (D / kWG) + q * 8);
+                    tmem_ld8(tO + col, o);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
+                    for (int e = 0; e < 8; ++e)
                         o[e] *= factor;
-                    tmem_st32(tO + col, o);
+                    tmem_st8(tO + col, o);
                 }
             }
-            tmem_st32u(tS + (uint32_t)(w * (kHalf / 2)), pk);  // P of keys 64w.. over columns 32w..
+            // P of keys kPart*w.. over columns (kPart/2)*w..
+#if D3D_ATTN_WG == 2
+            tmem_st32u(tS + (uint32_t)(w * (kPart / 2)), pk);
+#else
+            tmem_st16(tS + (uint32_t)(w * (kPart / 2)), pk);
+#endif
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -680,45 +699,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             n_done = k + 1;
         }
 
-        // ---- epilogue: every MMA done, then the two warpgroups combine
+        // ---- epilogue: every MMA done, then the warpgroups' parts combine
         wait_drain(bar(B_DONE), 0, status);
         // (max, column-half sum, tiles done) of this thread's row; a negative sum
         // marks a void row (failed descriptor check or an abandoned wait)
-        float4 *s_ml4 = reinterpret_cast<float4 *>(s_ml);
-        s_ml4[w * kBM + row] = make_float4(m_ref, (aborted || row_bad) ? -1.f : l, (float)n_done, 0.f);
+        s_ml[w * kBM + row] = make_float4(m_ref, (aborted || row_bad) ? -1.f : l, (float)n_done, 0.f);
         tc_fence_before();
         asm volatile("bar.sync 2, %0;" ::"n"(kSoftmaxThreads) : "memory");
         tc_fence_after();
-        const float4 mine = s_ml4[w * kBM + row], other = s_ml4[(1 - w) * kBM + row];
-        const bool void_row = mine.y < 0.f || other.y < 0.f;
-        const float M = fmaxf(mine.x, other.x);  // both halves keep the same running max
-        const float L = fmaxf(mine.y, 0.f) + fmaxf(other.y, 0.f);
-        const bool have = fminf(mine.z, other.z) > 0.f;  // uniform over each warp
+        bool void_row = false;
+        float M = -INFINITY, L = 0.f, done = 1e30f;
+#pragma unroll
+        for (int w2 = 0; w2 < kWG; ++w2) {
+            const float4 t = s_ml[w2 * kBM + row];
+            void_row = void_row || t.y < 0.f;
+            M = fmaxf(M, t.x);  // every part keeps the same running max
+            L += fmaxf(t.y, 0.f);
+            done = fminf(done, t.z);
+        }
+        const bool have = done > 0.f;  // uniform over each warp
         const float inv = (void_row || !(L > 0.f)) ? 0.f : 1.f / L;
-        // this thread's half of the head dimension: columns [w*D/2, (w+1)*D/2)
-        uint16_t *orow = p.out + ((size_t)(b.q0 + token) * p.Hq + hk * p.G + (row % p.G)) * D + w * (D / 2);
+        // this thread's part of the head dimension: columns [w*D/kWG, (w+1)*D/kWG)
+        uint16_t *orow = p.out + ((size_t)(b.q0 + token) * p.Hq + hk * p.G + (row % p.G)) * D + w * (D / kWG);
         const uint32_t part = Xchg<D>::part(sK);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-            float x0[32];
+        for (int q = 0; q < D / kWG / 8; ++q) {
+            float x0[8];
             if (have) {
-                tmem_ld32(tO + (uint32_t)(w * (D / 2) + c * 32), x0);
+                tmem_ld8(tO + (uint32_t)(w * (D / kWG) + q * 8), x0);
             } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
+                for (int e = 0; e < 8; ++e)
                     x0[e] = 0.f;
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 v = pack8(x0 + 8 * q, inv);
-                if (p.S == 1) {
-                    if (row_valid)
-                        *reinterpret_cast<uint4 *>(orow + c * 32 + q * 8) = v;
-                } else {
-                    // the CTA's partial for the cluster's combine (every MMA is done)
-                    const uint32_t unit = (uint32_t)(w * (D / 16) + c * 4 + q);
-                    smem_st_v4(part + (unit * kBM + (uint32_t)row) * 16u, v);
-                }
+            const uint4 v = pack8(x0, inv);
+            if (p.S == 1) {
+                if (row_valid)
+                    *reinterpret_cast<uint4 *>(orow + q * 8) = v;
+            } else {
+                // the CTA's partial for the cluster's combine (every MMA is done)
+                const uint32_t unit = (uint32_t)(w * (D / kWG / 8) + q);
+                smem_st_v4(part + (unit * kBM + (uint32_t)row) * 16u, v);
             }
         }
         if (p.S > 1 && w == 0)
