@@ -152,6 +152,44 @@ __device__ inline void load_chunk(const T *row, int v0, int v1, float c, float (
     }
 }
 
+// One row chunk's 16-byte loads, issued ahead of use (phase A prefetches
+// the next item while it reduces the current one).  bf16 rows only: an f32
+// row chunk would need twice the registers, so f32 rows load at use.
+template <typename T, int NT> struct RawChunk {
+    __device__ void issue(const T *, int, int) {}
+    __device__ void take(const T *row, int v0, int v1, float c, float (&x)[kVPer]) { load_chunk<T, NT>(row, v0, v1, c, x); }
+};
+
+template <int NT> struct RawChunk<uint16_t, NT> {
+    uint4 u[kVPer / 8];
+    bool ok;
+    __device__ void issue(const uint16_t *row, int v0, int v1)
+    {
+        ok = v1 - v0 == VCfg<NT>::kChunk && aligned16(row + v0);
+        if (ok) {
+#pragma unroll
+            for (int g = 0; g < kVPer / 8; ++g)
+                u[g] = __ldg(reinterpret_cast<const uint4 *>(row + slot_pos<NT>(v0, 8 * g)));
+        }
+    }
+    __device__ void take(const uint16_t *row, int v0, int v1, float c, float (&x)[kVPer])
+    {
+        if (!ok) {
+            load_chunk<uint16_t, NT>(row, v0, v1, c, x);
+            return;
+        }
+#pragma unroll
+        for (int g = 0; g < kVPer / 8; ++g) {
+            const uint32_t w[4] = {u[g].x, u[g].y, u[g].z, u[g].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[8 * g + 2 * e] = __uint_as_float(w[e] << 16) * c;
+                x[8 * g + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u) * c;
+            }
+        }
+    }
+};
+
 // 2^x with the hardware approximation (relative error about 2^-22, far
 // inside the 1e-5 tolerance on probabilities); -inf gives 0.
 __device__ __forceinline__ float fast_exp2(float x)
@@ -574,22 +612,50 @@ __global__ void __launch_bounds__(NT, NT == kNTDevice ? 2 : 1)
     // one phase-A item per CTA: its exponentials stay in registers for phase C
     const bool keep = nA <= (long long)gridDim.x;
 
-    // ---- phase A: per (request, position, chunk) statistics of the row pair
+    // ---- phase A: per (request, position, chunk) statistics of the row pair;
+    // the next item's loads are in flight while the current one is reduced
     float eP[kVPer], eQ[kVPer];
     float mtP = -INFINITY, mtQ = -INFINITY;
+    auto target_row = [&](long long it, int &v0, int &v1, int &j) -> const T * {
+        const int chunk = (int)(it % nch);
+        const int rj = (int)(it / nch);
+        j = rj % B;
+        v0 = chunk * C::kChunk;
+        v1 = min(V, v0 + C::kChunk);
+        return target + (size_t)rj * V;
+    };
+    auto draft_row = [&](long long it) -> const T * {
+        const int rj = (int)(it / nch);
+        return draft + ((size_t)(rj / B) * (B - 1) + (rj % B)) * V;  // valid only when j < B - 1
+    };
+    RawChunk<T, NT> rawP, rawQ;
+    if ((long long)blockIdx.x < nA) {
+        int v0, v1, j;
+        const T *rp = target_row(blockIdx.x, v0, v1, j);
+        rawP.issue(rp, v0, v1);
+        if (j < B - 1)
+            rawQ.issue(draft_row(blockIdx.x), v0, v1);
+    }
     for (long long item = blockIdx.x; item < nA; item += gridDim.x) {
-        const int chunk = (int)(item % nch);
-        const int rj = (int)(item / nch);
-        const int r = rj / B, j = rj % B;
-        const int v0 = chunk * C::kChunk, v1 = min(V, v0 + C::kChunk);
+        int v0, v1, j;
+        const T *rowP = target_row(item, v0, v1, j);
+        const int r = (int)(item / nch) / B;
         const int yv = (j < B - 1) ? __ldg(y + (size_t)r * (B - 1) + j) : -1;
-        load_chunk<T, NT>(target + ((size_t)r * B + j) * V, v0, v1, c, eP);
+        rawP.take(rowP, v0, v1, c, eP);
         if (j < B - 1) {
-            load_chunk<T, NT>(draft + ((size_t)r * (B - 1) + j) * V, v0, v1, c, eQ);
+            rawQ.take(draft_row(item), v0, v1, c, eQ);
         } else {
 #pragma unroll
             for (int i = 0; i < kVPer; ++i)
                 eQ[i] = -INFINITY;
+        }
+        const long long next = item + gridDim.x;
+        if (next < nA) {
+            int nv0, nv1, nj;
+            const T *np = target_row(next, nv0, nv1, nj);
+            rawP.issue(np, nv0, nv1);
+            if (nj < B - 1)
+                rawQ.issue(draft_row(next), nv0, nv1);
         }
         if (yv >= v0 && yv < v1) {  // the thread holding position y keeps both logits for the record
             const int rel = yv - v0;
@@ -725,8 +791,10 @@ __global__ void __launch_bounds__(NT, NT == kNTDevice ? 2 : 1)
         return;
     }
 
-    // ---- phase C (several items per CTA): the request's selection, then this
-    // chunk's masses from a reload
+    // ---- phase C: the request's selection, then this chunk's masses from a
+    // reload.  With at most one C item per CTA, the CTA's D item is the same
+    // (request, chunk): it keeps the selection and the masses.
+    const bool cd_same = nC <= (int)gridDim.x;
     float w[kVPer];
     for (int item = blockIdx.x; item < nC; item += gridDim.x) {
         const int r = item / nch, chunk = item % nch;
@@ -756,15 +824,18 @@ __global__ void __launch_bounds__(NT, NT == kNTDevice ? 2 : 1)
         if (!wait_count(bar + kBarInts * r + 2, nch, status))
             return;
         // every phase-C item of r waited for r's phase A, so the records are complete
-        select_request<NT>(r, B, V, nch, rec, s_y, s_u, false, accept_len, out_tokens, num_tokens, alpha_out, p_out,
-                       q_out, status, sel, s_rec);
+        if (!cd_same)
+            select_request<NT>(r, B, V, nch, rec, s_y, s_u, false, accept_len, out_tokens, num_tokens, alpha_out,
+                               p_out, q_out, status, sel, s_rec);
         decide(r, sel);
         if (s_owner == chunk) {
             const int c0 = chunk * C::kChunk, c1 = min(V, c0 + C::kChunk);
-            const T *prow = target + ((size_t)r * B + sel.row) * V;
-            const T *qrow = draft + ((size_t)r * (B - 1) + (sel.mode == 0 ? sel.row : 0)) * V;
-            float a1, a2;
-            chunk_masses<T, NT>(prow, qrow, s_kind_used, c0, c1, c, sel, w, a1, a2);
+            if (!cd_same || s_kind_used != sel.mode) {  // masses not kept (or the fallback kind)
+                const T *prow = target + ((size_t)r * B + sel.row) * V;
+                const T *qrow = draft + ((size_t)r * (B - 1) + (sel.mode == 0 ? sel.row : 0)) * V;
+                float a1, a2;
+                chunk_masses<T, NT>(prow, qrow, s_kind_used, c0, c1, c, sel, w, a1, a2);
+            }
             scan_owner<NT>(w, c0, s_prefix, s_target, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
         } else if (s_owner < 0 && chunk == 0 && threadIdx.x == 0) {
             record_status(status, D3D_ERR_DEVICE_INPUT);
