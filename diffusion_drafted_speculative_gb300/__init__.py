@@ -54,7 +54,8 @@ EXPORTED = {
                                    _F, _P, _P, _Z, _P]),
     "d3d_spec_verify_workspace_size": (_Z, [_I, _I, _I]),
     "d3d_packed_draft_attn_ctas": (_I, [_I, _I, _I, _I, _I, _I]),
-    "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _Z, _I, _P]),
+    "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P,
+                             _P, _Z, _I, _P]),
     "d3d_branch_match": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "d3d_debug_inject_fault": (None, [_I]),
     "d3d_spec_verify_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P]),
@@ -198,7 +199,7 @@ def d3d_spec_verify_workspace_size(R, B, V) -> int:
 
 def d3d_spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature: float,
                     accept_len, out_tokens, num_tokens, ws, alpha=None, p_draft=None, q_draft=None,
-                    sm_limit: int = 0, stream=None) -> None:
+                    heads=None, head_len=None, branch=None, sm_limit: int = 0, stream=None) -> None:
     """Speculative-sampling verification; logits f32 or bf16 [R,B,V] / [R,B-1,V]."""
     if target_logits.dtype == torch.bfloat16:
         dt = D3D_DTYPE_BF16
@@ -226,11 +227,20 @@ def d3d_spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sampl
                 raise ValueError("%s must be [R, B-1]" % n)
     if draft_tokens.shape != (R, B - 1) or u_accept.shape != (R, B - 1) or u_sample.shape != (R,):
         raise ValueError("draft_tokens/u_accept must be [R, B-1], u_sample [R]")
+    M = 0
+    if branch is not None:
+        _need(branch, "branch", torch.int32, 1)
+        _need(heads, "heads", torch.int32, 3)
+        _need(head_len, "head_len", torch.int32, 2)
+        M = heads.shape[1]
+        if tuple(heads.shape) != (R, M, B) or tuple(head_len.shape) != (R, M) or tuple(branch.shape) != (R,):
+            raise ValueError("heads must be [R, M, B], head_len [R, M], branch [R]")
     _need(ws, "ws", torch.uint8, 1)
     rc = lib.d3d_spec_verify(
         _ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), R, B, V,
         float(temperature), _ptr(accept_len), _ptr(out_tokens), _ptr(num_tokens), _ptr(alpha), _ptr(p_draft),
-        _ptr(q_draft), _ptr(ws), ws.numel(), int(sm_limit), _stream(stream))
+        _ptr(q_draft), _ptr(heads) if branch is not None else None, _ptr(head_len) if branch is not None else None,
+        M, _ptr(branch), _ptr(ws), ws.numel(), int(sm_limit), _stream(stream))
     _check("d3d_spec_verify", rc)
 
 

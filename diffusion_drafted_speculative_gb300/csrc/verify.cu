@@ -586,13 +586,42 @@ __device__ void scan_owner(const float (&w)[kVPer], int c0, float prefix, float 
     __syncthreads();
 }
 
+// Branch cache-hit match of request r fused after its sample ([D3D]
+// "Background: asynchronous drafting and cache hits"): the verified tokens are
+// y_0..y_{a-1} (shared memory) and the sampled token; the smallest head index
+// of equal length and equal tokens wins, -1 on a miss.  Run by warp 0.
+__device__ void match_request(int r, int a, int tok, const int32_t *s_y, int B, int M,
+                              const int32_t *__restrict__ heads, const int32_t *__restrict__ head_len,
+                              int32_t *__restrict__ branch)
+{
+    const int lane = threadIdx.x & 31, n = a + 1;
+    int hit = -1;
+    for (int k0 = 0; k0 < M && hit < 0; k0 += 32) {
+        const int k = k0 + lane;
+        bool same = false;
+        if (k < M && __ldg(head_len + (size_t)r * M + k) == n) {
+            const int32_t *h = heads + ((size_t)r * M + k) * B;
+            same = true;
+            for (int i = 0; i < n && same; ++i)
+                same = __ldg(h + i) == (i < a ? s_y[i] : tok);
+        }
+        const unsigned ballot = __ballot_sync(0xffffffffu, same);
+        if (ballot)
+            hit = k0 + __ffs(ballot) - 1;
+    }
+    if (lane == 0)
+        branch[r] = hit;
+}
+
 template <typename T, int NT>
 __global__ void __launch_bounds__(NT, NT == kNTDevice ? 2 : 1)
     verify_kernel(const T *__restrict__ target, const T *__restrict__ draft, const int32_t *__restrict__ y,
                   const float *__restrict__ u_acc, const float *__restrict__ u_s, int R, int B, int V, float c,
                   int32_t *__restrict__ accept_len, int32_t *__restrict__ out_tokens,
                   int32_t *__restrict__ num_tokens, float *__restrict__ alpha_out, float *__restrict__ p_out,
-                  float *__restrict__ q_out, unsigned char *__restrict__ ws)
+                  float *__restrict__ q_out, const int32_t *__restrict__ heads,
+                  const int32_t *__restrict__ head_len, int M, int32_t *__restrict__ branch,
+                  unsigned char *__restrict__ ws)
 {
     extern __shared__ float4 s_dyn[];  // request records when staged; chunk sums in phase D
     using C = VCfg<NT>;
@@ -730,6 +759,14 @@ __global__ void __launch_bounds__(NT, NT == kNTDevice ? 2 : 1)
         }
         __syncthreads();
     };
+    // The match of request r once its sampled token is written (the writer is a
+    // thread of this CTA, and a barrier separates the write from this read).
+    auto fused_match = [&](int r, int a) {
+        if (branch != nullptr && threadIdx.x < 32) {
+            const int tok = *reinterpret_cast<volatile const int32_t *>(out_tokens + (size_t)r * B + a);
+            match_request(r, a, tok, s_y, B, M, heads, head_len, branch);
+        }
+    };
     // The request's last phase-D item resets the phase-C/D counters (every
     // phase-C signal has arrived and every phase-D waiter has passed).
     auto finish_d = [&](int r) {
@@ -781,10 +818,15 @@ __global__ void __launch_bounds__(NT, NT == kNTDevice ? 2 : 1)
                 kept_masses(1, eP, eQ, mtP, mtQ, sel, a1, a2);
             }
             scan_owner<NT>(eQ, c0, s_prefix, s_target, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
-        } else if (s_owner < 0 && chunk == 0 && threadIdx.x == 0) {
+            fused_match(r, sel.a);
+        } else if (s_owner < 0 && chunk == 0) {
             // no mass anywhere: cannot happen for a finite softmax row
-            record_status(status, D3D_ERR_DEVICE_INPUT);
-            out_tokens[(size_t)r * B + sel.a] = 0;
+            if (threadIdx.x == 0) {
+                record_status(status, D3D_ERR_DEVICE_INPUT);
+                out_tokens[(size_t)r * B + sel.a] = 0;
+            }
+            __syncthreads();
+            fused_match(r, sel.a);
         }
         finish_d(r);
         passed_a(r, B * nch);
@@ -837,9 +879,14 @@ __global__ void __launch_bounds__(NT, NT == kNTDevice ? 2 : 1)
                 chunk_masses<T, NT>(prow, qrow, s_kind_used, c0, c1, c, sel, w, a1, a2);
             }
             scan_owner<NT>(w, c0, s_prefix, s_target, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
-        } else if (s_owner < 0 && chunk == 0 && threadIdx.x == 0) {
-            record_status(status, D3D_ERR_DEVICE_INPUT);
-            out_tokens[(size_t)r * B + sel.a] = 0;
+            fused_match(r, sel.a);
+        } else if (s_owner < 0 && chunk == 0) {
+            if (threadIdx.x == 0) {
+                record_status(status, D3D_ERR_DEVICE_INPUT);
+                out_tokens[(size_t)r * B + sel.a] = 0;
+            }
+            __syncthreads();
+            fused_match(r, sel.a);
         }
         finish_d(r);
         __syncthreads();
@@ -849,7 +896,8 @@ __global__ void __launch_bounds__(NT, NT == kNTDevice ? 2 : 1)
 template <typename T, int NT>
 int launch_verify_nt(const void *target, const void *draft, const int32_t *y, const float *u_acc, const float *u_s,
                      int R, int B, int V, float c, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
-                     float *alpha, float *p, float *q, unsigned char *ws, int sm_limit, cudaStream_t stream)
+                     float *alpha, float *p, float *q, const int32_t *heads, const int32_t *head_len, int M,
+                     int32_t *branch, unsigned char *ws, int sm_limit, cudaStream_t stream)
 {
     const VerifyLayout L = verify_layout(R, B, V, VCfg<NT>::kChunk);
     const long long nA = (long long)R * B * L.nch;
@@ -885,7 +933,7 @@ int launch_verify_nt(const void *target, const void *draft, const int32_t *y, co
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, verify_kernel<T, NT>, static_cast<const T *>(target),
                                              static_cast<const T *>(draft), y, u_acc, u_s, R, B, V, c, accept_len,
-                                             out_tokens, num_tokens, alpha, p, q, ws);
+                                             out_tokens, num_tokens, alpha, p, q, heads, head_len, M, branch, ws);
     return cuda_status(e);
 }
 
@@ -894,13 +942,15 @@ int launch_verify_nt(const void *target, const void *draft, const int32_t *y, co
 template <typename T>
 int launch_verify(const void *target, const void *draft, const int32_t *y, const float *u_acc, const float *u_s,
                   int R, int B, int V, float c, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
-                  float *alpha, float *p, float *q, unsigned char *ws, int sm_limit, cudaStream_t stream)
+                  float *alpha, float *p, float *q, const int32_t *heads, const int32_t *head_len, int M,
+                  int32_t *branch, unsigned char *ws, int sm_limit, cudaStream_t stream)
 {
     if (sm_limit > 0)
         return launch_verify_nt<T, kNTLimited>(target, draft, y, u_acc, u_s, R, B, V, c, accept_len, out_tokens,
-                                               num_tokens, alpha, p, q, ws, sm_limit, stream);
+                                               num_tokens, alpha, p, q, heads, head_len, M, branch, ws, sm_limit,
+                                               stream);
     return launch_verify_nt<T, kNTDevice>(target, draft, y, u_acc, u_s, R, B, V, c, accept_len, out_tokens,
-                                          num_tokens, alpha, p, q, ws, 0, stream);
+                                          num_tokens, alpha, p, q, heads, head_len, M, branch, ws, 0, stream);
 }
 
 }  // namespace
@@ -919,10 +969,12 @@ size_t d3d_spec_verify_workspace_size(int R, int B, int V)
 int d3d_spec_verify(const void *target_logits, const void *draft_logits, int logits_dtype,
                     const int32_t *draft_tokens, const float *u_accept, const float *u_sample, int R, int B,
                     int V, float temperature, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
-                    float *alpha, float *p_draft, float *q_draft, void *ws, size_t ws_bytes, int sm_limit,
-                    cudaStream_t stream)
+                    float *alpha, float *p_draft, float *q_draft, const int32_t *heads, const int32_t *head_len,
+                    int M, int32_t *branch, void *ws, size_t ws_bytes, int sm_limit, cudaStream_t stream)
 {
-    if (R < 0 || B < 2 || V < 1 || !(temperature > 0.f) || !isfinite(temperature) || sm_limit < 0)
+    if (R < 0 || B < 2 || V < 1 || !(temperature > 0.f) || !isfinite(temperature) || sm_limit < 0 || M < 0)
+        return D3D_ERR_INVALID_ARG;
+    if (branch != nullptr && M > 0 && (!heads || !head_len))
         return D3D_ERR_INVALID_ARG;
     if (logits_dtype != D3D_DTYPE_F32 && logits_dtype != D3D_DTYPE_BF16)
         return D3D_ERR_INVALID_ARG;
@@ -939,11 +991,11 @@ int d3d_spec_verify(const void *target_logits, const void *draft_logits, int log
     unsigned char *w = static_cast<unsigned char *>(ws);
     if (logits_dtype == D3D_DTYPE_BF16)
         return d3d::launch_verify<uint16_t>(target_logits, draft_logits, draft_tokens, u_accept, u_sample, R, B, V,
-                                            c, accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w,
-                                            sm_limit, stream);
+                                            c, accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, heads,
+                                            head_len, M, branch, w, sm_limit, stream);
     return d3d::launch_verify<float>(target_logits, draft_logits, draft_tokens, u_accept, u_sample, R, B, V, c,
-                                     accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w, sm_limit,
-                                     stream);
+                                     accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, heads, head_len,
+                                     M, branch, w, sm_limit, stream);
 }
 
 }  // extern "C"
@@ -1033,8 +1085,9 @@ extern "C" int d3d_spec_verify_noalloc(const void *target_logits, const void *dr
     unsigned char *w = static_cast<unsigned char *>(scratch);
     if (logits_dtype == D3D_DTYPE_BF16)
         return d3d::launch_verify<uint16_t>(target_logits, draft_logits, draft_tokens, u_accept, u_sample, R, B, V,
-                                            c, accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w, 0,
-                                            stream);
+                                            c, accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, nullptr,
+                                            nullptr, 0, nullptr, w, 0, stream);
     return d3d::launch_verify<float>(target_logits, draft_logits, draft_tokens, u_accept, u_sample, R, B, V, c,
-                                     accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, w, 0, stream);
+                                     accept_len, out_tokens, num_tokens, alpha, p_draft, q_draft, nullptr, nullptr,
+                                     0, nullptr, w, 0, stream);
 }

@@ -199,6 +199,14 @@ void d3d_debug_inject_fault(int mode);
  *   accept_len [R], out_tokens [R, B], num_tokens [R]  int32 outputs
  *   alpha, p_draft, q_draft [R, B-1] float32 outputs, each may be NULL
  *               (p_draft = P_j(y_j), q_draft = Q_j(y_j))
+ *   heads [R, M, B], head_len [R, M], branch [R]  int32; optional fused
+ *               branch match: when branch is not NULL, the kernel writes
+ *               branch[r] exactly as d3d_branch_match would for the verified
+ *               tokens out_tokens[r, :num_tokens[r]] (heads/head_len may be
+ *               NULL when M == 0).  The heads are the round's inputs ([D3D]
+ *               "Background: asynchronous drafting and cache hits": each
+ *               branch hypothesises an accepted prefix and its corrected
+ *               token), so the match needs nothing from the drafting pass.
  *   ws          workspace, d3d_spec_verify_workspace_size() bytes
  *   sm_limit    0: the kernel may use every SM.  n > 0: at most n CTAs, each
  *               holding a whole SM, so that a kernel launched beside it on
@@ -213,8 +221,8 @@ size_t d3d_spec_verify_workspace_size(int R, int B, int V);
 int d3d_spec_verify(const void *target_logits, const void *draft_logits, int logits_dtype,
                     const int32_t *draft_tokens, const float *u_accept, const float *u_sample, int R, int B,
                     int V, float temperature, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
-                    float *alpha, float *p_draft, float *q_draft, void *ws, size_t ws_bytes, int sm_limit,
-                    cudaStream_t stream);
+                    float *alpha, float *p_draft, float *q_draft, const int32_t *heads, const int32_t *head_len,
+                    int M, int32_t *branch, void *ws, size_t ws_bytes, int sm_limit, cudaStream_t stream);
 
 /*
  * Verification that allocates nothing (the pages have no counterpart: this

@@ -42,7 +42,7 @@ def assert_attn_close(got, ref, what=""):
                                                                                                   excess.shape))
 
 
-def run_verify(d3d, v, ws=None, want_probs=True, sm_limit=0):
+def run_verify(d3d, v, ws=None, want_probs=True, sm_limit=0, heads=None):
     dev = "cuda"
     R, B = v["R"], v["B"]
     if v["dtype"] == 1:
@@ -55,9 +55,13 @@ def run_verify(d3d, v, ws=None, want_probs=True, sm_limit=0):
     probs = {k: torch.full((R, B - 1), float("nan"), device=dev) for k in ("alpha", "p", "q")} if want_probs else {}
     if ws is None:
         ws = d3d.new_workspace(d3d.d3d_spec_verify_workspace_size(R, B, v["V"]), dev)
+    fused = {}
+    if heads is not None:  # the branch match fused into the verification
+        out["branch"] = torch.full((R,), -7, dtype=torch.int32, device=dev)
+        fused = dict(heads=i32(heads["heads"]), head_len=i32(heads["head_len"]), branch=out["branch"])
     d3d.d3d_spec_verify(tgt, dr, i32(v["y"]), f32(v["u_accept"]), f32(v["u_sample"]), v.get("temperature", 1.0),
                         out["accept_len"], out["out_tokens"], out["num_tokens"], ws, alpha=probs.get("alpha"),
-                        p_draft=probs.get("p"), q_draft=probs.get("q"), sm_limit=sm_limit)
+                        p_draft=probs.get("p"), q_draft=probs.get("q"), sm_limit=sm_limit, **fused)
     torch.cuda.synchronize()
     res = {k: t.cpu().numpy() for k, t in {**out, **probs}.items()}
     return res, ws

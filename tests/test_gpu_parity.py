@@ -253,6 +253,42 @@ def test_verify_sm_limit_same_results(d3d, sm_limit):
         assert d3d.d3d_workspace_status(ws2) == 0
 
 
+def _heads_hitting(ref, B, V, M, seed):
+    """Branch heads for a verification batch: random heads of every length plus,
+    for most requests, one copy of the oracle's verified tokens (a planted hit)
+    and for some a copy placed twice (lowest index wins)."""
+    rng = np.random.default_rng(seed)
+    R = ref["out_tokens"].shape[0]
+    heads = rng.integers(0, V, size=(R, M, B)).astype(np.int32)
+    head_len = rng.integers(0, B + 1, size=(R, M)).astype(np.int32)
+    for r in range(R):
+        n = int(ref["num_tokens"][r])
+        if r == 0 or rng.random() < 0.7:
+            for k in sorted(rng.choice(M, size=2 if rng.random() < 0.3 else 1, replace=False)):
+                heads[r, k, :n] = ref["out_tokens"][r, :n]
+                head_len[r, k] = n
+    return dict(heads=heads, head_len=head_len)
+
+
+@pytest.mark.parametrize("cfg,sm_limit", [("async8b", 0), ("async8b", 56), ("serve32b", 0), ("serve32b", 40),
+                                          ("tiny", 0)])
+def test_verify_fused_match(d3d, cfg, sm_limit):
+    # the match fused into the verification equals the match of the tokens the
+    # verification produced (oracle), hits planted from the oracle's tokens
+    c = dict(W.CONFIGS[cfg])
+    if cfg == "tiny":
+        c["R"] = 300
+    v = W.verify_inputs(**c, seed=8)
+    ref = oracle.spec_verify(v)
+    hb = _heads_hitting(ref, c["B"], c["V"], 24, seed=9)
+    got, ws = run_verify(d3d, v, sm_limit=sm_limit, heads=hb)
+    compare_verify(got, ref, min_kept=0.0)
+    want = oracle.branch_match(dict(verified=got["out_tokens"], verified_len=got["num_tokens"], **hb))
+    np.testing.assert_array_equal(got["branch"], want)
+    assert want[0] >= 0 and (want >= 0).mean() > 0.3  # hits are exercised
+    assert d3d.d3d_workspace_status(ws) == 0
+
+
 def test_attention_cta_count_matches_plan(d3d):
     # one CTA per query tile and key split, all in one wave on this GPU
     n = d3d.d3d_packed_draft_attn_ctas(1, 32, 8, 128, 384, 2048)

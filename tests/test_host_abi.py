@@ -68,8 +68,9 @@ def test_invalid_arguments_rejected_on_host(d3d):
     L = d3d.lib
     fake = ctypes.c_void_p(256)  # never dereferenced: the checks fail first
     # verify: B < 2, V < 1, T <= 0, bad dtype, missing workspace
-    args = lambda R, B, V, T, dt, ws, wsb, sm=0: (fake, fake, dt, fake, fake, fake, R, B, V, T, fake, fake,  # noqa
-                                                  fake, None, None, None, ws, wsb, sm, None)
+    args = lambda R, B, V, T, dt, ws, wsb, sm=0, M=0, heads=None, br=None: (  # noqa
+        fake, fake, dt, fake, fake, fake, R, B, V, T, fake, fake, fake, None, None, None, heads, heads, M, br, ws, wsb,
+        sm, None)
     assert L.d3d_spec_verify(*args(1, 1, 10, 1.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 0, 1.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 10, 0.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
@@ -82,6 +83,8 @@ def test_invalid_arguments_rejected_on_host(d3d):
     assert L.d3d_spec_verify(*args(1, 300, 10, 1.0, 1, fake, 1 << 30)) == d3d.D3D_ERR_UNSUPPORTED
     assert L.d3d_spec_verify(*args(0, 4, 10, 1.0, 1, None, 0)) == d3d.D3D_OK  # nothing to do
     assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 1 << 20, -1)) == d3d.D3D_ERR_INVALID_ARG
+    assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 1 << 20, 0, -1)) == d3d.D3D_ERR_INVALID_ARG
+    assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 1 << 20, 0, 3, None, fake)) == d3d.D3D_ERR_INVALID_ARG
 
     def attn(R=1, Hq=32, Hkv=8, d=128, max_q=16, scale=0.1, ws=fake, wsb=1 << 30):
         return L.d3d_packed_draft_attn(fake, fake, fake, fake, fake, fake, fake, fake, fake, R, Hq, Hkv, d, max_q,
