@@ -11,9 +11,10 @@ F=2 (N_async = 384 packed query tokens), verification of 16 positions over a
 151936-entry vocabulary, and a match against 24 branch heads.  Within a
 round the packed drafting pass and the verification are independent (the
 drafter prepares the successor blocks while the current block is verified),
-so they run concurrently on two streams, the verification on the SMs the
-attention leaves; the branch match runs inside the verification's last
-phase (``parts.match_us`` times the stand-alone match entry point).
+so they run concurrently: the verification first, on the SMs the attention
+leaves, and the attention as its programmatic dependent on the same stream;
+the branch match runs inside the verification's last phase
+(``parts.match_us`` times the stand-alone match entry point).
 
 Timing: inputs resident in HBM; steps rotate over input sets whose total
 size exceeds twice the L2 cache, so no step finds its inputs in L2; each
@@ -258,9 +259,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     side_sms = props.multi_processor_count - attn_ctas
     verify_sms = side_sms if 0 < attn_ctas and side_sms > 0 else 0
 
-    def attn(s):
+    def attn(s, after_independent=False):
         d3d.d3d_packed_draft_attn(s["q"], s["kp"], s["vp"], s["kn"], s["vn"], s["segs"], s["cu_prefix"], s["cu_q"],
-                                  s["cu_seg"], max_q, max_prefix, scale, s["out"], ws_a)
+                                  s["cu_seg"], max_q, max_prefix, scale, s["out"], ws_a,
+                                  after_independent=after_independent)
 
     def verify(s, sm_limit=0, fused_match=False):
         extra = dict(heads=s["heads"], head_len=s["head_len"], branch=s["branch"]) if fused_match else {}
@@ -271,20 +273,17 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         d3d.d3d_branch_match(s["out_tokens"], s["num_tokens"], s["heads"], s["head_len"], s["branch"])
 
     stream = torch.cuda.Stream(device=dev)
-    side = torch.cuda.Stream(device=dev)
 
     def step(s):
         # the asynchronous round: the packed drafting pass and the verification
-        # of the current block are independent and run concurrently (the
-        # verification on a second stream, on the SMs the attention leaves);
+        # of the current block are independent and run concurrently.  The
+        # verification goes first on the SMs the attention leaves; the
+        # attention is its programmatic dependent on the same stream (it
+        # starts once every verification CTA runs and finishes after it);
         # the branch match runs inside the verification's last phase (it needs
         # the verified tokens and the round's branch heads only)
-        cur = torch.cuda.current_stream()
-        side.wait_stream(cur)
-        attn(s)
-        with torch.cuda.stream(side):
-            verify(s, verify_sms, fused_match=True)
-        cur.wait_stream(side)
+        verify(s, verify_sms, fused_match=True)
+        attn(s, after_independent=verify_sms > 0)
 
     torch.cuda.synchronize()
 

@@ -23,7 +23,7 @@ __all__ = [
     "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
     "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
     "D3D_ERR_DEVICE_TIMEOUT", "D3D_ERR_DEVICE_INPUT", "D3D_DTYPE_F32", "D3D_DTYPE_BF16",
-    "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR",
+    "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR", "D3D_ATTN_AFTER_INDEPENDENT",
 ]
 
 D3D_OK = 0
@@ -37,6 +37,7 @@ D3D_DTYPE_F32 = 0
 D3D_DTYPE_BF16 = 1
 D3D_SEG_CAUSAL = 0
 D3D_SEG_BIDIR = 1
+D3D_ATTN_AFTER_INDEPENDENT = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libd3d.so")
@@ -51,7 +52,7 @@ EXPORTED = {
     "d3d_validate_segments": (_I, [_P, _P, _P, _I]),
     "d3d_packed_draft_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "d3d_packed_draft_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
-                                   _F, _P, _P, _Z, _P]),
+                                   _F, _P, _P, _Z, _I, _P]),
     "d3d_spec_verify_workspace_size": (_Z, [_I, _I, _I]),
     "d3d_packed_draft_attn_ctas": (_I, [_I, _I, _I, _I, _I, _I]),
     "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P,
@@ -169,7 +170,8 @@ def d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix) -> int:
 
 
 def d3d_packed_draft_attn(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q, cu_seg,
-                          max_q: int, max_prefix: int, scale: float, out, ws, stream=None) -> None:
+                          max_q: int, max_prefix: int, scale: float, out, ws, after_independent: bool = False,
+                          stream=None) -> None:
     """Packed drafting attention; shapes as in include/d3d.h (bf16 tensors, int32 tables)."""
     for t, n in ((q, "q"), (k_prefix, "k_prefix"), (v_prefix, "v_prefix"), (k_packed, "k_packed"),
                  (v_packed, "v_packed"), (out, "out")):
@@ -189,7 +191,8 @@ def d3d_packed_draft_attn(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_pr
     rc = lib.d3d_packed_draft_attn(
         _ptr(q), _ptr(k_prefix), _ptr(v_prefix), _ptr(k_packed), _ptr(v_packed), _ptr(segs), _ptr(cu_prefix),
         _ptr(cu_q), _ptr(cu_seg), R, Hq, Hkv, d, int(max_q), int(max_prefix), NT, LT, segs.shape[0],
-        float(scale), _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+        float(scale), _ptr(out), _ptr(ws), ws.numel(), D3D_ATTN_AFTER_INDEPENDENT if after_independent else 0,
+        _stream(stream))
     _check("d3d_packed_draft_attn", rc)
 
 

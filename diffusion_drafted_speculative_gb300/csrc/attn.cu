@@ -292,16 +292,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (int)(u / (unsigned)p.Hkv);
     int32_t *status = reinterpret_cast<int32_t *>(p.ws);
 
-    // early exits are uniform over the CTAs of a cluster (same r and tile)
+    // early exits are uniform over the CTAs of a cluster (same r and tile).
+    // Every exit first waits for a kernel this launch overlaps (programmatic
+    // dependent launch): the stream moves on only when both have finished.
     ReqBounds b;
     if (!request_bounds(p.cu_prefix, p.cu_q, p.cu_seg, r, p.max_q, p.max_prefix, p.total_q, p.total_prefix,
                         p.total_segs, b)) {
         if (tid == 0 && sp == 0)
             record_status(status, D3D_ERR_DEVICE_INPUT);
+        pdl_wait();
         return;
     }
-    if (mt * p.TQ >= b.n_q)
+    if (mt * p.TQ >= b.n_q) {
+        pdl_wait();
         return;
+    }
 
     // ---- this split's key list: prefix tiles [pb, pe), then (last split only) packed tiles
     const int nP = (b.L + kBN - 1) / kBN;
@@ -781,6 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    pdl_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -919,7 +925,7 @@ bool make_map(CUtensorMap *m, const void *ptr, int d, int heads, long long rows,
 int g_fault_mode = 0;
 
 template <int D>
-int launch_attn(const CUtensorMap (&maps)[5], const AttnParams &prm, long long units, cudaStream_t stream)
+int launch_attn(const CUtensorMap (&maps)[5], const AttnParams &prm, long long units, int flags, cudaStream_t stream)
 {
     if (set_smem_attr<D>() != cudaSuccess)
         return D3D_ERR_CUDA;
@@ -928,15 +934,22 @@ int launch_attn(const CUtensorMap (&maps)[5], const AttnParams &prm, long long u
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Layout<D>::alloc;
     cfg.stream = stream;
-    cudaLaunchAttribute a[1];
-    if (prm.S > 1) {  // the splits of one query-tile pair form a cluster (consecutive CTAs)
-        a[0].id = cudaLaunchAttributeClusterDimension;
-        a[0].val.clusterDim.x = (unsigned)prm.S;
-        a[0].val.clusterDim.y = 1;
-        a[0].val.clusterDim.z = 1;
-        cfg.attrs = a;
-        cfg.numAttrs = 1;
+    cudaLaunchAttribute a[2];
+    unsigned na = 0;
+    if (prm.S > 1) {  // the splits of one query tile form a cluster (consecutive CTAs)
+        a[na].id = cudaLaunchAttributeClusterDimension;
+        a[na].val.clusterDim.x = (unsigned)prm.S;
+        a[na].val.clusterDim.y = 1;
+        a[na].val.clusterDim.z = 1;
+        ++na;
     }
+    if (flags & D3D_ATTN_AFTER_INDEPENDENT) {  // may start while the previous kernel runs
+        a[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        a[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = na ? a : nullptr;
+    cfg.numAttrs = na;
     return cuda_status(cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, maps[0], maps[1], maps[2], maps[3], maps[4], prm));
 }
 
@@ -974,10 +987,11 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
                           const void *v_packed, const d3d_segment_t *segs, const int32_t *cu_prefix,
                           const int32_t *cu_q, const int32_t *cu_seg, int R, int Hq, int Hkv, int d, int max_q,
                           int max_prefix, int total_q, int total_prefix, int total_segs, float scale, void *out,
-                          void *ws, size_t ws_bytes, cudaStream_t stream)
+                          void *ws, size_t ws_bytes, int flags, cudaStream_t stream)
 {
     if (R < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_q < 0 || max_prefix < 0 || total_q < 0 ||
-        total_prefix < 0 || total_segs < 0 || !(scale > 0.f) || !isfinite(scale))
+        total_prefix < 0 || total_segs < 0 || !(scale > 0.f) || !isfinite(scale) ||
+        (flags & ~D3D_ATTN_AFTER_INDEPENDENT) != 0)
         return D3D_ERR_INVALID_ARG;
     if (d != 64 && d != 128)
         return D3D_ERR_UNSUPPORTED;
@@ -1037,8 +1051,8 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.fault = d3d::g_fault_mode;
     if (d == 64)
-        return d3d::launch_attn<64>(maps, prm, pl.units, stream);
-    return d3d::launch_attn<128>(maps, prm, pl.units, stream);
+        return d3d::launch_attn<64>(maps, prm, pl.units, flags, stream);
+    return d3d::launch_attn<128>(maps, prm, pl.units, flags, stream);
 }
 
 }  // extern "C"

@@ -276,6 +276,15 @@ __device__ __forceinline__ void fadd2(float &d0, float &d1, float a0, float a1, 
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+// The kernel launched after this one on the stream with programmatic stream
+// serialization may start once every CTA of this grid has signalled (or
+// exited).  Without such a dependent it does nothing.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Block until the grids this one depends on programmatically have completed
+// and their memory is visible; returns at once for a normal launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- thread-block clusters --------------------------------------------------
 // Cluster-wide barrier in two halves: every non-exited thread of every CTA of
 // the cluster arrives once per phase; the release/acquire pair orders shared

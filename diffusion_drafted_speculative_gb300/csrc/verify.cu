@@ -31,6 +31,7 @@
 #include <mutex>
 
 #include "d3d_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace d3d {
 namespace {
@@ -638,6 +639,10 @@ __global__ void __launch_bounds__(NT, NT == kNTDevice ? 2 : 1)
     int *bar = reinterpret_cast<int *>(ws + L.bar);
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     Rec *s_rec = reinterpret_cast<Rec *>(s_dyn);
+    // a kernel launched after this one as an independent programmatic
+    // dependent (the drafting attention of the same round) may start now
+    if (threadIdx.x == 0)
+        sm100::pdl_trigger();
     // one phase-A item per CTA: its exponentials stay in registers for phase C
     const bool keep = nA <= (long long)gridDim.x;
 

@@ -137,10 +137,19 @@ int d3d_validate_segments(const d3d_segment_t *segs, const int32_t *cu_q, const 
  *               status word only: the key splits of a query tile combine
  *               their partial results through distributed shared memory of
  *               a thread-block cluster, not through global scratch)
+ *   flags       0, or D3D_ATTN_AFTER_INDEPENDENT: the launch may start while
+ *               the kernel before it on the stream still runs (programmatic
+ *               dependent launch) -- for the verification of the same round,
+ *               launched first with an sm_limit, whose output the attention
+ *               does not read.  The attention still finishes only after that
+ *               kernel has finished, so later work on the stream sees both.
+ *               Other bits: D3D_ERR_INVALID_ARG.
  * Device-side checks: offsets out of the totals' range or a segment table
  * that breaks the rules of d3d_validate_segments set D3D_ERR_DEVICE_INPUT
  * in the status word (the affected rows are written as zeros).
  * ======================================================================== */
+#define D3D_ATTN_AFTER_INDEPENDENT 1
+
 size_t d3d_packed_draft_attn_workspace_size(int R, int Hq, int Hkv, int d, int max_q, int max_prefix);
 
 /* Number of CTAs the d3d_packed_draft_attn launch for these sizes uses on the
@@ -156,7 +165,7 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
                           const void *v_packed, const d3d_segment_t *segs, const int32_t *cu_prefix,
                           const int32_t *cu_q, const int32_t *cu_seg, int R, int Hq, int Hkv, int d,
                           int max_q, int max_prefix, int total_q, int total_prefix, int total_segs,
-                          float scale, void *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+                          float scale, void *out, void *ws, size_t ws_bytes, int flags, cudaStream_t stream);
 
 /*
  * Failure-detection hook (no counterpart on the pages).  mode 1 makes every

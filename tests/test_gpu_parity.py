@@ -289,6 +289,45 @@ def test_verify_fused_match(d3d, cfg, sm_limit):
     assert d3d.d3d_workspace_status(ws) == 0
 
 
+def test_round_verification_then_overlapping_attention(d3d):
+    # one stream: the verification on the SMs the attention leaves, then the
+    # attention as its programmatic dependent, repeated; both outputs meet the
+    # oracle and a later reader sees both complete
+    cfg = W.CONFIGS["async8b"]
+    a = W.attn_inputs(**cfg, seed=21)
+    v = W.verify_inputs(**cfg, seed=21)
+    ref_v = oracle.spec_verify(v)
+    ref_a = oracle.packed_attn(a, heads=(28, 32))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    side = sms - d3d.d3d_packed_draft_attn_ctas(1, cfg["Hq"], cfg["Hkv"], cfg["d"], a["max_q"], a["max_prefix"])
+    assert side > 0
+    from gpu_util import bf16, f32, i32
+    t = {k: bf16(a[k]) for k in ("q", "kp", "vp", "kn", "vn")}
+    ix = {k: i32(a[k]) for k in ("segs", "cu_prefix", "cu_q", "cu_seg")}
+    wsa = d3d.new_workspace(d3d.d3d_packed_draft_attn_workspace_size(1, cfg["Hq"], cfg["Hkv"], cfg["d"], a["max_q"],
+                                                                      a["max_prefix"]))
+    wsv = d3d.new_workspace(d3d.d3d_spec_verify_workspace_size(1, cfg["B"], cfg["V"]))
+    tg, dr = bf16(v["target"]), bf16(v["draft"])
+    acc = torch.empty(1, dtype=torch.int32, device="cuda")
+    toks = torch.empty(1, cfg["B"], dtype=torch.int32, device="cuda")
+    nt = torch.empty(1, dtype=torch.int32, device="cuda")
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        for _ in range(5):
+            out = torch.full_like(t["q"], float("nan"))
+            toks.fill_(-7)
+            d3d.d3d_spec_verify(tg, dr, i32(v["y"]), f32(v["u_accept"]), f32(v["u_sample"]), 1.0, acc, toks, nt, wsv,
+                                sm_limit=side)
+            d3d.d3d_packed_draft_attn(t["q"], t["kp"], t["vp"], t["kn"], t["vn"], ix["segs"], ix["cu_prefix"],
+                                      ix["cu_q"], ix["cu_seg"], a["max_q"], a["max_prefix"], a["scale"], out, wsa,
+                                      after_independent=True)
+            got_t, got_o = toks.cpu().numpy(), out.float().cpu().numpy()  # read after both, same stream
+            keep = (ref_v["margin_accept"] >= 1e-5) & (ref_v["margin_sample"] >= 1e-5)
+            np.testing.assert_array_equal(got_t[keep], ref_v["out_tokens"][keep])
+            assert_attn_close(got_o[:, 28:32], ref_a[:, 28:32], "overlapped attention")
+    assert d3d.d3d_workspace_status(wsa) == 0 and d3d.d3d_workspace_status(wsv) == 0
+
+
 def test_attention_cta_count_matches_plan(d3d):
     # one CTA per query tile and key split, all in one wave on this GPU
     n = d3d.d3d_packed_draft_attn_ctas(1, 32, 8, 128, 384, 2048)

@@ -86,9 +86,10 @@ def test_invalid_arguments_rejected_on_host(d3d):
     assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 1 << 20, 0, -1)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 1 << 20, 0, 3, None, fake)) == d3d.D3D_ERR_INVALID_ARG
 
-    def attn(R=1, Hq=32, Hkv=8, d=128, max_q=16, scale=0.1, ws=fake, wsb=1 << 30):
+    def attn(R=1, Hq=32, Hkv=8, d=128, max_q=16, scale=0.1, ws=fake, wsb=1 << 30, flags=0):
         return L.d3d_packed_draft_attn(fake, fake, fake, fake, fake, fake, fake, fake, fake, R, Hq, Hkv, d, max_q,
-                                       64, 16, 64, 1, scale, fake, ws, wsb, None)
+                                       64, 16, 64, 1, scale, fake, ws, wsb, flags, None)
+    assert attn(flags=2) == d3d.D3D_ERR_INVALID_ARG
     assert attn(Hq=30, Hkv=8) == d3d.D3D_ERR_INVALID_ARG
     assert attn(d=96) == d3d.D3D_ERR_UNSUPPORTED
     assert attn(Hq=24, Hkv=8) == d3d.D3D_ERR_UNSUPPORTED  # G = 3 does not divide 128
