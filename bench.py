@@ -11,10 +11,11 @@ F=2 (N_async = 384 packed query tokens), verification of 16 positions over a
 151936-entry vocabulary, and a match against 24 branch heads.  Within a
 round the packed drafting pass and the verification are independent (the
 drafter prepares the successor blocks while the current block is verified),
-so they run concurrently: the verification first, on the SMs the attention
-leaves, and the attention as its programmatic dependent on the same stream;
-the branch match runs inside the verification's last phase
-(``parts.match_us`` times the stand-alone match entry point).
+so they run concurrently: the verification on the SMs the attention leaves
+and the attention as its programmatic dependent on the same stream
+(``--round fused``: one cooperative launch holding both); the branch match
+runs inside the verification's last phase (``parts.match_us`` times the
+stand-alone match entry point).
 
 Timing: inputs resident in HBM; steps rotate over input sets whose total
 size exceeds twice the L2 cache, so no step finds its inputs in L2; each
@@ -48,9 +49,9 @@ import workloads as W  # noqa: E402
 
 METRIC = "packed-draft query tokens/s + verified positions/s; % HBM/tensor roofline"
 UNIT = "packed-draft query tokens/s"
-# our kernel launches per step: the attention, and the verification with the
-# branch match fused into its last phase
-LAUNCHES = {"attn": 1, "verify": 1}
+# our kernel launches per step: one fused round launch, or the attention and
+# the verification (with the branch match fused into its last phase)
+LAUNCHES = {"fused": 1, "split": 2}
 CSRC = os.path.join(ROOT, "diffusion_drafted_speculative_gb300", "csrc")
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of this bench's workload, keyed by a hash of the sources the
@@ -89,6 +90,9 @@ def parse_args():
     ap.add_argument("--workload", default="async8b", choices=["async8b", "long_block", "serve32b"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--round", choices=["split", "fused"], default="split",
+                    help="split: verification, then the attention as its programmatic dependent; "
+                         "fused: both in one cooperative launch (d3d_async_round)")
     return ap.parse_args()
 
 
@@ -274,16 +278,39 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     stream = torch.cuda.Stream(device=dev)
 
+    def round_calls(s):
+        a = dict(q=s["q"], k_prefix=s["kp"], v_prefix=s["vp"], k_packed=s["kn"], v_packed=s["vn"], segs=s["segs"],
+                 cu_prefix=s["cu_prefix"], cu_q=s["cu_q"], cu_seg=s["cu_seg"], max_q=max_q, max_prefix=max_prefix,
+                 scale=scale, out=s["out"], ws=ws_a)
+        v = dict(target_logits=s["target"], draft_logits=s["draft"], draft_tokens=s["y"], u_accept=s["u_accept"],
+                 u_sample=s["u_sample"], temperature=1.0, accept_len=s["accept_len"], out_tokens=s["out_tokens"],
+                 num_tokens=s["num_tokens"], ws=ws_v, heads=s["heads"], head_len=s["head_len"], branch=s["branch"])
+        return a, v
+
+    # one launch per round (on request) when the attention leaves SMs and
+    # needs no key splits
+    fused_round = args.round == "fused" and verify_sms > 0
+    if fused_round:
+        try:
+            d3d.d3d_async_round(*round_calls(sets[0]))
+            torch.cuda.synchronize()
+        except d3d.D3DError as e:
+            if e.rc != d3d.D3D_ERR_UNSUPPORTED:
+                raise
+            fused_round = False
+
     def step(s):
         # the asynchronous round: the packed drafting pass and the verification
-        # of the current block are independent and run concurrently.  The
-        # verification goes first on the SMs the attention leaves; the
-        # attention is its programmatic dependent on the same stream (it
-        # starts once every verification CTA runs and finishes after it);
-        # the branch match runs inside the verification's last phase (it needs
-        # the verified tokens and the round's branch heads only)
-        verify(s, verify_sms, fused_match=True)
-        attn(s, after_independent=verify_sms > 0)
+        # of the current block are independent and run concurrently: the
+        # verification on the SMs the attention leaves, then the attention as
+        # its programmatic dependent (or both in one cooperative launch with
+        # --round fused); the branch match runs inside the verification's last
+        # phase (it needs the verified tokens and the round's branch heads only)
+        if fused_round:
+            d3d.d3d_async_round(*round_calls(s))
+        else:
+            verify(s, verify_sms, fused_match=True)
+            attn(s, after_independent=verify_sms > 0)
 
     torch.cuda.synchronize()
 
@@ -404,7 +431,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "timing": "CUDA graph replays, CUDA events on the launching stream"},
         "verified_positions_per_s": round(world * wl["positions"] / (ms_step * 1e-3), 1),
         "parts": {"attn_us": round(t_attn * 1e3, 3), "verify_us": round(t_verify * 1e3, 3),
-                  "attn_ctas": attn_ctas, "verify_side_sms": verify_sms,
+                  "attn_ctas": attn_ctas, "verify_side_sms": verify_sms, "round_launch": "fused" if fused_round
+                  else "split",
                   "verify_side_us": round(t_verify_side * 1e3, 3),
                   "match_us": round(t_match * 1e3, 3),
                   "attn_query_tokens_per_s": round(wl["n_q"] * R / (t_attn * 1e-3), 1),
@@ -413,7 +441,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                  "frac": round(verify_gbs / peaks["hbm"], 4),
                                  "bytes": wl["verify_bytes"], "traffic": ncu_traffic(args.workload, "verify")}},
         "roofline": roof,
-        "gpu_launches": args.steps * (LAUNCHES["attn"] + LAUNCHES["verify"]),
+        "gpu_launches": args.steps * LAUNCHES["fused" if fused_round else "split"],
         "clocks": clk, "wall_s_timed_region": round(wall, 4),
     }
     if e2e is not None:

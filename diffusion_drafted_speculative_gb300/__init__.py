@@ -18,9 +18,8 @@ import torch
 __all__ = [
     "D3DError", "lib", "d3d_status_string", "d3d_version", "d3d_validate_segments",
     "d3d_packed_draft_attn", "d3d_packed_draft_attn_workspace_size", "d3d_packed_draft_attn_ctas",
-    "d3d_spec_verify",
-    "d3d_spec_verify_workspace_size", "d3d_spec_verify_noalloc", "d3d_branch_match", "d3d_workspace_status",
-    "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
+    "d3d_spec_verify", "d3d_spec_verify_workspace_size", "d3d_spec_verify_noalloc", "d3d_async_round",
+    "AttnCall", "VerifyCall", "d3d_branch_match", "d3d_workspace_status", "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
     "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
     "D3D_ERR_DEVICE_TIMEOUT", "D3D_ERR_DEVICE_INPUT", "D3D_DTYPE_F32", "D3D_DTYPE_BF16",
     "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR", "D3D_ATTN_AFTER_INDEPENDENT",
@@ -60,6 +59,7 @@ EXPORTED = {
     "d3d_branch_match": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "d3d_debug_inject_fault": (None, [_I]),
     "d3d_spec_verify_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P]),
+    "d3d_async_round": (_I, [_P, _P, _P]),
 }
 
 
@@ -169,10 +169,9 @@ def d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix) -> int:
     return n
 
 
-def d3d_packed_draft_attn(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q, cu_seg,
-                          max_q: int, max_prefix: int, scale: float, out, ws, after_independent: bool = False,
-                          stream=None) -> None:
-    """Packed drafting attention; shapes as in include/d3d.h (bf16 tensors, int32 tables)."""
+def _attn_args(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q, cu_seg, max_q, max_prefix, scale,
+               out, ws):
+    """Checked argument tuple of d3d_packed_draft_attn (without flags and stream)."""
     for t, n in ((q, "q"), (k_prefix, "k_prefix"), (v_prefix, "v_prefix"), (k_packed, "k_packed"),
                  (v_packed, "v_packed"), (out, "out")):
         _need(t, n, torch.bfloat16, 3)
@@ -188,11 +187,18 @@ def d3d_packed_draft_attn(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_pr
     R = cu_q.numel() - 1
     if cu_prefix.numel() != R + 1 or cu_seg.numel() != R + 1:
         raise ValueError("cu_prefix, cu_q and cu_seg must all have R+1 entries")
-    rc = lib.d3d_packed_draft_attn(
-        _ptr(q), _ptr(k_prefix), _ptr(v_prefix), _ptr(k_packed), _ptr(v_packed), _ptr(segs), _ptr(cu_prefix),
-        _ptr(cu_q), _ptr(cu_seg), R, Hq, Hkv, d, int(max_q), int(max_prefix), NT, LT, segs.shape[0],
-        float(scale), _ptr(out), _ptr(ws), ws.numel(), D3D_ATTN_AFTER_INDEPENDENT if after_independent else 0,
-        _stream(stream))
+    return (_ptr(q), _ptr(k_prefix), _ptr(v_prefix), _ptr(k_packed), _ptr(v_packed), _ptr(segs), _ptr(cu_prefix),
+            _ptr(cu_q), _ptr(cu_seg), R, Hq, Hkv, d, int(max_q), int(max_prefix), NT, LT, segs.shape[0],
+            float(scale), _ptr(out), _ptr(ws), ws.numel())
+
+
+def d3d_packed_draft_attn(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q, cu_seg,
+                          max_q: int, max_prefix: int, scale: float, out, ws, after_independent: bool = False,
+                          stream=None) -> None:
+    """Packed drafting attention; shapes as in include/d3d.h (bf16 tensors, int32 tables)."""
+    args = _attn_args(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q, cu_seg, max_q, max_prefix,
+                      scale, out, ws)
+    rc = lib.d3d_packed_draft_attn(*args, D3D_ATTN_AFTER_INDEPENDENT if after_independent else 0, _stream(stream))
     _check("d3d_packed_draft_attn", rc)
 
 
@@ -200,10 +206,9 @@ def d3d_spec_verify_workspace_size(R, B, V) -> int:
     return int(lib.d3d_spec_verify_workspace_size(R, B, V))
 
 
-def d3d_spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature: float,
-                    accept_len, out_tokens, num_tokens, ws, alpha=None, p_draft=None, q_draft=None,
-                    heads=None, head_len=None, branch=None, sm_limit: int = 0, stream=None) -> None:
-    """Speculative-sampling verification; logits f32 or bf16 [R,B,V] / [R,B-1,V]."""
+def _verify_args(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature, accept_len, out_tokens,
+                 num_tokens, ws, alpha, p_draft, q_draft, heads, head_len, branch):
+    """Checked argument tuple of d3d_spec_verify (without sm_limit and stream)."""
     if target_logits.dtype == torch.bfloat16:
         dt = D3D_DTYPE_BF16
     elif target_logits.dtype == torch.float32:
@@ -239,12 +244,53 @@ def d3d_spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sampl
         if tuple(heads.shape) != (R, M, B) or tuple(head_len.shape) != (R, M) or tuple(branch.shape) != (R,):
             raise ValueError("heads must be [R, M, B], head_len [R, M], branch [R]")
     _need(ws, "ws", torch.uint8, 1)
-    rc = lib.d3d_spec_verify(
-        _ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), R, B, V,
-        float(temperature), _ptr(accept_len), _ptr(out_tokens), _ptr(num_tokens), _ptr(alpha), _ptr(p_draft),
-        _ptr(q_draft), _ptr(heads) if branch is not None else None, _ptr(head_len) if branch is not None else None,
-        M, _ptr(branch), _ptr(ws), ws.numel(), int(sm_limit), _stream(stream))
+    return (_ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), R, B, V,
+            float(temperature), _ptr(accept_len), _ptr(out_tokens), _ptr(num_tokens), _ptr(alpha), _ptr(p_draft),
+            _ptr(q_draft), _ptr(heads) if branch is not None else None,
+            _ptr(head_len) if branch is not None else None, M, _ptr(branch), _ptr(ws), ws.numel())
+
+
+def d3d_spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature: float,
+                    accept_len, out_tokens, num_tokens, ws, alpha=None, p_draft=None, q_draft=None,
+                    heads=None, head_len=None, branch=None, sm_limit: int = 0, stream=None) -> None:
+    """Speculative-sampling verification; logits f32 or bf16 [R,B,V] / [R,B-1,V]."""
+    args = _verify_args(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature, accept_len,
+                        out_tokens, num_tokens, ws, alpha, p_draft, q_draft, heads, head_len, branch)
+    rc = lib.d3d_spec_verify(*args, int(sm_limit), _stream(stream))
     _check("d3d_spec_verify", rc)
+
+
+class AttnCall(ctypes.Structure):
+    """d3d_attn_call_t (include/d3d.h)."""
+    _fields_ = [(n, _P) for n in ("q", "k_prefix", "v_prefix", "k_packed", "v_packed", "segs", "cu_prefix", "cu_q",
+                                  "cu_seg")] + \
+               [(n, _I) for n in ("R", "Hq", "Hkv", "d", "max_q", "max_prefix", "total_q", "total_prefix",
+                                  "total_segs")] + \
+               [("scale", _F), ("out", _P), ("ws", _P), ("ws_bytes", _Z)]
+
+
+class VerifyCall(ctypes.Structure):
+    """d3d_verify_call_t (include/d3d.h)."""
+    _fields_ = [("target_logits", _P), ("draft_logits", _P), ("logits_dtype", _I), ("draft_tokens", _P),
+                ("u_accept", _P), ("u_sample", _P), ("R", _I), ("B", _I), ("V", _I), ("temperature", _F),
+                ("accept_len", _P), ("out_tokens", _P), ("num_tokens", _P), ("alpha", _P), ("p_draft", _P),
+                ("q_draft", _P), ("heads", _P), ("head_len", _P), ("M", _I), ("branch", _P), ("ws", _P),
+                ("ws_bytes", _Z)]
+
+
+def d3d_async_round(attn: dict, verify: dict, stream=None) -> None:
+    """The drafting attention and the verification of one round in one launch.
+
+    ``attn`` holds d3d_packed_draft_attn's keyword arguments (q, k_prefix, ...,
+    out, ws) and ``verify`` d3d_spec_verify's (target_logits, ..., ws, and the
+    optional alpha/p_draft/q_draft/heads/head_len/branch)."""
+    a = _attn_args(**attn)
+    vkw = dict(alpha=None, p_draft=None, q_draft=None, heads=None, head_len=None, branch=None)
+    vkw.update(verify)
+    v = _verify_args(**vkw)
+    ac, vc = AttnCall(*a), VerifyCall(*v)
+    rc = lib.d3d_async_round(ctypes.byref(ac), ctypes.byref(vc), _stream(stream))
+    _check("d3d_async_round", rc)
 
 
 def d3d_spec_verify_noalloc(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature: float,

@@ -52,6 +52,7 @@
 
 #include "attn_common.cuh"
 #include "sm100_ptx.cuh"
+#include "verify_body.cuh"
 
 namespace d3d {
 namespace {
@@ -272,18 +273,20 @@ __device__ __forceinline__ void cluster_merge(int sp, int w, uint32_t part, uint
     }
 }
 
+// The attention of work unit `unit` (see the top of this file).  Threads past
+// the kThreads roles (a fused round launch has more) only pass the CTA's
+// barriers.  The tensor maps live in the kernel's parameter space.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
-                   const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kn,
-                   const __grid_constant__ CUtensorMap tm_vn, const AttnParams p)
+__device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q, const CUtensorMap *tm_kp,
+                                          const CUtensorMap *tm_vp, const CUtensorMap *tm_kn,
+                                          const CUtensorMap *tm_vn, const AttnParams &p)
 {
     using Lay = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- unit: ((r * Hkv + hk) * MT + mt) * S + sp
-    unsigned u = blockIdx.x;
+    unsigned u = unit;
     const int sp = (int)(u % (unsigned)p.S);
     u /= (unsigned)p.S;
     const int mt = (int)(u % (unsigned)p.MT);
@@ -351,11 +354,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
     }
     if (warp == kTmaWarp && lane == 0) {
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_kp);
-        prefetch_tmap(&tm_vp);
-        prefetch_tmap(&tm_kn);
-        prefetch_tmap(&tm_vn);
+        prefetch_tmap(tm_q);
+        prefetch_tmap(tm_kp);
+        prefetch_tmap(tm_vp);
+        prefetch_tmap(tm_kn);
+        prefetch_tmap(tm_vn);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int k_cnt[kKStages] = {}, v_cnt[kVStages] = {};
             mbar_arrive_expect_tx(bar(B_Q), Lay::kQBytes);
             for (int cb = 0; cb < D / 64; ++cb)
-                tma_load_3d(sQ + cb * kBlockBytes, &tm_q, bar(B_Q), cb * 64, hk * p.G, b.q0 + mt * p.TQ);
+                tma_load_3d(sQ + cb * kBlockBytes, tm_q, bar(B_Q), cb * 64, hk * p.G, b.q0 + mt * p.TQ);
             auto issue = [&](int k, bool is_k) -> bool {
                 const int ns = is_k ? kKStages : kVStages;
                 const int s = k % ns;
@@ -417,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return true;  // injected fault: this tile never arrives
                 bool pre;
                 const int row = tile_row(k, pre);
-                const CUtensorMap *m = is_k ? (pre ? &tm_kp : &tm_kn) : (pre ? &tm_vp : &tm_vn);
+                const CUtensorMap *m = is_k ? (pre ? tm_kp : tm_kn) : (pre ? tm_vp : tm_vn);
                 const uint32_t dst = (is_k ? sK : sV) + s * Lay::kKBytes;
                 mbar_arrive_expect_tx(bar(full + s), Lay::kKBytes);
                 for (int cb = 0; cb < D / 64; ++cb)
@@ -528,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_drain(bar(B_DONE), 0, status);
         }
         __syncwarp();
-    } else {
+    } else if (warp < kTmaWarp) {
         // =================== softmax warpgroups ===================
         const int w = warp >> 2;  // warpgroup: key columns [32w, 32w + 32) of every tile
         const int row = tid & 127;
@@ -789,6 +792,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
 }
 
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
+                   const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kn,
+                   const __grid_constant__ CUtensorMap tm_vn, const AttnParams p)
+{
+    attn_body<D>(blockIdx.x, &tm_q, &tm_kp, &tm_vp, &tm_kn, &tm_vn, p);
+}
+
+// One launch for the asynchronous round ([D3D] "Background: asynchronous
+// drafting and cache hits": the drafter's packed pass runs while the current
+// block is verified): CTAs [0, n_attn) are the drafting attention's units,
+// the others the verification's CTAs (512 threads, every one resident: the
+// launch is cooperative).  Each CTA holds one SM, so the two parts share the
+// GPU exactly as the split launches do, without a second launch.
+template <int D, typename T>
+__global__ void __launch_bounds__(kNTLimited, 1)
+    round_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
+                 const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kn,
+                 const __grid_constant__ CUtensorMap tm_vn, const AttnParams p, const VArgs va, int n_attn)
+{
+    if (blockIdx.x < (unsigned)n_attn)
+        attn_body<D>(blockIdx.x, &tm_q, &tm_kp, &tm_vp, &tm_kn, &tm_vn, p);
+    else
+        verify_body<T, kNTLimited>(blockIdx.x - (unsigned)n_attn, gridDim.x - (unsigned)n_attn, va);
+}
+static_assert(kThreads <= kNTLimited, "the fused round launch holds the attention's roles");
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -953,6 +984,120 @@ int launch_attn(const CUtensorMap (&maps)[5], const AttnParams &prm, long long u
     return cuda_status(cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, maps[0], maps[1], maps[2], maps[3], maps[4], prm));
 }
 
+// Host-side checks of d3d_packed_draft_attn's arguments and the tensor maps,
+// parameters and plan of its launch.  Returns D3D_OK, a status, or 1 when
+// there is nothing to compute.
+int attn_prepare(const void *q, const void *k_prefix, const void *v_prefix, const void *k_packed,
+                 const void *v_packed, const d3d_segment_t *segs, const int32_t *cu_prefix, const int32_t *cu_q,
+                 const int32_t *cu_seg, int R, int Hq, int Hkv, int d, int max_q, int max_prefix, int total_q,
+                 int total_prefix, int total_segs, float scale, void *out, void *ws, size_t ws_bytes,
+                 CUtensorMap (&maps)[5], AttnParams &prm, AttnPlan &pl)
+{
+    if (R < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_q < 0 || max_prefix < 0 || total_q < 0 ||
+        total_prefix < 0 || total_segs < 0 || !(scale > 0.f) || !isfinite(scale))
+        return D3D_ERR_INVALID_ARG;
+    if (d != 64 && d != 128)
+        return D3D_ERR_UNSUPPORTED;
+    if (kBM % (Hq / Hkv) != 0 || max_q > kMaxPackedTiles * kBN)
+        return D3D_ERR_UNSUPPORTED;
+    if (R == 0 || max_q == 0)
+        return 1;
+    if (!q || !k_packed || !v_packed || !segs || !cu_prefix || !cu_q || !cu_seg || !out ||
+        (total_prefix > 0 && (!k_prefix || !v_prefix)) || total_q < 1)
+        return D3D_ERR_INVALID_ARG;
+    const void *aligned_ptrs[4] = {q, k_packed, v_packed, out};
+    for (const void *ptr : aligned_ptrs)
+        if (reinterpret_cast<uintptr_t>(ptr) % 16)
+            return D3D_ERR_INVALID_ARG;
+    if (total_prefix > 0 && (reinterpret_cast<uintptr_t>(k_prefix) % 16 || reinterpret_cast<uintptr_t>(v_prefix) % 16))
+        return D3D_ERR_INVALID_ARG;
+    if (!ws_ok(ws, ws_bytes, sizeof(WsHeader)))
+        return D3D_ERR_WORKSPACE;
+    pl = d == 64 ? make_plan<64>(R, Hq, Hkv, max_q, max_prefix) : make_plan<128>(R, Hq, Hkv, max_q, max_prefix);
+    if (pl.units > 0x7fffffffLL)
+        return D3D_ERR_UNSUPPORTED;
+    if (!make_map(&maps[0], q, d, Hq, total_q, pl.G, pl.TQ) || !make_map(&maps[3], k_packed, d, Hkv, total_q, 1, kBN) ||
+        !make_map(&maps[4], v_packed, d, Hkv, total_q, 1, kBN))
+        return D3D_ERR_CUDA;
+    if (total_prefix > 0) {
+        if (!make_map(&maps[1], k_prefix, d, Hkv, total_prefix, 1, kBN) ||
+            !make_map(&maps[2], v_prefix, d, Hkv, total_prefix, 1, kBN))
+            return D3D_ERR_CUDA;
+    } else {  // no prefix rows anywhere: the prefix maps are never used
+        maps[1] = maps[3];
+        maps[2] = maps[4];
+    }
+    prm.segs = segs;
+    prm.cu_prefix = cu_prefix;
+    prm.cu_q = cu_q;
+    prm.cu_seg = cu_seg;
+    prm.out = static_cast<uint16_t *>(out);
+    prm.ws = static_cast<unsigned char *>(ws);
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.G = pl.G;
+    prm.TQ = pl.TQ;
+    prm.MT = pl.MT;
+    prm.S = pl.S;
+    prm.PK = pl.PK;
+    prm.max_q = max_q;
+    prm.max_prefix = max_prefix;
+    prm.total_q = total_q;
+    prm.total_prefix = total_prefix;
+    prm.total_segs = total_segs;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.fault = g_fault_mode;
+    return D3D_OK;
+}
+
+// The fused round launch: n_attn attention CTAs, then n_verify verification
+// CTAs, one per SM, cooperative.
+template <int D, typename T>
+int launch_round(const CUtensorMap (&maps)[5], const AttnParams &prm, int n_attn, const VArgs &va, cudaStream_t stream)
+{
+    const VerifyLayout L = verify_layout(va.R, va.B, va.V, VCfg<kNTLimited>::kChunk);
+    const long long nA = (long long)va.R * va.B * L.nch;
+    size_t dyn = verify_dyn_smem(va.B, L.nch);
+    if (dyn < Layout<D>::alloc)
+        dyn = Layout<D>::alloc;
+    // the attention's carve-up is the larger one (a verification CTA stages at
+    // most 32 KB of records); the static shared memory of the verification
+    // part comes on top of it
+    if (dyn > Layout<D>::alloc)
+        return D3D_ERR_UNSUPPORTED;
+    dyn = Layout<D>::alloc;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(round_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)Layout<D>::alloc);
+    });
+    int dev = 0, nsm = 0, per_sm = 0;
+    if (attr_err != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, round_kernel<D, T>, kNTLimited, dyn) != cudaSuccess ||
+        per_sm < 1) {
+        cudaGetLastError();
+        return D3D_ERR_CUDA;
+    }
+    if (n_attn >= nsm * per_sm || nA > 0x7fffffffLL)
+        return D3D_ERR_UNSUPPORTED;
+    const long long room = (long long)nsm * per_sm - n_attn;
+    const int n_verify = (int)(nA < room ? nA : room);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(n_attn + n_verify));
+    cfg.blockDim = dim3(kNTLimited);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, round_kernel<D, T>, maps[0], maps[1], maps[2], maps[3], maps[4], prm,
+                                          va, n_attn));
+}
+
 }  // namespace
 }  // namespace d3d
 
@@ -989,70 +1134,55 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
                           int max_prefix, int total_q, int total_prefix, int total_segs, float scale, void *out,
                           void *ws, size_t ws_bytes, int flags, cudaStream_t stream)
 {
-    if (R < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_q < 0 || max_prefix < 0 || total_q < 0 ||
-        total_prefix < 0 || total_segs < 0 || !(scale > 0.f) || !isfinite(scale) ||
-        (flags & ~D3D_ATTN_AFTER_INDEPENDENT) != 0)
+    if ((flags & ~D3D_ATTN_AFTER_INDEPENDENT) != 0)
         return D3D_ERR_INVALID_ARG;
-    if (d != 64 && d != 128)
-        return D3D_ERR_UNSUPPORTED;
-    if (d3d::kBM % (Hq / Hkv) != 0 || max_q > d3d::kMaxPackedTiles * d3d::kBN)
-        return D3D_ERR_UNSUPPORTED;
-    if (R == 0 || max_q == 0)
-        return D3D_OK;
-    if (!q || !k_packed || !v_packed || !segs || !cu_prefix || !cu_q || !cu_seg || !out ||
-        (total_prefix > 0 && (!k_prefix || !v_prefix)) || total_q < 1)
-        return D3D_ERR_INVALID_ARG;
-    const void *aligned_ptrs[4] = {q, k_packed, v_packed, out};
-    for (const void *ptr : aligned_ptrs)
-        if (reinterpret_cast<uintptr_t>(ptr) % 16)
-            return D3D_ERR_INVALID_ARG;
-    if (total_prefix > 0 && (reinterpret_cast<uintptr_t>(k_prefix) % 16 || reinterpret_cast<uintptr_t>(v_prefix) % 16))
-        return D3D_ERR_INVALID_ARG;
-    if (!d3d::ws_ok(ws, ws_bytes, sizeof(d3d::WsHeader)))
-        return D3D_ERR_WORKSPACE;
-    const d3d::AttnPlan pl = d == 64 ? d3d::make_plan<64>(R, Hq, Hkv, max_q, max_prefix)
-                                     : d3d::make_plan<128>(R, Hq, Hkv, max_q, max_prefix);
-    if (pl.units > 0x7fffffffLL)
-        return D3D_ERR_UNSUPPORTED;
-
     CUtensorMap maps[5];
-    if (!d3d::make_map(&maps[0], q, d, Hq, total_q, pl.G, pl.TQ) ||
-        !d3d::make_map(&maps[3], k_packed, d, Hkv, total_q, 1, d3d::kBN) ||
-        !d3d::make_map(&maps[4], v_packed, d, Hkv, total_q, 1, d3d::kBN))
-        return D3D_ERR_CUDA;
-    if (total_prefix > 0) {
-        if (!d3d::make_map(&maps[1], k_prefix, d, Hkv, total_prefix, 1, d3d::kBN) ||
-            !d3d::make_map(&maps[2], v_prefix, d, Hkv, total_prefix, 1, d3d::kBN))
-            return D3D_ERR_CUDA;
-    } else {  // no prefix rows anywhere: the prefix maps are never used
-        maps[1] = maps[3];
-        maps[2] = maps[4];
-    }
-
     d3d::AttnParams prm;
-    prm.segs = segs;
-    prm.cu_prefix = cu_prefix;
-    prm.cu_q = cu_q;
-    prm.cu_seg = cu_seg;
-    prm.out = static_cast<uint16_t *>(out);
-    prm.ws = static_cast<unsigned char *>(ws);
-    prm.Hq = Hq;
-    prm.Hkv = Hkv;
-    prm.G = pl.G;
-    prm.TQ = pl.TQ;
-    prm.MT = pl.MT;
-    prm.S = pl.S;
-    prm.PK = pl.PK;
-    prm.max_q = max_q;
-    prm.max_prefix = max_prefix;
-    prm.total_q = total_q;
-    prm.total_prefix = total_prefix;
-    prm.total_segs = total_segs;
-    prm.scale_log2 = scale * 1.4426950408889634f;
-    prm.fault = d3d::g_fault_mode;
+    d3d::AttnPlan pl;
+    const int rc = d3d::attn_prepare(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q, cu_seg, R, Hq,
+                                     Hkv, d, max_q, max_prefix, total_q, total_prefix, total_segs, scale, out, ws,
+                                     ws_bytes, maps, prm, pl);
+    if (rc != D3D_OK)
+        return rc == 1 ? D3D_OK : rc;
     if (d == 64)
         return d3d::launch_attn<64>(maps, prm, pl.units, flags, stream);
     return d3d::launch_attn<128>(maps, prm, pl.units, flags, stream);
+}
+
+int d3d_async_round(const d3d_attn_call_t *a, const d3d_verify_call_t *v, cudaStream_t stream)
+{
+    if (!a || !v)
+        return D3D_ERR_INVALID_ARG;
+    // the verification's checks first: they make no CUDA call
+    d3d::VArgs va;
+    const int rv = d3d::verify_prepare(v->target_logits, v->draft_logits, v->logits_dtype, v->draft_tokens,
+                                       v->u_accept, v->u_sample, v->R, v->B, v->V, v->temperature, v->accept_len,
+                                       v->out_tokens, v->num_tokens, v->alpha, v->p_draft, v->q_draft, v->heads,
+                                       v->head_len, v->M, v->branch, va);
+    if (rv < 0)
+        return rv;
+    CUtensorMap maps[5];
+    d3d::AttnParams prm;
+    d3d::AttnPlan pl;
+    const int ra = d3d::attn_prepare(a->q, a->k_prefix, a->v_prefix, a->k_packed, a->v_packed, a->segs, a->cu_prefix,
+                                     a->cu_q, a->cu_seg, a->R, a->Hq, a->Hkv, a->d, a->max_q, a->max_prefix,
+                                     a->total_q, a->total_prefix, a->total_segs, a->scale, a->out, a->ws,
+                                     a->ws_bytes, maps, prm, pl);
+    if (ra < 0)
+        return ra;
+    if (ra == 1 || rv == 1)  // a part with nothing to compute: nothing to fuse
+        return D3D_ERR_UNSUPPORTED;
+    if (!d3d::ws_ok(v->ws, v->ws_bytes, d3d::verify_layout(v->R, v->B, v->V, d3d::kVChunkMin).total))
+        return D3D_ERR_WORKSPACE;
+    va.ws = static_cast<unsigned char *>(v->ws);
+    if (pl.S != 1)  // the fused launch takes whole query tiles only (no key-split clusters)
+        return D3D_ERR_UNSUPPORTED;
+    const int n_attn = (int)pl.units;
+    if (a->d == 64)
+        return v->logits_dtype == D3D_DTYPE_BF16 ? d3d::launch_round<64, uint16_t>(maps, prm, n_attn, va, stream)
+                                                 : d3d::launch_round<64, float>(maps, prm, n_attn, va, stream);
+    return v->logits_dtype == D3D_DTYPE_BF16 ? d3d::launch_round<128, uint16_t>(maps, prm, n_attn, va, stream)
+                                             : d3d::launch_round<128, float>(maps, prm, n_attn, va, stream);
 }
 
 }  // extern "C"

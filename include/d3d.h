@@ -264,6 +264,51 @@ int d3d_spec_verify_noalloc(const void *target_logits, const void *draft_logits,
                             float *alpha, float *p_draft, float *q_draft, cudaStream_t stream);
 
 /* ========================================================================
+ * The asynchronous round in one launch.
+ *
+ * [D3D] "Background: asynchronous drafting and cache hits": while the target
+ * verifies the current block, the drafter's packed pass drafts the successor
+ * blocks; the two do not depend on each other.  d3d_async_round runs
+ * d3d_packed_draft_attn (*attn) and d3d_spec_verify (*verify, with its
+ * optional fused branch match) as one cooperative launch: the attention's
+ * CTAs (d3d_packed_draft_attn_ctas of them) and the verification's CTAs on
+ * the remaining SMs, one CTA per SM.  Outputs, workspaces, status words and
+ * error codes are those of the two calls.  D3D_ERR_UNSUPPORTED when the
+ * attention would split keys across CTAs or fill every SM, or when a part
+ * has nothing to compute: then make the two calls (the verification with
+ * an sm_limit, the attention with D3D_ATTN_AFTER_INDEPENDENT).
+ * Field meanings are those of the arguments of the two calls.
+ * ======================================================================== */
+typedef struct {
+    const void *q, *k_prefix, *v_prefix, *k_packed, *v_packed;
+    const d3d_segment_t *segs;
+    const int32_t *cu_prefix, *cu_q, *cu_seg;
+    int R, Hq, Hkv, d, max_q, max_prefix, total_q, total_prefix, total_segs;
+    float scale;
+    void *out;
+    void *ws;
+    size_t ws_bytes;
+} d3d_attn_call_t;
+
+typedef struct {
+    const void *target_logits, *draft_logits;
+    int logits_dtype;
+    const int32_t *draft_tokens;
+    const float *u_accept, *u_sample;
+    int R, B, V;
+    float temperature;
+    int32_t *accept_len, *out_tokens, *num_tokens;
+    float *alpha, *p_draft, *q_draft;
+    const int32_t *heads, *head_len;
+    int M;
+    int32_t *branch;
+    void *ws;
+    size_t ws_bytes;
+} d3d_verify_call_t;
+
+int d3d_async_round(const d3d_attn_call_t *attn, const d3d_verify_call_t *verify, cudaStream_t stream);
+
+/* ========================================================================
  * Branch cache-hit match.
  *
  * [D3D] "Background: asynchronous drafting and cache hits": in the next

@@ -328,6 +328,63 @@ def test_round_verification_then_overlapping_attention(d3d):
     assert d3d.d3d_workspace_status(wsa) == 0 and d3d.d3d_workspace_status(wsv) == 0
 
 
+def _round_calls(d3d, cfg, seed):
+    """Device inputs and outputs of one round (attention + verification with
+    the fused match) as the keyword dicts d3d_async_round takes."""
+    from gpu_util import bf16, f32, i32
+    a = W.attn_inputs(**cfg, seed=seed)
+    v = W.verify_inputs(**cfg, seed=seed)
+    ref_v = oracle.spec_verify(v)
+    hb = _heads_hitting(ref_v, cfg["B"], cfg["V"], 24, seed=seed + 1)
+    R, B = v["R"], v["B"]
+    attn = dict(q=bf16(a["q"]), k_prefix=bf16(a["kp"]), v_prefix=bf16(a["vp"]), k_packed=bf16(a["kn"]),
+                v_packed=bf16(a["vn"]), segs=i32(a["segs"]), cu_prefix=i32(a["cu_prefix"]), cu_q=i32(a["cu_q"]),
+                cu_seg=i32(a["cu_seg"]), max_q=a["max_q"], max_prefix=a["max_prefix"], scale=a["scale"])
+    attn["out"] = torch.full_like(attn["q"], float("nan"))
+    attn["ws"] = d3d.new_workspace(d3d.d3d_packed_draft_attn_workspace_size(a["R"], a["Hq"], a["Hkv"], a["d"],
+                                                                            a["max_q"], a["max_prefix"]))
+    verify = dict(target_logits=bf16(v["target"]), draft_logits=bf16(v["draft"]), draft_tokens=i32(v["y"]),
+                  u_accept=f32(v["u_accept"]), u_sample=f32(v["u_sample"]), temperature=1.0,
+                  accept_len=torch.full((R,), -7, dtype=torch.int32, device="cuda"),
+                  out_tokens=torch.full((R, B), -7, dtype=torch.int32, device="cuda"),
+                  num_tokens=torch.full((R,), -7, dtype=torch.int32, device="cuda"),
+                  heads=i32(hb["heads"]), head_len=i32(hb["head_len"]),
+                  branch=torch.full((R,), -7, dtype=torch.int32, device="cuda"),
+                  ws=d3d.new_workspace(d3d.d3d_spec_verify_workspace_size(R, B, v["V"])))
+    return a, v, ref_v, hb, attn, verify
+
+
+def test_async_round_in_one_launch(d3d):
+    # the drafting attention and the verification (with the fused match) of
+    # the 384-token async round as one cooperative launch, three times over
+    # the same workspaces: every output meets the oracle
+    cfg = W.CONFIGS["async8b"]
+    a, v, ref_v, hb, attn, verify = _round_calls(d3d, cfg, seed=33)
+    ref_a = oracle.packed_attn(a, heads=(0, 4))
+    for _ in range(3):
+        attn["out"].fill_(float("nan"))
+        for k in ("accept_len", "out_tokens", "num_tokens", "branch"):
+            verify[k].fill_(-7)
+        d3d.d3d_async_round(attn, verify)
+        torch.cuda.synchronize()
+        got = {k: verify[k].cpu().numpy() for k in ("accept_len", "out_tokens", "num_tokens", "branch")}
+        compare_verify(got, ref_v, min_kept=0.0)
+        want = oracle.branch_match(dict(verified=got["out_tokens"], verified_len=got["num_tokens"], **hb))
+        np.testing.assert_array_equal(got["branch"], want)
+        assert_attn_close(attn["out"].float().cpu().numpy()[:, 0:4], ref_a[:, 0:4], "fused round attention")
+    assert d3d.d3d_workspace_status(attn["ws"]) == 0 and d3d.d3d_workspace_status(verify["ws"]) == 0
+
+
+def test_async_round_declines_key_splits(d3d):
+    # a long prefix with few query tiles splits keys across a cluster: the
+    # fused launch declines and the two calls do the round
+    cfg = dict(W.CONFIGS["long_block"], V=4096)
+    a, v, ref_v, hb, attn, verify = _round_calls(d3d, cfg, seed=34)
+    with pytest.raises(d3d.D3DError) as e:
+        d3d.d3d_async_round(attn, verify)
+    assert e.value.rc == d3d.D3D_ERR_UNSUPPORTED
+
+
 def test_attention_cta_count_matches_plan(d3d):
     # one CTA per query tile and key split, all in one wave on this GPU
     n = d3d.d3d_packed_draft_attn_ctas(1, 32, 8, 128, 384, 2048)

@@ -103,6 +103,19 @@ def test_invalid_arguments_rejected_on_host(d3d):
     assert ctas(1, 24, 8, 128, 16, 64) == d3d.D3D_ERR_UNSUPPORTED
     assert ctas(0, 32, 8, 128, 16, 64) == 0 and ctas(1, 32, 8, 128, 0, 64) == 0
 
+    # the fused round: missing calls, then each part's own argument checks
+    assert L.d3d_async_round(None, None, None) == d3d.D3D_ERR_INVALID_ARG
+    ac = d3d.AttnCall(*([fake] * 9 + [1, 30, 8, 128, 16, 64, 16, 64, 1, 0.1, fake, fake, 1 << 30]))
+    vc = d3d.VerifyCall(fake, fake, 1, fake, fake, fake, 1, 4, 10, 1.0, fake, fake, fake, None, None, None, None,
+                        None, 0, None, fake, 1 << 20)
+    assert L.d3d_async_round(ctypes.byref(ac), ctypes.byref(vc), None) == d3d.D3D_ERR_INVALID_ARG  # Hq % Hkv
+    ac.Hq = 32
+    vc.temperature = 0.0
+    assert L.d3d_async_round(ctypes.byref(ac), ctypes.byref(vc), None) == d3d.D3D_ERR_INVALID_ARG  # T <= 0
+    vc.temperature = 1.0
+    ac.d = 96
+    assert L.d3d_async_round(ctypes.byref(ac), ctypes.byref(vc), None) == d3d.D3D_ERR_UNSUPPORTED
+
     assert L.d3d_branch_match(fake, fake, fake, fake, 1, 2, 0, fake, None) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_branch_match(None, fake, fake, fake, 1, 2, 4, fake, None) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_branch_match(fake, fake, fake, fake, 0, 2, 4, fake, None) == d3d.D3D_OK
