@@ -1053,8 +1053,12 @@ int attn_prepare(const void *q, const void *k_prefix, const void *v_prefix, cons
 // The fused round launch: n_attn attention CTAs, then n_verify verification
 // CTAs, one per SM, cooperative.
 template <int D, typename T>
-int launch_round(const CUtensorMap (&maps)[5], const AttnParams &prm, int n_attn, const VArgs &va, cudaStream_t stream)
+int launch_round(const CUtensorMap (&maps)[5], const AttnParams &prm, int n_attn, const VArgs &va_in,
+                 cudaStream_t stream)
 {
+    VArgs va = va_in;
+    if (ring_fits<T, kNTLimited>(va) && Ring<kNTLimited>::bytes(kRingSlots) <= Layout<D>::alloc)
+        va.ring = kRingSlots;  // the attention's shared memory holds the verification's phase-A ring
     const VerifyLayout L = verify_layout(va.R, va.B, va.V, VCfg<kNTLimited>::kChunk);
     const long long nA = (long long)va.R * va.B * L.nch;
     size_t dyn = verify_dyn_smem(va.B, L.nch);

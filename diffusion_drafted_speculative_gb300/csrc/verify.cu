@@ -10,13 +10,29 @@ namespace d3d {
 namespace {
 
 template <typename T, int NT>
-int launch_verify_nt(const VArgs &a, int sm_limit, cudaStream_t stream)
+int launch_verify_nt(const VArgs &a_in, int sm_limit, cudaStream_t stream)
 {
+    VArgs a = a_in;
     const VerifyLayout L = verify_layout(a.R, a.B, a.V, VCfg<NT>::kChunk);
     const long long nA = (long long)a.R * a.B * L.nch;
     if (nA > 0x7fffffffLL)
         return D3D_ERR_UNSUPPORTED;
-    const size_t dyn = verify_dyn_smem(a.B, L.nch);
+    size_t dyn = verify_dyn_smem(a.B, L.nch);
+    if (ring_fits<T, NT>(a)) {  // phase A through a shared-memory ring (one CTA per SM)
+        static std::once_flag once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(once, [] {
+            attr_err = cudaFuncSetAttribute(verify_kernel<T, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)Ring<NT>::bytes(kRingSlots));
+        });
+        if (attr_err == cudaSuccess) {
+            a.ring = kRingSlots;
+            if (dyn < Ring<NT>::bytes(kRingSlots))
+                dyn = Ring<NT>::bytes(kRingSlots);
+        } else {
+            cudaGetLastError();
+        }
+    }
     // every CTA must be resident (CTAs wait on one another): at most the
     // occupancy limit (and the SM limit), and no more than there are phase-A items
     int dev = 0, nsm = 0, per_sm = 0;

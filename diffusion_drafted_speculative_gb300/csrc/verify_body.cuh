@@ -163,6 +163,16 @@ template <typename T, int NT> struct RawChunk {
     __device__ void take(const T *row, int v0, int v1, float c, float (&x)[kVPer]) { load_chunk<T, NT>(row, v0, v1, c, x); }
 };
 
+// The 512-thread launch streams bf16 rows through its shared-memory ring; its
+// fallback for rows off the 16-byte grid loads at use, keeping registers free.
+template <> struct RawChunk<uint16_t, kNTLimited> {
+    __device__ void issue(const uint16_t *, int, int) {}
+    __device__ void take(const uint16_t *row, int v0, int v1, float c, float (&x)[kVPer])
+    {
+        load_chunk<uint16_t, kNTLimited>(row, v0, v1, c, x);
+    }
+};
+
 template <int NT> struct RawChunk<uint16_t, NT> {
     uint4 u[kVPer / 8];
     bool ok;
@@ -232,7 +242,35 @@ __device__ inline void thread_exp(float (&x)[kVPer], float &m, float &z)
     }
 }
 
+// The same on raw (unscaled) logits with the scale c > 0 folded into the
+// exponent: x[i] becomes exp2(c*x[i] - m) with m = c * max(raw) this thread's
+// scaled max, by one fused multiply-add per pair of entries.
+__device__ inline void thread_exp_scaled(float (&x)[kVPer], float c, float &m, float &z)
+{
+    float m4[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+    for (int i = 4; i < kVPer; i += 4)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            m4[e] = fmaxf(m4[e], x[i + e]);
+    const float mr = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    m = (mr == -INFINITY) ? -INFINITY : mr * c;
+    const float nm = (mr == -INFINITY) ? 0.f : -m;
+    float za = 0.f, zb = 0.f;
+#pragma unroll
+    for (int i = 0; i < kVPer; i += 2) {
+        float a0, a1;
+        sm100::ffma2(a0, a1, x[i], x[i + 1], c, c, nm, nm);
+        x[i] = fast_exp2(a0);
+        x[i + 1] = fast_exp2(a1);
+        sm100::fadd2(za, zb, za, zb, x[i], x[i + 1]);
+    }
+    z = za + zb;
+}
+
 // Block-wide merge of two (max, sum) pairs; the result is valid in thread 0.
+// Warps reduce by shuffles; warp 0 then merges the per-warp pairs by a
+// shuffle tree (log2 of the warp count steps instead of a serial loop).
 template <int NT>
 __device__ inline void block_ms2(float &m1, float &z1, float &m2, float &z2, float *red)
 {
@@ -243,19 +281,26 @@ __device__ inline void block_ms2(float &m1, float &z1, float &m2, float &z2, flo
         ms_merge(m1, z1, a, b);
         ms_merge(m2, z2, c, d);
     }
-    const int w = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
         red[4 * w + 0] = m1;
         red[4 * w + 1] = z1;
         red[4 * w + 2] = m2;
         red[4 * w + 3] = z2;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        m1 = red[0], z1 = red[1], m2 = red[2], z2 = red[3];
-        for (int i = 1; i < VCfg<NT>::kWarps; ++i) {
-            ms_merge(m1, z1, red[4 * i + 0], red[4 * i + 1]);
-            ms_merge(m2, z2, red[4 * i + 2], red[4 * i + 3]);
+    if (w == 0) {
+        constexpr int kW = VCfg<NT>::kWarps;
+        m1 = lane < kW ? red[4 * lane + 0] : -INFINITY;
+        z1 = lane < kW ? red[4 * lane + 1] : 0.f;
+        m2 = lane < kW ? red[4 * lane + 2] : -INFINITY;
+        z2 = lane < kW ? red[4 * lane + 3] : 0.f;
+#pragma unroll
+        for (int o = kW / 2; o; o >>= 1) {
+            const float a = __shfl_xor_sync(kFull, m1, o), b = __shfl_xor_sync(kFull, z1, o);
+            const float c = __shfl_xor_sync(kFull, m2, o), d = __shfl_xor_sync(kFull, z2, o);
+            ms_merge(m1, z1, a, b);
+            ms_merge(m2, z2, c, d);
         }
     }
 }
@@ -629,6 +674,16 @@ struct VArgs {
     const int32_t *heads, *head_len;
     int32_t *branch;
     unsigned char *ws;
+    int ring;  // > 0: phase A streams items through this many shared-memory slots (bf16 rows, bulk copies)
+};
+
+// Phase-A ring of the SM-limited launch: per slot, the target row's and the
+// draft row's chunk as bf16, then one mbarrier per slot.
+constexpr int kRingSlots = 3;
+template <int NT> struct Ring {
+    static constexpr uint32_t kRowBytes = VCfg<NT>::kChunk * 2;
+    static constexpr uint32_t kSlotBytes = 2 * kRowBytes;
+    static constexpr size_t bytes(int slots) { return (size_t)slots * kSlotBytes + (size_t)slots * 8; }
 };
 
 // The verification of CTA vb of vgrid (all vgrid CTAs resident: they wait on
@@ -693,33 +748,104 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
         return draft + ((size_t)(rj / B) * (B - 1) + (rj % B)) * V;  // valid only when j < B - 1
     };
     RawChunk<T, NT> rawP, rawQ;
-    if ((long long)vb < nA) {
+    // ring path: each slot's two row chunks arrive by bulk copies, issued
+    // kRingSlots items ahead (the host enables it for bf16 rows whose chunks
+    // are 16-byte aligned, with the ring's shared memory)
+    // (compiled for the 512-thread launch only; the 256-thread one keeps its registers)
+    const int nring = (NT == kNTLimited) ? a.ring : 0;
+    uint8_t *ring = reinterpret_cast<uint8_t *>(s_dyn);  // reused for the staged records after phase A
+    const uint32_t ring_s = sm100::smem_u32(ring), ring_bar = ring_s + (uint32_t)nring * Ring<NT>::kSlotBytes;
+    auto ring_issue = [&](long long it, int slot) {
+        int v0, v1, j;
+        const T *rp = target_row(it, v0, v1, j);
+        const uint32_t row_bytes = (uint32_t)(v1 - v0) * 2u;
+        const uint32_t bar = ring_bar + 8u * (uint32_t)slot, dst = ring_s + (uint32_t)slot * Ring<NT>::kSlotBytes;
+        sm100::mbar_arrive_expect_tx(bar, j < B - 1 ? 2u * row_bytes : row_bytes);
+        sm100::bulk_load(dst, rp + v0, row_bytes, bar);
+        if (j < B - 1)
+            sm100::bulk_load(dst + Ring<NT>::kRowBytes, draft_row(it) + v0, row_bytes, bar);
+    };
+    // slot values in the thread's slot order, raw (unscaled); -inf past v1
+    auto ring_take = [&](int slot, int row, int v0, int v1, float (&x)[kVPer]) {
+        const uint8_t *src = ring + (size_t)slot * Ring<NT>::kSlotBytes + (size_t)row * Ring<NT>::kRowBytes;
+        const bool full = v1 - v0 == C::kChunk;
+#pragma unroll
+        for (int g = 0; g < kVPer / 8; ++g) {
+            const int off = g * C::kGroup + 8 * (int)threadIdx.x;
+            const uint4 u = *reinterpret_cast<const uint4 *>(src + 2 * off);
+            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[8 * g + 2 * e] = __uint_as_float(wv[e] << 16);
+                x[8 * g + 2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
+            }
+        }
+        if (!full) {
+#pragma unroll
+            for (int i = 0; i < kVPer; ++i)
+                x[i] = slot_pos<NT>(v0, i) < v1 ? x[i] : -INFINITY;
+        }
+    };
+    if (nring > 0) {
+        if (threadIdx.x == 0) {
+            for (int sl = 0; sl < nring; ++sl)
+                sm100::mbar_init(ring_bar + 8u * (uint32_t)sl, 1);
+            sm100::fence_barrier_init();
+        }
+        __syncthreads();
+        if (threadIdx.x == 0)
+            for (int sl = 0; sl < nring && (long long)vb + (long long)sl * vgrid < nA; ++sl)
+                ring_issue((long long)vb + (long long)sl * vgrid, sl);
+    } else if ((long long)vb < nA) {
         int v0, v1, j;
         const T *rp = target_row(vb, v0, v1, j);
         rawP.issue(rp, v0, v1);
         if (j < B - 1)
             rawQ.issue(draft_row(vb), v0, v1);
     }
-    for (long long item = vb; item < nA; item += vgrid) {
+    int k_item = 0;  // this CTA's item count
+    for (long long item = vb; item < nA; item += vgrid, ++k_item) {
         int v0, v1, j;
         const T *rowP = target_row(item, v0, v1, j);
         const int r = (int)(item / nch) / B;
         const int yv = (j < B - 1) ? __ldg(y + (size_t)r * (B - 1) + j) : -1;
-        rawP.take(rowP, v0, v1, c, eP);
-        if (j < B - 1) {
-            rawQ.take(draft_row(item), v0, v1, c, eQ);
-        } else {
+        if (NT == kNTLimited && nring > 0) {
+            const int slot = k_item % nring;
+            const uint32_t bar = ring_bar + 8u * (uint32_t)slot;
+            const uint32_t parity = (uint32_t)(k_item / nring) & 1u;
+            if (!sm100::mbar_try_wait(bar, parity)) {  // bounded wait for the slot's copies
+                const uint64_t t0 = sm100::global_ns();
+                while (!sm100::mbar_try_wait_sleep(bar, parity))
+                    if (sm100::global_ns() - t0 > kBarrierTimeoutNs) {
+                        record_status(reinterpret_cast<int32_t *>(ws), D3D_ERR_DEVICE_TIMEOUT);
+                        break;
+                    }
+            }
+            ring_take(slot, 0, v0, v1, eP);
+            if (j < B - 1) {
+                ring_take(slot, 1, v0, v1, eQ);
+            } else {
 #pragma unroll
-            for (int i = 0; i < kVPer; ++i)
-                eQ[i] = -INFINITY;
-        }
-        const long long next = item + vgrid;
-        if (next < nA) {
-            int nv0, nv1, nj;
-            const T *np = target_row(next, nv0, nv1, nj);
-            rawP.issue(np, nv0, nv1);
-            if (nj < B - 1)
-                rawQ.issue(draft_row(next), nv0, nv1);
+                for (int i = 0; i < kVPer; ++i)
+                    eQ[i] = -INFINITY;
+            }
+        } else {
+            rawP.take(rowP, v0, v1, 1.f, eP);  // raw logits: the scale goes into the exponent
+            if (j < B - 1) {
+                rawQ.take(draft_row(item), v0, v1, 1.f, eQ);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kVPer; ++i)
+                    eQ[i] = -INFINITY;
+            }
+            const long long next = item + vgrid;
+            if (next < nA) {
+                int nv0, nv1, nj;
+                const T *np = target_row(next, nv0, nv1, nj);
+                rawP.issue(np, nv0, nv1);
+                if (nj < B - 1)
+                    rawQ.issue(draft_row(next), nv0, nv1);
+            }
         }
         if (yv >= v0 && yv < v1) {  // the thread holding position y keeps both logits for the record
             const int rel = yv - v0;
@@ -731,23 +857,31 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
                     xp = (i == slot) ? eP[i] : xp;
                     xq = (i == slot) ? eQ[i] : xq;
                 }
-                s_xy[0] = xp;
-                s_xy[1] = xq;
+                s_xy[0] = xp * c;
+                s_xy[1] = xq * c;
             }
         }
         float zP, zQ;
-        thread_exp(eP, mtP, zP);
-        thread_exp(eQ, mtQ, zQ);
+        thread_exp_scaled(eP, c, mtP, zP);
+        thread_exp_scaled(eQ, c, mtQ, zQ);
         float m1 = mtP, z1 = zP, m2 = mtQ, z2 = zQ;
         block_ms2<NT>(m1, z1, m2, z2, red);  // has a __syncthreads: s_xy is visible to thread 0 after it
+        const bool has = yv >= v0 && yv < v1;
+        const float xyP = (threadIdx.x == 0 && has) ? s_xy[0] : 0.f, xyQ = (threadIdx.x == 0 && has) ? s_xy[1] : 0.f;
+        __syncthreads();  // red and s_xy are reused by the next item; the slot has been read
+        // the record and its signal after the barrier: the release's wait
+        // overlaps the next item's loads and exponentials in the other warps
         if (threadIdx.x == 0) {
-            const bool has = yv >= v0 && yv < v1;
             float4 *dst = reinterpret_cast<float4 *>(rec + item);
             dst[0] = make_float4(m1, z1, m2, z2);
-            dst[1] = make_float4(has ? s_xy[0] : 0.f, has ? s_xy[1] : 0.f, 0.f, 0.f);
+            dst[1] = make_float4(xyP, xyQ, 0.f, 0.f);
             signal_count(bar + kBarInts * r);
         }
-        __syncthreads();  // red and s_xy are reused by the next item
+        if (nring > 0 && threadIdx.x == 0) {
+            const long long nxt = item + (long long)nring * vgrid;
+            if (nxt < nA)
+                ring_issue(nxt, k_item % nring);
+        }
     }
 
     __shared__ int s_kind_used, s_owner, s_takelast;
@@ -979,7 +1113,16 @@ inline int verify_prepare(const void *target_logits, const void *draft_logits, i
     a.alpha = alpha, a.p = p_draft, a.q = q_draft;
     a.heads = heads, a.head_len = head_len, a.branch = branch;
     a.ws = nullptr;
+    a.ring = 0;
     return D3D_OK;
+}
+
+// Whether a launch of NT-thread CTAs may stream phase A through the ring:
+// bf16 rows whose chunks start and end on 16-byte boundaries.
+template <typename T, int NT> inline bool ring_fits(const VArgs &a)
+{
+    return NT == kNTLimited && sizeof(T) == 2 && a.V % 8 == 0 &&
+           (reinterpret_cast<uintptr_t>(a.target) % 16) == 0 && (reinterpret_cast<uintptr_t>(a.draft) % 16) == 0;
 }
 
 }  // namespace
