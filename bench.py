@@ -51,7 +51,7 @@ METRIC = "packed-draft query tokens/s + verified positions/s; % HBM/tensor roofl
 UNIT = "packed-draft query tokens/s"
 # our kernel launches per step: one fused round launch, or the attention and
 # the verification (with the branch match fused into its last phase)
-LAUNCHES = {"fused": 1, "split": 2}
+LAUNCHES = {"fused": 1, "split": 2, "split-attention-first": 2}
 CSRC = os.path.join(ROOT, "diffusion_drafted_speculative_gb300", "csrc")
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of this bench's workload, keyed by a hash of the sources the
@@ -90,8 +90,9 @@ def parse_args():
     ap.add_argument("--workload", default="async8b", choices=["async8b", "long_block", "serve32b"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--round", choices=["split", "fused"], default="split",
-                    help="split: verification, then the attention as its programmatic dependent; "
+    ap.add_argument("--round", choices=["split", "split-attention-first", "fused"], default="split",
+                    help="split: the verification, then the attention as its programmatic dependent; "
+                         "split-attention-first: the other way round; "
                          "fused: both in one cooperative launch (d3d_async_round)")
     return ap.parse_args()
 
@@ -268,10 +269,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                   s["cu_seg"], max_q, max_prefix, scale, s["out"], ws_a,
                                   after_independent=after_independent)
 
-    def verify(s, sm_limit=0, fused_match=False):
+    def verify(s, sm_limit=0, fused_match=False, after_independent=False):
         extra = dict(heads=s["heads"], head_len=s["head_len"], branch=s["branch"]) if fused_match else {}
         d3d.d3d_spec_verify(s["target"], s["draft"], s["y"], s["u_accept"], s["u_sample"], 1.0, s["accept_len"],
-                            s["out_tokens"], s["num_tokens"], ws_v, sm_limit=sm_limit, **extra)
+                            s["out_tokens"], s["num_tokens"], ws_v, sm_limit=sm_limit,
+                            after_independent=after_independent, **extra)
 
     def match(s):
         d3d.d3d_branch_match(s["out_tokens"], s["num_tokens"], s["heads"], s["head_len"], s["branch"])
@@ -303,11 +305,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         # the asynchronous round: the packed drafting pass and the verification
         # of the current block are independent and run concurrently: the
         # verification on the SMs the attention leaves, then the attention as
-        # its programmatic dependent (or both in one cooperative launch with
-        # --round fused); the branch match runs inside the verification's last
-        # phase (it needs the verified tokens and the round's branch heads only)
+        # its programmatic dependent (--round split-attention-first: the other
+        # way round; --round fused: both in one cooperative launch); the branch
+        # match runs inside the verification's last phase (it needs the
+        # verified tokens and the round's branch heads only)
         if fused_round:
             d3d.d3d_async_round(*round_calls(s))
+        elif args.round == "split-attention-first":
+            attn(s)
+            verify(s, verify_sms, fused_match=True, after_independent=verify_sms > 0)
         else:
             verify(s, verify_sms, fused_match=True)
             attn(s, after_independent=verify_sms > 0)
@@ -432,7 +438,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "verified_positions_per_s": round(world * wl["positions"] / (ms_step * 1e-3), 1),
         "parts": {"attn_us": round(t_attn * 1e3, 3), "verify_us": round(t_verify * 1e3, 3),
                   "attn_ctas": attn_ctas, "verify_side_sms": verify_sms, "round_launch": "fused" if fused_round
-                  else "split",
+                  else args.round,
                   "verify_side_us": round(t_verify_side * 1e3, 3),
                   "match_us": round(t_match * 1e3, 3),
                   "attn_query_tokens_per_s": round(wl["n_q"] * R / (t_attn * 1e-3), 1),
@@ -441,7 +447,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                  "frac": round(verify_gbs / peaks["hbm"], 4),
                                  "bytes": wl["verify_bytes"], "traffic": ncu_traffic(args.workload, "verify")}},
         "roofline": roof,
-        "gpu_launches": args.steps * LAUNCHES["fused" if fused_round else "split"],
+        "gpu_launches": args.steps * LAUNCHES["fused" if fused_round else args.round],
         "clocks": clk, "wall_s_timed_region": round(wall, 4),
     }
     if e2e is not None:

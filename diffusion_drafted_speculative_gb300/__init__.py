@@ -22,7 +22,7 @@ __all__ = [
     "AttnCall", "VerifyCall", "d3d_branch_match", "d3d_workspace_status", "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
     "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
     "D3D_ERR_DEVICE_TIMEOUT", "D3D_ERR_DEVICE_INPUT", "D3D_DTYPE_F32", "D3D_DTYPE_BF16",
-    "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR", "D3D_ATTN_AFTER_INDEPENDENT",
+    "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR", "D3D_ATTN_AFTER_INDEPENDENT", "D3D_VERIFY_AFTER_INDEPENDENT",
 ]
 
 D3D_OK = 0
@@ -37,6 +37,7 @@ D3D_DTYPE_BF16 = 1
 D3D_SEG_CAUSAL = 0
 D3D_SEG_BIDIR = 1
 D3D_ATTN_AFTER_INDEPENDENT = 1
+D3D_VERIFY_AFTER_INDEPENDENT = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libd3d.so")
@@ -55,7 +56,7 @@ EXPORTED = {
     "d3d_spec_verify_workspace_size": (_Z, [_I, _I, _I]),
     "d3d_packed_draft_attn_ctas": (_I, [_I, _I, _I, _I, _I, _I]),
     "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P,
-                             _P, _Z, _I, _P]),
+                             _P, _Z, _I, _I, _P]),
     "d3d_branch_match": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "d3d_debug_inject_fault": (None, [_I]),
     "d3d_spec_verify_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P]),
@@ -252,11 +253,13 @@ def _verify_args(target_logits, draft_logits, draft_tokens, u_accept, u_sample, 
 
 def d3d_spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature: float,
                     accept_len, out_tokens, num_tokens, ws, alpha=None, p_draft=None, q_draft=None,
-                    heads=None, head_len=None, branch=None, sm_limit: int = 0, stream=None) -> None:
+                    heads=None, head_len=None, branch=None, sm_limit: int = 0, after_independent: bool = False,
+                    stream=None) -> None:
     """Speculative-sampling verification; logits f32 or bf16 [R,B,V] / [R,B-1,V]."""
     args = _verify_args(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature, accept_len,
                         out_tokens, num_tokens, ws, alpha, p_draft, q_draft, heads, head_len, branch)
-    rc = lib.d3d_spec_verify(*args, int(sm_limit), _stream(stream))
+    rc = lib.d3d_spec_verify(*args, int(sm_limit), D3D_VERIFY_AFTER_INDEPENDENT if after_independent else 0,
+                             _stream(stream))
     _check("d3d_spec_verify", rc)
 
 

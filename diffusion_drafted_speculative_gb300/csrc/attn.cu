@@ -294,6 +294,10 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
     const int hk = (int)(u % (unsigned)p.Hkv);
     const int r = (int)(u / (unsigned)p.Hkv);
     int32_t *status = reinterpret_cast<int32_t *>(p.ws);
+    // a kernel launched after this one as an independent programmatic
+    // dependent (the verification of the same round) may start now
+    if (tid == 0)
+        pdl_trigger();
 
     // early exits are uniform over the CTAs of a cluster (same r and tile).
     // Every exit first waits for a kernel this launch overlaps (programmatic

@@ -10,7 +10,7 @@ namespace d3d {
 namespace {
 
 template <typename T, int NT>
-int launch_verify_nt(const VArgs &a_in, int sm_limit, cudaStream_t stream)
+int launch_verify_nt(const VArgs &a_in, int sm_limit, int flags, cudaStream_t stream)
 {
     VArgs a = a_in;
     const VerifyLayout L = verify_layout(a.R, a.B, a.V, VCfg<NT>::kChunk);
@@ -50,22 +50,28 @@ int launch_verify_nt(const VArgs &a_in, int sm_limit, cudaStream_t stream)
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = dyn;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    unsigned na = 1;
+    if (flags & D3D_VERIFY_AFTER_INDEPENDENT) {  // may start while the previous kernel runs
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, verify_kernel<T, NT>, a);
     return cuda_status(e);
 }
 
 // With an SM limit the CTAs are 512 threads, one per SM (the register file
 // holds one): a launch beside another kernel takes at most sm_limit SMs.
-template <typename T> int launch_verify(const VArgs &a, int sm_limit, cudaStream_t stream)
+template <typename T> int launch_verify(const VArgs &a, int sm_limit, int flags, cudaStream_t stream)
 {
     if (sm_limit > 0)
-        return launch_verify_nt<T, kNTLimited>(a, sm_limit, stream);
-    return launch_verify_nt<T, kNTDevice>(a, 0, stream);
+        return launch_verify_nt<T, kNTLimited>(a, sm_limit, flags, stream);
+    return launch_verify_nt<T, kNTDevice>(a, 0, flags, stream);
 }
 
 }  // namespace
@@ -85,9 +91,10 @@ int d3d_spec_verify(const void *target_logits, const void *draft_logits, int log
                     const int32_t *draft_tokens, const float *u_accept, const float *u_sample, int R, int B,
                     int V, float temperature, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
                     float *alpha, float *p_draft, float *q_draft, const int32_t *heads, const int32_t *head_len,
-                    int M, int32_t *branch, void *ws, size_t ws_bytes, int sm_limit, cudaStream_t stream)
+                    int M, int32_t *branch, void *ws, size_t ws_bytes, int sm_limit, int flags,
+                    cudaStream_t stream)
 {
-    if (sm_limit < 0)
+    if (sm_limit < 0 || (flags & ~D3D_VERIFY_AFTER_INDEPENDENT) != 0)
         return D3D_ERR_INVALID_ARG;
     d3d::VArgs a;
     const int rc = d3d::verify_prepare(target_logits, draft_logits, logits_dtype, draft_tokens, u_accept, u_sample,
@@ -99,8 +106,8 @@ int d3d_spec_verify(const void *target_logits, const void *draft_logits, int log
         return D3D_ERR_WORKSPACE;
     a.ws = static_cast<unsigned char *>(ws);
     if (logits_dtype == D3D_DTYPE_BF16)
-        return d3d::launch_verify<uint16_t>(a, sm_limit, stream);
-    return d3d::launch_verify<float>(a, sm_limit, stream);
+        return d3d::launch_verify<uint16_t>(a, sm_limit, flags, stream);
+    return d3d::launch_verify<float>(a, sm_limit, flags, stream);
 }
 
 }  // extern "C"
@@ -183,6 +190,6 @@ extern "C" int d3d_spec_verify_noalloc(const void *target_logits, const void *dr
         return D3D_ERR_CUDA;
     a.ws = static_cast<unsigned char *>(scratch);
     if (logits_dtype == D3D_DTYPE_BF16)
-        return d3d::launch_verify<uint16_t>(a, 0, stream);
-    return d3d::launch_verify<float>(a, 0, stream);
+        return d3d::launch_verify<uint16_t>(a, 0, 0, stream);
+    return d3d::launch_verify<float>(a, 0, 0, stream);
 }

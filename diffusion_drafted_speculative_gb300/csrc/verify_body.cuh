@@ -725,7 +725,7 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     Rec *s_rec = reinterpret_cast<Rec *>(s_dyn);
     // a kernel launched after this one as an independent programmatic
-    // dependent (the drafting attention of the same round) may start now
+    // dependent may start now
     if (threadIdx.x == 0)
         sm100::pdl_trigger();
     // one phase-A item per CTA: its exponentials stay in registers for phase C
@@ -1067,6 +1067,9 @@ template <typename T, int NT>
 __global__ void __launch_bounds__(NT, NT == kNTDevice ? 2 : 1) verify_kernel(const VArgs a)
 {
     verify_body<T, NT>(blockIdx.x, gridDim.x, a);
+    // launched as the programmatic dependent of an independent kernel (the
+    // drafting attention of the round): finish only after it has finished
+    sm100::pdl_wait();
 }
 
 // Dynamic shared memory of a verification CTA: the request's records when

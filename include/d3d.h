@@ -222,16 +222,26 @@ void d3d_debug_inject_fault(int mode);
  *               another stream (the drafting attention of the same round)
  *               keeps the remaining SMs whichever starts first.  Results do
  *               not depend on it.  Negative: D3D_ERR_INVALID_ARG.
+ *   flags       0, or D3D_VERIFY_AFTER_INDEPENDENT: the launch may start
+ *               while the kernel before it on the stream still runs
+ *               (programmatic dependent launch) -- for the drafting attention
+ *               of the same round, launched first, whose output the
+ *               verification does not read; give an sm_limit that leaves the
+ *               attention's SMs.  The verification still finishes only after
+ *               that kernel has finished.  Other bits: D3D_ERR_INVALID_ARG.
  * A draft token outside [0, V) sets D3D_ERR_DEVICE_INPUT in the status word
  * and is treated as rejected (alpha = 0).
  * ======================================================================== */
+#define D3D_VERIFY_AFTER_INDEPENDENT 1
+
 size_t d3d_spec_verify_workspace_size(int R, int B, int V);
 
 int d3d_spec_verify(const void *target_logits, const void *draft_logits, int logits_dtype,
                     const int32_t *draft_tokens, const float *u_accept, const float *u_sample, int R, int B,
                     int V, float temperature, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
                     float *alpha, float *p_draft, float *q_draft, const int32_t *heads, const int32_t *head_len,
-                    int M, int32_t *branch, void *ws, size_t ws_bytes, int sm_limit, cudaStream_t stream);
+                    int M, int32_t *branch, void *ws, size_t ws_bytes, int sm_limit, int flags,
+                    cudaStream_t stream);
 
 /*
  * Verification that allocates nothing (the pages have no counterpart: this

@@ -289,10 +289,13 @@ def test_verify_fused_match(d3d, cfg, sm_limit):
     assert d3d.d3d_workspace_status(ws) == 0
 
 
-def test_round_verification_then_overlapping_attention(d3d):
-    # one stream: the verification on the SMs the attention leaves, then the
-    # attention as its programmatic dependent, repeated; both outputs meet the
-    # oracle and a later reader sees both complete
+@pytest.mark.parametrize("attention_first", [False, True])
+def test_round_on_one_stream_overlapping(d3d, attention_first):
+    # one stream, the two parts of a round overlapping: the verification on
+    # the SMs the attention leaves and the attention as its programmatic
+    # dependent, or the attention first and the verification as its
+    # dependent; repeated, both outputs meet the oracle and a later reader
+    # sees both complete
     cfg = W.CONFIGS["async8b"]
     a = W.attn_inputs(**cfg, seed=21)
     v = W.verify_inputs(**cfg, seed=21)
@@ -316,11 +319,20 @@ def test_round_verification_then_overlapping_attention(d3d):
         for _ in range(5):
             out = torch.full_like(t["q"], float("nan"))
             toks.fill_(-7)
-            d3d.d3d_spec_verify(tg, dr, i32(v["y"]), f32(v["u_accept"]), f32(v["u_sample"]), 1.0, acc, toks, nt, wsv,
-                                sm_limit=side)
-            d3d.d3d_packed_draft_attn(t["q"], t["kp"], t["vp"], t["kn"], t["vn"], ix["segs"], ix["cu_prefix"],
-                                      ix["cu_q"], ix["cu_seg"], a["max_q"], a["max_prefix"], a["scale"], out, wsa,
-                                      after_independent=True)
+            def ver():
+                d3d.d3d_spec_verify(tg, dr, i32(v["y"]), f32(v["u_accept"]), f32(v["u_sample"]), 1.0, acc, toks, nt,
+                                    wsv, sm_limit=side, after_independent=attention_first)
+
+            def att():
+                d3d.d3d_packed_draft_attn(t["q"], t["kp"], t["vp"], t["kn"], t["vn"], ix["segs"], ix["cu_prefix"],
+                                          ix["cu_q"], ix["cu_seg"], a["max_q"], a["max_prefix"], a["scale"], out, wsa,
+                                          after_independent=not attention_first)
+            if attention_first:
+                att()
+                ver()
+            else:
+                ver()
+                att()
             got_t, got_o = toks.cpu().numpy(), out.float().cpu().numpy()  # read after both, same stream
             keep = (ref_v["margin_accept"] >= 1e-5) & (ref_v["margin_sample"] >= 1e-5)
             np.testing.assert_array_equal(got_t[keep], ref_v["out_tokens"][keep])

@@ -68,10 +68,11 @@ def test_invalid_arguments_rejected_on_host(d3d):
     L = d3d.lib
     fake = ctypes.c_void_p(256)  # never dereferenced: the checks fail first
     # verify: B < 2, V < 1, T <= 0, bad dtype, missing workspace
-    args = lambda R, B, V, T, dt, ws, wsb, sm=0, M=0, heads=None, br=None: (  # noqa
+    args = lambda R, B, V, T, dt, ws, wsb, sm=0, M=0, heads=None, br=None, fl=0: (  # noqa
         fake, fake, dt, fake, fake, fake, R, B, V, T, fake, fake, fake, None, None, None, heads, heads, M, br, ws, wsb,
-        sm, None)
+        sm, fl, None)
     assert L.d3d_spec_verify(*args(1, 1, 10, 1.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
+    assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 1 << 20, fl=2)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 0, 1.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 10, 0.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 10, -1.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
