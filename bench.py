@@ -57,10 +57,11 @@ CSRC = os.path.join(ROOT, "diffusion_drafted_speculative_gb300", "csrc")
 # ncu capture of this bench's workload, keyed by a hash of the sources the
 # kernel is built from: reported only while those sources are unchanged.
 NCU_TRAFFIC = {
-    ("async8b", "attn"): {"sources": ("attn.cu", "attn_common.cuh", "sm100_ptx.cuh", "d3d_common.cuh"),
-                          "sha": "f93ee60f6ec46a75", "bytes": 13359616},
-    ("async8b", "verify"): {"sources": ("verify.cu", "d3d_common.cuh"),
-                            "sha": "3465a241d1d59d30", "bytes": 9506304},
+    ("async8b", "attn"): {"sources": ("attn.cu", "attn_common.cuh", "sm100_ptx.cuh", "d3d_common.cuh",
+                                      "verify_body.cuh"),
+                          "sha": "e17ecde69c3d18fa", "bytes": 13178624},
+    ("async8b", "verify"): {"sources": ("verify.cu", "verify_body.cuh", "sm100_ptx.cuh", "d3d_common.cuh"),
+                            "sha": "539e4a1fb522aa60", "bytes": 9551872},
 }
 
 
