@@ -47,7 +47,7 @@ def _load():
         if _lib is None:
             _lib = ctypes.CDLL(build())
             for name in ("oracle_packed_attn", "oracle_packed_attn_sel", "oracle_dense_attn",
-                         "oracle_dense_mask", "oracle_spec_verify", "oracle_branch_match",
+                         "oracle_dense_mask", "oracle_spec_verify", "oracle_greedy_verify", "oracle_branch_match",
                          "oracle_check_segments"):
                 getattr(_lib, name).restype = ctypes.c_int
     return _lib
@@ -175,6 +175,28 @@ def spec_verify(inp: dict) -> dict:
         _p(out["used_fallback"]))
     if rc != OK:
         raise ValueError("oracle_spec_verify: invalid arguments (rc=%d)" % rc)
+    return out
+
+
+def greedy_verify(inp: dict) -> dict:
+    """Greedy (temperature 0) verification of R requests.
+
+    D3D, "Experiments" and DScout, "Experiments" (greedy decoding): the T -> 0
+    limit of the sampling rule.  Accept y_j iff it is the target's argmax
+    (ties to the lowest index); emit the target's argmax at the first
+    rejection, or the bonus argmax of row B-1.  Only the target logits are read.
+    """
+    R, B, V = inp["R"], inp["B"], inp["V"]
+    dt = np.uint16 if inp["dtype"] == 1 else np.float32
+    tgt = _c(inp["target"], dt)
+    y = _c(inp["y"], np.int32)
+    out = dict(accept_len=np.zeros(R, np.int32), out_tokens=np.zeros((R, B), np.int32),
+               num_tokens=np.zeros(R, np.int32), accept=np.zeros((R, B - 1)), argmax=np.zeros((R, B), np.int32))
+    rc = _load().oracle_greedy_verify(
+        _p(tgt), ctypes.c_int(inp["dtype"]), _p(y), ctypes.c_int(R), ctypes.c_int(B), ctypes.c_int(V),
+        _p(out["accept_len"]), _p(out["out_tokens"]), _p(out["num_tokens"]), _p(out["accept"]), _p(out["argmax"]))
+    if rc != OK:
+        raise ValueError("oracle_greedy_verify: invalid arguments (rc=%d)" % rc)
     return out
 
 

@@ -511,6 +511,66 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype, const i
     return OR_OK;
 }
 
+/*
+ * Greedy verification (temperature 0), the decoding setting of the pages'
+ * results (D3D, "Experiments": greedy decoding; DScout, "Experiments").
+ * The acceptance rule at T = 0 is the limit of the sampling rule: P_j and
+ * Q_j become point masses at their argmax, so a draft token is accepted
+ * exactly when it is the target's argmax, and the residual (or the bonus
+ * distribution) is the point mass at the target's argmax.  Reading: ties go
+ * to the lowest token index.
+ * Per request r: g_j = argmax_v target[r, j, v] for j = 0..B-1; a = the
+ * number of leading positions with y_j == g_j; out_tokens = y_0..y_{a-1},
+ * g_a, then -1; num_tokens = a + 1.  accept [R, B-1] (may be NULL) = 1.0
+ * where y_j == g_j, else 0.0; argmax [R, B] (may be NULL) = g.  The draft
+ * logits are not needed.
+ */
+int oracle_greedy_verify(const void *target, int dtype, const int32_t *y, int R, int B, int V,
+                         int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens, double *accept,
+                         int32_t *argmax)
+{
+    if (R < 0 || B < 2 || V < 1 || (dtype != OR_F32 && dtype != OR_BF16))
+        return OR_BAD_ARG;
+    int32_t *g = malloc(sizeof(int32_t) * (size_t)B);
+    if (!g)
+        return OR_NOMEM;
+    for (int r = 0; r < R; ++r) {
+        for (int j = 0; j < B; ++j) {
+            size_t off = ((size_t)r * B + j) * V;
+            double best = logit_value(target, dtype, off);
+            int bi = 0;
+            for (int v = 1; v < V; ++v) {
+                double x = logit_value(target, dtype, off + v);
+                if (x > best) { /* strict: an equal value later in the row never wins */
+                    best = x;
+                    bi = v;
+                }
+            }
+            g[j] = bi;
+            if (argmax)
+                argmax[(size_t)r * B + j] = bi;
+        }
+        int a = 0;
+        for (int j = 0; j < B - 1; ++j) {
+            int yj = y[(size_t)r * (B - 1) + j];
+            if (yj < 0 || yj >= V) {
+                free(g);
+                return OR_BAD_ARG;
+            }
+            if (accept)
+                accept[(size_t)r * (B - 1) + j] = (yj == g[j]) ? 1.0 : 0.0;
+        }
+        while (a < B - 1 && y[(size_t)r * (B - 1) + a] == g[a])
+            ++a;
+        accept_len[r] = a;
+        num_tokens[r] = a + 1;
+        for (int j = 0; j < B; ++j)
+            out_tokens[(size_t)r * B + j] = j < a ? y[(size_t)r * (B - 1) + j] : (j == a ? g[a] : -1);
+    }
+    free(g);
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------------------
  * Branch cache-hit match: the smallest branch index k whose head has the
  * verified prefix's length and equals it token for token; -1 on a miss.

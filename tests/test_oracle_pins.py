@@ -78,6 +78,64 @@ def test_verify_hand_worked(case):
     assert (r["out_tokens"][0, n:] == -1).all()
 
 
+# ---------------------------------------------------------------- greedy (temperature 0)
+@pytest.mark.parametrize("case", json.load(open(os.path.join(GOLD, "verify_greedy.json")))["cases"],
+                         ids=lambda c: c["name"])
+def test_greedy_hand_worked(case):
+    B, V = case["B"], case["V"]
+    r = oracle.greedy_verify(dict(target=np.array(case["target"], np.float32).reshape(1, B, V), dtype=W.DT_F32,
+                                  y=np.array(case["y"], np.int32).reshape(1, B - 1), R=1, B=B, V=V))
+    assert r["argmax"][0].tolist() == case["argmax"]
+    assert r["accept"][0].tolist() == case["accept"]
+    assert int(r["accept_len"][0]) == case["accept_len"]
+    n = case["accept_len"] + 1
+    assert int(r["num_tokens"][0]) == n
+    assert r["out_tokens"][0, :n].tolist() == case["tokens"]
+    assert (r["out_tokens"][0, n:] == -1).all()
+
+
+def test_greedy_is_the_zero_temperature_limit_of_sampling():
+    # distinct logits 0.1 apart: at T = 1e-3 the softmaxes are point masses to
+    # within exp(-100), so the sampling rule with any uniforms in (0, 1)
+    # accepts exactly the drafts that are the target's argmax and emits the
+    # target's argmax; the draft tokens are the draft rows' argmax
+    rng = np.random.default_rng(31)
+    R, B, V = 64, 6, 40
+    tgt = np.stack([[rng.permutation(V) * 0.1 for _ in range(B)] for _ in range(R)]).astype(np.float32)
+    dr = tgt[:, : B - 1].copy()
+    redo = rng.random((R, B - 1)) < 0.35  # some draft rows disagree with the target
+    dr[redo] = np.stack([rng.permutation(V) * 0.1 for _ in range(int(redo.sum()))]).astype(np.float32)
+    y = dr.argmax(-1).astype(np.int32)
+    u = (rng.integers(1, 1 << 24, size=(R, B)) * 2.0 ** -24).astype(np.float32)  # never 0
+    samp = oracle.spec_verify(dict(target=tgt, draft=dr, dtype=W.DT_F32, y=y, u_accept=u[:, : B - 1].copy(),
+                                   u_sample=u[:, B - 1].copy(), R=R, B=B, V=V, temperature=1e-3))
+    gr = oracle.greedy_verify(dict(target=tgt, dtype=W.DT_F32, y=y, R=R, B=B, V=V))
+    np.testing.assert_array_equal(gr["accept_len"], samp["accept_len"])
+    np.testing.assert_array_equal(gr["out_tokens"], samp["out_tokens"])
+    assert (gr["accept_len"] < B - 1).any() and (gr["accept_len"] == B - 1).any()  # both outcomes occur
+
+
+@pytest.mark.parametrize("dt", [W.DT_F32, W.DT_BF16])
+def test_greedy_matches_first_max_scan_with_many_ties(dt):
+    # integer logits in 0..3 make ties common: numpy's argmax returns the
+    # first maximum, the reading the oracle follows
+    rng = np.random.default_rng(32)
+    R, B, V = 50, 5, 23
+    vals = rng.integers(0, 4, size=(R, B, V)).astype(np.float32)
+    g = vals.argmax(-1)
+    y = np.where(rng.random((R, B - 1)) < 0.7, g[:, : B - 1], rng.integers(0, V, size=(R, B - 1))).astype(np.int32)
+    tgt = W.bf16_bits(vals) if dt == W.DT_BF16 else vals
+    r = oracle.greedy_verify(dict(target=tgt, dtype=dt, y=y, R=R, B=B, V=V))
+    np.testing.assert_array_equal(r["argmax"], g)
+    for i in range(R):
+        a = 0
+        while a < B - 1 and y[i, a] == g[i, a]:
+            a += 1
+        assert r["accept_len"][i] == a
+        assert r["out_tokens"][i].tolist() == y[i, :a].tolist() + [g[i, a]] + [-1] * (B - 1 - a)
+    np.testing.assert_array_equal(r["accept"], (y == g[:, : B - 1]).astype(np.float64))
+
+
 # ---------------------------------------------------------------- statistics helpers
 def _fixed_rows_inputs(x, z, T, R, seed):
     """R trials of one fixed verification problem: target rows x [B, V], draft
