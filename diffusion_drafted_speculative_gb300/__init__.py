@@ -209,7 +209,12 @@ def d3d_spec_verify_workspace_size(R, B, V) -> int:
 
 def _verify_args(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature, accept_len, out_tokens,
                  num_tokens, ws, alpha, p_draft, q_draft, heads, head_len, branch):
-    """Checked argument tuple of d3d_spec_verify (without sm_limit and stream)."""
+    """Checked argument tuple of d3d_spec_verify (without sm_limit and stream).
+
+    temperature 0 is greedy verification: draft_logits, u_accept and u_sample
+    may then be None (they are not read) and q_draft must be None.
+    """
+    greedy = float(temperature) == 0.0
     if target_logits.dtype == torch.bfloat16:
         dt = D3D_DTYPE_BF16
     elif target_logits.dtype == torch.float32:
@@ -217,13 +222,17 @@ def _verify_args(target_logits, draft_logits, draft_tokens, u_accept, u_sample, 
     else:
         raise TypeError("logits must be float32 or bfloat16")
     _need(target_logits, "target_logits", target_logits.dtype, 3)
-    _need(draft_logits, "draft_logits", target_logits.dtype, 3)
     R, B, V = target_logits.shape
-    if draft_logits.shape != (R, B - 1, V):
-        raise ValueError("draft_logits must be [R, B-1, V]")
+    if not greedy or draft_logits is not None:
+        _need(draft_logits, "draft_logits", target_logits.dtype, 3)
+        if draft_logits.shape != (R, B - 1, V):
+            raise ValueError("draft_logits must be [R, B-1, V]")
     _need(draft_tokens, "draft_tokens", torch.int32, 2)
-    _need(u_accept, "u_accept", torch.float32, 2)
-    _need(u_sample, "u_sample", torch.float32, 1)
+    if not greedy or u_accept is not None or u_sample is not None:
+        _need(u_accept, "u_accept", torch.float32, 2)
+        _need(u_sample, "u_sample", torch.float32, 1)
+        if u_accept.shape != (R, B - 1) or u_sample.shape != (R,):
+            raise ValueError("u_accept must be [R, B-1], u_sample [R]")
     for t, n, shp in ((accept_len, "accept_len", (R,)), (out_tokens, "out_tokens", (R, B)),
                       (num_tokens, "num_tokens", (R,))):
         _need(t, n, torch.int32, len(shp))
@@ -234,8 +243,8 @@ def _verify_args(target_logits, draft_logits, draft_tokens, u_accept, u_sample, 
             _need(t, n, torch.float32, 2)
             if tuple(t.shape) != (R, B - 1):
                 raise ValueError("%s must be [R, B-1]" % n)
-    if draft_tokens.shape != (R, B - 1) or u_accept.shape != (R, B - 1) or u_sample.shape != (R,):
-        raise ValueError("draft_tokens/u_accept must be [R, B-1], u_sample [R]")
+    if draft_tokens.shape != (R, B - 1):
+        raise ValueError("draft_tokens must be [R, B-1]")
     M = 0
     if branch is not None:
         _need(branch, "branch", torch.int32, 1)
@@ -307,9 +316,12 @@ def d3d_spec_verify_noalloc(target_logits, draft_logits, draft_tokens, u_accept,
     else:
         raise TypeError("logits must be float32 or bfloat16")
     R, B, V = target_logits.shape
+    greedy = float(temperature) == 0.0  # draft logits and uniforms are not read
     for t, n in ((target_logits, "target_logits"), (draft_logits, "draft_logits"), (draft_tokens, "draft_tokens"),
                  (u_accept, "u_accept"), (u_sample, "u_sample"), (accept_len, "accept_len"),
                  (out_tokens, "out_tokens"), (num_tokens, "num_tokens")):
+        if t is None and greedy and n in ("draft_logits", "u_accept", "u_sample"):
+            continue
         _need(t, n, t.dtype)
     rc = lib.d3d_spec_verify_noalloc(
         _ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), R, B, V,

@@ -1169,6 +1169,8 @@ int d3d_async_round(const d3d_attn_call_t *a, const d3d_verify_call_t *v, cudaSt
                                        v->head_len, v->M, v->branch, va);
     if (rv < 0)
         return rv;
+    if (v->temperature == 0.f)  // greedy verification has its own launch
+        return D3D_ERR_UNSUPPORTED;
     CUtensorMap maps[5];
     d3d::AttnParams prm;
     d3d::AttnPlan pl;

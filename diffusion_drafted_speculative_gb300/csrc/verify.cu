@@ -4,6 +4,7 @@
 
 #include <mutex>
 
+#include "greedy_body.cuh"
 #include "verify_body.cuh"
 
 namespace d3d {
@@ -105,6 +106,9 @@ int d3d_spec_verify(const void *target_logits, const void *draft_logits, int log
     if (!d3d::ws_ok(ws, ws_bytes, d3d::verify_layout(R, B, V, d3d::kVChunkMin).total))
         return D3D_ERR_WORKSPACE;
     a.ws = static_cast<unsigned char *>(ws);
+    if (temperature == 0.f)
+        return logits_dtype == D3D_DTYPE_BF16 ? d3d::launch_greedy<uint16_t>(a, sm_limit, flags, stream)
+                                              : d3d::launch_greedy<float>(a, sm_limit, flags, stream);
     if (logits_dtype == D3D_DTYPE_BF16)
         return d3d::launch_verify<uint16_t>(a, sm_limit, flags, stream);
     return d3d::launch_verify<float>(a, sm_limit, flags, stream);
@@ -189,6 +193,9 @@ extern "C" int d3d_spec_verify_noalloc(const void *target_logits, const void *dr
     if (cudaMemsetAsync(scratch, 0, L.rec, stream) != cudaSuccess)
         return D3D_ERR_CUDA;
     a.ws = static_cast<unsigned char *>(scratch);
+    if (temperature == 0.f)
+        return logits_dtype == D3D_DTYPE_BF16 ? d3d::launch_greedy<uint16_t>(a, 0, 0, stream)
+                                              : d3d::launch_greedy<float>(a, 0, 0, stream);
     if (logits_dtype == D3D_DTYPE_BF16)
         return d3d::launch_verify<uint16_t>(a, 0, 0, stream);
     return d3d::launch_verify<float>(a, 0, 0, stream);

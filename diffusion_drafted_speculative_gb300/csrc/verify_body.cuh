@@ -1092,7 +1092,11 @@ inline int verify_prepare(const void *target_logits, const void *draft_logits, i
                           float *alpha, float *p_draft, float *q_draft, const int32_t *heads,
                           const int32_t *head_len, int M, int32_t *branch, VArgs &a)
 {
-    if (R < 0 || B < 2 || V < 1 || !(temperature > 0.f) || !isfinite(temperature) || M < 0)
+    // temperature 0: greedy verification (no draft logits, no uniforms)
+    const bool greedy = temperature == 0.f;
+    if (R < 0 || B < 2 || V < 1 || !(temperature >= 0.f) || !isfinite(temperature) || M < 0)
+        return D3D_ERR_INVALID_ARG;
+    if (greedy && q_draft != nullptr)
         return D3D_ERR_INVALID_ARG;
     if (branch != nullptr && M > 0 && (!heads || !head_len))
         return D3D_ERR_INVALID_ARG;
@@ -1102,8 +1106,9 @@ inline int verify_prepare(const void *target_logits, const void *draft_logits, i
         return D3D_ERR_UNSUPPORTED;
     if (R == 0)
         return 1;
-    if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_sample || !accept_len ||
-        !out_tokens || !num_tokens)
+    if (!target_logits || !draft_tokens || !accept_len || !out_tokens || !num_tokens)
+        return D3D_ERR_INVALID_ARG;
+    if (!greedy && (!draft_logits || !u_accept || !u_sample))
         return D3D_ERR_INVALID_ARG;
     a.target = target_logits;
     a.draft = draft_logits;
@@ -1111,7 +1116,7 @@ inline int verify_prepare(const void *target_logits, const void *draft_logits, i
     a.u_acc = u_accept;
     a.u_s = u_sample;
     a.R = R, a.B = B, a.V = V, a.M = branch ? M : 0;
-    a.c = (float)(1.4426950408889634 / (double)temperature);  // log2(e) / T
+    a.c = greedy ? 0.f : (float)(1.4426950408889634 / (double)temperature);  // log2(e) / T
     a.accept_len = accept_len, a.out_tokens = out_tokens, a.num_tokens = num_tokens;
     a.alpha = alpha, a.p = p_draft, a.q = q_draft;
     a.heads = heads, a.head_len = head_len, a.branch = branch;

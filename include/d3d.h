@@ -200,10 +200,20 @@ void d3d_debug_inject_fault(int mode);
  *   out_tokens[r] = [y_0 .. y_{a-1}, t, -1, ...], num_tokens[r] = a + 1
  *   (the round's tau: accepted drafts plus the target's own token).
  *
+ * Greedy verification, temperature == 0 ([D3D] "Experiments", [DScout]
+ * "Experiments": the pages' results are greedy; the T -> 0 limit of the
+ * rule above).  g_j = argmax_v target[r,j,v], ties to the lowest index;
+ *   a = number of leading j with y_j == g_j,  t = g_a  (g_{B-1}: the bonus);
+ *   alpha_j = p_draft_j = 1 if y_j == g_j else 0.
+ * Only the target logits are read: draft_logits, u_accept and u_sample may
+ * be NULL, q_draft must be NULL (else D3D_ERR_INVALID_ARG).  The launch
+ * needs no co-residency: every CTA finishes its part without waiting.
+ *
  *   target_logits [R, B, V], draft_logits [R, B-1, V]  f32 or bf16 (logits_dtype)
  *   draft_tokens  [R, B-1] int32 in [0, V)
  *   u_accept [R, B-1], u_sample [R]  float32 in [0, 1)
- *   temperature   > 0 (else D3D_ERR_INVALID_ARG)
+ *   temperature   > 0 (sampling) or 0 (greedy); negative or not finite:
+ *               D3D_ERR_INVALID_ARG
  *   B >= 2, V >= 1
  *   accept_len [R], out_tokens [R, B], num_tokens [R]  int32 outputs
  *   alpha, p_draft, q_draft [R, B-1] float32 outputs, each may be NULL
@@ -284,8 +294,9 @@ int d3d_spec_verify_noalloc(const void *target_logits, const void *draft_logits,
  * CTAs (d3d_packed_draft_attn_ctas of them) and the verification's CTAs on
  * the remaining SMs, one CTA per SM.  Outputs, workspaces, status words and
  * error codes are those of the two calls.  D3D_ERR_UNSUPPORTED when the
- * attention would split keys across CTAs or fill every SM, or when a part
- * has nothing to compute: then make the two calls (the verification with
+ * attention would split keys across CTAs or fill every SM, when a part has
+ * nothing to compute, or for greedy verification (temperature 0): then make
+ * the two calls (the verification with
  * an sm_limit, the attention with D3D_ATTN_AFTER_INDEPENDENT).
  * Field meanings are those of the arguments of the two calls.
  * ======================================================================== */

@@ -404,6 +404,124 @@ def test_attention_cta_count_matches_plan(d3d):
     assert 0 < n <= sms
 
 
+# ------------------------------------------------------------------ greedy (temperature 0)
+def _greedy_inputs(cfg, seed, plant=True, **over):
+    """Verification inputs whose draft tokens follow the greedy drafter (the
+    draft rows' argmax, lowest index); with plant, request r's first r % B
+    tokens are replaced by the target's argmax so that every accepted length
+    occurs."""
+    v = W.verify_inputs(**dict(W.CONFIGS[cfg], **over), seed=seed)
+    dec = (lambda x: W.bf16_to_f32(x)) if v["dtype"] == W.DT_BF16 else (lambda x: x)
+    y = dec(v["draft"]).argmax(-1).astype(np.int32)
+    if plant:
+        g = oracle.greedy_verify(dict(v, y=y))["argmax"]
+        for r in range(v["R"]):
+            k = r % v["B"]
+            y[r, :k] = g[r, :k]
+    v["y"] = np.ascontiguousarray(y)
+    return v
+
+
+def _run_greedy(d3d, v, sm_limit=0, heads=None, noalloc=False, probs=True):
+    from gpu_util import bf16, f32, i32
+    R, B = v["R"], v["B"]
+    tgt = bf16(v["target"]) if v["dtype"] == W.DT_BF16 else f32(v["target"])
+    out = dict(accept_len=torch.full((R,), -7, dtype=torch.int32, device="cuda"),
+               out_tokens=torch.full((R, B), -7, dtype=torch.int32, device="cuda"),
+               num_tokens=torch.full((R,), -7, dtype=torch.int32, device="cuda"))
+    pr = {k: torch.full((R, B - 1), float("nan"), device="cuda") for k in ("alpha", "p")} if probs else {}
+    if noalloc:
+        d3d.d3d_spec_verify_noalloc(tgt, None, i32(v["y"]), None, None, 0.0, out["accept_len"], out["out_tokens"],
+                                    out["num_tokens"], alpha=pr.get("alpha"), p_draft=pr.get("p"))
+        ws = None
+    else:
+        ws = d3d.new_workspace(d3d.d3d_spec_verify_workspace_size(R, B, v["V"]))
+        extra = {}
+        if heads is not None:
+            out["branch"] = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+            extra = dict(heads=i32(heads["heads"]), head_len=i32(heads["head_len"]), branch=out["branch"])
+        d3d.d3d_spec_verify(tgt, None, i32(v["y"]), None, None, 0.0, out["accept_len"], out["out_tokens"],
+                            out["num_tokens"], ws, alpha=pr.get("alpha"), p_draft=pr.get("p"), sm_limit=sm_limit,
+                            **extra)
+    torch.cuda.synchronize()
+    got = {k: t.cpu().numpy() for k, t in out.items()}
+    got.update({k: t.cpu().numpy() for k, t in pr.items()})
+    return got, ws
+
+
+def _check_greedy(got, ref):
+    np.testing.assert_array_equal(got["accept_len"], ref["accept_len"])
+    np.testing.assert_array_equal(got["num_tokens"], ref["num_tokens"])
+    np.testing.assert_array_equal(got["out_tokens"], ref["out_tokens"])
+    if "alpha" in got:
+        np.testing.assert_array_equal(got["alpha"], ref["accept"].astype(np.float32))
+        np.testing.assert_array_equal(got["p"], ref["accept"].astype(np.float32))
+
+
+@pytest.mark.parametrize("cfg,over", [
+    ("tiny", {}),
+    ("tiny", dict(R=40)),
+    ("async8b", {}),
+    ("async8b", dict(R=5)),
+    ("long_block", {}),
+    ("serve32b", {}),
+    ("tiny", dict(R=9, V=1001)),                      # f32, V % 8 != 0: scalar loads
+    ("async8b", dict(R=3, V=151939)),                 # bf16, V % 8 != 0
+    ("async8b", dict(R=2, V=8192 * 3)),               # whole chunks only
+    ("async8b", dict(R=2, V=17)),                     # one short chunk
+])
+def test_greedy_verify_matches_oracle(d3d, cfg, over):
+    v = _greedy_inputs(cfg, seed=40, **over)
+    ref = oracle.greedy_verify(v)
+    got, ws = _run_greedy(d3d, v)
+    _check_greedy(got, ref)
+    assert d3d.d3d_workspace_status(ws) == 0
+    if v["R"] >= v["B"]:
+        assert len(set(ref["accept_len"].tolist())) > 3  # many accepted lengths occur
+
+
+@pytest.mark.parametrize("dt", [W.DT_F32, W.DT_BF16])
+def test_greedy_ties_go_to_the_lowest_index(d3d, dt):
+    # integer logits in a tiny range: most rows have their maximum many times
+    rng = np.random.default_rng(41)
+    R, B, V = 24, 16, 40000
+    vals = rng.integers(0, 3, size=(R, B, V)).astype(np.float32)
+    vals[:, :, rng.integers(0, V, size=7)] = 3.0  # a few columns hold the maximum in every row
+    tgt = W.bf16_bits(vals) if dt == W.DT_BF16 else vals
+    g = vals.argmax(-1)
+    y = np.where(rng.random((R, B - 1)) < 0.8, g[:, : B - 1], (g[:, : B - 1] + 1) % V).astype(np.int32)
+    v = dict(target=tgt, dtype=dt, y=y, R=R, B=B, V=V)
+    ref = oracle.greedy_verify(v)
+    got, _ = _run_greedy(d3d, v)
+    _check_greedy(got, ref)
+
+
+@pytest.mark.parametrize("cfg,sm_limit", [("async8b", 0), ("async8b", 56), ("serve32b", 40)])
+def test_greedy_fused_match_and_sm_limit(d3d, cfg, sm_limit):
+    v = _greedy_inputs(cfg, seed=42)
+    ref = oracle.greedy_verify(v)
+    hb = _heads_hitting(ref, v["B"], v["V"], 24, seed=43)
+    got, _ = _run_greedy(d3d, v, sm_limit=sm_limit, heads=hb)
+    _check_greedy(got, ref)
+    want = oracle.branch_match(dict(verified=ref["out_tokens"], verified_len=ref["num_tokens"], **hb))
+    np.testing.assert_array_equal(got["branch"], want)
+
+
+def test_greedy_bad_draft_token_and_noalloc(d3d):
+    v = _greedy_inputs("tiny", seed=44, R=6)
+    ref = oracle.greedy_verify(v)
+    got, _ = _run_greedy(d3d, v, noalloc=True)  # the library's own scratch
+    _check_greedy(got, ref)
+    # a draft token outside [0, V) is rejected there and reported
+    bad = dict(v, y=v["y"].copy())
+    bad["y"][2, 0] = v["V"] + 5
+    got, ws = _run_greedy(d3d, bad, probs=False)
+    assert d3d.d3d_workspace_status(ws) == d3d.D3D_ERR_DEVICE_INPUT
+    assert got["accept_len"][2] == 0 and got["out_tokens"][2, 0] == ref["argmax"][2, 0]
+    keep = np.arange(v["R"]) != 2
+    np.testing.assert_array_equal(got["out_tokens"][keep], ref["out_tokens"][keep])
+
+
 def test_verify_workspace_reuse_and_many_requests(d3d):
     v = W.verify_inputs(R=4096, B=4, V=64, logits=W.DT_F32, seed=10)
     got1, ws = run_verify(d3d, v)

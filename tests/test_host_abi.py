@@ -68,13 +68,15 @@ def test_invalid_arguments_rejected_on_host(d3d):
     L = d3d.lib
     fake = ctypes.c_void_p(256)  # never dereferenced: the checks fail first
     # verify: B < 2, V < 1, T <= 0, bad dtype, missing workspace
-    args = lambda R, B, V, T, dt, ws, wsb, sm=0, M=0, heads=None, br=None, fl=0: (  # noqa
-        fake, fake, dt, fake, fake, fake, R, B, V, T, fake, fake, fake, None, None, None, heads, heads, M, br, ws, wsb,
+    args = lambda R, B, V, T, dt, ws, wsb, sm=0, M=0, heads=None, br=None, fl=0, q=None: (  # noqa
+        fake, fake, dt, fake, fake, fake, R, B, V, T, fake, fake, fake, None, None, q, heads, heads, M, br, ws, wsb,
         sm, fl, None)
     assert L.d3d_spec_verify(*args(1, 1, 10, 1.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 1 << 20, fl=2)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 0, 1.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
-    assert L.d3d_spec_verify(*args(1, 4, 10, 0.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
+    # temperature 0 is greedy verification, which reads no draft logits: q_draft must be NULL
+    assert L.d3d_spec_verify(*args(1, 4, 10, 0.0, 1, fake, 1 << 20, q=fake)) == d3d.D3D_ERR_INVALID_ARG
+    assert L.d3d_spec_verify(*args(1, 4, 10, -0.5, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 10, -1.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 10, float("nan"), 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 7, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
@@ -111,8 +113,10 @@ def test_invalid_arguments_rejected_on_host(d3d):
                         None, 0, None, fake, 1 << 20)
     assert L.d3d_async_round(ctypes.byref(ac), ctypes.byref(vc), None) == d3d.D3D_ERR_INVALID_ARG  # Hq % Hkv
     ac.Hq = 32
-    vc.temperature = 0.0
-    assert L.d3d_async_round(ctypes.byref(ac), ctypes.byref(vc), None) == d3d.D3D_ERR_INVALID_ARG  # T <= 0
+    vc.temperature = -1.0
+    assert L.d3d_async_round(ctypes.byref(ac), ctypes.byref(vc), None) == d3d.D3D_ERR_INVALID_ARG  # T < 0
+    vc.temperature = 0.0  # greedy verification has a launch of its own
+    assert L.d3d_async_round(ctypes.byref(ac), ctypes.byref(vc), None) == d3d.D3D_ERR_UNSUPPORTED
     vc.temperature = 1.0
     ac.d = 96
     assert L.d3d_async_round(ctypes.byref(ac), ctypes.byref(vc), None) == d3d.D3D_ERR_UNSUPPORTED
