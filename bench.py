@@ -116,8 +116,9 @@ def workload(name: str) -> dict:
     flops = 4.0 * d * Hq * R * (n_q * L_mean + vis_packed)
     attn_bytes = 2.0 * R * (2 * L_mean * Hkv * d + 2 * n_q * Hq * d + 2 * n_q * Hkv * d)
     verify_bytes = 2.0 * R * ((2 * B - 1) * V + 2 * V)
+    greedy_bytes = 2.0 * R * B * V  # greedy verification reads the target logits only
     return dict(cfg=cfg, segs=segs, n_q=n_q, R=R, flops=flops, attn_bytes=attn_bytes, verify_bytes=verify_bytes,
-                positions=R * B, vis_packed=vis_packed)
+                greedy_bytes=greedy_bytes, positions=R * B, vis_packed=vis_packed)
 
 
 # ----------------------------------------------------------------------------
@@ -276,6 +277,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                             s["out_tokens"], s["num_tokens"], ws_v, sm_limit=sm_limit,
                             after_independent=after_independent, **extra)
 
+    def greedy(s):  # temperature 0: argmax verification of the same rows
+        d3d.d3d_spec_verify(s["target"], None, s["y"], None, None, 0.0, s["accept_len"], s["out_tokens"],
+                            s["num_tokens"], ws_v)
+
     def match(s):
         d3d.d3d_branch_match(s["out_tokens"], s["num_tokens"], s["heads"], s["head_len"], s["branch"])
 
@@ -400,6 +405,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     t_verify = timed(verify, n_part)
     t_verify_side = timed(lambda s: verify(s, verify_sms, fused_match=True), n_part)
     t_match = timed(match, n_part)
+    t_greedy = timed(greedy, n_part)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -423,6 +429,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                  "peak_source": peaks["source"] + (" (burst bf16)" if roof["bound"] == "tensor" else " (copy bandwidth)"),
                  "algorithmic": {"flops": wl["flops"], "bytes": wl["attn_bytes"]}})
     verify_gbs = wl["verify_bytes"] / (t_verify * 1e-3) / 1e9
+    greedy_gbs = wl["greedy_bytes"] / (t_greedy * 1e-3) / 1e9
 
     value = whole_job_rate(wl["n_q"] * R, world, ms_step)
     line = {
@@ -446,7 +453,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                   "verify_positions_per_s": round(wl["positions"] / (t_verify * 1e-3), 1),
                   "verify_hbm": {"achieved": round(verify_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
                                  "frac": round(verify_gbs / peaks["hbm"], 4),
-                                 "bytes": wl["verify_bytes"], "traffic": ncu_traffic(args.workload, "verify")}},
+                                 "bytes": wl["verify_bytes"], "traffic": ncu_traffic(args.workload, "verify")},
+                  "greedy_verify_us": round(t_greedy * 1e3, 3),
+                  "greedy_hbm": {"achieved": round(greedy_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                                 "frac": round(greedy_gbs / peaks["hbm"], 4), "bytes": wl["greedy_bytes"]}},
         "roofline": roof,
         "gpu_launches": args.steps * LAUNCHES["fused" if fused_round else args.round],
         "clocks": clk, "wall_s_timed_region": round(wall, 4),
