@@ -47,7 +47,8 @@ def _load():
         if _lib is None:
             _lib = ctypes.CDLL(build())
             for name in ("oracle_packed_attn", "oracle_packed_attn_sel", "oracle_dense_attn",
-                         "oracle_dense_mask", "oracle_spec_verify", "oracle_greedy_verify", "oracle_branch_match",
+                         "oracle_dense_mask", "oracle_spec_verify", "oracle_greedy_verify", "oracle_build_branches",
+                         "oracle_branch_match",
                          "oracle_check_segments"):
                 getattr(_lib, name).restype = ctypes.c_int
     return _lib
@@ -175,6 +176,33 @@ def spec_verify(inp: dict) -> dict:
         _p(out["used_fallback"]))
     if rc != OK:
         raise ValueError("oracle_spec_verify: invalid arguments (rc=%d)" % rc)
+    return out
+
+
+def build_branches(inp: dict) -> dict:
+    """Branch construction for the asynchronous packed pass (D3D, "Background:
+    asynchronous drafting and cache hits", "Method steps" step 4).
+
+    Anchors of rejection position r: the F most likely tokens of the draft row
+    Q_r (largest logit first, ties to the lowest index), y_r excluded; heads,
+    head lengths and the packed pass's segment rows (see d3d_oracle.c).
+    ``bonus_guess`` [R] is optional.
+    """
+    R, B, V, C, F = inp["R"], inp["B"], inp["V"], inp["C"], inp["F"]
+    dt = np.uint16 if inp["dtype"] == 1 else np.float32
+    dr, y = _c(inp["draft"], dt), _c(inp["y"], np.int32)
+    bg = inp.get("bonus_guess")
+    bg = None if bg is None else _c(bg, np.int32)
+    M = (C - 1) * F + 2
+    out = dict(anchors=np.zeros((R, max(C - 1, 0), F), np.int32), heads=np.zeros((R, M, B), np.int32),
+               head_len=np.zeros((R, M), np.int32), segs=np.zeros((R * M, 5), np.int32),
+               cu_q=np.zeros(R + 1, np.int32), cu_seg=np.zeros(R + 1, np.int32))
+    rc = _load().oracle_build_branches(
+        _p(dr), ctypes.c_int(inp["dtype"]), _p(y), None if bg is None else _p(bg), ctypes.c_int(R), ctypes.c_int(B),
+        ctypes.c_int(V), ctypes.c_int(C), ctypes.c_int(F), _p(out["anchors"]), _p(out["heads"]),
+        _p(out["head_len"]), _p(out["segs"]), _p(out["cu_q"]), _p(out["cu_seg"]))
+    if rc != OK:
+        raise ValueError("oracle_build_branches: invalid arguments (rc=%d)" % rc)
     return out
 
 

@@ -512,6 +512,116 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype, const i
 }
 
 /*
+ * Branch construction for the asynchronous packed pass (D3D, "Background:
+ * asynchronous drafting and cache hits" and "Method steps", step 4: for
+ * every rejection position, several alternative anchors, plus the
+ * all-accept block).  Readings (the pages do not say how the anchors are
+ * chosen): the F alternative anchors of rejection position r (0-based draft
+ * index r, r = 0..C-2) are the F most likely tokens of the drafter's own
+ * distribution Q_r at that position (largest logit first, ties to the
+ * lowest index), the drafted token y_r excluded; the all-accept head's last
+ * token is the caller's guess of the bonus token (no guess: that head has
+ * length 0 and never matches).
+ * Outputs, per request (M = (C-1)F + 2 branches, indexed like the segments):
+ *   anchors [R, C-1, F];
+ *   head_len[r,0] = 0 (the block under verification);
+ *   branch k = 1 + r*F + f: head = y_0 .. y_{r-1}, anchor (r, f); len r + 1;
+ *   branch M-1: head = y_0 .. y_{B-2}, bonus guess; len B (0 without a guess);
+ *   head entries past the length are -1;
+ *   segs [R*M, 5] request-local rows: (0, B, causal, -1, 0) for the block
+ *   under verification, (k*B, B, bidirectional, 0, r+1) for branch (r, f),
+ *   ((M-1)*B, B, bidirectional, 0, B) for the all-accept block;
+ *   cu_q[r] = r*M*B, cu_seg[r] = r*M (R+1 entries).
+ */
+int oracle_build_branches(const void *draft, int dtype, const int32_t *y, const int32_t *bonus_guess, int R,
+                          int B, int V, int C, int F, int32_t *anchors, int32_t *heads, int32_t *head_len,
+                          int32_t *segs, int32_t *cu_q, int32_t *cu_seg)
+{
+    if (R < 0 || B < 2 || V < 1 || C < 1 || C > B || F < 0 || (dtype != OR_F32 && dtype != OR_BF16))
+        return OR_BAD_ARG;
+    if ((C - 1) * F > 0 && F > V - 1)
+        return OR_BAD_ARG; /* not enough tokens besides y */
+    const int M = (C - 1) * F + 2;
+    char *taken = malloc((size_t)V);
+    if (!taken)
+        return OR_NOMEM;
+    for (int r = 0; r < R; ++r) {
+        const int32_t *yr = y + (size_t)r * (B - 1);
+        for (int j = 0; j < B - 1; ++j)
+            if (yr[j] < 0 || yr[j] >= V) {
+                free(taken);
+                return OR_BAD_ARG;
+            }
+        /* anchors: repeated maximum over the tokens not yet taken */
+        for (int p = 0; p < C - 1; ++p) {
+            size_t off = ((size_t)r * (B - 1) + p) * V;
+            memset(taken, 0, (size_t)V);
+            taken[yr[p]] = 1;
+            for (int f = 0; f < F; ++f) {
+                int bi = -1;
+                double best = 0.0;
+                for (int v = 0; v < V; ++v) {
+                    if (taken[v])
+                        continue;
+                    double x = logit_value(draft, dtype, off + v);
+                    if (bi < 0 || x > best) {
+                        best = x;
+                        bi = v;
+                    }
+                }
+                taken[bi] = 1;
+                anchors[((size_t)r * (C - 1) + p) * F + f] = bi;
+            }
+        }
+        /* heads */
+        int32_t *h = heads + (size_t)r * M * B;
+        int32_t *hl = head_len + (size_t)r * M;
+        for (int k = 0; k < M; ++k)
+            for (int i = 0; i < B; ++i)
+                h[(size_t)k * B + i] = -1;
+        hl[0] = 0;
+        for (int p = 0; p < C - 1; ++p)
+            for (int f = 0; f < F; ++f) {
+                int k = 1 + p * F + f;
+                for (int i = 0; i < p; ++i)
+                    h[(size_t)k * B + i] = yr[i];
+                h[(size_t)k * B + p] = anchors[((size_t)r * (C - 1) + p) * F + f];
+                hl[k] = p + 1;
+            }
+        if (bonus_guess) {
+            for (int i = 0; i < B - 1; ++i)
+                h[(size_t)(M - 1) * B + i] = yr[i];
+            h[(size_t)(M - 1) * B + B - 1] = bonus_guess[r];
+            hl[M - 1] = B;
+        } else {
+            hl[M - 1] = 0;
+        }
+        /* segment rows of the packed pass */
+        if (segs) {
+            int32_t *sg = segs + (size_t)r * M * 5;
+            for (int k = 0; k < M; ++k) {
+                int32_t row[5];
+                if (k == 0) {
+                    row[0] = 0, row[1] = B, row[2] = OR_CAUSAL, row[3] = -1, row[4] = 0;
+                } else if (k == M - 1) {
+                    row[0] = k * B, row[1] = B, row[2] = OR_BIDIR, row[3] = 0, row[4] = B;
+                } else {
+                    row[0] = k * B, row[1] = B, row[2] = OR_BIDIR, row[3] = 0, row[4] = (k - 1) / F + 1;
+                }
+                memcpy(sg + (size_t)k * 5, row, sizeof(row));
+            }
+        }
+    }
+    if (cu_q && cu_seg)
+        for (int r = 0; r <= R; ++r) {
+            cu_q[r] = r * M * B;
+            cu_seg[r] = r * M;
+        }
+    free(taken);
+    return OR_OK;
+}
+
+/*
  * Greedy verification (temperature 0), the decoding setting of the pages'
  * results (D3D, "Experiments": greedy decoding; DScout, "Experiments").
  * The acceptance rule at T = 0 is the limit of the sampling rule: P_j and

@@ -136,6 +136,58 @@ def test_greedy_matches_first_max_scan_with_many_ties(dt):
     np.testing.assert_array_equal(r["accept"], (y == g[:, : B - 1]).astype(np.float64))
 
 
+# ---------------------------------------------------------------- branch construction
+@pytest.mark.parametrize("case", json.load(open(os.path.join(GOLD, "build_branches.json")))["cases"],
+                         ids=lambda c: c["name"])
+def test_build_branches_hand_worked(case):
+    B, V, C, F = case["B"], case["V"], case["C"], case["F"]
+    bg = None if case["bonus_guess"] is None else np.array([case["bonus_guess"]], np.int32)
+    r = oracle.build_branches(dict(draft=np.array(case["draft"], np.float32).reshape(1, B - 1, V), dtype=W.DT_F32,
+                                   y=np.array(case["y"], np.int32).reshape(1, B - 1), bonus_guess=bg,
+                                   R=1, B=B, V=V, C=C, F=F))
+    assert r["anchors"][0].tolist() == case["anchors"]
+    assert r["heads"][0].tolist() == case["heads"]
+    assert r["head_len"][0].tolist() == case["head_len"]
+
+
+@pytest.mark.parametrize("B,C,F", [(16, 12, 2), (16, 4, 1), (16, 16, 5), (8, 3, 2), (4, 1, 3)])
+def test_build_branches_segments_are_the_async_layout(B, C, F):
+    # the segment rows equal the layout whose size is the printed N_async
+    R, V = 3, 50
+    rng = np.random.default_rng(33)
+    r = oracle.build_branches(dict(draft=rng.standard_normal((R, B - 1, V)).astype(np.float32), dtype=W.DT_F32,
+                                   y=rng.integers(0, V, size=(R, B - 1)).astype(np.int32), R=R, B=B, V=V, C=C, F=F))
+    lay = W.async_segments(B, C, F)
+    M = len(lay)
+    assert M == (C - 1) * F + 2 and int(lay[:, 1].sum()) == oracle.n_async(B, C, F)
+    np.testing.assert_array_equal(r["segs"], np.concatenate([lay] * R))
+    np.testing.assert_array_equal(r["cu_q"], np.arange(R + 1) * M * B)
+    np.testing.assert_array_equal(r["cu_seg"], np.arange(R + 1) * M)
+
+
+@pytest.mark.parametrize("dt", [W.DT_F32, W.DT_BF16])
+def test_build_branches_anchors_match_a_sort(dt):
+    # integer logits make ties common; a stable sort by (-logit, index) with
+    # y removed gives the anchors; every head is y's prefix then the anchor
+    rng = np.random.default_rng(34)
+    R, B, V, C, F = 20, 8, 30, 6, 3
+    vals = rng.integers(0, 5, size=(R, B - 1, V)).astype(np.float32)
+    y = rng.integers(0, V, size=(R, B - 1)).astype(np.int32)
+    dr = W.bf16_bits(vals) if dt == W.DT_BF16 else vals
+    bg = rng.integers(0, V, size=R).astype(np.int32)
+    r = oracle.build_branches(dict(draft=dr, dtype=dt, y=y, bonus_guess=bg, R=R, B=B, V=V, C=C, F=F))
+    for i in range(R):
+        for p in range(C - 1):
+            order = [v for v in np.lexsort((np.arange(V), -vals[i, p])) if v != y[i, p]]
+            assert r["anchors"][i, p].tolist() == order[:F]
+            for f in range(F):
+                k = 1 + p * F + f
+                assert r["head_len"][i, k] == p + 1
+                assert r["heads"][i, k, :p].tolist() == y[i, :p].tolist()
+                assert r["heads"][i, k, p] == order[f] and (r["heads"][i, k, p + 1:] == -1).all()
+        assert r["head_len"][i, -1] == B and r["heads"][i, -1].tolist() == y[i].tolist() + [bg[i]]
+
+
 # ---------------------------------------------------------------- statistics helpers
 def _fixed_rows_inputs(x, z, T, R, seed):
     """R trials of one fixed verification problem: target rows x [B, V], draft
