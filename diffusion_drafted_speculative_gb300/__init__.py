@@ -19,7 +19,7 @@ __all__ = [
     "D3DError", "lib", "d3d_status_string", "d3d_version", "d3d_validate_segments",
     "d3d_packed_draft_attn", "d3d_packed_draft_attn_workspace_size", "d3d_packed_draft_attn_ctas",
     "d3d_spec_verify", "d3d_spec_verify_workspace_size", "d3d_spec_verify_noalloc", "d3d_async_round",
-    "AttnCall", "VerifyCall", "d3d_branch_match", "d3d_workspace_status", "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
+    "AttnCall", "VerifyCall", "d3d_build_branches", "d3d_build_branches_workspace_size", "d3d_branch_match", "d3d_workspace_status", "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
     "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
     "D3D_ERR_DEVICE_TIMEOUT", "D3D_ERR_DEVICE_INPUT", "D3D_DTYPE_F32", "D3D_DTYPE_BF16",
     "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR", "D3D_ATTN_AFTER_INDEPENDENT", "D3D_VERIFY_AFTER_INDEPENDENT",
@@ -61,6 +61,8 @@ EXPORTED = {
     "d3d_debug_inject_fault": (None, [_I]),
     "d3d_spec_verify_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P]),
     "d3d_async_round": (_I, [_P, _P, _P]),
+    "d3d_build_branches_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "d3d_build_branches": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
 }
 
 
@@ -270,6 +272,46 @@ def d3d_spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sampl
     rc = lib.d3d_spec_verify(*args, int(sm_limit), D3D_VERIFY_AFTER_INDEPENDENT if after_independent else 0,
                              _stream(stream))
     _check("d3d_spec_verify", rc)
+
+
+def d3d_build_branches_workspace_size(R, B, V, C, F) -> int:
+    return int(lib.d3d_build_branches_workspace_size(R, B, V, C, F))
+
+
+def d3d_build_branches(draft_logits, draft_tokens, C: int, F: int, heads, head_len, ws, anchors=None,
+                       bonus_guess=None, segs=None, cu_q=None, cu_seg=None, stream=None) -> None:
+    """Anchors, branch heads and the packed pass's segment rows (include/d3d.h).
+
+    draft_logits [R, B-1, V] f32/bf16, draft_tokens [R, B-1] int32; outputs
+    anchors [R, C-1, F], heads [R, M, B], head_len [R, M], segs [R*M, 5],
+    cu_q / cu_seg [R+1] (int32), M = (C-1)F + 2.
+    """
+    if draft_logits.dtype == torch.bfloat16:
+        dt = D3D_DTYPE_BF16
+    elif draft_logits.dtype == torch.float32:
+        dt = D3D_DTYPE_F32
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    _need(draft_logits, "draft_logits", draft_logits.dtype, 3)
+    R, Bm1, V = draft_logits.shape
+    B = Bm1 + 1
+    M = (C - 1) * F + 2
+    _need(draft_tokens, "draft_tokens", torch.int32, 2)
+    if tuple(draft_tokens.shape) != (R, B - 1):
+        raise ValueError("draft_tokens must be [R, B-1]")
+    for t, n, shp in ((heads, "heads", (R, M, B)), (head_len, "head_len", (R, M)),
+                      (anchors, "anchors", (R, C - 1, F)), (bonus_guess, "bonus_guess", (R,)),
+                      (segs, "segs", (R * M, 5)), (cu_q, "cu_q", (R + 1,)), (cu_seg, "cu_seg", (R + 1,))):
+        if t is None:
+            continue
+        _need(t, n, torch.int32, len(shp))
+        if tuple(t.shape) != shp:
+            raise ValueError("%s must be %s" % (n, shp))
+    _need(ws, "ws", torch.uint8, 1)
+    rc = lib.d3d_build_branches(_ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(bonus_guess), R, B, V, C, F,
+                                _ptr(anchors), _ptr(heads), _ptr(head_len), _ptr(segs), _ptr(cu_q), _ptr(cu_seg),
+                                _ptr(ws), ws.numel(), _stream(stream))
+    _check("d3d_build_branches", rc)
 
 
 class AttnCall(ctypes.Structure):

@@ -179,6 +179,45 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
 void d3d_debug_inject_fault(int mode);
 
 /* ========================================================================
+ * Branch construction for the asynchronous packed pass.
+ *
+ * [D3D] "Background: asynchronous drafting and cache hits", "Method steps"
+ * (step 4): the packed pass drafts, for every rejection position, one block
+ * from each of F alternative anchors, plus the all-accept block.  This call
+ * builds that pass's segment rows and the branches' heads (the inputs of
+ * d3d_packed_draft_attn and of the branch match) from the drafter's logits.
+ * Reading (the pages do not say how anchors are chosen): the anchors of
+ * rejection position p (0-based draft index, p = 0..C-2) are the F tokens
+ * with the largest draft logit in row p (ties to the lowest index), the
+ * drafted token y_p excluded.
+ *
+ * With M = (C-1)F + 2 branches per request, indexed like the segments:
+ *   anchors  [R, C-1, F] int32 (may be NULL when (C-1)F == 0)
+ *   heads    [R, M, B] int32: branch 0 (the block under verification) is
+ *            empty; branch k = 1 + pF + f is y_0 .. y_{p-1}, anchor (p, f);
+ *            branch M-1 is y_0 .. y_{B-2}, bonus_guess[r]; entries past the
+ *            length are -1
+ *   head_len [R, M] int32: 0, p + 1, and B (0 when bonus_guess is NULL:
+ *            without a guess of the bonus token that branch never matches)
+ *   segs     [R*M] d3d_segment_t, request-local rows (may be NULL):
+ *            (0, B, causal, -1, 0), (kB, B, bidirectional, 0, p+1),
+ *            ((M-1)B, B, bidirectional, 0, B)
+ *   cu_q, cu_seg [R+1] int32: r*M*B and r*M (both NULL or both given)
+ *   draft_logits [R, B-1, V] f32 or bf16; draft_tokens [R, B-1] int32;
+ *   bonus_guess [R] int32 or NULL
+ *   ws       d3d_build_branches_workspace_size() bytes
+ * 1 <= C <= B <= 256, 0 <= F <= 8, F <= V-1 when there are anchors.  A draft
+ * token outside [0, V) sets D3D_ERR_DEVICE_INPUT (nothing is excluded in its
+ * row).  No CTA of the launch waits for another.
+ * ======================================================================== */
+size_t d3d_build_branches_workspace_size(int R, int B, int V, int C, int F);
+
+int d3d_build_branches(const void *draft_logits, int logits_dtype, const int32_t *draft_tokens,
+                       const int32_t *bonus_guess, int R, int B, int V, int C, int F, int32_t *anchors,
+                       int32_t *heads, int32_t *head_len, d3d_segment_t *segs, int32_t *cu_q, int32_t *cu_seg,
+                       void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ========================================================================
  * Speculative-sampling verification.
  *
  * [D3D] "Background: speculative decoding": accept the drafted prefix by

@@ -522,6 +522,90 @@ def test_greedy_bad_draft_token_and_noalloc(d3d):
     np.testing.assert_array_equal(got["out_tokens"][keep], ref["out_tokens"][keep])
 
 
+# ------------------------------------------------------------------ branch construction
+def _run_branches(d3d, v, C, F, bonus=None, full=True):
+    from gpu_util import bf16, f32, i32
+    R, B = v["R"], v["B"]
+    M = (C - 1) * F + 2
+    dr = bf16(v["draft"]) if v["dtype"] == W.DT_BF16 else f32(v["draft"])
+    o = dict(anchors=torch.full((R, C - 1, F), -7, dtype=torch.int32, device="cuda"),
+             heads=torch.full((R, M, B), -7, dtype=torch.int32, device="cuda"),
+             head_len=torch.full((R, M), -7, dtype=torch.int32, device="cuda"))
+    if full:
+        o.update(segs=torch.full((R * M, 5), -7, dtype=torch.int32, device="cuda"),
+                 cu_q=torch.full((R + 1,), -7, dtype=torch.int32, device="cuda"),
+                 cu_seg=torch.full((R + 1,), -7, dtype=torch.int32, device="cuda"))
+    ws = d3d.new_workspace(d3d.d3d_build_branches_workspace_size(R, B, v["V"], C, F))
+    d3d.d3d_build_branches(dr, i32(v["y"]), C, F, o["heads"], o["head_len"], ws, anchors=o["anchors"],
+                           bonus_guess=None if bonus is None else i32(bonus), segs=o.get("segs"),
+                           cu_q=o.get("cu_q"), cu_seg=o.get("cu_seg"))
+    torch.cuda.synchronize()
+    return {k: t.cpu().numpy() for k, t in o.items()}, ws
+
+
+@pytest.mark.parametrize("cfg,C,F,over,bonus", [
+    ("async8b", 12, 2, {}, True),
+    ("async8b", 12, 2, {}, False),
+    ("serve32b", 12, 2, {}, True),
+    ("sweep", 16, 5, {}, True),
+    ("sweep", 8, 3, dict(R=3), False),
+    ("tiny", 12, 2, dict(R=7), True),                 # f32, V = 1024
+    ("async8b", 5, 4, dict(R=2, V=151939), True),     # V % 8 != 0
+    ("async8b", 16, 8, dict(R=2, V=9), True),         # every token but y is an anchor
+    ("async8b", 1, 2, dict(R=3), True),               # C = 1: no anchors
+    ("async8b", 12, 0, dict(R=2), True),              # F = 0
+])
+def test_build_branches_matches_oracle(d3d, cfg, C, F, over, bonus):
+    v = W.verify_inputs(**dict(W.CONFIGS[cfg], **over), seed=50)
+    bg = np.random.default_rng(51).integers(0, v["V"], size=v["R"]).astype(np.int32) if bonus else None
+    ref = oracle.build_branches(dict(draft=v["draft"], dtype=v["dtype"], y=v["y"], bonus_guess=bg, R=v["R"],
+                                     B=v["B"], V=v["V"], C=C, F=F))
+    got, ws = _run_branches(d3d, v, C, F, bonus=bg)
+    for k in ("anchors", "heads", "head_len", "segs", "cu_q", "cu_seg"):
+        np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
+    assert d3d.d3d_workspace_status(ws) == 0
+    # a second call on the same workspace (its counters reset themselves)
+    got2, _ = _run_branches(d3d, v, C, F, bonus=bg, full=False)
+    np.testing.assert_array_equal(got2["heads"], ref["heads"])
+
+
+@pytest.mark.parametrize("dt", [W.DT_F32, W.DT_BF16])
+def test_build_branches_ties_and_bad_token(d3d, dt):
+    rng = np.random.default_rng(52)
+    R, B, V, C, F = 6, 16, 20000, 12, 3
+    vals = rng.integers(0, 3, size=(R, B - 1, V)).astype(np.float32)
+    vals[:, :, rng.integers(0, V, size=5)] = 3.0
+    y = vals.argmax(-1).astype(np.int32)  # the drafted token is the first maximum: the anchors are the next ones
+    v = dict(draft=W.bf16_bits(vals) if dt == W.DT_BF16 else vals, dtype=dt, y=y, R=R, B=B, V=V)
+    ref = oracle.build_branches(dict(v, C=C, F=F, bonus_guess=None))
+    got, ws = _run_branches(d3d, v, C, F)
+    np.testing.assert_array_equal(got["anchors"], ref["anchors"])
+    np.testing.assert_array_equal(got["heads"], ref["heads"])
+    bad = dict(v, y=y.copy())
+    bad["y"][1, 3] = V + 2
+    got, ws = _run_branches(d3d, bad, C, F)
+    assert d3d.d3d_workspace_status(ws) == d3d.D3D_ERR_DEVICE_INPUT
+
+
+def test_built_branches_drive_attention_and_match(d3d):
+    # the segment rows and heads built on the device are what the packed
+    # attention and the fused match consume: both against the oracle
+    from gpu_util import bf16, i32
+    cfg = W.CONFIGS["async8b"]
+    C, F = cfg["C"], cfg["F"]
+    v = W.verify_inputs(**cfg, seed=53)
+    ref_v = oracle.spec_verify(v)
+    bg = ref_v["out_tokens"][:, -1].copy()  # any guess; on full acceptance a matching one makes a hit
+    got, _ = _run_branches(d3d, v, C, F, bonus=bg)
+    a = W.attn_inputs(**cfg, seed=53, segs=got["segs"])
+    out, _ = run_attn(d3d, a)
+    assert_attn_close(out[:, 4:8], oracle.packed_attn(a, heads=(4, 8))[:, 4:8], "device-built segments")
+    hb = dict(heads=got["heads"], head_len=got["head_len"])
+    res = run_verify(d3d, v, heads=hb)[0]
+    want = oracle.branch_match(dict(verified=res["out_tokens"], verified_len=res["num_tokens"], **hb))
+    np.testing.assert_array_equal(res["branch"], want)
+
+
 def test_verify_workspace_reuse_and_many_requests(d3d):
     v = W.verify_inputs(R=4096, B=4, V=64, logits=W.DT_F32, seed=10)
     got1, ws = run_verify(d3d, v)

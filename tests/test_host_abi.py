@@ -121,6 +121,22 @@ def test_invalid_arguments_rejected_on_host(d3d):
     ac.d = 96
     assert L.d3d_async_round(ctypes.byref(ac), ctypes.byref(vc), None) == d3d.D3D_ERR_UNSUPPORTED
 
+    # branch construction: shapes and flags checked before any device work
+    bb = lambda R=1, B=16, V=100, C=12, F=2, anc=fake, h=fake, hl=fake, cq=None, cs=None, ws=fake, wsb=1 << 20: (  # noqa
+        fake, d3d.D3D_DTYPE_BF16, fake, None, R, B, V, C, F, anc, h, hl, None, cq, cs, ws, wsb, None)
+    assert L.d3d_build_branches(*bb(C=17)) == d3d.D3D_ERR_INVALID_ARG        # C > B
+    assert L.d3d_build_branches(*bb(C=0)) == d3d.D3D_ERR_INVALID_ARG
+    assert L.d3d_build_branches(*bb(F=-1)) == d3d.D3D_ERR_INVALID_ARG
+    assert L.d3d_build_branches(*bb(V=2)) == d3d.D3D_ERR_INVALID_ARG         # F > V - 1
+    assert L.d3d_build_branches(*bb(F=9)) == d3d.D3D_ERR_UNSUPPORTED
+    assert L.d3d_build_branches(*bb(cq=fake)) == d3d.D3D_ERR_INVALID_ARG     # cu_q without cu_seg
+    assert L.d3d_build_branches(*bb(h=None)) == d3d.D3D_ERR_INVALID_ARG
+    assert L.d3d_build_branches(*bb(anc=None)) == d3d.D3D_ERR_INVALID_ARG
+    assert L.d3d_build_branches(*bb(ws=None)) == d3d.D3D_ERR_WORKSPACE
+    assert L.d3d_build_branches(*bb(R=0)) == d3d.D3D_OK
+    assert d3d.d3d_build_branches_workspace_size(1, 16, 151936, 12, 2) > 256
+    assert d3d.d3d_build_branches_workspace_size(1, 16, 151936, 17, 2) == 0
+
     assert L.d3d_branch_match(fake, fake, fake, fake, 1, 2, 0, fake, None) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_branch_match(None, fake, fake, fake, 1, 2, 4, fake, None) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_branch_match(fake, fake, fake, fake, 0, 2, 4, fake, None) == d3d.D3D_OK
