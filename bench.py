@@ -284,6 +284,23 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     def match(s):
         d3d.d3d_branch_match(s["out_tokens"], s["num_tokens"], s["heads"], s["head_len"], s["branch"])
 
+    # branch construction for the next round's packed pass (async layouts):
+    # anchors, heads and segment rows from this round's draft rows
+    bC, bF = (cfg["C"], cfg["F"]) if cfg["layout"] == "async" else (1, 0)
+    bM = (bC - 1) * bF + 2
+    ws_b = d3d.new_workspace(d3d.d3d_build_branches_workspace_size(R, B, V, bC, bF), dev)
+    b_out = dict(anchors=torch.empty((R, bC - 1, bF), dtype=torch.int32, device=dev),
+                 heads=torch.empty((R, bM, B), dtype=torch.int32, device=dev),
+                 head_len=torch.empty((R, bM), dtype=torch.int32, device=dev),
+                 segs=torch.empty((R * bM, 5), dtype=torch.int32, device=dev),
+                 cu_q=torch.empty(R + 1, dtype=torch.int32, device=dev),
+                 cu_seg=torch.empty(R + 1, dtype=torch.int32, device=dev))
+
+    def branches(s):
+        d3d.d3d_build_branches(s["draft"], s["y"], bC, bF, b_out["heads"], b_out["head_len"], ws_b,
+                               anchors=b_out["anchors"], bonus_guess=None, segs=b_out["segs"], cu_q=b_out["cu_q"],
+                               cu_seg=b_out["cu_seg"])
+
     stream = torch.cuda.Stream(device=dev)
 
     def round_calls(s):
@@ -406,6 +423,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     t_verify_side = timed(lambda s: verify(s, verify_sms, fused_match=True), n_part)
     t_match = timed(match, n_part)
     t_greedy = timed(greedy, n_part)
+    t_branches = timed(branches, n_part)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -455,6 +473,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                  "frac": round(verify_gbs / peaks["hbm"], 4),
                                  "bytes": wl["verify_bytes"], "traffic": ncu_traffic(args.workload, "verify")},
                   "greedy_verify_us": round(t_greedy * 1e3, 3),
+                  "build_branches_us": round(t_branches * 1e3, 3),
                   "greedy_hbm": {"achieved": round(greedy_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
                                  "frac": round(greedy_gbs / peaks["hbm"], 4), "bytes": wl["greedy_bytes"]}},
         "roofline": roof,

@@ -61,6 +61,23 @@ __host__ __device__ inline BLayout branch_layout(int R, int V, int C, int F)
 __device__ __forceinline__ float logit_at(const float *p, long long i) { return __ldg(p + i); }
 __device__ __forceinline__ float logit_at(const uint16_t *p, long long i) { return bf16_bits_to_float(__ldg(p + i)); }
 
+// 8 consecutive entries from a 16-byte aligned address
+__device__ __forceinline__ void load8(const float *p, float (&x)[8])
+{
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p)), b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+}
+__device__ __forceinline__ void load8(const uint16_t *p, float (&x)[8])
+{
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(wv[e] << 16);
+        x[2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
+    }
+}
+
 // Larger value first, then the lower index.
 __device__ __forceinline__ bool ahead(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
@@ -75,22 +92,16 @@ __device__ __forceinline__ void warp_best(float &v, int &i)
     }
 }
 
-// Insert (x, v) into the sorted list (bv, bi) of length F (best first): the
-// carried pair swaps into every slot it is ahead of, so the list stays
+// Insert (x, v) into the sorted list (bv, bi) of length kF (best first):
+// the carried pair swaps into every slot it is ahead of, so the list stays
 // sorted and its last pair drops out.
-__device__ __forceinline__ void keep_best(float (&bv)[kMaxF], int (&bi)[kMaxF], int F, float x, int v)
+template <int kF> __device__ __forceinline__ void keep_best(float (&bv)[kF], int (&bi)[kF], float x, int v)
 {
-    float lv = bv[0];
-    int li = bi[0];
-#pragma unroll
-    for (int t = 1; t < kMaxF; ++t)
-        if (t == F - 1)
-            lv = bv[t], li = bi[t];
-    if (!ahead(x, v, lv, li))  // behind the list's last pair
+    if (!ahead(x, v, bv[kF - 1], bi[kF - 1]))  // behind the list's last pair
         return;
 #pragma unroll
-    for (int t = 0; t < kMaxF; ++t) {
-        if (t < F && ahead(x, v, bv[t], bi[t])) {
+    for (int t = 0; t < kF; ++t) {
+        if (ahead(x, v, bv[t], bi[t])) {
             const float tx = bv[t];
             const int tv = bi[t];
             bv[t] = x, bi[t] = v;
@@ -99,20 +110,22 @@ __device__ __forceinline__ void keep_best(float (&bv)[kMaxF], int (&bi)[kMaxF], 
     }
 }
 
-// F rounds of a block-wide best over each thread's sorted list: the F best
-// pairs of the block, to thread 0's out arrays.  Indices are distinct, so
+// kF rounds of a block-wide best over each thread's sorted list: the kF best
+// pairs of the block, to the shared out arrays.  Indices are distinct, so
 // exactly one thread's list moves on per round.
-__device__ __forceinline__ void block_top(const float (&bv)[kMaxF], const int (&bi)[kMaxF], int F, float *s_v, int *s_i,
-                          float *out_v, int *out_i)
+template <int kF>
+__device__ __forceinline__ void block_top(const float (&bv)[kF], const int (&bi)[kF], float *s_v, int *s_i,
+                                          float *out_v, int *out_i)
 {
     int head = 0;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int f = 0; f < F; ++f) {
+#pragma unroll
+    for (int f = 0; f < kF; ++f) {
         float hv = -INFINITY;
         int hi = INT_MAX;
 #pragma unroll
-        for (int t = 0; t < kMaxF; ++t)
-            if (t == head && t < F)
+        for (int t = 0; t < kF; ++t)
+            if (t == head)
                 hv = bv[t], hi = bi[t];
         float v = hv;
         int i = hi;
@@ -176,7 +189,7 @@ __device__ void write_request(const BArgs &a, int r, const int32_t *s_y, const i
     }
 }
 
-template <typename T>
+template <typename T, int kF>
 __global__ void __launch_bounds__(kBThreads) branch_build_kernel(const BArgs a)
 {
     __shared__ float s_v[kBThreads / 32 + 1];
@@ -194,6 +207,7 @@ __global__ void __launch_bounds__(kBThreads) branch_build_kernel(const BArgs a)
     float2 *rec = reinterpret_cast<float2 *>(a.ws + L.rec);
     int32_t *status = reinterpret_cast<int32_t *>(a.ws);
     const T *dr = static_cast<const T *>(a.draft);
+    const bool vec = V % 8 == 0 && (reinterpret_cast<uintptr_t>(dr) & 15) == 0;
     const long long n_items = F > 0 ? (long long)R * P * nch : 0;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -219,18 +233,33 @@ __global__ void __launch_bounds__(kBThreads) branch_build_kernel(const BArgs a)
         }
         const T *row = dr + ((long long)r * (B - 1) + p) * V;
         const int v0 = c * kBChunk, v1 = min(V, v0 + kBChunk);
-        float bv[kMaxF];
-        int bi[kMaxF];
+        float bv[kF];
+        int bi[kF];
 #pragma unroll
-        for (int t = 0; t < kMaxF; ++t)
+        for (int t = 0; t < kF; ++t)
             bv[t] = -INFINITY, bi[t] = INT_MAX;
+        if (vec) {  // 16-byte loads of 8 entries (V % 8 == 0, aligned rows)
+#pragma unroll
+            for (int g = 0; g < kBPer / 8; ++g) {
+                const int v = v0 + g * (8 * kBThreads) + 8 * (int)threadIdx.x;
+                if (v < v1) {
+                    float x[8];
+                    load8(row + v, x);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (v + e != yv)
+                            keep_best<kF>(bv, bi, x[e], v + e);
+                }
+            }
+        } else {
 #pragma unroll 4
-        for (int q = 0; q < kBPer; ++q) {
-            const int v = v0 + q * kBThreads + (int)threadIdx.x;
-            if (v < v1 && v != yv)
-                keep_best(bv, bi, F, logit_at(row, v), v);
+            for (int q = 0; q < kBPer; ++q) {
+                const int v = v0 + q * kBThreads + (int)threadIdx.x;
+                if (v < v1 && v != yv)
+                    keep_best<kF>(bv, bi, logit_at(row, v), v);
+            }
         }
-        block_top(bv, bi, F, s_v, s_i, s_ov, s_oi);
+        block_top<kF>(bv, bi, s_v, s_i, s_ov, s_oi);
         if (threadIdx.x == 0) {
             float2 *dst = rec + (rp * nch + c) * F;
             for (int f = 0; f < F; ++f)
@@ -278,21 +307,38 @@ __global__ void __launch_bounds__(kBThreads) branch_build_kernel(const BArgs a)
     }
 }
 
-template <typename T> int launch_branches(const BArgs &a, cudaStream_t stream)
+template <typename T, int kF> int launch_branches_f(const BArgs &a, cudaStream_t stream)
 {
     const BLayout L = branch_layout(a.R, a.V, a.C, a.F);
     const long long n_items = a.F > 0 ? (long long)a.R * (a.C - 1) * L.nch : 0;
     int dev = 0, nsm = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, branch_build_kernel<T>, kBThreads, 0) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, branch_build_kernel<T, kF>, kBThreads, 0) !=
+            cudaSuccess ||
         per_sm < 1)
         return D3D_ERR_CUDA;
     const long long want = n_items > 0 ? n_items : a.R;
     const long long cap = (long long)nsm * per_sm;
     const unsigned grid = (unsigned)(want < cap ? want : cap);
-    branch_build_kernel<T><<<grid, kBThreads, 0, stream>>>(a);
+    branch_build_kernel<T, kF><<<grid, kBThreads, 0, stream>>>(a);
     return cuda_status(cudaGetLastError());
+}
+
+// the list length is a compile-time constant of the kernel (registers only)
+template <typename T> int launch_branches(const BArgs &a, cudaStream_t stream)
+{
+    switch (a.F) {
+    case 0:  // no anchors: the kernel writes heads and rows only
+    case 1: return launch_branches_f<T, 1>(a, stream);
+    case 2: return launch_branches_f<T, 2>(a, stream);
+    case 3: return launch_branches_f<T, 3>(a, stream);
+    case 4: return launch_branches_f<T, 4>(a, stream);
+    case 5: return launch_branches_f<T, 5>(a, stream);
+    case 6: return launch_branches_f<T, 6>(a, stream);
+    case 7: return launch_branches_f<T, 7>(a, stream);
+    default: return launch_branches_f<T, 8>(a, stream);
+    }
 }
 
 }  // namespace
