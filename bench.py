@@ -59,9 +59,12 @@ CSRC = os.path.join(ROOT, "diffusion_drafted_speculative_gb300", "csrc")
 NCU_TRAFFIC = {
     ("async8b", "attn"): {"sources": ("attn.cu", "attn_common.cuh", "sm100_ptx.cuh", "d3d_common.cuh",
                                       "verify_body.cuh"),
-                          "sha": "e17ecde69c3d18fa", "bytes": 13178624},
+                          "sha": "b4e7272360c94a0b", "bytes": 13178624},
     ("async8b", "verify"): {"sources": ("verify.cu", "verify_body.cuh", "sm100_ptx.cuh", "d3d_common.cuh"),
-                            "sha": "539e4a1fb522aa60", "bytes": 9551872},
+                            "sha": "a085d427b37220de", "bytes": 9546496},
+    ("async8b", "greedy"): {"sources": ("verify.cu", "greedy_body.cuh", "verify_body.cuh", "sm100_ptx.cuh",
+                                        "d3d_common.cuh"),
+                            "sha": "a6a7783e755adbca", "bytes": 4903168},
 }
 
 
@@ -475,7 +478,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                   "greedy_verify_us": round(t_greedy * 1e3, 3),
                   "build_branches_us": round(t_branches * 1e3, 3),
                   "greedy_hbm": {"achieved": round(greedy_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
-                                 "frac": round(greedy_gbs / peaks["hbm"], 4), "bytes": wl["greedy_bytes"]}},
+                                 "frac": round(greedy_gbs / peaks["hbm"], 4), "bytes": wl["greedy_bytes"],
+                                 "traffic": ncu_traffic(args.workload, "greedy")}},
         "roofline": roof,
         "gpu_launches": args.steps * LAUNCHES["fused" if fused_round else args.round],
         "clocks": clk, "wall_s_timed_region": round(wall, 4),
