@@ -94,6 +94,8 @@ def parse_args():
     ap.add_argument("--workload", default="async8b", choices=["async8b", "long_block", "serve32b"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-layout-parts", action="store_true",
+                    help="skip timing the attention on the target-verify and training layouts")
     ap.add_argument("--round", choices=["split", "split-attention-first", "fused"], default="split",
                     help="split: the verification, then the attention as its programmatic dependent; "
                          "split-attention-first: the other way round; "
@@ -106,7 +108,8 @@ def parse_args():
 # ----------------------------------------------------------------------------
 def workload(name: str) -> dict:
     cfg = dict(W.CONFIGS[name])
-    segs = W.block_segments(cfg["B"]) if cfg["layout"] == "block" else W.async_segments(cfg["B"], cfg["C"], cfg["F"])
+    segs = W.layout_segments(cfg["layout"], cfg["B"], cfg.get("C", 12), cfg.get("F", 2), cfg.get("T", 2048),
+                             cfg.get("anchors", 128))
     n_q = int(segs[:, 1].sum())
     # visible packed keys per query token, from the segment rows
     vis_packed = 0
@@ -428,6 +431,57 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     t_greedy = timed(greedy, n_part)
     t_branches = timed(branches, n_part)
 
+    def layout_part(name):
+        """The attention on another segment layout (the target's verification
+        pass, the training-time packed pass): its time per call over input
+        sets larger than 2x L2, and its tensor throughput."""
+        c = dict(W.CONFIGS[name])
+        lw = workload(name)
+        parts_sets, tot = [], 0
+        for k in range(16):
+            a = W.attn_inputs(**c, seed=1000 + k)
+            t = {n: bf(a[n]).to(dev) for n in ("q", "kp", "vp", "kn", "vn")}
+            t.update({n: torch.from_numpy(a[n]).to(dev) for n in ("segs", "cu_prefix", "cu_q", "cu_seg")})
+            t["out"] = torch.empty_like(t["q"])
+            parts_sets.append(t)
+            tot += sum(x.numel() * x.element_size() for x in t.values())
+            if tot > 2.2 * l2 and k >= 1:
+                break
+        ws_l = d3d.new_workspace(d3d.d3d_packed_draft_attn_workspace_size(
+            c["R"], c["Hq"], c["Hkv"], c["d"], a["max_q"], a["max_prefix"]), dev)
+
+        def call(t):
+            d3d.d3d_packed_draft_attn(t["q"], t["kp"], t["vp"], t["kn"], t["vn"], t["segs"], t["cu_prefix"],
+                                      t["cu_q"], t["cu_seg"], a["max_q"], a["max_prefix"], a["scale"], t["out"], ws_l)
+        with torch.cuda.stream(stream):
+            for t in parts_sets:
+                call(t)  # eager pass validates the calls
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        reps = max(1, 48 // len(parts_sets))
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                for t in parts_sets:
+                    call(t)
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(4):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (4 * reps * len(parts_sets))
+        tf = lw["flops"] / (ms * 1e-3) / 1e12
+        return {"attn_us": round(ms * 1e3, 3), "query_tokens": lw["n_q"] * c["R"], "prefix": c["L"],
+                "tflops": round(tf, 1),
+                "ctas": d3d.d3d_packed_draft_attn_ctas(c["R"], c["Hq"], c["Hkv"], c["d"], a["max_q"],
+                                                       a["max_prefix"])}
+
+    layout_parts = {} if args.no_layout_parts else {n: layout_part(n) for n in ("target_verify", "train_mask")}
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -436,6 +490,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # attention and verification are each timed alone in a short loop: the
     # burst peaks apply (sustained is for a kernel inside a seconds-long step)
     peaks = load_peaks()
+    for lp in layout_parts.values():  # against the same bf16 peak as the headline attention
+        lp["frac"] = round(lp["tflops"] / peaks["bf16"], 4)
     achieved_tf = wl["flops"] / (t_attn * 1e-3) / 1e12
     att_ai = wl["flops"] / wl["attn_bytes"]
     ridge = peaks["bf16"] * 1e12 / (peaks["hbm"] * 1e9)
@@ -477,6 +533,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                  "bytes": wl["verify_bytes"], "traffic": ncu_traffic(args.workload, "verify")},
                   "greedy_verify_us": round(t_greedy * 1e3, 3),
                   "build_branches_us": round(t_branches * 1e3, 3),
+                  "attn_layouts": layout_parts,
                   "greedy_hbm": {"achieved": round(greedy_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
                                  "frac": round(greedy_gbs / peaks["hbm"], 4), "bytes": wl["greedy_bytes"],
                                  "traffic": ncu_traffic(args.workload, "greedy")}},

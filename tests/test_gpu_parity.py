@@ -132,6 +132,20 @@ def test_attn_sweep_full_size_sampled_head(d3d, C, F):
     assert_attn_close(got[:, heads], _oracle_heads(a, heads)[:, heads], "sweep C%d F%d" % (C, F))
 
 
+@pytest.mark.parametrize("cfg,heads", [("target_verify", [0, 13, 31]), ("train_mask", [0, 22])])
+def test_attn_target_verify_and_training_layouts(d3d, cfg, heads):
+    # the same kernel on two more layouts: the target's verification pass
+    # (one causal block over an 8192-token KV, key splits) and the
+    # training-time packed pass (a causal 2048-token response plus 128 anchor
+    # blocks that see the response before their anchor; 129 segments, more
+    # than the kernel stages in shared memory)
+    a = W.attn_inputs(**W.CONFIGS[cfg], seed=60)
+    got, ws = run_attn(d3d, a)
+    assert np.isfinite(got).all()
+    assert_attn_close(got[:, heads], _oracle_heads(a, heads)[:, heads], cfg)
+    assert d3d.d3d_workspace_status(ws) == 0
+
+
 def test_attn_bad_device_descriptor_sets_status(d3d):
     a = W.attn_inputs(R=1, L=64, Hq=2, Hkv=1, d=64, B=8, C=3, F=2, layout="async", seed=7)
     a["segs"] = a["segs"].copy()

@@ -25,7 +25,8 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "bf16_bits", "bf16_to_f32", "uniform24", "async_segments", "block_segments",
+    "bf16_bits", "bf16_to_f32", "uniform24", "async_segments", "block_segments", "verify_segments",
+    "train_segments", "layout_segments",
     "attn_inputs", "verify_inputs", "branch_heads", "match_inputs", "CONFIGS",
     "SEG_CAUSAL", "SEG_BIDIR", "DT_F32", "DT_BF16",
 ]
@@ -41,6 +42,7 @@ _S_Q, _S_KP, _S_VP, _S_KN, _S_VN = 1, 2, 3, 4, 5
 _S_LPREF = 6
 _S_XT, _S_XD, _S_YU, _S_UACC = 10, 11, 12, 13
 _S_ANCH, _S_MATCH = 20, 21
+_S_TRAIN = 22
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -80,6 +82,27 @@ def block_segments(B: int) -> np.ndarray:
     return np.array([[0, B, SEG_BIDIR, -1, 0]], dtype=np.int32)
 
 
+def verify_segments(B: int) -> np.ndarray:
+    """The target's verification pass over one drafted block: B tokens, causal
+    (each position sees the prefix and the earlier tokens of the block)."""
+    return np.array([[0, B, SEG_CAUSAL, -1, 0]], dtype=np.int32)
+
+
+def train_segments(T: int, n_anchor: int, B: int, seed: int = 0) -> np.ndarray:
+    """Training-time packed layout (forward only): segment 0 is the clean
+    response of T tokens, causal; then one bidirectional block of B tokens
+    (anchor + B-1 masks) per anchor, which sees the response tokens before its
+    anchor (parent 0, parent_len = the anchor's position).  Anchor positions
+    are distinct, drawn uniformly from [1, T) and sorted (input synthesis)."""
+    pos = np.sort(_rng(seed, _S_TRAIN).choice(np.arange(1, T), size=n_anchor, replace=False))
+    rows = [[0, T, SEG_CAUSAL, -1, 0]]
+    q = T
+    for p in pos.tolist():
+        rows.append([q, B, SEG_BIDIR, 0, int(p)])
+        q += B
+    return np.array(rows, dtype=np.int32)
+
+
 def async_segments(B: int, C: int, F: int) -> np.ndarray:
     """Layout of D3D's asynchronous packed pass (D3D, "Method steps", step 4).
 
@@ -112,6 +135,12 @@ CONFIGS = {
                      layout="async", V=151936, logits=DT_BF16, sigma=0.5),
     "sweep": dict(R=1, L=32768, Hq=32, Hkv=8, d=128, B=16, C=12, F=2, layout="async",
                   V=151936, logits=DT_BF16, sigma=0.5),
+    # the target's verification attention: one causal block over a long KV
+    "target_verify": dict(R=1, L=8192, Hq=32, Hkv=8, d=128, B=16, layout="verify",
+                          V=151936, logits=DT_BF16, sigma=0.5),
+    # training-time packed pass: a 2048-token response with 128 anchor blocks
+    "train_mask": dict(R=1, L=512, Hq=32, Hkv=8, d=128, B=16, T=2048, anchors=128, layout="train",
+                       V=151936, logits=DT_BF16, sigma=0.5),
 }
 
 
@@ -122,8 +151,20 @@ def _prefix_lengths(R: int, L, seed: int) -> np.ndarray:
     return np.full(R, int(L), dtype=np.int32)
 
 
+def layout_segments(layout: str, B: int, C: int = 12, F: int = 2, T: int = 2048, anchors: int = 128,
+                    seed: int = 0) -> np.ndarray:
+    """Segment rows of one request for a named layout."""
+    if layout == "block":
+        return block_segments(B)
+    if layout == "verify":
+        return verify_segments(B)
+    if layout == "train":
+        return train_segments(T, anchors, B, seed)
+    return async_segments(B, C, F)
+
+
 def attn_inputs(R=1, L=256, Hq=2, Hkv=1, d=64, B=16, C=12, F=2, layout="block",
-                seed=0, k_scale=1.0, segs=None, **_unused) -> dict:
+                seed=0, k_scale=1.0, segs=None, T=2048, anchors=128, **_unused) -> dict:
     """Inputs of one packed drafting attention call.
 
     Q, K, V ~ N(0, 1) rounded to bf16 (K multiplied by ``k_scale`` first: the
@@ -131,8 +172,8 @@ def attn_inputs(R=1, L=256, Hq=2, Hkv=1, d=64, B=16, C=12, F=2, layout="block",
     prefix for every request) or a (lo, hi) range drawn per request.
     ``segs`` overrides the per-request segment table.
     """
-    if segs is None:
-        segs = block_segments(B) if layout == "block" else async_segments(B, C, F)
+    if segs is None:  # the layout is fixed by its shapes; seed varies the tensors only
+        segs = layout_segments(layout, B, C, F, T, anchors)
     segs = np.asarray(segs, dtype=np.int32).reshape(-1, 5)
     n_q = int(segs[-1, 0] + segs[-1, 1]) if len(segs) else 0
     Ls = _prefix_lengths(R, L, seed)
