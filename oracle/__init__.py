@@ -48,6 +48,7 @@ def _load():
             _lib = ctypes.CDLL(build())
             for name in ("oracle_packed_attn", "oracle_packed_attn_sel", "oracle_dense_attn",
                          "oracle_dense_mask", "oracle_spec_verify", "oracle_greedy_verify", "oracle_build_branches",
+                         "oracle_accept_probs",
                          "oracle_branch_match",
                          "oracle_check_segments"):
                 getattr(_lib, name).restype = ctypes.c_int
@@ -176,6 +177,23 @@ def spec_verify(inp: dict) -> dict:
         _p(out["used_fallback"]))
     if rc != OK:
         raise ValueError("oracle_spec_verify: invalid arguments (rc=%d)" % rc)
+    return out
+
+
+def accept_probs(inp: dict) -> dict:
+    """Per-position acceptance probabilities a_j = sum_v min(P_j, Q_j), the
+    prefix survivals S(k) = a_1 ... a_k and tau = 1 + sum_k S(k) of every
+    request (DScout, "Background: acceptance length tau", "Background: AWL
+    and the acceptance rule"); fp64 softmax at temperature T."""
+    R, B, V = inp["R"], inp["B"], inp["V"]
+    dt = np.uint16 if inp["dtype"] == 1 else np.float32
+    tgt, dr = _c(inp["target"], dt), _c(inp["draft"], dt)
+    out = dict(accept_prob=np.zeros((R, B - 1)), survival=np.zeros((R, B - 1)), tau=np.zeros(R))
+    rc = _load().oracle_accept_probs(_p(tgt), _p(dr), ctypes.c_int(inp["dtype"]), ctypes.c_int(R), ctypes.c_int(B),
+                                     ctypes.c_int(V), ctypes.c_double(inp.get("temperature", 1.0)),
+                                     _p(out["accept_prob"]), _p(out["survival"]), _p(out["tau"]))
+    if rc != OK:
+        raise ValueError("oracle_accept_probs: invalid arguments (rc=%d)" % rc)
     return out
 
 

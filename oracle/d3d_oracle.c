@@ -512,6 +512,47 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype, const i
 }
 
 /*
+ * Per-position acceptance probabilities and the round's expected acceptance
+ * length (DScout, "Background: acceptance length tau" and "Background: AWL
+ * and the acceptance rule"): with P_j = softmax(target row j / T) and
+ * Q_j = softmax(draft row j / T), a draft token y ~ Q_j is accepted with
+ * probability a_j = sum_v min(P_j(v), Q_j(v)); the prefix survival is
+ * S(k) = a_1 ... a_k and tau = 1 + sum_{k=1}^{B-1} S(k).
+ * Outputs: accept_prob [R, B-1] = a, survival [R, B-1] = S, tau [R].
+ */
+int oracle_accept_probs(const void *target, const void *draft, int dtype, int R, int B, int V, double T,
+                        double *accept_prob, double *survival, double *tau)
+{
+    if (R < 0 || B < 2 || V < 1 || !(T > 0.0) || (dtype != OR_F32 && dtype != OR_BF16))
+        return OR_BAD_ARG;
+    double *P = malloc(sizeof(double) * (size_t)V);
+    double *Q = malloc(sizeof(double) * (size_t)V);
+    if (!P || !Q) {
+        free(P);
+        free(Q);
+        return OR_NOMEM;
+    }
+    for (int r = 0; r < R; ++r) {
+        double surv = 1.0, t = 1.0;
+        for (int j = 0; j < B - 1; ++j) {
+            softmax_row(target, dtype, ((size_t)r * B + j) * V, V, T, P);
+            softmax_row(draft, dtype, ((size_t)r * (B - 1) + j) * V, V, T, Q);
+            double a = 0.0;
+            for (int v = 0; v < V; ++v)
+                a += P[v] < Q[v] ? P[v] : Q[v];
+            surv *= a;
+            t += surv;
+            accept_prob[(size_t)r * (B - 1) + j] = a;
+            survival[(size_t)r * (B - 1) + j] = surv;
+        }
+        tau[r] = t;
+    }
+    free(P);
+    free(Q);
+    return OR_OK;
+}
+
+/*
  * Branch construction for the asynchronous packed pass (D3D, "Background:
  * asynchronous drafting and cache hits" and "Method steps", step 4: for
  * every rejection position, several alternative anchors, plus the

@@ -55,6 +55,39 @@ def test_tau_closed_forms():
     assert oracle.expected_tau([0.5, 0.5, 0.5]) == pytest.approx(1.875)
 
 
+def test_accept_probs_special_cases_and_tau():
+    # P = Q: every draft is accepted (a = 1, tau = B); disjoint supports: a = 0
+    # (tau = 1); the hand case of test_tau_closed_forms: V = 2, P = (1/2, 1/2),
+    # Q = (1, 0) gives a = 1/2 and tau = 1.875 at B = 4
+    B, V = 4, 2
+    eq = np.array([[[0.3, -1.2]] * B], np.float32)
+    r = oracle.accept_probs(dict(target=eq, draft=eq[:, : B - 1], dtype=W.DT_F32, R=1, B=B, V=V))
+    np.testing.assert_allclose(r["accept_prob"], 1.0, rtol=1e-12)
+    assert r["tau"][0] == pytest.approx(B)
+    big = 1e4
+    disj_t = np.array([[[big, -big]] * B], np.float32)
+    disj_d = np.array([[[-big, big]] * (B - 1)], np.float32)
+    r = oracle.accept_probs(dict(target=disj_t, draft=disj_d, dtype=W.DT_F32, R=1, B=B, V=V))
+    assert r["accept_prob"].max() < 1e-300 and r["tau"][0] == pytest.approx(1.0)
+    half = np.array([[[0.0, 0.0]] * B], np.float32)
+    one = np.array([[[big, -big]] * (B - 1)], np.float32)
+    r = oracle.accept_probs(dict(target=half, draft=one, dtype=W.DT_F32, R=1, B=B, V=V))
+    np.testing.assert_allclose(r["accept_prob"], 0.5, rtol=1e-12)
+    assert r["tau"][0] == pytest.approx(1.875)
+    np.testing.assert_allclose(r["survival"][0], [0.5, 0.25, 0.125], rtol=1e-12)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_accept_probs_match_library_softmax(T):
+    x, z = _rows(200, 8, seed=35)
+    P = scipy.special.softmax(x.astype(np.float64) / T, axis=-1)
+    Q = scipy.special.softmax(z.astype(np.float64) / T, axis=-1)
+    a = np.minimum(P[: 7], Q).sum(-1)
+    r = oracle.accept_probs(dict(target=x[None], draft=z[None], dtype=W.DT_F32, R=1, B=8, V=200, temperature=T))
+    np.testing.assert_allclose(r["accept_prob"][0], a, rtol=1e-12)
+    assert r["tau"][0] == pytest.approx(oracle.expected_tau(a), rel=1e-12)
+
+
 # ---------------------------------------------------------------- hand-worked verify cases
 def _case_inputs(c):
     B, V = c["B"], c["V"]
