@@ -19,7 +19,8 @@ __all__ = [
     "D3DError", "lib", "d3d_status_string", "d3d_version", "d3d_validate_segments",
     "d3d_packed_draft_attn", "d3d_packed_draft_attn_workspace_size", "d3d_packed_draft_attn_ctas",
     "d3d_spec_verify", "d3d_spec_verify_workspace_size", "d3d_spec_verify_noalloc", "d3d_async_round",
-    "AttnCall", "VerifyCall", "d3d_build_branches", "d3d_build_branches_workspace_size", "d3d_branch_match", "d3d_workspace_status", "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
+    "AttnCall", "VerifyCall", "d3d_build_branches", "d3d_build_branches_workspace_size",
+    "d3d_accept_probs", "d3d_accept_probs_workspace_size", "d3d_branch_match", "d3d_workspace_status", "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
     "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
     "D3D_ERR_DEVICE_TIMEOUT", "D3D_ERR_DEVICE_INPUT", "D3D_DTYPE_F32", "D3D_DTYPE_BF16",
     "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR", "D3D_ATTN_AFTER_INDEPENDENT", "D3D_VERIFY_AFTER_INDEPENDENT",
@@ -62,6 +63,8 @@ EXPORTED = {
     "d3d_spec_verify_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P]),
     "d3d_async_round": (_I, [_P, _P, _P]),
     "d3d_build_branches_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "d3d_accept_probs_workspace_size": (_Z, [_I, _I, _I]),
+    "d3d_accept_probs": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _Z, _P]),
     "d3d_build_branches": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
 }
 
@@ -312,6 +315,37 @@ def d3d_build_branches(draft_logits, draft_tokens, C: int, F: int, heads, head_l
                                 _ptr(anchors), _ptr(heads), _ptr(head_len), _ptr(segs), _ptr(cu_q), _ptr(cu_seg),
                                 _ptr(ws), ws.numel(), _stream(stream))
     _check("d3d_build_branches", rc)
+
+
+def d3d_accept_probs_workspace_size(R, B, V) -> int:
+    return int(lib.d3d_accept_probs_workspace_size(R, B, V))
+
+
+def d3d_accept_probs(target_logits, draft_logits, temperature: float, accept_prob, ws, survival=None, tau=None,
+                     stream=None) -> None:
+    """a_j = sum min(P_j, Q_j), survivals S(k) and tau (include/d3d.h); float32 outputs."""
+    if target_logits.dtype == torch.bfloat16:
+        dt = D3D_DTYPE_BF16
+    elif target_logits.dtype == torch.float32:
+        dt = D3D_DTYPE_F32
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    _need(target_logits, "target_logits", target_logits.dtype, 3)
+    _need(draft_logits, "draft_logits", target_logits.dtype, 3)
+    R, B, V = target_logits.shape
+    if tuple(draft_logits.shape) != (R, B - 1, V):
+        raise ValueError("draft_logits must be [R, B-1, V]")
+    for t, n, shp in ((accept_prob, "accept_prob", (R, B - 1)), (survival, "survival", (R, B - 1)),
+                      (tau, "tau", (R,))):
+        if t is None:
+            continue
+        _need(t, n, torch.float32, len(shp))
+        if tuple(t.shape) != shp:
+            raise ValueError("%s must be %s" % (n, shp))
+    _need(ws, "ws", torch.uint8, 1)
+    rc = lib.d3d_accept_probs(_ptr(target_logits), _ptr(draft_logits), dt, R, B, V, float(temperature),
+                              _ptr(accept_prob), _ptr(survival), _ptr(tau), _ptr(ws), ws.numel(), _stream(stream))
+    _check("d3d_accept_probs", rc)
 
 
 class AttnCall(ctypes.Structure):

@@ -58,26 +58,6 @@ __host__ __device__ inline BLayout branch_layout(int R, int V, int C, int F)
     return L;
 }
 
-__device__ __forceinline__ float logit_at(const float *p, long long i) { return __ldg(p + i); }
-__device__ __forceinline__ float logit_at(const uint16_t *p, long long i) { return bf16_bits_to_float(__ldg(p + i)); }
-
-// 8 consecutive entries from a 16-byte aligned address
-__device__ __forceinline__ void load8(const float *p, float (&x)[8])
-{
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p)), b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
-    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
-}
-__device__ __forceinline__ void load8(const uint16_t *p, float (&x)[8])
-{
-    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
-    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        x[2 * e] = __uint_as_float(wv[e] << 16);
-        x[2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
-    }
-}
-
 // Larger value first, then the lower index.
 __device__ __forceinline__ bool ahead(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
@@ -244,7 +224,7 @@ __global__ void __launch_bounds__(kBThreads) branch_build_kernel(const BArgs a)
                 const int v = v0 + g * (8 * kBThreads) + 8 * (int)threadIdx.x;
                 if (v < v1) {
                     float x[8];
-                    load8(row + v, x);
+                    load_logits8(row + v, x);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         if (v + e != yv)
@@ -256,7 +236,7 @@ __global__ void __launch_bounds__(kBThreads) branch_build_kernel(const BArgs a)
             for (int q = 0; q < kBPer; ++q) {
                 const int v = v0 + q * kBThreads + (int)threadIdx.x;
                 if (v < v1 && v != yv)
-                    keep_best<kF>(bv, bi, logit_at(row, v), v);
+                    keep_best<kF>(bv, bi, load_logit(row, v), v);
             }
         }
         block_top<kF>(bv, bi, s_v, s_i, s_ov, s_oi);

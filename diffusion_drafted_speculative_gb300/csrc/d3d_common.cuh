@@ -28,6 +28,27 @@ __device__ inline void record_status(int32_t *status, int32_t code)
 
 __device__ inline float bf16_bits_to_float(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
+// One logit as float (f32, or bf16 bits: exact), read through the read-only path.
+__device__ inline float load_logit(const float *p, long long i) { return __ldg(p + i); }
+__device__ inline float load_logit(const uint16_t *p, long long i) { return bf16_bits_to_float(__ldg(p + i)); }
+
+// 8 consecutive logits from a 16-byte aligned address.
+__device__ inline void load_logits8(const float *p, float (&x)[8])
+{
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p)), b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+}
+__device__ inline void load_logits8(const uint16_t *p, float (&x)[8])
+{
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(wv[e] << 16);
+        x[2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
+    }
+}
+
 // Convert a CUDA error at enqueue time to a status code.
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? D3D_OK : D3D_ERR_CUDA; }
 

@@ -179,6 +179,31 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
 void d3d_debug_inject_fault(int mode);
 
 /* ========================================================================
+ * Acceptance probabilities and expected acceptance length.
+ *
+ * [DScout] "Background: AWL and the acceptance rule": position j accepts its
+ * draft token with probability a_j = sum_v min(P_j(v), Q_j(v));
+ * [DScout] "Background: acceptance length tau": the prefix survival
+ * S(k) = a_1 ... a_k and tau = 1 + sum_{k=1}^{B-1} S(k).  P_j and Q_j as in
+ * d3d_spec_verify (softmax of the target and draft rows at temperature T).
+ *
+ *   target_logits [R, B, V], draft_logits [R, B-1, V] f32 or bf16 (row B-1 of
+ *               the target is not read)
+ *   temperature > 0 (else D3D_ERR_INVALID_ARG)
+ *   accept_prob [R, B-1] float32 output; survival [R, B-1] and tau [R]
+ *               float32 outputs, each may be NULL
+ *   ws          d3d_accept_probs_workspace_size() bytes
+ * Two launches on the stream (the second a programmatic dependent of the
+ * first); fp32 arithmetic, sums in a fixed order (results do not depend on
+ * scheduling); a_j is clamped to 1.  2 <= B <= 257.
+ * ======================================================================== */
+size_t d3d_accept_probs_workspace_size(int R, int B, int V);
+
+int d3d_accept_probs(const void *target_logits, const void *draft_logits, int logits_dtype, int R, int B, int V,
+                     float temperature, float *accept_prob, float *survival, float *tau, void *ws, size_t ws_bytes,
+                     cudaStream_t stream);
+
+/* ========================================================================
  * Branch construction for the asynchronous packed pass.
  *
  * [D3D] "Background: asynchronous drafting and cache hits", "Method steps"

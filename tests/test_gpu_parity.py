@@ -620,6 +620,34 @@ def test_built_branches_drive_attention_and_match(d3d):
     np.testing.assert_array_equal(res["branch"], want)
 
 
+# ------------------------------------------------------------------ acceptance probabilities and tau
+@pytest.mark.parametrize("cfg,over", [
+    ("tiny", {}), ("tiny", dict(R=5, temperature=0.7)), ("async8b", {}), ("serve32b", {}),
+    ("long_block", dict(sigma=1.0)), ("tiny", dict(R=3, V=1001)), ("async8b", dict(R=2, V=151939)),
+])
+def test_accept_probs_and_tau_match_oracle(d3d, cfg, over):
+    from gpu_util import bf16, f32
+    v = W.verify_inputs(**dict(W.CONFIGS[cfg], **over), seed=70)
+    ref = oracle.accept_probs(v)
+    R, B = v["R"], v["B"]
+    tg, dr = (bf16(v["target"]), bf16(v["draft"])) if v["dtype"] == W.DT_BF16 else (f32(v["target"]), f32(v["draft"]))
+    ws = d3d.new_workspace(d3d.d3d_accept_probs_workspace_size(R, B, v["V"]))
+    outs = []
+    for _ in range(2):  # twice on one workspace: the counters reset themselves; the sums are in a fixed order
+        a = torch.full((R, B - 1), float("nan"), device="cuda")
+        sv = torch.full((R, B - 1), float("nan"), device="cuda")
+        tau = torch.full((R,), float("nan"), device="cuda")
+        d3d.d3d_accept_probs(tg, dr, v.get("temperature", 1.0), a, ws, survival=sv, tau=tau)
+        torch.cuda.synchronize()
+        outs.append((a.cpu().numpy(), sv.cpu().numpy(), tau.cpu().numpy()))
+    a, sv, tau = outs[0]
+    np.testing.assert_allclose(a, ref["accept_prob"], rtol=1e-4, atol=2e-6)
+    np.testing.assert_allclose(sv, ref["survival"], rtol=5e-4, atol=2e-6)
+    np.testing.assert_allclose(tau, ref["tau"], rtol=2e-4)
+    for x, y in zip(outs[0], outs[1]):
+        np.testing.assert_array_equal(x, y)
+
+
 def test_verify_workspace_reuse_and_many_requests(d3d):
     v = W.verify_inputs(R=4096, B=4, V=64, logits=W.DT_F32, seed=10)
     got1, ws = run_verify(d3d, v)

@@ -121,6 +121,18 @@ def test_invalid_arguments_rejected_on_host(d3d):
     ac.d = 96
     assert L.d3d_async_round(ctypes.byref(ac), ctypes.byref(vc), None) == d3d.D3D_ERR_UNSUPPORTED
 
+    # acceptance probabilities: argument checks before any device work
+    ap = lambda R=1, B=16, V=100, T=1.0, out=fake, ws=fake, wsb=1 << 20: (  # noqa
+        fake, fake, d3d.D3D_DTYPE_BF16, R, B, V, T, out, None, None, ws, wsb, None)
+    assert L.d3d_accept_probs(*ap(T=0.0)) == d3d.D3D_ERR_INVALID_ARG
+    assert L.d3d_accept_probs(*ap(T=float("inf"))) == d3d.D3D_ERR_INVALID_ARG
+    assert L.d3d_accept_probs(*ap(B=1)) == d3d.D3D_ERR_INVALID_ARG
+    assert L.d3d_accept_probs(*ap(out=None)) == d3d.D3D_ERR_INVALID_ARG
+    assert L.d3d_accept_probs(*ap(B=300)) == d3d.D3D_ERR_UNSUPPORTED
+    assert L.d3d_accept_probs(*ap(ws=None)) == d3d.D3D_ERR_WORKSPACE
+    assert L.d3d_accept_probs(*ap(R=0)) == d3d.D3D_OK
+    assert d3d.d3d_accept_probs_workspace_size(1, 16, 151936) > 256
+
     # branch construction: shapes and flags checked before any device work
     bb = lambda R=1, B=16, V=100, C=12, F=2, anc=fake, h=fake, hl=fake, cq=None, cs=None, ws=fake, wsb=1 << 20: (  # noqa
         fake, d3d.D3D_DTYPE_BF16, fake, None, R, B, V, C, F, anc, h, hl, None, cq, cs, ws, wsb, None)
