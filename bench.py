@@ -302,6 +302,13 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                  cu_q=torch.empty(R + 1, dtype=torch.int32, device=dev),
                  cu_seg=torch.empty(R + 1, dtype=torch.int32, device=dev))
 
+    ws_p = d3d.new_workspace(d3d.d3d_accept_probs_workspace_size(R, B, V), dev)
+    p_out = dict(a=torch.empty((R, B - 1), device=dev), sv=torch.empty((R, B - 1), device=dev),
+                 tau=torch.empty(R, device=dev))
+
+    def accept_probs(s):  # a_j = sum min(P_j, Q_j), survivals and tau of the same rows
+        d3d.d3d_accept_probs(s["target"], s["draft"], 1.0, p_out["a"], ws_p, survival=p_out["sv"], tau=p_out["tau"])
+
     def branches(s):
         d3d.d3d_build_branches(s["draft"], s["y"], bC, bF, b_out["heads"], b_out["head_len"], ws_b,
                                anchors=b_out["anchors"], bonus_guess=None, segs=b_out["segs"], cu_q=b_out["cu_q"],
@@ -430,6 +437,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     t_match = timed(match, n_part)
     t_greedy = timed(greedy, n_part)
     t_branches = timed(branches, n_part)
+    t_accept = timed(accept_probs, n_part)
 
     def layout_part(name):
         """The attention on another segment layout (the target's verification
@@ -533,6 +541,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                  "bytes": wl["verify_bytes"], "traffic": ncu_traffic(args.workload, "verify")},
                   "greedy_verify_us": round(t_greedy * 1e3, 3),
                   "build_branches_us": round(t_branches * 1e3, 3),
+                  "accept_probs_us": round(t_accept * 1e3, 3),
                   "attn_layouts": layout_parts,
                   "greedy_hbm": {"achieved": round(greedy_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
                                  "frac": round(greedy_gbs / peaks["hbm"], 4), "bytes": wl["greedy_bytes"],
