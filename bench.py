@@ -59,12 +59,12 @@ CSRC = os.path.join(ROOT, "diffusion_drafted_speculative_gb300", "csrc")
 NCU_TRAFFIC = {
     ("async8b", "attn"): {"sources": ("attn.cu", "attn_common.cuh", "sm100_ptx.cuh", "d3d_common.cuh",
                                       "verify_body.cuh"),
-                          "sha": "b4e7272360c94a0b", "bytes": 13178624},
+                          "sha": "97cfbf5b684ff13a", "bytes": 13178624},
     ("async8b", "verify"): {"sources": ("verify.cu", "verify_body.cuh", "sm100_ptx.cuh", "d3d_common.cuh"),
-                            "sha": "a085d427b37220de", "bytes": 9546496},
+                            "sha": "2f1784edcc033d03", "bytes": 9546752},
     ("async8b", "greedy"): {"sources": ("verify.cu", "greedy_body.cuh", "verify_body.cuh", "sm100_ptx.cuh",
                                         "d3d_common.cuh"),
-                            "sha": "a6a7783e755adbca", "bytes": 4903168},
+                            "sha": "e5969c79af57e049", "bytes": 4903168},
 }
 
 
