@@ -753,6 +753,7 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
     // are 16-byte aligned, with the ring's shared memory)
     // (compiled for the 512-thread launch only; the 256-thread one keeps its registers)
     const int nring = (NT == kNTLimited) ? a.ring : 0;
+    const int nring1 = nring > 0 ? nring : 1;  // divisor for the ring's slot arithmetic (used only with a ring)
     uint8_t *ring = reinterpret_cast<uint8_t *>(s_dyn);  // reused for the staged records after phase A
     const uint32_t ring_s = sm100::smem_u32(ring), ring_bar = ring_s + (uint32_t)nring * Ring<NT>::kSlotBytes;
     auto ring_issue = [&](long long it, int slot) {
@@ -810,9 +811,9 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
         const int r = (int)(item / nch) / B;
         const int yv = (j < B - 1) ? __ldg(y + (size_t)r * (B - 1) + j) : -1;
         if (NT == kNTLimited && nring > 0) {
-            const int slot = k_item % nring;
+            const int slot = k_item % nring1;
             const uint32_t bar = ring_bar + 8u * (uint32_t)slot;
-            const uint32_t parity = (uint32_t)(k_item / nring) & 1u;
+            const uint32_t parity = (uint32_t)(k_item / nring1) & 1u;
             if (!sm100::mbar_try_wait(bar, parity)) {  // bounded wait for the slot's copies
                 const uint64_t t0 = sm100::global_ns();
                 while (!sm100::mbar_try_wait_sleep(bar, parity))
@@ -880,7 +881,7 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
         if (nring > 0 && threadIdx.x == 0) {
             const long long nxt = item + (long long)nring * vgrid;
             if (nxt < nA)
-                ring_issue(nxt, k_item % nring);
+                ring_issue(nxt, k_item % nring1);
         }
     }
 
