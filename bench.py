@@ -59,9 +59,9 @@ CSRC = os.path.join(ROOT, "diffusion_drafted_speculative_gb300", "csrc")
 NCU_TRAFFIC = {
     ("async8b", "attn"): {"sources": ("attn.cu", "attn_common.cuh", "sm100_ptx.cuh", "d3d_common.cuh",
                                       "verify_body.cuh"),
-                          "sha": "97cfbf5b684ff13a", "bytes": 13178624},
+                          "sha": "7f3d645126d08223", "bytes": 13179648},
     ("async8b", "verify"): {"sources": ("verify.cu", "verify_body.cuh", "sm100_ptx.cuh", "d3d_common.cuh"),
-                            "sha": "2f1784edcc033d03", "bytes": 9546752},
+                            "sha": "802f314046cc7507", "bytes": 9547776},
     ("async8b", "greedy"): {"sources": ("verify.cu", "greedy_body.cuh", "verify_body.cuh", "sm100_ptx.cuh",
                                         "d3d_common.cuh"),
                             "sha": "e5969c79af57e049", "bytes": 4903168},

@@ -146,6 +146,22 @@ def test_attn_target_verify_and_training_layouts(d3d, cfg, heads):
     assert d3d.d3d_workspace_status(ws) == 0
 
 
+def test_attn_wait_runs_out_reports_status_and_context_survives(d3d):
+    # failure detection without a GPU fault: the producer skips the first key
+    # tile, the consumer's bounded wait runs out, the kernel records the
+    # timeout in the status word and returns; the next call is correct
+    a = W.attn_inputs(**W.CONFIGS["tiny"], seed=9)
+    d3d.d3d_debug_inject_fault(1)
+    try:
+        _, ws = run_attn(d3d, a)
+    finally:
+        d3d.d3d_debug_inject_fault(0)
+    assert d3d.d3d_workspace_status(ws, clear=True) == d3d.D3D_ERR_DEVICE_TIMEOUT
+    got, ws2 = run_attn(d3d, a)
+    assert_attn_close(got, oracle.packed_attn(a), "after a timed-out call")
+    assert d3d.d3d_workspace_status(ws2) == 0
+
+
 def test_attn_bad_device_descriptor_sets_status(d3d):
     a = W.attn_inputs(R=1, L=64, Hq=2, Hkv=1, d=64, B=8, C=3, F=2, layout="async", seed=7)
     a["segs"] = a["segs"].copy()
