@@ -13,7 +13,7 @@
 // (max, sum of exponentials) of both rows; the second merges its row's chunk
 // statistics into the softmax normalisers, sums min(P, Q) over its chunk, and
 // the CTA that counts a request's last chunk adds the chunk sums of each row
-// in chunk order (deterministic) and writes a_j, S(k) and tau.  No CTA waits
+// in a fixed order (deterministic) and writes a_j, S(k) and tau.  No CTA waits
 // for another.
 #include <math.h>
 
@@ -241,15 +241,16 @@ template <typename T> __global__ void __launch_bounds__(kAThreads) accept_min_ke
         __syncthreads();
         if (!s_last)
             continue;
-        // ---- the request's last chunk: a_j in chunk order, then S(k) and tau
+        // ---- the request's last chunk: a_j (fixed order), then S(k) and tau
         __threadfence();
         for (int j = w; j < B - 1; j += kAThreads / 32) {
-            if (lane == 0) {
-                float aj = 0.f;
-                for (int k = 0; k < nch; ++k)
-                    aj += __ldcg(part + ((long long)r * (B - 1) + j) * nch + k);
+            // every lane adds its chunks in order, then a fixed shuffle tree
+            float aj = 0.f;
+            for (int k = lane; k < nch; k += 32)
+                aj += __ldcg(part + ((long long)r * (B - 1) + j) * nch + k);
+            aj = warp_sum(aj);
+            if (lane == 0)
                 s_a[j] = fminf(aj, 1.f);  // a probability: rounding may carry the sum past 1
-            }
         }
         __syncthreads();
         if (threadIdx.x == 0) {

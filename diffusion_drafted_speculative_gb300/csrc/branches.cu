@@ -252,31 +252,53 @@ __global__ void __launch_bounds__(kBThreads) branch_build_kernel(const BArgs a)
             continue;
         // ---- the request's last item: merge every row's chunk lists
         __threadfence();
+        for (int j = threadIdx.x; j < B - 1; j += kBThreads)  // in flight while the lists merge
+            s_y[j] = __ldg(a.y + (long long)r * (B - 1) + j);
+        constexpr int kCache = 8;  // list entries each lane holds (rows of up to 256 entries)
         for (int pp = w; pp < P; pp += kBThreads / 32) {
             const float2 *lst = rec + ((long long)r * P + pp) * nch * F;
-            int taken = 0;  // the merged list so far is in s_anc[pp*F .. pp*F + taken)
+            const int n = nch * F;
+            const bool cached = n <= 32 * kCache;
+            float cv[kCache];
+            int ci[kCache];
+#pragma unroll
+            for (int t = 0; t < kCache; ++t) {  // one pass over the row's lists
+                const int k = lane + 32 * t;
+                const float2 e = (cached && k < n) ? __ldcg(lst + k) : make_float2(-INFINITY, __int_as_float(INT_MAX));
+                cv[t] = e.x, ci[t] = __float_as_int(e.y);
+            }
             for (int f = 0; f < F; ++f) {
                 float v = -INFINITY;
                 int i = INT_MAX;
-                for (int k = lane; k < nch * F; k += 32) {
-                    const float2 e = __ldcg(lst + k);
-                    const int ei = __float_as_int(e.y);
-                    bool used = false;
-                    for (int t = 0; t < taken; ++t)
-                        used = used || s_anc[pp * F + t] == ei;
-                    if (!used && ahead(e.x, ei, v, i))
-                        v = e.x, i = ei;
+                if (cached) {
+#pragma unroll
+                    for (int t = 0; t < kCache; ++t)
+                        if (ahead(cv[t], ci[t], v, i))
+                            v = cv[t], i = ci[t];
+                } else {  // long rows: read the lists again, skipping the pairs already taken
+                    for (int k = lane; k < n; k += 32) {
+                        const float2 e = __ldcg(lst + k);
+                        const int ei = __float_as_int(e.y);
+                        bool used = false;
+                        for (int t = 0; t < f; ++t)
+                            used = used || s_anc[pp * F + t] == ei;
+                        if (!used && ahead(e.x, ei, v, i))
+                            v = e.x, i = ei;
+                    }
                 }
                 warp_best(v, i);
                 i = __shfl_sync(0xffffffffu, i, 0);
                 if (lane == 0)
                     s_anc[pp * F + f] = i;
+                if (cached) {  // the winner leaves its lane's cache (indices are distinct)
+#pragma unroll
+                    for (int t = 0; t < kCache; ++t)
+                        if (ci[t] == i)
+                            cv[t] = -INFINITY, ci[t] = INT_MAX;
+                }
                 __syncwarp();
-                ++taken;
             }
         }
-        for (int j = threadIdx.x; j < B - 1; j += kBThreads)
-            s_y[j] = __ldg(a.y + (long long)r * (B - 1) + j);
         __syncthreads();
         for (int e = threadIdx.x; e < P * F; e += kBThreads)
             a.anchors[(long long)r * P * F + e] = s_anc[e];
