@@ -292,10 +292,11 @@ int d3d_build_branches(const void *draft_logits, int logits_dtype, const int32_t
  *               token), so the match needs nothing from the drafting pass.
  *   ws          workspace, d3d_spec_verify_workspace_size() bytes
  *   sm_limit    0: the kernel may use every SM.  n > 0: at most n CTAs, each
- *               holding a whole SM, so that a kernel launched beside it on
- *               another stream (the drafting attention of the same round)
- *               keeps the remaining SMs whichever starts first.  Results do
- *               not depend on it.  Negative: D3D_ERR_INVALID_ARG.
+ *               holding a whole SM, so that a kernel running beside it (the
+ *               drafting attention of the same round, launched as its
+ *               programmatic dependent or on another stream) keeps the
+ *               remaining SMs whichever starts first.  Results do not depend
+ *               on it.  Negative: D3D_ERR_INVALID_ARG.
  *   flags       0, or D3D_VERIFY_AFTER_INDEPENDENT: the launch may start
  *               while the kernel before it on the stream still runs
  *               (programmatic dependent launch) -- for the drafting attention
