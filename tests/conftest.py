@@ -11,3 +11,12 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running statistical test")
+
+
+# The mutation tests run the oracle's pins against a copy of the oracle with
+# one planted mistake; this variable points the oracle at that build.
+_ORACLE_LIB = os.environ.get("D3D_ORACLE_LIB_OVERRIDE")
+if _ORACLE_LIB:
+    import oracle
+
+    oracle.build = lambda force=False: _ORACLE_LIB

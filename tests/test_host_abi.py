@@ -158,9 +158,9 @@ def _t(a):
     return torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.int32)))
 
 
-@pytest.mark.parametrize("bad", [None, "overlap", "gap", "later_parent", "bidir_parent", "long_parent", "nested",
-                                 "len_without_parent", "empty_seg", "short_total", "bad_mode", "neg_parent_len",
-                                 "cu_start"])
+@pytest.mark.parametrize("bad", [None, "overlap", "gap", "shifted", "later_parent", "bidir_parent",
+                                 "bidir_parent_alone", "long_parent", "nested", "len_without_parent", "empty_seg",
+                                 "short_total", "bad_mode", "neg_parent_len", "cu_start"])
 def test_validate_segments_matches_oracle_rules(d3d, bad):
     segs = W.async_segments(4, 3, 2).astype(np.int64)
     N = int(segs[:, 1].sum())
@@ -170,10 +170,15 @@ def test_validate_segments_matches_oracle_rules(d3d, bad):
     elif bad == "gap":
         segs[2:, 0] += 1
         cu_q = [0, N + 1]
+    elif bad == "shifted":
+        segs[2, 0] += 1
     elif bad == "later_parent":
         segs[1, 3] = 2
     elif bad == "bidir_parent":
         segs[2, 3] = 1
+    elif bad == "bidir_parent_alone":
+        segs[1, 3], segs[1, 4] = -1, 0
+        segs[2, 3], segs[2, 4] = 1, 1
     elif bad == "long_parent":
         segs[1, 4] = 5
     elif bad == "nested":

@@ -508,8 +508,9 @@ def test_ragged_batch_equals_requests_alone():
         np.testing.assert_array_equal(out[q0:q1], oracle.packed_attn(one))
 
 
-@pytest.mark.parametrize("bad", ["overlap", "gap", "later_parent", "bidir_parent", "long_parent",
-                                 "nested", "len_without_parent", "empty_seg", "short_total", "bad_mode"])
+@pytest.mark.parametrize("bad", ["overlap", "gap", "shifted", "later_parent", "bidir_parent",
+                                 "bidir_parent_alone", "long_parent", "nested", "len_without_parent",
+                                 "empty_seg", "short_total", "bad_mode"])
 def test_segment_checker_rejects(bad):
     segs = W.async_segments(4, 3, 2).astype(np.int64)
     N = int(segs[:, 1].sum())
@@ -519,10 +520,15 @@ def test_segment_checker_rejects(bad):
     elif bad == "gap":
         segs[2:, 0] += 1
         cu_q = [0, N + 1]
+    elif bad == "shifted":  # a gap then an overlap: the lengths still add up
+        segs[2, 0] += 1
     elif bad == "later_parent":
         segs[1, 3] = 2
     elif bad == "bidir_parent":
         segs[2, 3] = 1
+    elif bad == "bidir_parent_alone":  # the parent has no parent but is not causal
+        segs[1, 3], segs[1, 4] = -1, 0
+        segs[2, 3], segs[2, 4] = 1, 1
     elif bad == "long_parent":
         segs[1, 4] = 5
     elif bad == "nested":
