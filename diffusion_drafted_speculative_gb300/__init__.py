@@ -130,7 +130,8 @@ def d3d_version() -> int:
 def new_workspace(nbytes: int, device=None) -> torch.Tensor:
     """Zero-filled uint8 device buffer for a workspace (torch allocations are 256-byte aligned)."""
     ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
-    assert ws.data_ptr() % 256 == 0
+    if ws.data_ptr() % 256:
+        raise RuntimeError("workspace allocation is not 256-byte aligned")
     return ws
 
 
