@@ -195,7 +195,8 @@ void d3d_debug_inject_fault(int mode);
  *   ws          d3d_accept_probs_workspace_size() bytes
  * Two launches on the stream (the second a programmatic dependent of the
  * first); fp32 arithmetic, sums in a fixed order (results do not depend on
- * scheduling); a_j is clamped to 1.  2 <= B <= 257.
+ * scheduling); a_j is clamped to 1.  2 <= B <= 257 (B > 257:
+ * D3D_ERR_UNSUPPORTED).
  * ======================================================================== */
 size_t d3d_accept_probs_workspace_size(int R, int B, int V);
 
@@ -278,7 +279,8 @@ int d3d_build_branches(const void *draft_logits, int logits_dtype, const int32_t
  *   u_accept [R, B-1], u_sample [R]  float32 in [0, 1)
  *   temperature   > 0 (sampling) or 0 (greedy); negative or not finite:
  *               D3D_ERR_INVALID_ARG
- *   B >= 2, V >= 1
+ *   B >= 2, V >= 1 (else D3D_ERR_INVALID_ARG); B > 256 or V > 8388608
+ *               (1024 chunks of 8192 logits): D3D_ERR_UNSUPPORTED
  *   accept_len [R], out_tokens [R, B], num_tokens [R]  int32 outputs
  *   alpha, p_draft, q_draft [R, B-1] float32 outputs, each may be NULL
  *               (p_draft = P_j(y_j), q_draft = Q_j(y_j))

@@ -84,6 +84,11 @@ def test_invalid_arguments_rejected_on_host(d3d):
     assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 16)) == d3d.D3D_ERR_WORKSPACE
     assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, ctypes.c_void_p(264), 1 << 20)) == d3d.D3D_ERR_WORKSPACE
     assert L.d3d_spec_verify(*args(1, 300, 10, 1.0, 1, fake, 1 << 30)) == d3d.D3D_ERR_UNSUPPORTED
+    assert L.d3d_spec_verify(*args(1, 257, 10, 1.0, 1, fake, 1 << 30)) == d3d.D3D_ERR_UNSUPPORTED
+    assert L.d3d_spec_verify(*args(1, 4, 8388609, 1.0, 1, fake, 1 << 40)) == d3d.D3D_ERR_UNSUPPORTED
+    assert d3d.d3d_spec_verify_workspace_size(1, 257, 10) == 0
+    assert d3d.d3d_spec_verify_workspace_size(1, 4, 8388609) == 0
+    assert d3d.d3d_spec_verify_workspace_size(1, 256, 8388608) > 256
     assert L.d3d_spec_verify(*args(0, 4, 10, 1.0, 1, None, 0)) == d3d.D3D_OK  # nothing to do
     assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 1 << 20, -1)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 1 << 20, 0, -1)) == d3d.D3D_ERR_INVALID_ARG
@@ -141,6 +146,7 @@ def test_invalid_arguments_rejected_on_host(d3d):
     assert L.d3d_build_branches(*bb(F=-1)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_build_branches(*bb(V=2)) == d3d.D3D_ERR_INVALID_ARG         # F > V - 1
     assert L.d3d_build_branches(*bb(F=9)) == d3d.D3D_ERR_UNSUPPORTED
+    assert L.d3d_build_branches(*bb(B=257)) == d3d.D3D_ERR_UNSUPPORTED
     assert L.d3d_build_branches(*bb(cq=fake)) == d3d.D3D_ERR_INVALID_ARG     # cu_q without cu_seg
     assert L.d3d_build_branches(*bb(h=None)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_build_branches(*bb(anc=None)) == d3d.D3D_ERR_INVALID_ARG
