@@ -128,7 +128,10 @@ int d3d_validate_segments(const d3d_segment_t *segs, const int32_t *cu_q, const 
  *   cu_seg      [R+1] int32 (device) segment offsets, cu_seg[R] = total_segs
  *   max_q, max_prefix  host upper bounds of any request's packed / prefix
  *               length (they size the grid; a request beyond them is a
- *               device input error)
+ *               device input error); max_q <= 8192 (64 tiles of 128 rows,
+ *               else D3D_ERR_UNSUPPORTED)
+ *   q, k_*, v_*, out  16-byte aligned (the tensor maps' base rule; else
+ *               D3D_ERR_INVALID_ARG)
  *   d           64 or 128 (else D3D_ERR_UNSUPPORTED); Hq % Hkv == 0 and
  *               128 % (Hq/Hkv) == 0
  *   scale       softmax scale (normally 1/sqrt(d))

@@ -101,6 +101,9 @@ def test_invalid_arguments_rejected_on_host(d3d):
     assert attn(Hq=30, Hkv=8) == d3d.D3D_ERR_INVALID_ARG
     assert attn(d=96) == d3d.D3D_ERR_UNSUPPORTED
     assert attn(Hq=24, Hkv=8) == d3d.D3D_ERR_UNSUPPORTED  # G = 3 does not divide 128
+    assert attn(max_q=8193) == d3d.D3D_ERR_UNSUPPORTED
+    assert L.d3d_packed_draft_attn(ctypes.c_void_p(264), fake, fake, fake, fake, fake, fake, fake, fake, 1, 32, 8,
+                                   128, 16, 64, 16, 64, 1, 0.1, fake, fake, 1 << 30, 0, None) == d3d.D3D_ERR_INVALID_ARG
     assert attn(scale=0.0) == d3d.D3D_ERR_INVALID_ARG
     assert attn(scale=float("inf")) == d3d.D3D_ERR_INVALID_ARG
     assert attn(ws=None) == d3d.D3D_ERR_WORKSPACE
