@@ -235,9 +235,11 @@ int d3d_accept_probs(const void *target_logits, const void *draft_logits, int lo
  *   draft_logits [R, B-1, V] f32 or bf16; draft_tokens [R, B-1] int32;
  *   bonus_guess [R] int32 or NULL
  *   ws       d3d_build_branches_workspace_size() bytes
- * 1 <= C <= B <= 256, 0 <= F <= 8, F <= V-1 when there are anchors.  A draft
- * token outside [0, V) sets D3D_ERR_DEVICE_INPUT (nothing is excluded in its
- * row).  No CTA of the launch waits for another.
+ * 1 <= C <= B, F >= 0, F <= V-1 when there are anchors (else
+ * D3D_ERR_INVALID_ARG); B <= 256, F <= 8, (C-1)F <= 256 and R*M*B < 2^31
+ * (else D3D_ERR_UNSUPPORTED).  A draft token outside [0, V) sets
+ * D3D_ERR_DEVICE_INPUT (nothing is excluded in its row).  No CTA of the
+ * launch waits for another.
  * ======================================================================== */
 size_t d3d_build_branches_workspace_size(int R, int B, int V, int C, int F);
 
