@@ -337,6 +337,40 @@ def test_disjoint_support_always_rejects_first_and_samples_P1():
     assert _chi2_p(r["out_tokens"][:, 0], P[0]) > 1e-4
 
 
+def test_one_token_vocabulary():
+    """V = 1: every distribution is the point mass on token 0 whatever the
+    logits and the temperature, so alpha = 1 > u for every u in [0, 1): all
+    drafts are accepted and the bonus is token 0; the greedy argmax is 0;
+    a_j = 1, S(k) = 1 and tau = B.  No anchor exists besides the drafted
+    token, so F > 0 is rejected; with F = 0 the pass holds only the block
+    under verification and the all-accept block."""
+    R, B, V, T = 3, 5, 1, 0.7
+    rng = np.random.default_rng(3)
+    tgt = (rng.standard_normal((R, B, V)) * 5).astype(np.float32)
+    dr = (rng.standard_normal((R, B - 1, V)) * 5).astype(np.float32)
+    y = np.zeros((R, B - 1), np.int32)
+    inp = dict(target=tgt, draft=dr, dtype=W.DT_F32, y=y, R=R, B=B, V=V, temperature=T,
+               u_accept=np.full((R, B - 1), np.nextafter(np.float32(1), np.float32(0))),
+               u_sample=rng.random(R).astype(np.float32))
+    r = oracle.spec_verify(inp)
+    assert (r["alpha"] == 1.0).all() and (r["p"] == 1.0).all() and (r["q"] == 1.0).all()
+    assert (r["accept_len"] == B - 1).all() and (r["num_tokens"] == B).all()
+    assert (r["out_tokens"] == 0).all() and not r["used_fallback"].any()
+    g = oracle.greedy_verify(inp)
+    assert (g["argmax"] == 0).all() and (g["accept"] == 1.0).all()
+    assert (g["accept_len"] == B - 1).all() and (g["out_tokens"] == 0).all()
+    a = oracle.accept_probs(inp)
+    assert (a["accept_prob"] == 1.0).all() and (a["survival"] == 1.0).all() and (a["tau"] == B).all()
+    br = dict(draft=dr, dtype=W.DT_F32, y=y, R=R, B=B, V=V, C=3, bonus_guess=np.zeros(R, np.int32))
+    with pytest.raises(ValueError):
+        oracle.build_branches(dict(br, F=1))
+    b = oracle.build_branches(dict(br, F=0))
+    assert b["head_len"].tolist() == [[0, B]] * R
+    assert (b["heads"][:, 1] == 0).all() and (b["heads"][:, 0] == -1).all()
+    assert b["segs"].tolist() == [[0, B, W.SEG_CAUSAL, -1, 0], [B, B, W.SEG_BIDIR, 0, B]] * R
+    assert b["cu_q"].tolist() == [2 * B * r for r in range(R + 1)]
+
+
 def test_rejection_never_emits_rejected_token():
     V, B, R = 10, 6, 50_000
     x, z = _rows(V, B, seed=41, sigma=2.0)
