@@ -47,6 +47,11 @@ MUTANTS = [
      "res[v] = (Q[v] > P[v]) ? Q[v] - P[v] : 0.0;"),
     ("residual_is_target", "res[v] = (P[v] > Q[v]) ? P[v] - Q[v] : 0.0;", "res[v] = P[v];"),
     ("cdf_target_not_scaled", "double target = u * S, c = 0.0;", "double target = u, c = 0.0;"),
+    ("margin_sample_unnormalised", "*margin = (lo < hi ? lo : hi) / S;", "*margin = (lo < hi ? lo : hi);"),
+    ("margin_sample_far_end", "*margin = (lo < hi ? lo : hi) / S;", "*margin = (lo > hi ? lo : hi) / S;"),
+    ("margin_accept_last_test_only", "if (gap < mA)\n                mA = gap;", "mA = gap;"),
+    ("fallback_not_recorded", "fb = 1;\n                t = inverse_cdf(P,", "fb = 0;\n                t = inverse_cdf(P,"),
+    ("fallback_never_fires", "if (t < 0) {\n                fb = 1;", "if (t < -1) {\n                fb = 1;"),
     ("bonus_from_wrong_row", "softmax_row(target, dtype, ((size_t)r * B + (B - 1)) * V, V, T, P);",
      "softmax_row(target, dtype, ((size_t)r * B + (B - 2)) * V, V, T, P);"),
     ("resample_from_next_row", "softmax_row(target, dtype, ((size_t)r * B + a) * V, V, T, P);",

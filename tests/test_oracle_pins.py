@@ -109,6 +109,83 @@ def test_verify_hand_worked(case):
     assert int(r["num_tokens"][0]) == n
     assert r["out_tokens"][0, :n].tolist() == case["tokens"]
     assert (r["out_tokens"][0, n:] == -1).all()
+    # the near-tie margins and the zero-residual fallback, worked out by hand
+    # (abs 1e-7: the uniforms are float32, within 6e-8 of the decimals written)
+    assert r["margin_accept"][0] == pytest.approx(case["margin_accept"], abs=1e-7)
+    assert r["margin_sample"][0] == pytest.approx(case["margin_sample"], abs=1e-7)
+    assert int(r["used_fallback"][0]) == case["used_fallback"]
+
+
+def _margins_by_library(inp):
+    """The oracle's margins restated with library routines: scipy softmax for
+    P, Q and alpha, numpy cumsum/searchsorted for the inverse CDF."""
+    R, B, V, T = inp["R"], inp["B"], inp["V"], inp["temperature"]
+    P = scipy.special.softmax(inp["target"].astype(np.float64) / T, axis=-1)
+    Q = scipy.special.softmax(inp["draft"].astype(np.float64) / T, axis=-1)
+    ma, ms, fb, tok = np.zeros(R), np.zeros(R), np.zeros(R, np.int32), np.zeros(R, np.int32)
+    for r in range(R):
+        y = inp["y"][r]
+        p, q = P[r, np.arange(B - 1), y], Q[r, np.arange(B - 1), y]
+        al = np.minimum(1.0, p / q)
+        u = inp["u_accept"][r].astype(np.float64)
+        rej = np.nonzero(~(u < al))[0]
+        a = int(rej[0]) if len(rej) else B - 1
+        decided = np.arange(min(a + 1, B - 1))
+        ma[r] = np.abs(u[decided] - al[decided]).min()
+        w = np.maximum(P[r, a] - Q[r, a], 0.0) if a < B - 1 else P[r, B - 1]
+        if not w.sum() > 0:
+            fb[r], w = 1, P[r, a]
+        c = np.cumsum(w)
+        S = c[-1]
+        x = float(inp["u_sample"][r]) * S
+        v = min(int(np.searchsorted(c, x, side="right")), V - 1)
+        lo = x - (c[v - 1] if v > 0 else 0.0)
+        ms[r] = min(lo, c[v] - x) / S
+        tok[r] = v
+    return ma, ms, fb, tok
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_margins_match_library_restatement(T):
+    # random rows whose acceptance uniforms sit close to alpha and whose sample
+    # uniforms sit close to a CDF step: the oracle's two margins and tokens
+    # equal the scipy/numpy restatement
+    rng = np.random.default_rng(61)
+    R, B, V = 400, 5, 40
+    x = (rng.standard_normal((R, B, V)) * 2).astype(np.float32)
+    z = (x[:, : B - 1] + rng.standard_normal((R, B - 1, V)) * 0.8).astype(np.float32)
+    Q = scipy.special.softmax(z.astype(np.float64) / T, axis=-1)
+    y = np.array([[rng.choice(V, p=Q[r, j]) for j in range(B - 1)] for r in range(R)], np.int32)
+    inp = dict(target=x, draft=z, dtype=W.DT_F32, y=y, R=R, B=B, V=V, temperature=T,
+               u_accept=rng.random((R, B - 1)).astype(np.float32),
+               u_sample=rng.random(R).astype(np.float32))
+    P = scipy.special.softmax(x.astype(np.float64) / T, axis=-1)
+    al = np.minimum(1.0, P[np.arange(R)[:, None], np.arange(B - 1)[None], y] /
+                    Q[np.arange(R)[:, None], np.arange(B - 1)[None], y])
+    near = rng.random((R, B - 1)) < 0.3  # some uniforms a known small distance from alpha
+    inp["u_accept"] = np.where(near, np.clip(al + rng.choice([-1, 1], (R, B - 1)) * 1e-4, 0, 0.999999),
+                               inp["u_accept"]).astype(np.float32)
+    r = oracle.spec_verify(inp)
+    ma, ms, fb, tok = _margins_by_library(inp)
+    np.testing.assert_allclose(r["margin_accept"], ma, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["margin_sample"], ms, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(r["used_fallback"], fb)
+    keep = ms > 1e-9
+    np.testing.assert_array_equal(r["out_tokens"][np.arange(R), r["accept_len"]][keep], tok[keep])
+    assert (r["margin_accept"] < 2e-4).sum() > 50 and (r["margin_sample"] < 0.05).sum() > 20
+
+
+def test_zero_residual_falls_back_to_P_in_distribution():
+    # identical target and draft rows with u = 1 (outside [0, 1)) reject with a
+    # residual of exactly zero: the token then follows P at that row
+    V, B, R = 12, 3, 100_000
+    x, _ = _rows(V, B, seed=71)
+    inp = _fixed_rows_inputs(x, x[: B - 1].copy(), 1.0, R, seed=72)
+    inp["u_accept"][:, 1] = 1.0
+    r = oracle.spec_verify(inp)
+    assert (r["accept_len"] == 1).all() and (r["used_fallback"] == 1).all()
+    P = scipy.special.softmax(x.astype(np.float64), axis=-1)
+    assert _chi2_p(r["out_tokens"][:, 1], P[1]) > 1e-4
 
 
 # ---------------------------------------------------------------- greedy (temperature 0)
