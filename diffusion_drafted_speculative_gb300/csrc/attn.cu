@@ -374,11 +374,12 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
     const uint32_t tmem = *tmem_slot;
 
     // number of packed tiles of the query tile; waits for the mask on first use
+    // (called by whole warps: the vote keeps the answer warp-uniform)
     int npk_cache = -1;
     uint32_t mk0 = 0, mk1 = 0;
     auto npk = [&]() -> int {
         if (npk_cache < 0) {
-            if (!wait_bar(bar(B_MASK), 0, abort_flag, status))
+            if (!__all_sync(0xffffffffu, wait_bar(bar(B_MASK), 0, abort_flag, status)))
                 return -1;
             mk0 = *(volatile uint32_t *)&mask[0];
             mk1 = *(volatile uint32_t *)&mask[1];
@@ -407,68 +408,91 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
 
     if (warp == kTmaWarp) {
         // =================== TMA producer ===================
-        // issue order = the tensor core's consumption order: K0, K1, then
+        // The whole warp runs the loop (warp-uniform control flow: every value
+        // the copies need stays warp-uniform); one elected lane issues.
+        // Issue order = the tensor core's consumption order: K0, K1, then
         // V(k), K(k+2) for k = 0, 1, ...
-        if (lane == 0) {
-            int k_cnt[kKStages] = {}, v_cnt[kVStages] = {};
+        const bool leader = elect_one();
+        int nk = 0, nv = 0;     // K / V tiles handled, in list order
+        bool skipped0 = false;  // the injected fault left K tile 0 unissued
+        if (leader) {
             mbar_arrive_expect_tx(bar(B_Q), Lay::kQBytes);
             for (int cb = 0; cb < D / 64; ++cb)
                 tma_load_3d(sQ + cb * kBlockBytes, tm_q, bar(B_Q), cb * 64, hk * p.G, b.q0 + mt * p.TQ);
-            auto issue = [&](int k, bool is_k) -> bool {
-                const int ns = is_k ? kKStages : kVStages;
-                const int s = k % ns;
-                const int empty = is_k ? B_KE : B_VE, full = is_k ? B_KF : B_VF;
-                if (k >= ns && !wait_bar(bar(empty + s), ((k - ns) / ns) & 1, abort_flag, status))
-                    return false;
-                if (p.fault == 1 && is_k && k == 0)
-                    return true;  // injected fault: this tile never arrives
-                bool pre;
-                const int row = tile_row(k, pre);
-                const CUtensorMap *m = is_k ? (pre ? tm_kp : tm_kn) : (pre ? tm_vp : tm_vn);
-                const uint32_t dst = (is_k ? sK : sV) + s * Lay::kKBytes;
+        }
+        __syncwarp();
+        auto issue = [&](int k, bool is_k) -> bool {
+            const int ns = is_k ? kKStages : kVStages;
+            const int s = k % ns;
+            const int empty = is_k ? B_KE : B_VE, full = is_k ? B_KF : B_VF;
+            if (k >= ns && !__all_sync(0xffffffffu, wait_bar(bar(empty + s), ((k - ns) / ns) & 1, abort_flag, status)))
+                return false;
+            ++(is_k ? nk : nv);
+            if (p.fault == 1 && is_k && k == 0) {
+                skipped0 = true;  // injected fault: this tile never arrives
+                return true;
+            }
+            bool pre;
+            const int row = tile_row(k, pre);
+            const CUtensorMap *m = is_k ? (pre ? tm_kp : tm_kn) : (pre ? tm_vp : tm_vn);
+            const uint32_t dst = (is_k ? sK : sV) + s * Lay::kKBytes;
+            if (leader) {
                 mbar_arrive_expect_tx(bar(full + s), Lay::kKBytes);
                 for (int cb = 0; cb < D / 64; ++cb)
                     tma_load_3d(dst + cb * kBlockBytes, m, bar(full + s), cb * 64, hk, row);
-                ++(is_k ? k_cnt[s] : v_cnt[s]);
-                return true;
-            };
-            bool ok = true;
-            for (int k = 0; ok && k < 2; ++k) {
-                const int e = exists(k);
-                ok = e >= 0;
-                if (e == 1)
-                    ok = issue(k, true);
             }
-            for (int k = 0; ok; ++k) {
-                const int e = exists(k);
-                if (e != 1)
-                    break;
-                ok = issue(k, false);
-                const int e2 = ok ? exists(k + 2) : -1;
-                if (e2 < 0)
-                    break;
-                if (e2 == 1)
-                    ok = issue(k + 2, true);
-            }
-            // every copy this thread started must land before the CTA exits
-            wait_drain(bar(B_Q), 0, status);
-            for (int s = 0; s < kKStages; ++s)
-                if (k_cnt[s] > 0)
-                    wait_drain(bar(B_KF + s), (k_cnt[s] - 1) & 1, status);
-            for (int s = 0; s < kVStages; ++s)
-                if (v_cnt[s] > 0)
-                    wait_drain(bar(B_VF + s), (v_cnt[s] - 1) & 1, status);
+            __syncwarp();
+            return true;
+        };
+        bool ok = true;
+        for (int k = 0; ok && k < 2; ++k) {
+            const int e = exists(k);
+            ok = e >= 0;
+            if (e == 1)
+                ok = issue(k, true);
+        }
+        for (int k = 0; ok; ++k) {
+            const int e = exists(k);
+            if (e != 1)
+                break;
+            ok = issue(k, false);
+            const int e2 = ok ? exists(k + 2) : -1;
+            if (e2 < 0)
+                break;
+            if (e2 == 1)
+                ok = issue(k + 2, true);
+        }
+        // every copy this warp started must land before the CTA exits: the
+        // last phase of each stage (tiles s, s + ns, ... of the n handled)
+        auto issued = [](int n, int s, int ns) { return n > s ? (n - 1 - s) / ns + 1 : 0; };
+        wait_drain(bar(B_Q), 0, status);
+        for (int s = 0; s < kKStages; ++s) {
+            const int c = issued(nk, s, kKStages) - ((s == 0 && skipped0) ? 1 : 0);
+            if (c > 0)
+                wait_drain(bar(B_KF + s), (c - 1) & 1, status);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            const int c = issued(nv, s, kVStages);
+            if (c > 0)
+                wait_drain(bar(B_VF + s), (c - 1) & 1, status);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // =================== MMA issuer ===================
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
-            constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 0, 1);
-            // S(k) = Q K_k^T into TMEM buffer k % 2, then release the K stage
-            auto issue_s = [&](int k) {
-                const int ks = k % kKStages;
-                const uint32_t tS = tmem + (uint32_t)(k & 1) * kBN;
+        // The whole warp runs the loop and waits (warp-uniform control flow,
+        // so the descriptors stay warp-uniform); one elected lane issues the
+        // MMAs and their commits.
+        const bool leader = elect_one();
+        constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
+        constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 0, 1);
+        auto wait_all = [&](uint32_t bar_addr, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, wait_bar(bar_addr, parity, abort_flag, status));
+        };
+        // S(k) = Q K_k^T into TMEM buffer k % 2, then release the K stage
+        auto issue_s = [&](int k) {
+            const int ks = k % kKStages;
+            const uint32_t tS = tmem + (uint32_t)(k & 1) * kBN;
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * kBlockBytes + (kk % 4) * 32;
@@ -478,11 +502,14 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
                 }
                 mma_commit(bar(B_SF + (k & 1)));
                 mma_commit(bar(B_KE + ks));
-            };
-            // O += P(k) V_k with P read from buffer k % 2, then release the V stage
-            auto issue_pv = [&](int k) {
-                const int vs = k % kVStages;
-                const uint32_t tP = tmem + (uint32_t)(k & 1) * kBN, tO = tmem + 2u * kBN;
+            }
+            __syncwarp();
+        };
+        // O += P(k) V_k with P read from buffer k % 2, then release the V stage
+        auto issue_pv = [&](int k) {
+            const int vs = k % kVStages;
+            const uint32_t tP = tmem + (uint32_t)(k & 1) * kBN, tO = tmem + 2u * kBN;
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
                     // A = P in TMEM (8 columns of bf16 pairs per 16 keys); B = V
@@ -493,47 +520,52 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
                 }
                 mma_commit(bar(B_OW));
                 mma_commit(bar(B_VE + vs));
-            };
-            bool ok = wait_bar(bar(B_Q), 0, abort_flag, status);
-            for (int k = 0; ok && k < 2; ++k) {
-                const int e = exists(k);
-                ok = e >= 0;
-                if (e == 1) {
-                    ok = wait_bar(bar(B_KF + k % kKStages), (k / kKStages) & 1, abort_flag, status);
-                    if (ok) {
-                        tc_fence_after();
-                        issue_s(k);
-                    }
+            }
+            __syncwarp();
+        };
+        bool ok = wait_all(bar(B_Q), 0);
+        for (int k = 0; ok && k < 2; ++k) {
+            const int e = exists(k);
+            ok = e >= 0;
+            if (e == 1) {
+                ok = wait_all(bar(B_KF + k % kKStages), (k / kKStages) & 1);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(k);
                 }
             }
-            // per tile k: PV(k) once P(k) is written, then S(k+2) into the buffer PV(k)
-            // has just read; the tensor core computes these while the softmax
-            // works on tile k+1
-            for (int k = 0; ok; ++k) {
-                const int e = exists(k);
-                if (e != 1) {
-                    ok = e >= 0;
-                    break;
-                }
-                ok = wait_bar(bar(B_VF + k % kVStages), (k / kVStages) & 1, abort_flag, status) &&
-                     wait_bar(bar(B_PR + (k & 1)), (k >> 1) & 1, abort_flag, status);
-                if (!ok)
-                    break;
-                tc_fence_after();
-                issue_pv(k);
-                const int e2 = exists(k + 2);
-                ok = e2 >= 0;
-                if (e2 == 1) {
-                    ok = wait_bar(bar(B_KF + (k + 2) % kKStages), ((k + 2) / kKStages) & 1, abort_flag, status);
-                    if (ok)
-                        issue_s(k + 2);
-                }
-            }
-            // every MMA is complete when B_DONE fires: O_0, O_1 final, and the
-            // Q and K/V buffers free; TMEM is released only after it
-            mma_commit(bar(B_DONE));
-            wait_drain(bar(B_DONE), 0, status);
         }
+        // per tile k: PV(k) once P(k) is written, then S(k+2) into the buffer
+        // PV(k) has just read; the tensor core computes these while the softmax
+        // works on tile k+1.  S(k+2) is attempted after every PV (its own K wait
+        // returns at once when the CTA aborts); only then does a failure end
+        // the loop, and no MMA is issued without its data.
+        for (int k = 0; ok; ++k) {
+            const int e = exists(k);
+            if (e != 1) {
+                ok = e >= 0;
+                break;
+            }
+            ok = wait_all(bar(B_VF + k % kVStages), (k / kVStages) & 1) &&
+                 wait_all(bar(B_PR + (k & 1)), (k >> 1) & 1);
+            if (!ok)
+                break;
+            tc_fence_after();
+            issue_pv(k);
+            const int e2 = exists(k + 2);
+            ok = e2 >= 0;
+            if (e2 == 1) {
+                ok = wait_all(bar(B_KF + (k + 2) % kKStages), ((k + 2) / kKStages) & 1);
+                if (ok)
+                    issue_s(k + 2);
+            }
+        }
+        // every MMA is complete when B_DONE fires: O final, and the Q and K/V
+        // buffers free; TMEM is released only after it
+        if (leader)
+            mma_commit(bar(B_DONE));
+        __syncwarp();
+        wait_drain(bar(B_DONE), 0, status);
         __syncwarp();
     } else if (warp < kTmaWarp) {
         // =================== softmax warpgroups ===================
