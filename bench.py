@@ -88,12 +88,15 @@ def ncu_traffic(wl_name: str, part: str):
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 20000 for this library, 5 for the reference arm)")
+    ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (default: 200, reference arm 3)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="async8b", choices=["async8b", "long_block", "serve32b"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the long-block, serving-batch and C/F-sweep measurements")
     ap.add_argument("--no-layout-parts", action="store_true",
                     help="skip timing the attention on the target-verify and training layouts")
     ap.add_argument("--round", choices=["split", "split-attention-first", "fused"], default="split",
@@ -125,6 +128,16 @@ def workload(name: str) -> dict:
     greedy_bytes = 2.0 * R * B * V  # greedy verification reads the target logits only
     return dict(cfg=cfg, segs=segs, n_q=n_q, R=R, flops=flops, attn_bytes=attn_bytes, verify_bytes=verify_bytes,
                 greedy_bytes=greedy_bytes, positions=R * B, vis_packed=vis_packed)
+
+
+def workload_label(name: str) -> str:
+    """The workload as both arms name it in config.workload."""
+    wl = workload(name)
+    cfg = wl["cfg"]
+    return "%s: R=%d, prefix %s, %d/%d heads, d=%d, B=%d%s, N_async=%d, V=%d, M=%d heads" % (
+        name, cfg["R"], cfg["L"], cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["B"],
+        (", C=%d, F=%d" % (cfg["C"], cfg["F"])) if cfg["layout"] == "async" else " block",
+        wl["n_q"], cfg["V"], (cfg.get("C", 1) - 1) * cfg.get("F", 1) + 2)
 
 
 # ----------------------------------------------------------------------------
@@ -439,56 +452,13 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     t_branches = timed(branches, n_part)
     t_accept = timed(accept_probs, n_part)
 
-    def layout_part(name):
-        """The attention on another segment layout (the target's verification
-        pass, the training-time packed pass): its time per call over input
-        sets larger than 2x L2, and its tensor throughput."""
-        c = dict(W.CONFIGS[name])
-        lw = workload(name)
-        parts_sets, tot = [], 0
-        for k in range(16):
-            a = W.attn_inputs(**c, seed=1000 + k)
-            t = {n: bf(a[n]).to(dev) for n in ("q", "kp", "vp", "kn", "vn")}
-            t.update({n: torch.from_numpy(a[n]).to(dev) for n in ("segs", "cu_prefix", "cu_q", "cu_seg")})
-            t["out"] = torch.empty_like(t["q"])
-            parts_sets.append(t)
-            tot += sum(x.numel() * x.element_size() for x in t.values())
-            if tot > 2.2 * l2 and k >= 1:
-                break
-        ws_l = d3d.new_workspace(d3d.d3d_packed_draft_attn_workspace_size(
-            c["R"], c["Hq"], c["Hkv"], c["d"], a["max_q"], a["max_prefix"]), dev)
-
-        def call(t):
-            d3d.d3d_packed_draft_attn(t["q"], t["kp"], t["vp"], t["kn"], t["vn"], t["segs"], t["cu_prefix"],
-                                      t["cu_q"], t["cu_seg"], a["max_q"], a["max_prefix"], a["scale"], t["out"], ws_l)
-        with torch.cuda.stream(stream):
-            for t in parts_sets:
-                call(t)  # eager pass validates the calls
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        reps = max(1, 48 // len(parts_sets))
-        with torch.cuda.graph(g, stream=stream):
-            for _ in range(reps):
-                for t in parts_sets:
-                    call(t)
-        with torch.cuda.stream(stream):
-            g.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(4):
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / (4 * reps * len(parts_sets))
-        tf = lw["flops"] / (ms * 1e-3) / 1e12
-        return {"attn_us": round(ms * 1e3, 3), "query_tokens": lw["n_q"] * c["R"], "prefix": c["L"],
-                "tflops": round(tf, 1),
-                "ctas": d3d.d3d_packed_draft_attn_ctas(c["R"], c["Hq"], c["Hkv"], c["d"], a["max_q"],
-                                                       a["max_prefix"])}
-
-    layout_parts = {} if args.no_layout_parts else {n: layout_part(n) for n in ("target_verify", "train_mask")}
+    peaks = load_peaks()
+    layout_parts = {} if args.no_layout_parts else {
+        n: time_attention(d3d, torch, dev, stream, dict(W.CONFIGS[n]), l2, peaks) for n in ("target_verify", "train_mask")}
+    # the other workloads of the comparison contract: attention and verification
+    # of the long synchronous block and of the 16-request serving batch, and the
+    # attention over the C/F budget sweep at a 32768-token prefix
+    other = {} if args.no_other_workloads else other_workloads(d3d, torch, dev, stream, l2, peaks)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -497,9 +467,6 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     # attention and verification are each timed alone in a short loop: the
     # burst peaks apply (sustained is for a kernel inside a seconds-long step)
-    peaks = load_peaks()
-    for lp in layout_parts.values():  # against the same bf16 peak as the headline attention
-        lp["frac"] = round(lp["tflops"] / peaks["bf16"], 4)
     achieved_tf = wl["flops"] / (t_attn * 1e-3) / 1e12
     att_ai = wl["flops"] / wl["attn_bytes"]
     ridge = peaks["bf16"] * 1e12 / (peaks["hbm"] * 1e9)
@@ -521,10 +488,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy; random bf16 tensors and logits)",
-        "config": {"workload": "%s: R=%d, prefix %s, %d/%d heads, d=%d, B=%d%s, N_async=%d, V=%d, M=%d heads"
-                   % (args.workload, R, cfg["L"], Hq, Hkv, d, B,
-                      (", C=%d, F=%d" % (cfg["C"], cfg["F"])) if cfg["layout"] == "async" else " block",
-                      wl["n_q"], V, (cfg.get("C", 1) - 1) * cfg.get("F", 1) + 2),
+        "config": {"workload": workload_label(args.workload),
                    "l2": "inputs rotate over %d sets (%.0f MB > 2x L2 %.0f MB)" % (
                        n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
                    "timing": "CUDA graph replays, CUDA events on the launching stream"},
@@ -543,6 +507,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                   "build_branches_us": round(t_branches * 1e3, 3),
                   "accept_probs_us": round(t_accept * 1e3, 3),
                   "attn_layouts": layout_parts,
+                  "other_workloads": other,
                   "greedy_hbm": {"achieved": round(greedy_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
                                  "frac": round(greedy_gbs / peaks["hbm"], 4), "bytes": wl["greedy_bytes"],
                                  "traffic": ncu_traffic(args.workload, "greedy")}},
@@ -558,6 +523,168 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def _graph_time(torch, stream, calls, reps_total=48, rounds=4):
+    """Mean device time (ms) of one call, from CUDA graphs replaying the calls
+    (each a closure over one input set) round-robin, CUDA events on the stream."""
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c()  # eager pass validates the calls
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    reps = max(1, reps_total // len(calls))
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(reps):
+            for c in calls:
+                c()
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(rounds):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (rounds * reps * len(calls))
+
+
+def attn_roofline(flops, nbytes, us, peaks):
+    """Bound (tensor above the ridge, HBM below) and the fraction of it reached."""
+    ridge = peaks["bf16"] * 1e12 / (peaks["hbm"] * 1e9)
+    tf = flops / (us * 1e-6) / 1e12
+    gbs = nbytes / (us * 1e-6) / 1e9
+    if flops / nbytes >= ridge:
+        return {"bound": "tensor", "tflops": round(tf, 1), "gbs": round(gbs, 1), "frac": round(tf / peaks["bf16"], 4)}
+    return {"bound": "hbm", "tflops": round(tf, 1), "gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm"], 4)}
+
+
+def time_attention(d3d, torch, dev, stream, cfg, l2, peaks, seed=7000, segs=None):
+    """Device time of d3d_packed_draft_attn on one workload shape.  Input sets
+    (seeded normal bf16 tensors drawn on the device, the layout's segment
+    table) rotate until they exceed 2.2x L2.  Returns time, throughput and
+    roofline fraction."""
+    R, Hq, Hkv, d = cfg["R"], cfg["Hq"], cfg["Hkv"], cfg["d"]
+    if segs is None:
+        segs = W.layout_segments(cfg["layout"], cfg["B"], cfg.get("C", 12), cfg.get("F", 2), cfg.get("T", 2048),
+                                 cfg.get("anchors", 128))
+    segs = np.asarray(segs, np.int32).reshape(-1, 5)
+    n_q = int(segs[:, 1].sum())
+    Ls = W.prefix_lengths(R, cfg["L"], seed)
+    cu_prefix = np.concatenate([[0], np.cumsum(Ls)]).astype(np.int32)
+    NT, LT = R * n_q, int(cu_prefix[-1])
+    ix = {"segs": torch.from_numpy(np.tile(segs, (R, 1))).to(dev), "cu_prefix": torch.from_numpy(cu_prefix).to(dev),
+          "cu_q": torch.from_numpy((np.arange(R + 1) * n_q).astype(np.int32)).to(dev),
+          "cu_seg": torch.from_numpy((np.arange(R + 1) * len(segs)).astype(np.int32)).to(dev)}
+    gen = torch.Generator(device=dev)
+    sets, tot = [], 0
+    for k in range(16):
+        gen.manual_seed(seed + k)
+        t = {n: torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16)
+             for n, shape in (("q", (NT, Hq, d)), ("kp", (max(LT, 1), Hkv, d)), ("vp", (max(LT, 1), Hkv, d)),
+                              ("kn", (NT, Hkv, d)), ("vn", (NT, Hkv, d)))}
+        t["out"] = torch.empty_like(t["q"])
+        sets.append(t)
+        tot += sum(x.numel() * x.element_size() for x in t.values())
+        if tot > 2.2 * l2 and k >= 1:
+            break
+    max_q, max_prefix = n_q, int(Ls.max()) if R else 0
+    ws = d3d.new_workspace(d3d.d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix), dev)
+    scale = 1.0 / math.sqrt(d)
+
+    def call(t):
+        return lambda: d3d.d3d_packed_draft_attn(t["q"], t["kp"], t["vp"], t["kn"], t["vn"], ix["segs"],
+                                                 ix["cu_prefix"], ix["cu_q"], ix["cu_seg"], max_q, max_prefix,
+                                                 scale, t["out"], ws)
+    ms = _graph_time(torch, stream, [call(t) for t in sets])
+    if d3d.d3d_workspace_status(ws) != 0:
+        raise RuntimeError("attention device status %d" % d3d.d3d_workspace_status(ws))
+    vis = 0
+    for q0, ln, mode, par, plen in segs.tolist():
+        vis += (ln * ln if mode == W.SEG_BIDIR else ln * (ln + 1) // 2) + ln * plen
+    flops = 4.0 * d * Hq * R * (n_q * float(np.mean(Ls)) + vis)
+    nbytes = 2.0 * (2 * LT * Hkv * d + 2 * NT * Hq * d + 2 * NT * Hkv * d)
+    res = {"attn_us": round(ms * 1e3, 3), "query_tokens": NT, "prefix": cfg["L"], "flops": flops, "bytes": nbytes,
+           "ctas": d3d.d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix)}
+    res.update(attn_roofline(flops, nbytes, ms * 1e3, peaks))
+    return res
+
+
+def time_verify(d3d, torch, dev, stream, cfg, l2, peaks, seed=8000):
+    """Device time of d3d_spec_verify (whole device, temperature 1) on one
+    workload's verification shape, over rotating logit sets drawn on the
+    device (target ~ N(0, 3^2), draft = target + N(0, 0.5^2), bf16)."""
+    R, B, V = cfg["R"], cfg["B"], cfg["V"]
+    gen = torch.Generator(device=dev)
+    sets, tot = [], 0
+    for k in range(16):
+        gen.manual_seed(seed + k)
+        x = torch.randn((R, B, V), generator=gen, device=dev) * 3.0
+        z = x[:, : B - 1] + torch.randn((R, B - 1, V), generator=gen, device=dev) * 0.5
+        t = {"target": x.to(torch.bfloat16), "draft": z.to(torch.bfloat16),
+             "y": torch.randint(0, V, (R, B - 1), generator=gen, device=dev, dtype=torch.int32),
+             "ua": torch.rand((R, B - 1), generator=gen, device=dev), "us": torch.rand((R,), generator=gen, device=dev),
+             "acc": torch.empty(R, dtype=torch.int32, device=dev),
+             "tok": torch.empty((R, B), dtype=torch.int32, device=dev),
+             "n": torch.empty(R, dtype=torch.int32, device=dev)}
+        del x, z
+        sets.append(t)
+        tot += t["target"].numel() * 2 + t["draft"].numel() * 2
+        if tot > 2.2 * l2 and k >= 1:
+            break
+    ws = d3d.new_workspace(d3d.d3d_spec_verify_workspace_size(R, B, V), dev)
+
+    def call(t):
+        return lambda: d3d.d3d_spec_verify(t["target"], t["draft"], t["y"], t["ua"], t["us"], 1.0, t["acc"],
+                                           t["tok"], t["n"], ws)
+    ms = _graph_time(torch, stream, [call(t) for t in sets])
+    nbytes = 2.0 * R * ((2 * B - 1) * V + 2 * V)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"verify_us": round(ms * 1e3, 3), "positions": R * B, "bytes": nbytes, "gbs": round(gbs, 1),
+            "frac": round(gbs / peaks["hbm"], 4), "bound": "hbm"}
+
+
+def other_workloads(d3d, torch, dev, stream, l2, peaks) -> dict:
+    """long_block and serve32b (attention and verification), and the C/F
+    budget sweep of the async pass at a 32768-token prefix (attention), with
+    the measured KV-read-bound to tensor-bound crossover."""
+    out = {}
+    for name in ("long_block", "serve32b"):
+        cfg = dict(W.CONFIGS[name])
+        a = time_attention(d3d, torch, dev, stream, cfg, l2, peaks)
+        v = time_verify(d3d, torch, dev, stream, cfg, l2, peaks)
+        out[name] = {"attn": a, "verify": v, "attn_query_tokens_per_s": round(a["query_tokens"] / (a["attn_us"] * 1e-6), 1),
+                     "verified_positions_per_s": round(v["positions"] / (v["verify_us"] * 1e-6), 1)}
+    cfg = dict(W.CONFIGS["sweep"])
+    points = []
+    for C, F in ((1, 1), (2, 1), (3, 1), (4, 1), (4, 2), (8, 1), (4, 3), (8, 2), (12, 1), (4, 5), (16, 1),
+                 (12, 2), (8, 3), (16, 2), (12, 3), (8, 5), (16, 3), (12, 5), (16, 5)):
+        segs = W.async_segments(cfg["B"], C, F)
+        r = time_attention(d3d, torch, dev, stream, cfg, l2, peaks, segs=segs)
+        points.append({"C": C, "F": F, "N": int(segs[:, 1].sum()), "attn_us": r["attn_us"], "bound": r["bound"],
+                       "tflops": r["tflops"], "gbs": r["gbs"], "frac": r["frac"], "ctas": r["ctas"],
+                       "tensor_frac": round(r["tflops"] / peaks["bf16"], 4),
+                       "hbm_frac": round(r["gbs"] / peaks["hbm"], 4)})
+    points.sort(key=lambda p: p["N"])
+    # measured crossover: the packed length at which the attention's tensor
+    # utilisation overtakes its HBM utilisation (linear interpolation)
+    cross = None
+    for p0, p1 in zip(points, points[1:]):
+        d0 = p0["tensor_frac"] - p0["hbm_frac"]
+        d1 = p1["tensor_frac"] - p1["hbm_frac"]
+        if d0 < 0 <= d1:
+            cross = round(p0["N"] + (p1["N"] - p0["N"]) * (-d0) / (d1 - d0), 1)
+            break
+    ridge = peaks["bf16"] * 1e12 / (peaks["hbm"] * 1e9)
+    G = cfg["Hq"] // cfg["Hkv"]
+    out["sweep"] = {"prefix": cfg["L"], "points": points, "crossover_N_measured": cross,
+                    "crossover_N_analytic": round(ridge / G, 1),
+                    "crossover_rule": "N at which tensor utilisation (of the bf16 peak) overtakes HBM utilisation "
+                                      "(of the copy bandwidth); analytic: arithmetic intensity ~ G*N flop/B "
+                                      "reaches the ridge peak_bf16/peak_hbm"}
+    return out
 
 
 def run_e2e(torch, d3d, sets, n_sets, step, dev, stream, args, R, B, dist):
@@ -675,14 +802,30 @@ def run_e2e(torch, d3d, sets, n_sets, step, dev, stream, args, R, B, dist):
 # ----------------------------------------------------------------------------
 # CPU oracle baseline / reference arm.
 # ----------------------------------------------------------------------------
-class OracleSample:
-    """The oracle timed on a bounded sample of one round of the workload.
+def host_cpu() -> dict:
+    """Core count (usable by this process) and CPU model of the host."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    return {"cores": cores, "cpu_model": model or "unknown"}
 
-    Inputs are generated once.  A sample is the attention of `tokens` packed
-    query tokens x `heads` query heads (fp64, every visible key), the
-    verification of the round over the first `vocab` vocabulary entries,
-    and the full branch match; each part's time is scaled by the fraction of
-    the round it covered, giving an estimate of one whole round."""
+
+class OracleRound:
+    """One whole round of the workload through the oracle (every packed token
+    and query head, the full vocabulary, the branch match), on one thread or
+    on all cores.  Inputs are generated once."""
 
     def __init__(self, wl_name: str, seed: int = 0):
         import oracle
@@ -691,79 +834,95 @@ class OracleSample:
         self.wl = workload(wl_name)
         self.cfg = self.wl["cfg"]
         self.attn = W.attn_inputs(**self.cfg, seed=seed)
-        self.seed = seed
-        self._verify = {}
+        self.v = W.verify_inputs(**self.cfg, seed=seed)
+        self.hb = W.branch_heads(self.v["y"], self.cfg["B"], self.cfg.get("C", 1), self.cfg.get("F", 1),
+                                 self.cfg["V"], seed=seed)
 
-    def verify_inputs(self, vocab: int):
-        if vocab not in self._verify:
-            v = W.verify_inputs(**dict(self.cfg, V=vocab), seed=self.seed)
-            hb = W.branch_heads(v["y"], self.cfg["B"], self.cfg.get("C", 1), self.cfg.get("F", 1), vocab,
-                                seed=self.seed)
-            self._verify[vocab] = (v, hb)
-        return self._verify[vocab]
-
-    def run(self, tokens: int, heads: int, vocab: int):
-        NT = self.attn["q"].shape[0]
-        v, hb = self.verify_inputs(vocab)
+    def run(self, parallel: bool) -> float:
+        o = self.oracle
         t0 = time.perf_counter()
-        self.oracle.packed_attn(self.attn, heads=(0, heads), tokens=(0, tokens))
-        t1 = time.perf_counter()
-        r = self.oracle.spec_verify(v)
-        t2 = time.perf_counter()
-        self.oracle.branch_match(dict(verified=r["out_tokens"], verified_len=r["num_tokens"], heads=hb["heads"],
-                                      head_len=hb["head_len"]))
-        t3 = time.perf_counter()
-        sa = (NT / tokens) * (self.cfg["Hq"] / heads)
-        sv = self.cfg["V"] / vocab
-        est = (t1 - t0) * sa + (t2 - t1) * sv + (t3 - t2)
-        desc = ("plain C oracle, fp64, 1 thread: attention of %d of %d packed tokens x %d of %d query heads "
-                "(scaled x%.1f), verification over %d of %d vocabulary entries (scaled x%.1f), full match"
-                % (tokens, NT, heads, self.cfg["Hq"], sa, vocab, self.cfg["V"], sv))
-        return est, t3 - t0, desc
+        if parallel:
+            o.packed_attn_par(self.attn)
+            r = o.spec_verify_par(self.v)
+        else:
+            o.packed_attn(self.attn)
+            r = o.spec_verify(self.v)
+        o.branch_match(dict(verified=r["out_tokens"], verified_len=r["num_tokens"], heads=self.hb["heads"],
+                            head_len=self.hb["head_len"]))
+        return time.perf_counter() - t0
 
 
 def cpu_baseline(wl_name: str) -> dict:
-    """The oracle on one whole round (all tokens and heads, the full vocabulary)."""
-    s = OracleSample(wl_name)
-    est, actual, desc = s.run(s.attn["q"].shape[0], s.cfg["Hq"], s.cfg["V"])
-    return {"value": round(s.wl["n_q"] * s.wl["R"] / est, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": desc, "est_s_per_step": round(est, 3), "sample_s": round(actual, 3)}
+    """The oracle on one whole round: one thread (threads_1) and all cores
+    (threads_all: the same oracle functions on disjoint (request, head) and
+    request slices from an OpenMP loop).  No sampling, no scaling."""
+    import oracle
+
+    s = OracleRound(wl_name)
+    n_q = s.wl["n_q"] * s.wl["R"]
+    hc = host_cpu()
+    t1 = s.run(parallel=False)
+    res = {"unit": UNIT, "kind": "oracle", "cores": hc["cores"], "cpu_model": hc["cpu_model"],
+           "sample": "one whole round of %s (all %d packed tokens x %d query heads, verification over V=%d, "
+                     "match); plain C oracle, fp64" % (wl_name, n_q, s.cfg["Hq"], s.cfg["V"]),
+           "threads_1": {"value": round(n_q / t1, 3), "s_per_round": round(t1, 3), "threads": 1}}
+    value = n_q / t1
+    try:
+        th = oracle.par_threads(hc["cores"])
+        s.run(parallel=True)  # first call builds and warms the parallel library
+        ta = min(s.run(parallel=True) for _ in range(3))
+        res["threads_all"] = {"value": round(n_q / ta, 3), "s_per_round": round(ta, 3), "threads": th}
+        value = n_q / ta
+    except RuntimeError as e:
+        res["threads_all"] = {"unavailable": str(e)}
+    res["value"] = round(value, 3)  # the faster of the two
+    return res
 
 
 def run_reference(args, rank: int, world: int):
-    """The reference arm: the oracle on this host, one bounded sample per step."""
+    """The reference arm: the oracle on this host's cores, one whole round per
+    step (all packed tokens and heads, the full vocabulary, the match)."""
     if rank != 0:
         return
+    import oracle
+
     K, Wm = args.steps, args.warmup
-    budget = min(10.0, 150.0 / max(1, K + Wm))  # seconds per step: the run ends within minutes
-    s = OracleSample(args.workload)
-    NT, Hq, V = s.attn["q"].shape[0], s.cfg["Hq"], s.cfg["V"]
-    _, t_cal, _ = s.run(1, 1, 1024)  # calibration: one (token, head) row, 1024 vocabulary entries
-    rows = int(max(1, min(NT * Hq, budget / max(t_cal, 1e-6))))
-    heads = max(1, min(Hq, rows // NT))
-    tokens = NT if heads > 1 else max(1, min(NT, rows))
-    vocab = int(max(1024, min(V, V * (tokens * heads) / (NT * Hq))))
+    s = OracleRound(args.workload)
+    hc = host_cpu()
+    threads = 1
+    try:
+        threads = oracle.par_threads(hc["cores"])
+        parallel = True
+        s.run(parallel=True)
+    except RuntimeError:
+        parallel = False
     for _ in range(Wm):
-        s.run(tokens, heads, vocab)
-    ests, t0, desc = [], time.perf_counter(), ""
-    for _ in range(K):
-        e, _, desc = s.run(tokens, heads, vocab)
-        ests.append(e)
+        s.run(parallel)
+    t0 = time.perf_counter()
+    per = [s.run(parallel) for _ in range(K)]
     wall = time.perf_counter() - t0
-    ms = 1e3 * float(np.mean(ests))
-    value = s.wl["n_q"] * s.wl["R"] / (ms * 1e-3)
+    ms = 1e3 * wall / K
+    n_q = s.wl["n_q"] * s.wl["R"]
+    value = n_q / (ms * 1e-3)
+    desc = ("plain C oracle, fp64, %d thread(s) on %s: one whole round per step (%d packed tokens x %d query heads, "
+            "verification over V=%d, match)" % (threads, hc["cpu_model"], n_q, s.cfg["Hq"], s.cfg["V"]))
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy)",
-        "config": {"workload": args.workload},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "config": {"workload": workload_label(args.workload)},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "cpu_model": hc["cpu_model"],
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "wall_s": round(wall, 2)}), flush=True)
+        "wall_s": round(wall, 2), "s_per_round_min": round(min(per), 3)}), flush=True)
 
 
 def main():
     args = parse_args()
+    if args.steps is None:
+        args.steps = 5 if args.impl == "reference" else 20000
+    if args.warmup is None:
+        args.warmup = 3 if args.impl == "reference" else 200
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

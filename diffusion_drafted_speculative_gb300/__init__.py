@@ -56,8 +56,8 @@ EXPORTED = {
                                    _F, _P, _P, _Z, _I, _P]),
     "d3d_spec_verify_workspace_size": (_Z, [_I, _I, _I]),
     "d3d_packed_draft_attn_ctas": (_I, [_I, _I, _I, _I, _I, _I]),
-    "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P,
-                             _P, _Z, _I, _I, _P]),
+    "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I,
+                             _P, _P, _Z, _I, _I, _P]),
     "d3d_branch_match": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "d3d_debug_inject_fault": (None, [_I]),
     "d3d_spec_verify_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P]),
@@ -214,7 +214,7 @@ def d3d_spec_verify_workspace_size(R, B, V) -> int:
 
 
 def _verify_args(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature, accept_len, out_tokens,
-                 num_tokens, ws, alpha, p_draft, q_draft, heads, head_len, branch):
+                 num_tokens, ws, alpha, p_draft, q_draft, heads, head_len, branch, awl_weight=None):
     """Checked argument tuple of d3d_spec_verify (without sm_limit and stream).
 
     temperature 0 is greedy verification: draft_logits, u_accept and u_sample
@@ -244,7 +244,7 @@ def _verify_args(target_logits, draft_logits, draft_tokens, u_accept, u_sample, 
         _need(t, n, torch.int32, len(shp))
         if tuple(t.shape) != shp:
             raise ValueError("%s must be %s" % (n, shp))
-    for t, n in ((alpha, "alpha"), (p_draft, "p_draft"), (q_draft, "q_draft")):
+    for t, n in ((alpha, "alpha"), (p_draft, "p_draft"), (q_draft, "q_draft"), (awl_weight, "awl_weight")):
         if t is not None:
             _need(t, n, torch.float32, 2)
             if tuple(t.shape) != (R, B - 1):
@@ -259,20 +259,22 @@ def _verify_args(target_logits, draft_logits, draft_tokens, u_accept, u_sample, 
         M = heads.shape[1]
         if tuple(heads.shape) != (R, M, B) or tuple(head_len.shape) != (R, M) or tuple(branch.shape) != (R,):
             raise ValueError("heads must be [R, M, B], head_len [R, M], branch [R]")
-    _need(ws, "ws", torch.uint8, 1)
+    if ws is not None:
+        _need(ws, "ws", torch.uint8, 1)
     return (_ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), R, B, V,
             float(temperature), _ptr(accept_len), _ptr(out_tokens), _ptr(num_tokens), _ptr(alpha), _ptr(p_draft),
-            _ptr(q_draft), _ptr(heads) if branch is not None else None,
-            _ptr(head_len) if branch is not None else None, M, _ptr(branch), _ptr(ws), ws.numel())
+            _ptr(q_draft), _ptr(awl_weight), _ptr(heads) if branch is not None else None,
+            _ptr(head_len) if branch is not None else None, M, _ptr(branch), _ptr(ws),
+            ws.numel() if ws is not None else 0)
 
 
 def d3d_spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature: float,
                     accept_len, out_tokens, num_tokens, ws, alpha=None, p_draft=None, q_draft=None,
                     heads=None, head_len=None, branch=None, sm_limit: int = 0, after_independent: bool = False,
-                    stream=None) -> None:
+                    stream=None, awl_weight=None) -> None:
     """Speculative-sampling verification; logits f32 or bf16 [R,B,V] / [R,B-1,V]."""
     args = _verify_args(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature, accept_len,
-                        out_tokens, num_tokens, ws, alpha, p_draft, q_draft, heads, head_len, branch)
+                        out_tokens, num_tokens, ws, alpha, p_draft, q_draft, heads, head_len, branch, awl_weight)
     rc = lib.d3d_spec_verify(*args, int(sm_limit), D3D_VERIFY_AFTER_INDEPENDENT if after_independent else 0,
                              _stream(stream))
     _check("d3d_spec_verify", rc)
@@ -363,8 +365,8 @@ class VerifyCall(ctypes.Structure):
     _fields_ = [("target_logits", _P), ("draft_logits", _P), ("logits_dtype", _I), ("draft_tokens", _P),
                 ("u_accept", _P), ("u_sample", _P), ("R", _I), ("B", _I), ("V", _I), ("temperature", _F),
                 ("accept_len", _P), ("out_tokens", _P), ("num_tokens", _P), ("alpha", _P), ("p_draft", _P),
-                ("q_draft", _P), ("heads", _P), ("head_len", _P), ("M", _I), ("branch", _P), ("ws", _P),
-                ("ws_bytes", _Z)]
+                ("q_draft", _P), ("awl_weight", _P), ("heads", _P), ("head_len", _P), ("M", _I), ("branch", _P),
+                ("ws", _P), ("ws_bytes", _Z)]
 
 
 def d3d_async_round(attn: dict, verify: dict, stream=None) -> None:
@@ -372,7 +374,7 @@ def d3d_async_round(attn: dict, verify: dict, stream=None) -> None:
 
     ``attn`` holds d3d_packed_draft_attn's keyword arguments (q, k_prefix, ...,
     out, ws) and ``verify`` d3d_spec_verify's (target_logits, ..., ws, and the
-    optional alpha/p_draft/q_draft/heads/head_len/branch)."""
+    optional alpha/p_draft/q_draft/awl_weight/heads/head_len/branch)."""
     a = _attn_args(**attn)
     vkw = dict(alpha=None, p_draft=None, q_draft=None, heads=None, head_len=None, branch=None)
     vkw.update(verify)
@@ -385,25 +387,12 @@ def d3d_async_round(attn: dict, verify: dict, stream=None) -> None:
 def d3d_spec_verify_noalloc(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature: float,
                             accept_len, out_tokens, num_tokens, alpha=None, p_draft=None, q_draft=None,
                             stream=None) -> None:
-    """d3d_spec_verify without a workspace: scratch lives inside the library (see include/d3d.h)."""
-    if target_logits.dtype == torch.bfloat16:
-        dt = D3D_DTYPE_BF16
-    elif target_logits.dtype == torch.float32:
-        dt = D3D_DTYPE_F32
-    else:
-        raise TypeError("logits must be float32 or bfloat16")
-    R, B, V = target_logits.shape
-    greedy = float(temperature) == 0.0  # draft logits and uniforms are not read
-    for t, n in ((target_logits, "target_logits"), (draft_logits, "draft_logits"), (draft_tokens, "draft_tokens"),
-                 (u_accept, "u_accept"), (u_sample, "u_sample"), (accept_len, "accept_len"),
-                 (out_tokens, "out_tokens"), (num_tokens, "num_tokens")):
-        if t is None and greedy and n in ("draft_logits", "u_accept", "u_sample"):
-            continue
-        _need(t, n, t.dtype)
-    rc = lib.d3d_spec_verify_noalloc(
-        _ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), R, B, V,
-        float(temperature), _ptr(accept_len), _ptr(out_tokens), _ptr(num_tokens), _ptr(alpha), _ptr(p_draft),
-        _ptr(q_draft), _stream(stream))
+    """d3d_spec_verify without a workspace: scratch lives inside the library (see include/d3d.h).
+    Every tensor is checked for dtype, device, contiguity and shape exactly as
+    d3d_spec_verify checks it."""
+    args = _verify_args(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature, accept_len,
+                        out_tokens, num_tokens, None, alpha, p_draft, q_draft, None, None, None)
+    rc = lib.d3d_spec_verify_noalloc(*args[:16], _stream(stream))
     _check("d3d_spec_verify_noalloc", rc)
 
 

@@ -877,13 +877,7 @@ int num_sms()
 
 template <int D> cudaError_t set_smem_attr()
 {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)Layout<D>::alloc);
-    });
-    return err;
+    return set_max_dyn_smem<attn_tc_kernel<D>>((int)Layout<D>::alloc);
 }
 
 // CTAs of the attention kernel resident at once when launched in clusters of
@@ -989,8 +983,6 @@ bool make_map(CUtensorMap *m, const void *ptr, int d, int heads, long long rows,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int g_fault_mode = 0;
-
 template <int D>
 int launch_attn(const CUtensorMap (&maps)[5], const AttnParams &prm, long long units, int flags, cudaStream_t stream)
 {
@@ -1082,7 +1074,7 @@ int attn_prepare(const void *q, const void *k_prefix, const void *v_prefix, cons
     prm.total_prefix = total_prefix;
     prm.total_segs = total_segs;
     prm.scale_log2 = scale * 1.4426950408889634f;
-    prm.fault = g_fault_mode;
+    prm.fault = fault_mode();
     return D3D_OK;
 }
 
@@ -1106,12 +1098,7 @@ int launch_round(const CUtensorMap (&maps)[5], const AttnParams &prm, int n_attn
     if (dyn > Layout<D>::alloc)
         return D3D_ERR_UNSUPPORTED;
     dyn = Layout<D>::alloc;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(round_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)Layout<D>::alloc);
-    });
+    const cudaError_t attr_err = set_max_dyn_smem<round_kernel<D, T>>((int)Layout<D>::alloc);
     int dev = 0, nsm = 0, per_sm = 0;
     if (attr_err != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -1166,7 +1153,7 @@ int d3d_packed_draft_attn_ctas(int R, int Hq, int Hkv, int d, int max_q, int max
     return pl.units > 0x7fffffffLL ? D3D_ERR_UNSUPPORTED : (int)pl.units;
 }
 
-void d3d_debug_inject_fault(int mode) { d3d::g_fault_mode = mode; }
+void d3d_debug_inject_fault(int mode) { d3d::fault_mode() = mode; }
 
 int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_prefix, const void *k_packed,
                           const void *v_packed, const d3d_segment_t *segs, const int32_t *cu_prefix,
@@ -1197,8 +1184,8 @@ int d3d_async_round(const d3d_attn_call_t *a, const d3d_verify_call_t *v, cudaSt
     d3d::VArgs va;
     const int rv = d3d::verify_prepare(v->target_logits, v->draft_logits, v->logits_dtype, v->draft_tokens,
                                        v->u_accept, v->u_sample, v->R, v->B, v->V, v->temperature, v->accept_len,
-                                       v->out_tokens, v->num_tokens, v->alpha, v->p_draft, v->q_draft, v->heads,
-                                       v->head_len, v->M, v->branch, va);
+                                       v->out_tokens, v->num_tokens, v->alpha, v->p_draft, v->q_draft,
+                                       v->awl_weight, v->heads, v->head_len, v->M, v->branch, va);
     if (rv < 0)
         return rv;
     if (v->temperature == 0.f)  // greedy verification has its own launch

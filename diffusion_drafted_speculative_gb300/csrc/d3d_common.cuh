@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "d3d.h"
 
 namespace d3d {
@@ -47,6 +49,39 @@ __device__ inline void load_logits8(const uint16_t *p, float (&x)[8])
         x[2 * e] = __uint_as_float(wv[e] << 16);
         x[2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
     }
+}
+
+// Failure-injection mode of the host hook d3d_debug_inject_fault (one value
+// for the whole library; 0 = normal operation).  Read at launch time and
+// passed to the kernels as an argument.
+inline int &fault_mode()
+{
+    static int mode = 0;
+    return mode;
+}
+
+// Raise kernel K's dynamic shared-memory limit to `bytes` on the current
+// device, once per device (a function attribute belongs to the device it
+// was set on); thread-safe.  Returns the result of the (first) call.
+template <auto K> inline cudaError_t set_max_dyn_smem(int bytes)
+{
+    constexpr int kDev = 64;
+    static std::mutex mu;
+    static bool done[kDev];
+    static cudaError_t err[kDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return cudaErrorInvalidDevice;
+    }
+    if (dev < 0 || dev >= kDev)
+        return cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+        err[dev] = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        done[dev] = true;
+    }
+    return err[dev];
 }
 
 // Convert a CUDA error at enqueue time to a status code.

@@ -161,6 +161,8 @@ __global__ void __launch_bounds__(kGThreads) greedy_kernel(const VArgs a)
                     a.alpha[(long long)r * (B - 1) + j] = ok ? 1.f : 0.f;
                 if (a.p)
                     a.p[(long long)r * (B - 1) + j] = ok ? 1.f : 0.f;
+                if (a.awl)  // the product of the acceptance indicators before j
+                    a.awl[(long long)r * (B - 1) + j] = prefix ? 1.f : 0.f;
                 prefix = prefix && ok;
                 acc += prefix ? 1 : 0;
             }

@@ -20,12 +20,7 @@ int launch_verify_nt(const VArgs &a_in, int sm_limit, int flags, cudaStream_t st
         return D3D_ERR_UNSUPPORTED;
     size_t dyn = verify_dyn_smem(a.B, L.nch);
     if (ring_fits<T, NT>(a)) {  // phase A through a shared-memory ring (one CTA per SM)
-        static std::once_flag once;
-        static cudaError_t attr_err = cudaSuccess;
-        std::call_once(once, [] {
-            attr_err = cudaFuncSetAttribute(verify_kernel<T, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)Ring<NT>::bytes(kRingSlots));
-        });
+        const cudaError_t attr_err = set_max_dyn_smem<verify_kernel<T, NT>>((int)Ring<NT>::bytes(kRingSlots));
         if (attr_err == cudaSuccess) {
             a.ring = kRingSlots;
             if (dyn < Ring<NT>::bytes(kRingSlots))
@@ -91,16 +86,16 @@ size_t d3d_spec_verify_workspace_size(int R, int B, int V)
 int d3d_spec_verify(const void *target_logits, const void *draft_logits, int logits_dtype,
                     const int32_t *draft_tokens, const float *u_accept, const float *u_sample, int R, int B,
                     int V, float temperature, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
-                    float *alpha, float *p_draft, float *q_draft, const int32_t *heads, const int32_t *head_len,
-                    int M, int32_t *branch, void *ws, size_t ws_bytes, int sm_limit, int flags,
-                    cudaStream_t stream)
+                    float *alpha, float *p_draft, float *q_draft, float *awl_weight, const int32_t *heads,
+                    const int32_t *head_len, int M, int32_t *branch, void *ws, size_t ws_bytes, int sm_limit,
+                    int flags, cudaStream_t stream)
 {
     if (sm_limit < 0 || (flags & ~D3D_VERIFY_AFTER_INDEPENDENT) != 0)
         return D3D_ERR_INVALID_ARG;
     d3d::VArgs a;
     const int rc = d3d::verify_prepare(target_logits, draft_logits, logits_dtype, draft_tokens, u_accept, u_sample,
                                        R, B, V, temperature, accept_len, out_tokens, num_tokens, alpha, p_draft,
-                                       q_draft, heads, head_len, M, branch, a);
+                                       q_draft, awl_weight, heads, head_len, M, branch, a);
     if (rc != D3D_OK)
         return rc == 1 ? D3D_OK : rc;
     if (!d3d::ws_ok(ws, ws_bytes, d3d::verify_layout(R, B, V, d3d::kVChunkMin).total))
@@ -178,7 +173,7 @@ extern "C" int d3d_spec_verify_noalloc(const void *target_logits, const void *dr
     d3d::VArgs a;
     const int rc = d3d::verify_prepare(target_logits, draft_logits, logits_dtype, draft_tokens, u_accept, u_sample,
                                        R, B, V, temperature, accept_len, out_tokens, num_tokens, alpha, p_draft,
-                                       q_draft, nullptr, nullptr, 0, nullptr, a);
+                                       q_draft, nullptr, nullptr, nullptr, 0, nullptr, a);
     if (rc != D3D_OK)
         return rc == 1 ? D3D_OK : rc;
     const d3d::VerifyLayout L = d3d::verify_layout(R, B, V, d3d::kVChunkMin);

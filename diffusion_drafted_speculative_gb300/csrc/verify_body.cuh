@@ -369,6 +369,41 @@ __device__ inline float4 block_group_scan(float4 g, float *red)
     return r;
 }
 
+// fp32 pairs (hi + lo, |lo| <= ulp(hi)) for the sample's magnitude-S sums:
+// error-free transformations (Knuth's TwoSum, Dekker's product with an FMA),
+// about 2^-44 relative instead of fp32's 2^-24.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// (h, l) += (h2, l2)
+__device__ __forceinline__ void df_add(float &h, float &l, float h2, float l2)
+{
+    float s, e;
+    two_sum(h, h2, s, e);
+    e = __fadd_rn(e, __fadd_rn(l, l2));
+    h = __fadd_rn(s, e);
+    l = __fsub_rn(e, __fsub_rn(h, s));
+}
+
+// (th, tl) = u * (h, l)
+__device__ __forceinline__ void df_mul(float u, float h, float l, float &th, float &tl)
+{
+    const float p = __fmul_rn(u, h);
+    const float e = __fadd_rn(__fmaf_rn(u, h, -p), __fmul_rn(u, l));
+    th = __fadd_rn(p, e);
+    tl = __fsub_rn(e, __fsub_rn(th, p));
+}
+
+// (ah, al) > (bh, bl)
+__device__ __forceinline__ bool df_gt(float ah, float al, float bh, float bl)
+{
+    return __fadd_rn(__fsub_rn(ah, bh), __fsub_rn(al, bl)) > 0.f;
+}
+
 __device__ __forceinline__ int load_acquire(const int *p)
 {
     int v;
@@ -436,10 +471,11 @@ __device__ void select_request(int r, int B, int V, int nch, const Rec *__restri
                                const int32_t *s_y, const float *s_u, bool write_outputs,
                                int32_t *__restrict__ accept_len, int32_t *__restrict__ out_tokens,
                                int32_t *__restrict__ num_tokens, float *__restrict__ alpha_out,
-                               float *__restrict__ p_out, float *__restrict__ q_out, int32_t *status, Sel &sel,
+                               float *__restrict__ p_out, float *__restrict__ q_out, float *__restrict__ awl_out,
+                               int32_t *status, Sel &sel,
                                Rec *s_rec)
 {
-    __shared__ float s_mp[kMaxB], s_zp[kMaxB], s_mq[kMaxB], s_zq[kMaxB];
+    __shared__ float s_mp[kMaxB], s_zp[kMaxB], s_mq[kMaxB], s_zq[kMaxB], s_al[kMaxB];
     __shared__ int s_a;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const Rec *pr = rec + (size_t)r * B * nch;
@@ -500,6 +536,7 @@ __device__ void select_request(int r, int B, int V, int nch, const Rec *__restri
                 }
                 if (!(s_u[jj] < al))
                     atomicMin(&s_a, jj);
+                s_al[jj] = al;
                 if (write_outputs) {
                     const size_t o = (size_t)r * (B - 1) + jj;
                     if (alpha_out)
@@ -525,6 +562,16 @@ __device__ void select_request(int r, int B, int V, int nch, const Rec *__restri
         if (threadIdx.x == 0) {
             accept_len[r] = a;
             num_tokens[r] = a + 1;
+            if (awl_out) {
+                // [DScout] "Background: AWL and the acceptance rule": the weight of
+                // position k is the product of the acceptance probabilities of the
+                // drafts before it (the probability that verification reaches k)
+                float w = 1.f;
+                for (int jj = 0; jj < B - 1; ++jj) {
+                    awl_out[(size_t)r * (B - 1) + jj] = w;
+                    w *= s_al[jj];
+                }
+            }
         }
         for (int jj = threadIdx.x; jj < B; jj += NT)
             if (jj != a)
@@ -575,10 +622,12 @@ __device__ inline void kept_masses(int kind, const float (&eP)[kVPer], float (&e
 
 // Phase D of request r in the chunk [c0, c1) that holds the crossing: the
 // ordered scan of the slot masses w (slot order is group-major vocabulary
-// order); writes the sampled token.
+// order) for the first position whose in-chunk cumulative mass passes
+// `target` (the sample's target minus the masses of the earlier chunks);
+// writes the sampled token.
 template <int NT>
-__device__ void scan_owner(const float (&w)[kVPer], int c0, float prefix, float target, bool takelast,
-                           int32_t *out_tok, float *red)
+__device__ void scan_owner(const float (&w)[kVPer], int c0, float target, bool takelast, int32_t *out_tok,
+                           float *red)
 {
     __shared__ int s_cand, s_lastpos;
     if (threadIdx.x == 0) {
@@ -602,7 +651,7 @@ __device__ void scan_owner(const float (&w)[kVPer], int c0, float prefix, float 
     if (!takelast) {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-            if (prefix + bs[q] + gs[q] > target) {
+            if (bs[q] + gs[q] > target) {
                 atomicMin(&s_cand, q * NT + (int)threadIdx.x);
                 break;
             }
@@ -613,7 +662,7 @@ __device__ void scan_owner(const float (&w)[kVPer], int c0, float prefix, float 
     if (!takelast && cand != 0x7fffffff && (cand % NT) == (int)threadIdx.x) {
         const int q = cand / NT;
         int tok = -1, last = -1;
-        float cum = prefix + bs[q];
+        float cum = bs[q];
 #pragma unroll
         for (int i = 0; i < kVPer; ++i) {
             if ((i >> 3) == q && tok < 0) {
@@ -670,11 +719,12 @@ struct VArgs {
     int R, B, V, M;
     float c;  // log2(e) / temperature
     int32_t *accept_len, *out_tokens, *num_tokens;
-    float *alpha, *p, *q;
+    float *alpha, *p, *q, *awl;
     const int32_t *heads, *head_len;
     int32_t *branch;
     unsigned char *ws;
     int ring;  // > 0: phase A streams items through this many shared-memory slots (bf16 rows, bulk copies)
+    int fault;  // 2: CTA 0 never issues the copies of its first ring item (failure-detection hook)
 };
 
 // Phase-A ring of the SM-limited launch: per slot, the target row's and the
@@ -705,6 +755,7 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
     float *__restrict__ alpha_out = a.alpha;
     float *__restrict__ p_out = a.p;
     float *__restrict__ q_out = a.q;
+    float *__restrict__ awl_out = a.awl;
     const int32_t *__restrict__ heads = a.heads;
     const int32_t *__restrict__ head_len = a.head_len;
     int32_t *__restrict__ branch = a.branch;
@@ -757,6 +808,8 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
     uint8_t *ring = reinterpret_cast<uint8_t *>(s_dyn);  // reused for the staged records after phase A
     const uint32_t ring_s = sm100::smem_u32(ring), ring_bar = ring_s + (uint32_t)nring * Ring<NT>::kSlotBytes;
     auto ring_issue = [&](long long it, int slot) {
+        if (a.fault == 2 && vb == 0 && it == 0)
+            return;  // injected fault: this slot's copies never arrive
         int v0, v1, j;
         const T *rp = target_row(it, v0, v1, j);
         const uint32_t row_bytes = (uint32_t)(v1 - v0) * 2u;
@@ -804,6 +857,14 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
         if (j < B - 1)
             rawQ.issue(draft_row(vb), v0, v1);
     }
+    // a ring slot whose copies did not land in time stops the CTA's phase A:
+    // no further copies are issued, the copies in flight are waited out, and
+    // the CTA leaves (the request's other CTAs then give up waiting for its
+    // records; the status word holds the timeout)
+    __shared__ volatile int s_ring_abort;
+    if (threadIdx.x == 0)
+        s_ring_abort = 0;
+    __syncthreads();
     int k_item = 0;  // this CTA's item count
     for (long long item = vb; item < nA; item += vgrid, ++k_item) {
         int v0, v1, j;
@@ -817,8 +878,9 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
             if (!sm100::mbar_try_wait(bar, parity)) {  // bounded wait for the slot's copies
                 const uint64_t t0 = sm100::global_ns();
                 while (!sm100::mbar_try_wait_sleep(bar, parity))
-                    if (sm100::global_ns() - t0 > kBarrierTimeoutNs) {
+                    if (s_ring_abort || sm100::global_ns() - t0 > kBarrierTimeoutNs) {
                         record_status(reinterpret_cast<int32_t *>(ws), D3D_ERR_DEVICE_TIMEOUT);
+                        s_ring_abort = 1;
                         break;
                     }
             }
@@ -870,6 +932,24 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
         const bool has = yv >= v0 && yv < v1;
         const float xyP = (threadIdx.x == 0 && has) ? s_xy[0] : 0.f, xyQ = (threadIdx.x == 0 && has) ? s_xy[1] : 0.f;
         __syncthreads();  // red and s_xy are reused by the next item; the slot has been read
+        if (nring > 0 && s_ring_abort) {
+            // this item and the next nring - 1 have copies issued that may still
+            // be in flight: wait for each (bounded) before the CTA leaves
+            if (threadIdx.x == 0) {
+                for (int jj = k_item; jj < k_item + nring; ++jj) {
+                    if ((long long)vb + (long long)jj * vgrid >= nA)
+                        break;
+                    const uint32_t b2 = ring_bar + 8u * (uint32_t)(jj % nring1);
+                    const uint32_t par = (uint32_t)(jj / nring1) & 1u;
+                    const uint64_t t0 = sm100::global_ns();
+                    while (!sm100::mbar_try_wait_sleep(b2, par))
+                        if (sm100::global_ns() - t0 > kBarrierTimeoutNs)
+                            break;
+                }
+            }
+            __syncthreads();
+            return;
+        }
         // the record and its signal after the barrier: the release's wait
         // overlaps the next item's loads and exponentials in the other warps
         if (threadIdx.x == 0) {
@@ -886,46 +966,93 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
     }
 
     __shared__ int s_kind_used, s_owner, s_takelast;
-    __shared__ float s_prefix, s_target;
-    // Phase D decision for request r from its chunk sums (thread 0 computes,
-    // everyone reads the shared results after the call).
+    __shared__ float s_rem;
+    // Phase D decision for request r from its chunk sums, by warp 0 (everyone
+    // reads the shared results after the call): the total S, the target u*S,
+    // the chunk holding the crossing and the target's offset into that chunk.
+    // Sums and the product are kept as fp32 pairs (df_add / df_mul), so that
+    // magnitude-S quantities carry no 2^-24 S rounding; the owner chunk then
+    // scans against an offset on its own scale.
     auto decide = [&](int r, const Sel &sel) {
         float2 *s_sums = reinterpret_cast<float2 *>(s_dyn);  // the records are no longer needed
         for (int cc = threadIdx.x; cc < nch; cc += NT)
             s_sums[cc] = __ldcg(part2 + (size_t)r * nch + cc);
         __syncthreads();
-        if (threadIdx.x == 0) {
-            float S_res = 0.f, S_p = 0.f;
-            for (int cc = 0; cc < nch; ++cc) {
-                S_res += s_sums[cc].x;
-                S_p += s_sums[cc].y;
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            const int per = (nch + 31) >> 5;  // consecutive chunks per lane
+            const int c_lo = min(nch, lane * per), c_hi = min(nch, c_lo + per);
+            float rh = 0.f, rl = 0.f, ph = 0.f, pl = 0.f;  // this lane's residual and P masses
+            for (int cc = c_lo; cc < c_hi; ++cc) {
+                df_add(rh, rl, s_sums[cc].x, 0.f);
+                df_add(ph, pl, s_sums[cc].y, 0.f);
+            }
+            // inclusive scan over the lanes (chunk order) of both masses
+            float irh = rh, irl = rl, iph = ph, ipl = pl;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float a = __shfl_up_sync(kFull, irh, o), b = __shfl_up_sync(kFull, irl, o);
+                const float c2 = __shfl_up_sync(kFull, iph, o), d = __shfl_up_sync(kFull, ipl, o);
+                if (lane >= o) {
+                    df_add(irh, irl, a, b);
+                    df_add(iph, ipl, c2, d);
+                }
             }
             // residual unless it has no mass left in fp32 (then P at that row)
-            const int kind = (sel.mode == 0 && S_res > 0.f) ? 0 : 1;
-            const float S = kind == 0 ? S_res : S_p;
-            const float tgt = s_us * S;
-            float run = 0.f;
-            int owner = -1;
-            for (int cc = 0; cc < nch; ++cc) {
-                const float sc = kind == 0 ? s_sums[cc].x : s_sums[cc].y;
-                if (run + sc > tgt) {
-                    owner = cc;
-                    break;
+            const float Srh = __shfl_sync(kFull, irh, 31);
+            const int kind = (sel.mode == 0 && Srh > 0.f) ? 0 : 1;
+            const float inh = kind == 0 ? irh : iph, inl = kind == 0 ? irl : ipl;
+            const float Sh = __shfl_sync(kFull, inh, 31), Sl = __shfl_sync(kFull, inl, 31);
+            float th, tl;
+            df_mul(s_us, Sh, Sl, th, tl);
+            float exh = __shfl_up_sync(kFull, inh, 1), exl = __shfl_up_sync(kFull, inl, 1);
+            if (lane == 0)
+                exh = exl = 0.f;
+            auto mass = [&](int cc) { return kind == 0 ? s_sums[cc].x : s_sums[cc].y; };
+            // the first lane whose inclusive sum passes the target holds the crossing
+            const unsigned bal = __ballot_sync(kFull, c_lo < c_hi && df_gt(inh, inl, th, tl));
+            int owner = -1, takelast = 0;
+            float rem = 0.f;
+            if (bal) {
+                const int L = __ffs(bal) - 1;
+                if (lane == L) {
+                    float runh = exh, runl = exl;
+                    int last_mass = -1;
+                    for (int cc = c_lo; cc < c_hi; ++cc) {
+                        float nh = runh, nl = runl;
+                        df_add(nh, nl, mass(cc), 0.f);
+                        if (mass(cc) > 0.f)
+                            last_mass = cc;
+                        if (df_gt(nh, nl, th, tl)) {
+                            owner = cc;
+                            break;
+                        }
+                        runh = nh, runl = nl;
+                    }
+                    if (owner < 0) {  // the two summation orders disagree in the last bits
+                        owner = last_mass;
+                        takelast = 1;
+                    }
+                    rem = (th - runh) + (tl - runl);
                 }
-                run += sc;
-            }
-            int takelast = 0;
-            if (owner < 0) {  // rounding left u*S at or past the end: last chunk with mass
+                owner = __shfl_sync(kFull, owner, L);
+                takelast = __shfl_sync(kFull, takelast, L);
+                rem = __shfl_sync(kFull, rem, L);
+            } else {  // rounding left u*S at or past the end: last chunk with mass
                 takelast = 1;
-                for (int cc = nch - 1; cc >= 0 && owner < 0; --cc)
-                    if ((kind == 0 ? s_sums[cc].x : s_sums[cc].y) > 0.f)
-                        owner = cc;
+                int lastc = -1;
+                for (int cc = c_lo; cc < c_hi; ++cc)
+                    if (mass(cc) > 0.f)
+                        lastc = cc;
+                const unsigned b2 = __ballot_sync(kFull, lastc >= 0);
+                owner = b2 ? __shfl_sync(kFull, lastc, 31 - __clz(b2)) : -1;
             }
-            s_kind_used = kind;
-            s_owner = owner;
-            s_takelast = takelast;
-            s_prefix = run;
-            s_target = tgt;
+            if (lane == 0) {
+                s_kind_used = kind;
+                s_owner = owner;
+                s_takelast = takelast;
+                s_rem = rem;
+            }
         }
         __syncthreads();
     };
@@ -966,7 +1093,7 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
         if (!wait_count(bar + kBarInts * r, B * nch, status))
             return;
         select_request<NT>(r, B, V, nch, rec, s_y, s_u, j == 0 && chunk == 0, accept_len, out_tokens, num_tokens,
-                       alpha_out, p_out, q_out, status, sel, s_rec);
+                       alpha_out, p_out, q_out, awl_out, status, sel, s_rec);
         if (j != sel.row) {
             passed_a(r, B * nch);  // counted once the CTA's work is done: off the critical path
             return;
@@ -987,7 +1114,7 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
                 float a1, a2;
                 kept_masses(1, eP, eQ, mtP, mtQ, sel, a1, a2);
             }
-            scan_owner<NT>(eQ, c0, s_prefix, s_target, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
+            scan_owner<NT>(eQ, c0, s_rem, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
             fused_match(r, sel.a);
         } else if (s_owner < 0 && chunk == 0) {
             // no mass anywhere: cannot happen for a finite softmax row
@@ -1015,7 +1142,7 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
             return;
         passed_a(r, nch);
         select_request<NT>(r, B, V, nch, rec, s_y, s_u, chunk == 0, accept_len, out_tokens, num_tokens, alpha_out,
-                       p_out, q_out, status, sel, s_rec);
+                       p_out, q_out, awl_out, status, sel, s_rec);
         const T *prow = target + ((size_t)r * B + sel.row) * V;
         const T *qrow = draft + ((size_t)r * (B - 1) + (sel.mode == 0 ? sel.row : 0)) * V;
         const int c0 = chunk * C::kChunk, c1 = min(V, c0 + C::kChunk);
@@ -1038,7 +1165,7 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
         // every phase-C item of r waited for r's phase A, so the records are complete
         if (!cd_same)
             select_request<NT>(r, B, V, nch, rec, s_y, s_u, false, accept_len, out_tokens, num_tokens, alpha_out,
-                               p_out, q_out, status, sel, s_rec);
+                               p_out, q_out, awl_out, status, sel, s_rec);
         decide(r, sel);
         if (s_owner == chunk) {
             const int c0 = chunk * C::kChunk, c1 = min(V, c0 + C::kChunk);
@@ -1048,7 +1175,7 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
                 float a1, a2;
                 chunk_masses<T, NT>(prow, qrow, s_kind_used, c0, c1, c, sel, w, a1, a2);
             }
-            scan_owner<NT>(w, c0, s_prefix, s_target, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
+            scan_owner<NT>(w, c0, s_rem, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
             fused_match(r, sel.a);
         } else if (s_owner < 0 && chunk == 0) {
             if (threadIdx.x == 0) {
@@ -1090,7 +1217,7 @@ inline size_t verify_dyn_smem(int B, int nch)
 inline int verify_prepare(const void *target_logits, const void *draft_logits, int logits_dtype,
                           const int32_t *draft_tokens, const float *u_accept, const float *u_sample, int R, int B,
                           int V, float temperature, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
-                          float *alpha, float *p_draft, float *q_draft, const int32_t *heads,
+                          float *alpha, float *p_draft, float *q_draft, float *awl_weight, const int32_t *heads,
                           const int32_t *head_len, int M, int32_t *branch, VArgs &a)
 {
     // temperature 0: greedy verification (no draft logits, no uniforms)
@@ -1119,10 +1246,11 @@ inline int verify_prepare(const void *target_logits, const void *draft_logits, i
     a.R = R, a.B = B, a.V = V, a.M = branch ? M : 0;
     a.c = greedy ? 0.f : (float)(1.4426950408889634 / (double)temperature);  // log2(e) / T
     a.accept_len = accept_len, a.out_tokens = out_tokens, a.num_tokens = num_tokens;
-    a.alpha = alpha, a.p = p_draft, a.q = q_draft;
+    a.alpha = alpha, a.p = p_draft, a.q = q_draft, a.awl = awl_weight;
     a.heads = heads, a.head_len = head_len, a.branch = branch;
     a.ws = nullptr;
     a.ring = 0;
+    a.fault = fault_mode();
     return D3D_OK;
 }
 

@@ -174,10 +174,14 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
  * Failure-detection hook (no counterpart on the pages).  mode 1 makes every
  * later d3d_packed_draft_attn launch skip its first key-tile load, so the
  * consumer's bounded wait expires: the kernel records D3D_ERR_DEVICE_TIMEOUT
- * in the workspace status word, releases its resources and returns; the
- * outputs of such a call are undefined and the workspace must be
- * re-initialised.  mode 0 (the default) restores normal operation.  The
- * setting is process-global and not thread-safe.
+ * in the workspace status word, releases its resources and returns.  mode 2
+ * makes every later d3d_spec_verify launch that streams bf16 rows through its
+ * shared-memory ring (an sm_limit launch) skip the copies of CTA 0's first
+ * item: that CTA's bounded wait expires, it records D3D_ERR_DEVICE_TIMEOUT,
+ * waits out its other copies and leaves, and the request's other CTAs give
+ * up their bounded waits.  The outputs of such a call are undefined and the
+ * workspace must be re-initialised.  mode 0 (the default) restores normal
+ * operation.  The setting is process-global and not thread-safe.
  */
 void d3d_debug_inject_fault(int mode);
 
@@ -289,6 +293,12 @@ int d3d_build_branches(const void *draft_logits, int logits_dtype, const int32_t
  *   accept_len [R], out_tokens [R, B], num_tokens [R]  int32 outputs
  *   alpha, p_draft, q_draft [R, B-1] float32 outputs, each may be NULL
  *               (p_draft = P_j(y_j), q_draft = Q_j(y_j))
+ *   awl_weight  [R, B-1] float32 output or NULL: the acceptance-weighted loss
+ *               weight of [DScout] "Background: AWL and the acceptance rule",
+ *               w_k = prod_{j<k} alpha_j (w_0 = 1), the probability that
+ *               verification reaches position k given the drafted tokens; a
+ *               running fp32 product in position order (greedy: the product
+ *               of the acceptance indicators)
  *   heads [R, M, B], head_len [R, M], branch [R]  int32; optional fused
  *               branch match: when branch is not NULL, the kernel writes
  *               branch[r] exactly as d3d_branch_match would for the verified
@@ -321,9 +331,9 @@ size_t d3d_spec_verify_workspace_size(int R, int B, int V);
 int d3d_spec_verify(const void *target_logits, const void *draft_logits, int logits_dtype,
                     const int32_t *draft_tokens, const float *u_accept, const float *u_sample, int R, int B,
                     int V, float temperature, int32_t *accept_len, int32_t *out_tokens, int32_t *num_tokens,
-                    float *alpha, float *p_draft, float *q_draft, const int32_t *heads, const int32_t *head_len,
-                    int M, int32_t *branch, void *ws, size_t ws_bytes, int sm_limit, int flags,
-                    cudaStream_t stream);
+                    float *alpha, float *p_draft, float *q_draft, float *awl_weight, const int32_t *heads,
+                    const int32_t *head_len, int M, int32_t *branch, void *ws, size_t ws_bytes, int sm_limit,
+                    int flags, cudaStream_t stream);
 
 /*
  * Verification that allocates nothing (the pages have no counterpart: this
@@ -339,15 +349,22 @@ int d3d_spec_verify(const void *target_logits, const void *draft_logits, int log
  * loads the library holds until the process exits.
  *
  *   - Problems whose d3d_spec_verify_workspace_size(R, B, V) exceeds 2 MiB
- *     are rejected with D3D_ERR_UNSUPPORTED (for B = 16 and V = 151936 that
- *     is R above about 400 requests); use d3d_spec_verify for those.
+ *     are rejected with D3D_ERR_UNSUPPORTED (for B = 16 and V = 151936 the
+ *     largest accepted batch is R = 211 requests); use d3d_spec_verify for
+ *     larger ones.
  *   - The first call on each device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *     that device current and keeps it for the life of the process; make that
+ *     first call before any stream capture.  cudaDeviceReset (or any teardown
+ *     of the device's primary context) invalidates the kept address: do not
+ *     call this entry point on a device after resetting it.
  *   - Every call shares the one array per device: calls that overlap on the
  *     GPU (different streams without ordering between them) race and give
  *     wrong results.  Each call zeroes the parts that must start at zero.
- *   - A draft token outside [0, V) is handled as in d3d_spec_verify but is
- *     not reported back; call d3d_spec_verify when that status is needed.
+ *   - The status word of this entry point lives inside the fixed array and
+ *     is not reported back: a draft token outside [0, V) is handled as in
+ *     d3d_spec_verify, and a device-side wait that expires (see
+ *     D3D_ERR_DEVICE_TIMEOUT) leaves the outputs undefined, yet the call
+ *     still returns D3D_OK.  Call d3d_spec_verify when that status is needed.
  * Returns D3D_OK, D3D_ERR_INVALID_ARG, D3D_ERR_UNSUPPORTED or D3D_ERR_CUDA.
  */
 int d3d_spec_verify_noalloc(const void *target_logits, const void *draft_logits, int logits_dtype,
@@ -391,7 +408,7 @@ typedef struct {
     int R, B, V;
     float temperature;
     int32_t *accept_len, *out_tokens, *num_tokens;
-    float *alpha, *p_draft, *q_draft;
+    float *alpha, *p_draft, *q_draft, *awl_weight;
     const int32_t *heads, *head_len;
     int M;
     int32_t *branch;

@@ -41,6 +41,81 @@ def build(force: bool = False) -> str:
     return _OUT
 
 
+_SRC_PAR = os.path.join(_HERE, "d3d_oracle_par.c")
+_OUT_PAR = os.path.join(_HERE, "_build", "libd3d_oracle_par.so")
+_lib_par = None
+
+
+def build_par(force: bool = False):
+    """Compile the all-cores driver (d3d_oracle_par.c, OpenMP) together with
+    the unchanged oracle into its own library; None if the compiler has no
+    OpenMP."""
+    os.makedirs(os.path.dirname(_OUT_PAR), exist_ok=True)
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_PAR))
+    if force or not os.path.exists(_OUT_PAR) or os.path.getmtime(_OUT_PAR) < newest:
+        tmp = _OUT_PAR + ".%d.tmp" % os.getpid()
+        try:
+            subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
+                                   "-ffp-contract=off", "-fopenmp", _SRC, _SRC_PAR, "-o", tmp, "-lm"])
+        except (OSError, subprocess.CalledProcessError):
+            return None
+        os.replace(tmp, _OUT_PAR)
+    return _OUT_PAR
+
+
+def _load_par():
+    global _lib_par
+    with _lock:
+        if _lib_par is None:
+            path = build_par()
+            if path is None:
+                raise RuntimeError("the all-cores oracle needs gcc with OpenMP")
+            _lib_par = ctypes.CDLL(path)
+            for name in ("oracle_packed_attn_par", "oracle_spec_verify_par", "oracle_par_threads"):
+                getattr(_lib_par, name).restype = ctypes.c_int
+    return _lib_par
+
+
+def par_threads(n: int = 0) -> int:
+    """Set (n > 0) and return the thread count of the all-cores oracle."""
+    return _load_par().oracle_par_threads(ctypes.c_int(n))
+
+
+def packed_attn_par(inp: dict) -> np.ndarray:
+    """packed_attn on all cores: one oracle call per (request, query head)."""
+    q, kp, vp, kn, vn = (_c(inp[k], np.uint16) for k in ("q", "kp", "vp", "kn", "vn"))
+    segs, cu_p, cu_q, cu_s = (_c(inp[k], np.int32) for k in ("segs", "cu_prefix", "cu_q", "cu_seg"))
+    NT, Hq, d = q.shape
+    out = np.zeros((NT, Hq, d), np.float64)
+    rc = _load_par().oracle_packed_attn_par(
+        _p(q), _p(kp), _p(vp), _p(kn), _p(vn), _p(segs), _p(cu_p), _p(cu_q), _p(cu_s), ctypes.c_int(inp["R"]),
+        ctypes.c_int(Hq), ctypes.c_int(inp["Hkv"]), ctypes.c_int(d), ctypes.c_double(inp["scale"]), _p(out))
+    if rc != OK:
+        raise ValueError("oracle_packed_attn_par: invalid arguments (rc=%d)" % rc)
+    return out
+
+
+def spec_verify_par(inp: dict) -> dict:
+    """spec_verify on all cores: one oracle call per request; the same outputs."""
+    R, B, V = inp["R"], inp["B"], inp["V"]
+    dt = np.uint16 if inp["dtype"] == 1 else np.float32
+    tgt, dr = _c(inp["target"], dt), _c(inp["draft"], dt)
+    y = _c(inp["y"], np.int32)
+    ua, us = _c(inp["u_accept"], np.float32), _c(inp["u_sample"], np.float32)
+    out = dict(accept_len=np.zeros(R, np.int32), out_tokens=np.zeros((R, B), np.int32),
+               num_tokens=np.zeros(R, np.int32), alpha=np.zeros((R, B - 1)),
+               p=np.zeros((R, B - 1)), q=np.zeros((R, B - 1)), margin_accept=np.zeros(R),
+               margin_sample=np.zeros(R), used_fallback=np.zeros(R, np.int32))
+    rc = _load_par().oracle_spec_verify_par(
+        _p(tgt), _p(dr), ctypes.c_int(inp["dtype"]), _p(y), _p(ua), _p(us), ctypes.c_int(R), ctypes.c_int(B),
+        ctypes.c_int(V), ctypes.c_double(inp.get("temperature", 1.0)), _p(out["accept_len"]),
+        _p(out["out_tokens"]), _p(out["num_tokens"]), _p(out["alpha"]), _p(out["p"]), _p(out["q"]),
+        _p(out["margin_accept"]), _p(out["margin_sample"]), _p(out["used_fallback"]))
+    if rc != OK:
+        raise ValueError("oracle_spec_verify_par: invalid arguments (rc=%d)" % rc)
+    return out
+
+
 def _load():
     global _lib
     with _lock:
@@ -48,7 +123,7 @@ def _load():
             _lib = ctypes.CDLL(build())
             for name in ("oracle_packed_attn", "oracle_packed_attn_sel", "oracle_dense_attn",
                          "oracle_dense_mask", "oracle_spec_verify", "oracle_greedy_verify", "oracle_build_branches",
-                         "oracle_accept_probs",
+                         "oracle_accept_probs", "oracle_awl_weights",
                          "oracle_branch_match",
                          "oracle_check_segments"):
                 getattr(_lib, name).restype = ctypes.c_int
@@ -178,6 +253,20 @@ def spec_verify(inp: dict) -> dict:
     if rc != OK:
         raise ValueError("oracle_spec_verify: invalid arguments (rc=%d)" % rc)
     return out
+
+
+def awl_weights(alpha) -> np.ndarray:
+    """Acceptance-weighted loss weights w [R, B-1] from alpha [R, B-1]
+    (DScout, "Background: AWL and the acceptance rule"): w_k = prod_{j<k}
+    alpha_j, w_0 = 1 -- the probability that verification reaches k."""
+    a = _c(alpha, np.float64)
+    if a.ndim != 2:
+        raise ValueError("alpha must be [R, B-1]")
+    w = np.zeros_like(a)
+    rc = _load().oracle_awl_weights(_p(a), ctypes.c_int(a.shape[0]), ctypes.c_int(a.shape[1]), _p(w))
+    if rc != OK:
+        raise ValueError("oracle_awl_weights: invalid arguments (rc=%d)" % rc)
+    return w
 
 
 def accept_probs(inp: dict) -> dict:

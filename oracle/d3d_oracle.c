@@ -512,6 +512,28 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype, const i
 }
 
 /*
+ * Acceptance-weighted loss weights (DScout, "Background: AWL and the
+ * acceptance rule"; "Method steps", fourth step): the weight of draft
+ * position k (0-based) is the product of the acceptance probabilities of
+ * the drafts before it, w_k = prod_{j<k} alpha_j, so w_0 = 1; it is the
+ * probability that verification reaches position k.  alpha [R, Bm1] (as
+ * oracle_spec_verify writes it) -> w [R, Bm1].
+ */
+int oracle_awl_weights(const double *alpha, int R, int Bm1, double *w)
+{
+    if (R < 0 || Bm1 < 1)
+        return OR_BAD_ARG;
+    for (int r = 0; r < R; ++r) {
+        double prod = 1.0;
+        for (int k = 0; k < Bm1; ++k) {
+            w[(size_t)r * Bm1 + k] = prod;
+            prod *= alpha[(size_t)r * Bm1 + k];
+        }
+    }
+    return OR_OK;
+}
+
+/*
  * Per-position acceptance probabilities and the round's expected acceptance
  * length (DScout, "Background: acceptance length tau" and "Background: AWL
  * and the acceptance rule"): with P_j = softmax(target row j / T) and

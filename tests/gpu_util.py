@@ -6,7 +6,27 @@ import torch
 ATT_ATOL = 2e-2   # bf16 inputs, fp32 accumulate, bf16 output: |d| <= 2e-2 + 2e-2 |ref|
 ATT_RTOL = 2e-2
 PROB_RTOL = 1e-5  # p_j, q_j, alpha_j
-NEAR_TIE = 1e-5   # |u - alpha| and relative inverse-CDF margin below this are excluded
+# Draws excluded from the bit-exact comparison of accepted lengths and tokens:
+# |u_j - alpha_j| < 1e-5 at a test that decided the accepted length (the rule
+# the comparison contract states), and sample draws whose u*S lies within
+# SAMPLE_BAND * S of a step of the oracle's CDF.  The second band is set from
+# measurement: across seeded runs at every workload shape the largest margin
+# at which the fp32 device sample differed from the fp64 oracle was below a
+# tenth of it.
+NEAR_TIE = 1e-5
+SAMPLE_BAND = 1e-6
+
+
+def oracle_verify(v):
+    """The oracle's verification of a batch: one oracle call per request on
+    all host cores when the OpenMP build is available (identical results),
+    else the one-thread oracle."""
+    import oracle
+
+    try:
+        return oracle.spec_verify_par(v)
+    except RuntimeError:
+        return oracle.spec_verify(v)
 
 
 def bf16(a, dev="cuda"):
@@ -52,7 +72,8 @@ def run_verify(d3d, v, ws=None, want_probs=True, sm_limit=0, heads=None):
     out = dict(accept_len=torch.full((R,), -7, dtype=torch.int32, device=dev),
                out_tokens=torch.full((R, B), -7, dtype=torch.int32, device=dev),
                num_tokens=torch.full((R,), -7, dtype=torch.int32, device=dev))
-    probs = {k: torch.full((R, B - 1), float("nan"), device=dev) for k in ("alpha", "p", "q")} if want_probs else {}
+    probs = {k: torch.full((R, B - 1), float("nan"), device=dev) for k in ("alpha", "p", "q", "awl")} \
+        if want_probs else {}
     if ws is None:
         ws = d3d.new_workspace(d3d.d3d_spec_verify_workspace_size(R, B, v["V"]), dev)
     fused = {}
@@ -61,24 +82,36 @@ def run_verify(d3d, v, ws=None, want_probs=True, sm_limit=0, heads=None):
         fused = dict(heads=i32(heads["heads"]), head_len=i32(heads["head_len"]), branch=out["branch"])
     d3d.d3d_spec_verify(tgt, dr, i32(v["y"]), f32(v["u_accept"]), f32(v["u_sample"]), v.get("temperature", 1.0),
                         out["accept_len"], out["out_tokens"], out["num_tokens"], ws, alpha=probs.get("alpha"),
-                        p_draft=probs.get("p"), q_draft=probs.get("q"), sm_limit=sm_limit, **fused)
+                        p_draft=probs.get("p"), q_draft=probs.get("q"), awl_weight=probs.get("awl"),
+                        sm_limit=sm_limit, **fused)
     torch.cuda.synchronize()
     res = {k: t.cpu().numpy() for k, t in {**out, **probs}.items()}
     return res, ws
 
 
-def compare_verify(got, ref, min_kept=0.9):
-    """Bit-exact a / tokens / counts outside near ties; probabilities to 1e-5 relative.
-    Returns (kept, excluded)."""
+def compare_verify(got, ref, min_kept=0.9, what=""):
+    """Bit-exact a / tokens / counts outside the near-tie bands; probabilities
+    to 1e-5 relative.  Prints and returns (compared, excluded at alpha,
+    excluded at the sample); fails when fewer than min_kept of the draws are
+    compared."""
     for k in ("alpha", "p", "q"):
         if k in got:
             np.testing.assert_allclose(got[k], ref[k], rtol=PROB_RTOL, atol=1e-30, err_msg=k)
-    keep = (ref["margin_accept"] >= NEAR_TIE) & (ref["margin_sample"] >= NEAR_TIE)
+    if "awl" in got:  # the acceptance-weighted loss weights, prod_{j<k} alpha_j
+        import oracle
+
+        np.testing.assert_allclose(got["awl"], oracle.awl_weights(ref["alpha"]), rtol=PROB_RTOL, atol=1e-30,
+                                   err_msg="awl")
+    tie_a = ref["margin_accept"] < NEAR_TIE
+    tie_s = ~tie_a & (ref["margin_sample"] < SAMPLE_BAND)
+    keep = ~tie_a & ~tie_s
     for k in ("accept_len", "num_tokens", "out_tokens"):
         np.testing.assert_array_equal(got[k][keep], ref[k][keep], err_msg=k)
     n = len(keep)
+    print("verify %s: %d of %d draws compared, %d excluded at |u - alpha| < %g, %d at the sample band %g"
+          % (what, int(keep.sum()), n, int(tie_a.sum()), NEAR_TIE, int(tie_s.sum()), SAMPLE_BAND))
     assert keep.sum() >= min_kept * n, "too many near ties: %d of %d" % (n - keep.sum(), n)
-    return int(keep.sum()), int(n - keep.sum())
+    return int(keep.sum()), int(tie_a.sum()), int(tie_s.sum())
 
 
 def run_match(d3d, m):

@@ -9,7 +9,8 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_util import assert_attn_close, compare_verify, run_attn, run_match, run_verify
+from gpu_util import (NEAR_TIE, SAMPLE_BAND, assert_attn_close, compare_verify, oracle_verify, run_attn,
+                      run_match, run_verify)
 
 pytestmark = pytest.mark.gpu
 
@@ -197,31 +198,30 @@ def test_attn_many_splits_and_bad_descriptor(d3d):
 def test_verify_tiny_config_batched(d3d, seed):
     v = W.verify_inputs(**dict(W.CONFIGS["tiny"], R=256), seed=seed)
     got, ws = run_verify(d3d, v)
-    compare_verify(got, oracle.spec_verify(v))
+    compare_verify(got, oracle_verify(v), what="tiny")
     assert d3d.d3d_workspace_status(ws) == 0
 
 
-@pytest.mark.parametrize("seed", range(5))
+@pytest.mark.parametrize("seed", range(3))
 def test_verify_async8b_full_size(d3d, seed):
-    v = W.verify_inputs(**W.CONFIGS["async8b"], seed=seed)
+    # the benchmark's verification shape (B = 16, V = 151936) over 64 requests,
+    # so that the bit-exact comparison covers many draws
+    v = W.verify_inputs(**dict(W.CONFIGS["async8b"], R=64), seed=seed)
     got, _ = run_verify(d3d, v)
-    compare_verify(got, oracle.spec_verify(v), min_kept=0.0)
+    compare_verify(got, oracle_verify(v), min_kept=0.9, what="async8b x64")
 
 
 def test_verify_serve32b_batch(d3d):
-    v = W.verify_inputs(**W.CONFIGS["serve32b"], seed=1)
+    v = W.verify_inputs(**dict(W.CONFIGS["serve32b"], R=64), seed=1)
     got, _ = run_verify(d3d, v)
-    # at V = 151936 a quarter of the draws land in tail tokens whose CDF step is
-    # narrower than the 1e-5 near-tie band; those are excluded and counted
-    kept, excl = compare_verify(got, oracle.spec_verify(v), min_kept=0.5)
-    print("serve32b verify: %d compared, %d near ties excluded" % (kept, excl))
+    compare_verify(got, oracle_verify(v), min_kept=0.9, what="serve32b x64")
 
 
 @pytest.mark.parametrize("sigma", [0.25, 0.5, 1.0])
 def test_verify_long_block_sigma_sweep(d3d, sigma):
-    v = W.verify_inputs(**dict(W.CONFIGS["long_block"], R=4, sigma=sigma), seed=2)
+    v = W.verify_inputs(**dict(W.CONFIGS["long_block"], R=32, sigma=sigma), seed=2)
     got, _ = run_verify(d3d, v)
-    compare_verify(got, oracle.spec_verify(v), min_kept=0.5)
+    compare_verify(got, oracle_verify(v), min_kept=0.9, what="long block sigma %g" % sigma)
 
 
 @pytest.mark.parametrize("V", [1, 7, 1000, 8191, 8193, 12345, 16384])
@@ -229,21 +229,21 @@ def test_verify_long_block_sigma_sweep(d3d, sigma):
 def test_verify_ragged_vocab(d3d, V, dt):
     v = W.verify_inputs(R=64, B=5, V=V, logits=dt, seed=V)
     got, _ = run_verify(d3d, v)
-    compare_verify(got, oracle.spec_verify(v), min_kept=0.8)
+    compare_verify(got, oracle_verify(v), min_kept=0.9, what="V=%d" % V)
 
 
 @pytest.mark.parametrize("B,T", [(2, 1.0), (3, 0.7), (16, 2.0), (64, 1.0)])
 def test_verify_block_sizes_and_temperature(d3d, B, T):
     v = W.verify_inputs(R=128, B=B, V=2048, logits=W.DT_BF16, seed=B, temperature=T)
     got, _ = run_verify(d3d, v)
-    compare_verify(got, oracle.spec_verify(v), min_kept=0.8)
+    compare_verify(got, oracle_verify(v), min_kept=0.9, what="B=%d T=%g" % (B, T))
 
 
 def test_verify_high_acceptance_and_bonus_path(d3d):
     # draft == target rows: every draft accepted, the bonus comes from P_B
     v = W.verify_inputs(R=256, B=8, V=3000, logits=W.DT_F32, sigma=0.0, seed=9)
     got, _ = run_verify(d3d, v)
-    ref = oracle.spec_verify(v)
+    ref = oracle_verify(v)
     assert (ref["accept_len"] == 7).all()
     compare_verify(got, ref)
 
@@ -255,14 +255,17 @@ def test_verify_high_acceptance_and_bonus_path(d3d):
 def test_verify_one_item_per_cta(d3d, R, B, V, dt, sigma):
     # few requests: every (request, position, chunk) item has a CTA of its own,
     # and the sample reuses phase A's exponentials from registers
-    for seed in range(3):
+    kept = total = 0
+    for seed in range(8):
         v = W.verify_inputs(R=R, B=B, V=V, logits=dt, sigma=sigma, seed=seed + 31 * B)
         got, ws = run_verify(d3d, v)
-        ref = oracle.spec_verify(v)
+        ref = oracle_verify(v)
         if sigma == 0.0:
             assert (ref["accept_len"] == B - 1).all()
-        compare_verify(got, ref, min_kept=0.0 if V > 50000 else 0.5)
+        kept += compare_verify(got, ref, min_kept=0.0, what="R=%d B=%d V=%d seed %d" % (R, B, V, seed))[0]
+        total += R
         assert d3d.d3d_workspace_status(ws) == 0
+    assert kept >= 0.75 * total, "compared %d of %d draws" % (kept, total)
 
 
 @pytest.mark.parametrize("sm_limit", [1, 7, 56, 151])
@@ -271,13 +274,13 @@ def test_verify_sm_limit_same_results(d3d, sm_limit):
     # 16384-entry chunks, one CTA per SM.  Probabilities may differ from the
     # unlimited launch in the last bit (another summation order); both meet
     # the oracle under the same tolerances
-    for v in (W.verify_inputs(**W.CONFIGS["async8b"], seed=3),
+    for v in (W.verify_inputs(**dict(W.CONFIGS["async8b"], R=24), seed=3),
               W.verify_inputs(R=40, B=6, V=9000, logits=W.DT_F32, seed=4)):
-        ref = oracle.spec_verify(v)
+        ref = oracle_verify(v)
         free, ws = run_verify(d3d, v)
         lim, ws2 = run_verify(d3d, v, sm_limit=sm_limit)
-        compare_verify(free, ref, min_kept=0.0)
-        compare_verify(lim, ref, min_kept=0.0)
+        compare_verify(free, ref, min_kept=0.85, what="R=%d unlimited" % v["R"])
+        compare_verify(lim, ref, min_kept=0.85, what="R=%d sm_limit %d" % (v["R"], sm_limit))
         for k in ("alpha", "p", "q"):
             np.testing.assert_allclose(lim[k], free[k], rtol=1e-6, atol=1e-30, err_msg=k)
         assert d3d.d3d_workspace_status(ws2) == 0
@@ -306,13 +309,12 @@ def test_verify_fused_match(d3d, cfg, sm_limit):
     # the match fused into the verification equals the match of the tokens the
     # verification produced (oracle), hits planted from the oracle's tokens
     c = dict(W.CONFIGS[cfg])
-    if cfg == "tiny":
-        c["R"] = 300
+    c["R"] = {"tiny": 300, "async8b": 24, "serve32b": 32}[cfg]
     v = W.verify_inputs(**c, seed=8)
-    ref = oracle.spec_verify(v)
+    ref = oracle_verify(v)
     hb = _heads_hitting(ref, c["B"], c["V"], 24, seed=9)
     got, ws = run_verify(d3d, v, sm_limit=sm_limit, heads=hb)
-    compare_verify(got, ref, min_kept=0.0)
+    compare_verify(got, ref, min_kept=0.85, what="%s fused match" % cfg)
     want = oracle.branch_match(dict(verified=got["out_tokens"], verified_len=got["num_tokens"], **hb))
     np.testing.assert_array_equal(got["branch"], want)
     assert want[0] >= 0 and (want >= 0).mean() > 0.3  # hits are exercised
@@ -329,7 +331,7 @@ def test_round_on_one_stream_overlapping(d3d, attention_first):
     cfg = W.CONFIGS["async8b"]
     a = W.attn_inputs(**cfg, seed=21)
     v = W.verify_inputs(**cfg, seed=21)
-    ref_v = oracle.spec_verify(v)
+    ref_v = oracle_verify(v)
     ref_a = oracle.packed_attn(a, heads=(28, 32))
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     side = sms - d3d.d3d_packed_draft_attn_ctas(1, cfg["Hq"], cfg["Hkv"], cfg["d"], a["max_q"], a["max_prefix"])
@@ -364,7 +366,8 @@ def test_round_on_one_stream_overlapping(d3d, attention_first):
                 ver()
                 att()
             got_t, got_o = toks.cpu().numpy(), out.float().cpu().numpy()  # read after both, same stream
-            keep = (ref_v["margin_accept"] >= 1e-5) & (ref_v["margin_sample"] >= 1e-5)
+            keep = (ref_v["margin_accept"] >= NEAR_TIE) & (ref_v["margin_sample"] >= SAMPLE_BAND)
+            assert keep.all()  # the round's one draw (seed 21) has no near tie
             np.testing.assert_array_equal(got_t[keep], ref_v["out_tokens"][keep])
             assert_attn_close(got_o[:, 28:32], ref_a[:, 28:32], "overlapped attention")
     assert d3d.d3d_workspace_status(wsa) == 0 and d3d.d3d_workspace_status(wsv) == 0
@@ -376,7 +379,7 @@ def _round_calls(d3d, cfg, seed):
     from gpu_util import bf16, f32, i32
     a = W.attn_inputs(**cfg, seed=seed)
     v = W.verify_inputs(**cfg, seed=seed)
-    ref_v = oracle.spec_verify(v)
+    ref_v = oracle_verify(v)
     hb = _heads_hitting(ref_v, cfg["B"], cfg["V"], 24, seed=seed + 1)
     R, B = v["R"], v["B"]
     attn = dict(q=bf16(a["q"]), k_prefix=bf16(a["kp"]), v_prefix=bf16(a["vp"]), k_packed=bf16(a["kn"]),
@@ -410,7 +413,8 @@ def test_async_round_in_one_launch(d3d):
         d3d.d3d_async_round(attn, verify)
         torch.cuda.synchronize()
         got = {k: verify[k].cpu().numpy() for k in ("accept_len", "out_tokens", "num_tokens", "branch")}
-        compare_verify(got, ref_v, min_kept=0.0)
+        # one request: its draw must be compared (seed 33 has no near tie)
+        compare_verify(got, ref_v, min_kept=1.0, what="fused round")
         want = oracle.branch_match(dict(verified=got["out_tokens"], verified_len=got["num_tokens"], **hb))
         np.testing.assert_array_equal(got["branch"], want)
         assert_attn_close(attn["out"].float().cpu().numpy()[:, 0:4], ref_a[:, 0:4], "fused round attention")
@@ -460,6 +464,8 @@ def _run_greedy(d3d, v, sm_limit=0, heads=None, noalloc=False, probs=True):
                out_tokens=torch.full((R, B), -7, dtype=torch.int32, device="cuda"),
                num_tokens=torch.full((R,), -7, dtype=torch.int32, device="cuda"))
     pr = {k: torch.full((R, B - 1), float("nan"), device="cuda") for k in ("alpha", "p")} if probs else {}
+    if probs and not noalloc:
+        pr["awl"] = torch.full((R, B - 1), float("nan"), device="cuda")
     if noalloc:
         d3d.d3d_spec_verify_noalloc(tgt, None, i32(v["y"]), None, None, 0.0, out["accept_len"], out["out_tokens"],
                                     out["num_tokens"], alpha=pr.get("alpha"), p_draft=pr.get("p"))
@@ -471,8 +477,8 @@ def _run_greedy(d3d, v, sm_limit=0, heads=None, noalloc=False, probs=True):
             out["branch"] = torch.full((R,), -7, dtype=torch.int32, device="cuda")
             extra = dict(heads=i32(heads["heads"]), head_len=i32(heads["head_len"]), branch=out["branch"])
         d3d.d3d_spec_verify(tgt, None, i32(v["y"]), None, None, 0.0, out["accept_len"], out["out_tokens"],
-                            out["num_tokens"], ws, alpha=pr.get("alpha"), p_draft=pr.get("p"), sm_limit=sm_limit,
-                            **extra)
+                            out["num_tokens"], ws, alpha=pr.get("alpha"), p_draft=pr.get("p"),
+                            awl_weight=pr.get("awl"), sm_limit=sm_limit, **extra)
     torch.cuda.synchronize()
     got = {k: t.cpu().numpy() for k, t in out.items()}
     got.update({k: t.cpu().numpy() for k, t in pr.items()})
@@ -486,6 +492,8 @@ def _check_greedy(got, ref):
     if "alpha" in got:
         np.testing.assert_array_equal(got["alpha"], ref["accept"].astype(np.float32))
         np.testing.assert_array_equal(got["p"], ref["accept"].astype(np.float32))
+    if "awl" in got:  # the product of the acceptance indicators before each position
+        np.testing.assert_array_equal(got["awl"], oracle.awl_weights(ref["accept"]).astype(np.float32))
 
 
 @pytest.mark.parametrize("cfg,over", [
@@ -624,7 +632,7 @@ def test_built_branches_drive_attention_and_match(d3d):
     cfg = W.CONFIGS["async8b"]
     C, F = cfg["C"], cfg["F"]
     v = W.verify_inputs(**cfg, seed=53)
-    ref_v = oracle.spec_verify(v)
+    ref_v = oracle_verify(v)
     bg = ref_v["out_tokens"][:, -1].copy()  # any guess; on full acceptance a matching one makes a hit
     got, _ = _run_branches(d3d, v, C, F, bonus=bg)
     a = W.attn_inputs(**cfg, seed=53, segs=got["segs"])
@@ -670,7 +678,26 @@ def test_verify_workspace_reuse_and_many_requests(d3d):
     got2, _ = run_verify(d3d, v, ws=ws)
     for k in got1:
         np.testing.assert_array_equal(got1[k], got2[k])
-    compare_verify(got1, oracle.spec_verify(v))
+    compare_verify(got1, oracle_verify(v), what="R=4096")
+
+
+def test_verify_ring_wait_runs_out_reports_status_and_context_survives(d3d):
+    # failure detection without a GPU fault: with an SM limit the bf16 rows
+    # stream through a shared-memory ring; CTA 0 never issues its first
+    # item's copies, its bounded wait runs out, it records the timeout, waits
+    # out its other copies and leaves; the other CTAs give up their bounded
+    # waits.  The next call, on a re-initialised workspace, is correct
+    v = W.verify_inputs(**dict(W.CONFIGS["async8b"], R=2), seed=12)
+    d3d.d3d_debug_inject_fault(2)
+    try:
+        _, ws = run_verify(d3d, v, sm_limit=56)
+    finally:
+        d3d.d3d_debug_inject_fault(0)
+    assert d3d.d3d_workspace_status(ws, clear=True) == d3d.D3D_ERR_DEVICE_TIMEOUT
+    d3d.d3d_workspace_init(ws)
+    got, _ = run_verify(d3d, v, ws=ws, sm_limit=56)
+    compare_verify(got, oracle_verify(v), min_kept=1.0, what="after a timed-out call")
+    assert d3d.d3d_workspace_status(ws) == 0
 
 
 def test_verify_bad_draft_token_sets_status(d3d):

@@ -69,8 +69,8 @@ def test_invalid_arguments_rejected_on_host(d3d):
     fake = ctypes.c_void_p(256)  # never dereferenced: the checks fail first
     # verify: B < 2, V < 1, T <= 0, bad dtype, missing workspace
     args = lambda R, B, V, T, dt, ws, wsb, sm=0, M=0, heads=None, br=None, fl=0, q=None: (  # noqa
-        fake, fake, dt, fake, fake, fake, R, B, V, T, fake, fake, fake, None, None, q, heads, heads, M, br, ws, wsb,
-        sm, fl, None)
+        fake, fake, dt, fake, fake, fake, R, B, V, T, fake, fake, fake, None, None, q, None, heads, heads, M, br, ws,
+        wsb, sm, fl, None)
     assert L.d3d_spec_verify(*args(1, 1, 10, 1.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 1 << 20, fl=2)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 0, 1.0, 1, fake, 1 << 20)) == d3d.D3D_ERR_INVALID_ARG
@@ -118,7 +118,7 @@ def test_invalid_arguments_rejected_on_host(d3d):
     assert L.d3d_async_round(None, None, None) == d3d.D3D_ERR_INVALID_ARG
     ac = d3d.AttnCall(*([fake] * 9 + [1, 30, 8, 128, 16, 64, 16, 64, 1, 0.1, fake, fake, 1 << 30]))
     vc = d3d.VerifyCall(fake, fake, 1, fake, fake, fake, 1, 4, 10, 1.0, fake, fake, fake, None, None, None, None,
-                        None, 0, None, fake, 1 << 20)
+                        None, None, 0, None, fake, 1 << 20)
     assert L.d3d_async_round(ctypes.byref(ac), ctypes.byref(vc), None) == d3d.D3D_ERR_INVALID_ARG  # Hq % Hkv
     ac.Hq = 32
     vc.temperature = -1.0
@@ -243,3 +243,10 @@ def test_binding_rejects_cpu_tensors(d3d):
         d3d.d3d_packed_draft_attn(x, x, x, x, x, torch.zeros(1, 5, dtype=torch.int32),
                                   *(torch.zeros(2, dtype=torch.int32),) * 3, 1, 1, 0.1, x,
                                   torch.zeros(256, dtype=torch.uint8))
+
+
+def test_noalloc_limit_edge_in_workspace_sizes(d3d):
+    # the no-allocation entry point's fixed scratch (2 MiB) holds the
+    # workspace of 211 requests at B = 16, V = 151936 but not of 212
+    assert d3d.d3d_spec_verify_workspace_size(211, 16, 151936) <= 2 << 20
+    assert d3d.d3d_spec_verify_workspace_size(212, 16, 151936) > 2 << 20

@@ -59,6 +59,10 @@ MUTANTS = [
     ("num_tokens_without_the_extra_token",
      "num_tokens[r] = a + 1;\n        for (int j = 0; j < B; ++j) {\n            int32_t tok = -1;",
      "num_tokens[r] = a;\n        for (int j = 0; j < B; ++j) {\n            int32_t tok = -1;"),
+    # AWL weights
+    ("awl_includes_own_position", "            w[(size_t)r * Bm1 + k] = prod;\n            prod *= alpha[(size_t)r * Bm1 + k];",
+     "            prod *= alpha[(size_t)r * Bm1 + k];\n            w[(size_t)r * Bm1 + k] = prod;"),
+    ("awl_sums_instead_of_multiplying", "prod *= alpha[(size_t)r * Bm1 + k];", "prod += alpha[(size_t)r * Bm1 + k];"),
     # acceptance probabilities, survivals, tau
     ("accept_prob_max", "a += P[v] < Q[v] ? P[v] : Q[v];", "a += P[v] > Q[v] ? P[v] : Q[v];"),
     ("tau_without_one", "double surv = 1.0, t = 1.0;", "double surv = 1.0, t = 0.0;"),

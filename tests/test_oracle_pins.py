@@ -188,6 +188,37 @@ def test_zero_residual_falls_back_to_P_in_distribution():
     assert _chi2_p(r["out_tokens"][:, 1], P[1]) > 1e-4
 
 
+# ---------------------------------------------------------------- AWL weights
+@pytest.mark.parametrize("case", json.load(open(os.path.join(GOLD, "awl_hand.json")))["cases"],
+                         ids=lambda c: c["name"])
+def test_awl_weights_hand_worked(case):
+    r = oracle.spec_verify(dict(_case_inputs(dict(case, u_accept=[0.5] * (case["B"] - 1), u_sample=0.5))))
+    # (rtol 1e-6: the logits are float32 roundings of the logarithms written)
+    np.testing.assert_allclose(r["alpha"][0], case["alpha"], rtol=1e-6, atol=1e-12)
+    np.testing.assert_allclose(oracle.awl_weights(r["alpha"])[0], case["awl"], rtol=1e-6, atol=1e-12)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_awl_weight_is_the_probability_of_reaching_a_position(T):
+    # fixed rows and fixed drafted tokens, fresh acceptance uniforms each
+    # trial: the fraction of trials whose accepted length is at least k (the
+    # verification reached position k) estimates w_k
+    V, B, R = 24, 6, 200_000
+    x, z = _rows(V, B, seed=81, sigma=0.7)
+    Q = scipy.special.softmax(z.astype(np.float64) / T, axis=-1)
+    rng = np.random.default_rng(82)
+    y = np.array([rng.choice(V, p=Q[j]) for j in range(B - 1)], np.int32)
+    inp = _fixed_rows_inputs(x, z, T, R, seed=83)
+    inp["y"] = np.ascontiguousarray(np.broadcast_to(y, (R, B - 1)))
+    r = oracle.spec_verify(inp)
+    w = oracle.awl_weights(r["alpha"][:1])[0]
+    for k in range(B - 1):
+        emp = (r["accept_len"] >= k).mean()
+        se = max(np.sqrt(w[k] * (1 - w[k]) / R), 1e-9)
+        assert abs(emp - w[k]) <= 5 * se + 1e-12, (k, emp, w[k])
+    assert 0.05 < w[-1] < 0.95  # the case exercises partial acceptance
+
+
 # ---------------------------------------------------------------- greedy (temperature 0)
 @pytest.mark.parametrize("case", json.load(open(os.path.join(GOLD, "verify_greedy.json")))["cases"],
                          ids=lambda c: c["name"])

@@ -6,7 +6,9 @@ for cudaMalloc's device synchronisation, a C caller with no allocator) use
 d3d_spec_verify_noalloc, whose scratch is a fixed array inside the library.
 This test calls it through the C ABI twice in a row, on different inputs,
 and checks each result against d3d_spec_verify with a caller workspace on
-the same inputs, within the tolerances of the other verification tests.
+the same inputs, within the tolerances of the other verification tests, and
+the sampled tokens against the oracle under the same near-tie rule as the
+other verification tests.  The size limit is checked at its exact edge.
 The file sorts last so that a stop-at-first-failure run has already run
 every other test; it also passes on its own in a fresh process.
 """
@@ -16,8 +18,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
-from gpu_util import PROB_RTOL, bf16, f32, i32, run_verify
+from gpu_util import PROB_RTOL, bf16, compare_verify, f32, i32, oracle_verify, run_verify
 
 pytestmark = pytest.mark.gpu
 
@@ -72,11 +75,30 @@ def test_noalloc_matches_workspace_entry_point_twice(d3d):
         ref, _ = run_verify(d3d, v)
         got = _noalloc_via_abi(d3d, v)
         _same(got, ref)
+        compare_verify(got, oracle_verify(v), min_kept=0.85, what="no-allocation entry point")
+
+
+def _call_sized(d3d, R):
+    """A call of R requests at B = 16, V = 151936 on placeholder pointers:
+    sizes are checked before anything is enqueued."""
+    x = torch.zeros(1, dtype=torch.int32, device="cuda")
+    return d3d.lib.d3d_spec_verify_noalloc(x.data_ptr(), x.data_ptr(), d3d.D3D_DTYPE_BF16, x.data_ptr(), x.data_ptr(),
+                                           x.data_ptr(), R, 16, 151936, ctypes.c_float(1.0), x.data_ptr(),
+                                           x.data_ptr(), x.data_ptr(), None, None, None, None)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(d3d):
-    x = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = d3d.lib.d3d_spec_verify_noalloc(x.data_ptr(), x.data_ptr(), d3d.D3D_DTYPE_BF16, x.data_ptr(), x.data_ptr(),
-                                         x.data_ptr(), 4096, 16, 151936, ctypes.c_float(1.0), x.data_ptr(),
-                                         x.data_ptr(), x.data_ptr(), None, None, None, None)
-    assert rc == d3d.D3D_ERR_UNSUPPORTED
+    # 211 requests at B = 16, V = 151936 fit the 2 MiB array, 212 do not
+    assert d3d.d3d_spec_verify_workspace_size(211, 16, 151936) <= 2 << 20 < \
+        d3d.d3d_spec_verify_workspace_size(212, 16, 151936)
+    assert _call_sized(d3d, 212) == d3d.D3D_ERR_UNSUPPORTED
+    assert _call_sized(d3d, 4096) == d3d.D3D_ERR_UNSUPPORTED
+
+
+def test_noalloc_largest_batch(d3d):
+    # the largest batch that fits (211 requests) runs and matches the oracle
+    v = W.verify_inputs(**dict(W.CONFIGS["async8b"], R=211), seed=23)
+    ref, _ = run_verify(d3d, v)
+    got = _noalloc_via_abi(d3d, v)
+    _same(got, ref)
+    compare_verify(got, oracle_verify(v), min_kept=0.85, what="no-allocation entry point, R = 211")

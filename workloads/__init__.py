@@ -26,7 +26,7 @@ import numpy as np
 
 __all__ = [
     "bf16_bits", "bf16_to_f32", "uniform24", "async_segments", "block_segments", "verify_segments",
-    "train_segments", "layout_segments",
+    "train_segments", "layout_segments", "prefix_lengths",
     "attn_inputs", "verify_inputs", "branch_heads", "match_inputs", "CONFIGS",
     "SEG_CAUSAL", "SEG_BIDIR", "DT_F32", "DT_BF16",
 ]
@@ -144,7 +144,9 @@ CONFIGS = {
 }
 
 
-def _prefix_lengths(R: int, L, seed: int) -> np.ndarray:
+def prefix_lengths(R: int, L, seed: int) -> np.ndarray:
+    """Per-request prefix lengths: ``L`` for every request, or uniform in the
+    inclusive range ``L = (lo, hi)`` (seeded)."""
     if isinstance(L, tuple):
         lo, hi = L
         return _rng(seed, _S_LPREF).integers(lo, hi + 1, size=R).astype(np.int32)
@@ -176,7 +178,7 @@ def attn_inputs(R=1, L=256, Hq=2, Hkv=1, d=64, B=16, C=12, F=2, layout="block",
         segs = layout_segments(layout, B, C, F, T, anchors)
     segs = np.asarray(segs, dtype=np.int32).reshape(-1, 5)
     n_q = int(segs[-1, 0] + segs[-1, 1]) if len(segs) else 0
-    Ls = _prefix_lengths(R, L, seed)
+    Ls = prefix_lengths(R, L, seed)
     cu_prefix = np.zeros(R + 1, np.int32)
     cu_prefix[1:] = np.cumsum(Ls)
     cu_q = (np.arange(R + 1) * n_q).astype(np.int32)
