@@ -95,6 +95,9 @@ def parse_args():
     ap.add_argument("--workload", default="async8b", choices=["async8b", "long_block", "serve32b"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--round-attn-ctas", type=int, default=96,
+                    help="SMs the attention may hold in the split round (the verification takes the rest; "
+                         "0: the whole device)")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip the long-block, serving-batch and C/F-sweep measurements")
     ap.add_argument("--no-layout-parts", action="store_true",
@@ -279,16 +282,19 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         sets.append(dset)
     ws_a = d3d.new_workspace(d3d.d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix), dev)
     ws_v = d3d.new_workspace(d3d.d3d_spec_verify_workspace_size(R, B, V), dev)
-    # the attention holds one SM per CTA; the verification that runs beside it
-    # takes the SMs it leaves (0: the attention fills the GPU, no limit)
-    attn_ctas = d3d.d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix)
+    # the attention holds one SM per CTA; in the round it gets at most
+    # --round-attn-ctas of them and the verification beside it takes the SMs
+    # it leaves (0: the attention fills the GPU, no limit).  Timed alone, the
+    # attention uses the whole device.
+    round_budget = max(0, args.round_attn_ctas)
+    attn_ctas = d3d.d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix, round_budget)
     side_sms = props.multi_processor_count - attn_ctas
     verify_sms = side_sms if 0 < attn_ctas and side_sms > 0 else 0
 
-    def attn(s, after_independent=False):
+    def attn(s, after_independent=False, max_ctas=0):
         d3d.d3d_packed_draft_attn(s["q"], s["kp"], s["vp"], s["kn"], s["vn"], s["segs"], s["cu_prefix"], s["cu_q"],
                                   s["cu_seg"], max_q, max_prefix, scale, s["out"], ws_a,
-                                  after_independent=after_independent)
+                                  after_independent=after_independent, max_ctas=max_ctas)
 
     def verify(s, sm_limit=0, fused_match=False, after_independent=False):
         extra = dict(heads=s["heads"], head_len=s["head_len"], branch=s["branch"]) if fused_match else {}
@@ -361,11 +367,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         if fused_round:
             d3d.d3d_async_round(*round_calls(s))
         elif args.round == "split-attention-first":
-            attn(s)
+            attn(s, max_ctas=round_budget)
             verify(s, verify_sms, fused_match=True, after_independent=verify_sms > 0)
         else:
             verify(s, verify_sms, fused_match=True)
-            attn(s, after_independent=verify_sms > 0)
+            attn(s, after_independent=verify_sms > 0, max_ctas=round_budget)
 
     torch.cuda.synchronize()
 
@@ -464,6 +470,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(torch, d3d, sets, n_sets, step, dev, stream, args, R, B, dist)
+        eager = run_e2e(torch, d3d, sets, n_sets, step, dev, stream, args, R, B, dist, graphs=False)
+        e2e["no_graph"] = {k: eager[k] for k in ("value", "ms_per_step", "pipeline")}
 
     # attention and verification are each timed alone in a short loop: the
     # burst peaks apply (sustained is for a kernel inside a seconds-long step)
@@ -494,7 +502,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "timing": "CUDA graph replays, CUDA events on the launching stream"},
         "verified_positions_per_s": round(world * wl["positions"] / (ms_step * 1e-3), 1),
         "parts": {"attn_us": round(t_attn * 1e3, 3), "verify_us": round(t_verify * 1e3, 3),
-                  "attn_ctas": attn_ctas, "verify_side_sms": verify_sms, "round_launch": "fused" if fused_round
+                  "attn_ctas": d3d.d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix),
+                  "round_attn_ctas": attn_ctas, "verify_side_sms": verify_sms, "round_launch": "fused" if fused_round
                   else args.round,
                   "verify_side_us": round(t_verify_side * 1e3, 3),
                   "match_us": round(t_match * 1e3, 3),
@@ -687,17 +696,20 @@ def other_workloads(d3d, torch, dev, stream, l2, peaks) -> dict:
     return out
 
 
-def run_e2e(torch, d3d, sets, n_sets, step, dev, stream, args, R, B, dist):
+def run_e2e(torch, d3d, sets, n_sets, step, dev, stream, args, R, B, dist, graphs=True):
     """Same metric through the public API, inputs from pinned host memory and
     results read back every step; copies inside the timed region.
 
     A serving loop: each set's inputs live in one device buffer (views keep
     every tensor's shape and dtype) with a matching pinned host buffer, so a
-    step is one host-to-device copy, the step's kernels (one CUDA graph per
-    set, captured from the public calls) and one device-to-host copy of the
-    results.  The copies run on their own streams: step i+1's inputs move
-    while step i computes, step i-1's results move back meanwhile, and a set
-    is refilled only after its previous results have left."""
+    step is one host-to-device copy, the step's kernels and one device-to-host
+    copy of the results.  With graphs=True the kernels are one CUDA graph per
+    set, captured from the public calls; with graphs=False every step calls
+    the C ABI entry points themselves (argument checks, workspace carving,
+    tensor-map encoding and launches on the host each step).  The copies run
+    on their own streams: step i+1's inputs move while step i computes, step
+    i-1's results move back meanwhile, and a set is refilled only after its
+    previous results have left."""
     in_keys = ["q", "kp", "vp", "kn", "vn", "segs", "cu_prefix", "cu_q", "cu_seg", "target", "draft", "y",
                "u_accept", "u_sample", "heads", "head_len"]
     out_keys = ["out", "out_tokens", "num_tokens", "branch"]
@@ -736,7 +748,7 @@ def run_e2e(torch, d3d, sets, n_sets, step, dev, stream, args, R, B, dist):
             pk["din"].copy_(pk["hin"], non_blocking=True)
             step(pk["dset"])  # eager pass: validates the calls on the new buffers
     torch.cuda.synchronize()
-    for pk in packs:
+    for pk in packs if graphs else []:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             step(pk["dset"])
@@ -759,7 +771,10 @@ def run_e2e(torch, d3d, sets, n_sets, step, dev, stream, args, R, B, dist):
             ev_in[j].record(s_in)
         stream.wait_event(ev_in[j])
         with torch.cuda.stream(stream):
-            pk["graph"].replay()
+            if graphs:
+                pk["graph"].replay()
+            else:
+                step(pk["dset"])
             ev_done[j].record(stream)
         s_out.wait_event(ev_done[j])
         with torch.cuda.stream(s_out):
@@ -796,7 +811,8 @@ def run_e2e(torch, d3d, sets, n_sets, step, dev, stream, args, R, B, dist):
     return {"value": round(whole_job_rate(n_q, world, ms), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 5), "steps": n,
             "pipeline": "one copy each way per step on their own streams, overlapped with the previous and "
-                        "next steps; step kernels as one CUDA graph per input set"}
+                        "next steps; step kernels " + ("as one CUDA graph per input set" if graphs else
+                                                       "launched by the C ABI calls themselves every step")}
 
 
 # ----------------------------------------------------------------------------

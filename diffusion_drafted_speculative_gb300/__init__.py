@@ -53,9 +53,9 @@ EXPORTED = {
     "d3d_validate_segments": (_I, [_P, _P, _P, _I]),
     "d3d_packed_draft_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "d3d_packed_draft_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
-                                   _F, _P, _P, _Z, _I, _P]),
+                                   _F, _P, _P, _Z, _I, _I, _P]),
     "d3d_spec_verify_workspace_size": (_Z, [_I, _I, _I]),
-    "d3d_packed_draft_attn_ctas": (_I, [_I, _I, _I, _I, _I, _I]),
+    "d3d_packed_draft_attn_ctas": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I,
                              _P, _P, _Z, _I, _I, _P]),
     "d3d_branch_match": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
@@ -168,9 +168,9 @@ def d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix) -> in
     return int(lib.d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix))
 
 
-def d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix) -> int:
+def d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix, max_ctas: int = 0) -> int:
     """CTAs (one SM each) the attention launch uses on the current device."""
-    n = int(lib.d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix))
+    n = int(lib.d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix, int(max_ctas)))
     if n < 0:
         _check("d3d_packed_draft_attn_ctas", n)
     return n
@@ -201,11 +201,13 @@ def _attn_args(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q,
 
 def d3d_packed_draft_attn(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q, cu_seg,
                           max_q: int, max_prefix: int, scale: float, out, ws, after_independent: bool = False,
-                          stream=None) -> None:
-    """Packed drafting attention; shapes as in include/d3d.h (bf16 tensors, int32 tables)."""
+                          stream=None, max_ctas: int = 0) -> None:
+    """Packed drafting attention; shapes as in include/d3d.h (bf16 tensors, int32 tables).
+    max_ctas > 0 bounds the launch to one wave of that many CTAs (SMs)."""
     args = _attn_args(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q, cu_seg, max_q, max_prefix,
                       scale, out, ws)
-    rc = lib.d3d_packed_draft_attn(*args, D3D_ATTN_AFTER_INDEPENDENT if after_independent else 0, _stream(stream))
+    rc = lib.d3d_packed_draft_attn(*args, int(max_ctas), D3D_ATTN_AFTER_INDEPENDENT if after_independent else 0,
+                                   _stream(stream))
     _check("d3d_packed_draft_attn", rc)
 
 

@@ -29,16 +29,35 @@ struct ReqBounds {
     int q0, n_q, p0, L, s0, s1;
 };
 
+// The six offsets of request r as loaded (load_bounds issues the loads; a
+// caller may do other work before check_bounds consumes them).
+struct ReqRaw {
+    int q0, q1, p0, p1, s0, s1;
+};
+
+__device__ inline ReqRaw load_bounds(const int32_t *cu_prefix, const int32_t *cu_q, const int32_t *cu_seg, int r)
+{
+    ReqRaw w;
+    w.q0 = cu_q[r], w.q1 = cu_q[r + 1];
+    w.p0 = cu_prefix[r], w.p1 = cu_prefix[r + 1];
+    w.s0 = cu_seg[r], w.s1 = cu_seg[r + 1];
+    return w;
+}
+
+__device__ inline bool check_bounds(const ReqRaw &w, int max_q, int max_prefix, int total_q, int total_prefix,
+                                    int total_segs, ReqBounds &b)
+{
+    b.q0 = w.q0, b.n_q = w.q1 - w.q0, b.p0 = w.p0, b.L = w.p1 - w.p0, b.s0 = w.s0, b.s1 = w.s1;
+    return 0 <= w.q0 && w.q0 <= w.q1 && w.q1 <= total_q && w.q1 - w.q0 <= max_q && 0 <= w.p0 && w.p0 <= w.p1 &&
+           w.p1 <= total_prefix && w.p1 - w.p0 <= max_prefix && 0 <= w.s0 && w.s0 <= w.s1 && w.s1 <= total_segs;
+}
+
 __device__ inline bool request_bounds(const int32_t *cu_prefix, const int32_t *cu_q, const int32_t *cu_seg, int r,
                                       int max_q, int max_prefix, int total_q, int total_prefix, int total_segs,
                                       ReqBounds &b)
 {
-    const int q0 = cu_q[r], q1 = cu_q[r + 1];
-    const int p0 = cu_prefix[r], p1 = cu_prefix[r + 1];
-    const int s0 = cu_seg[r], s1 = cu_seg[r + 1];
-    b.q0 = q0, b.n_q = q1 - q0, b.p0 = p0, b.L = p1 - p0, b.s0 = s0, b.s1 = s1;
-    return 0 <= q0 && q0 <= q1 && q1 <= total_q && q1 - q0 <= max_q && 0 <= p0 && p0 <= p1 &&
-           p1 <= total_prefix && p1 - p0 <= max_prefix && 0 <= s0 && s0 <= s1 && s1 <= total_segs;
+    return check_bounds(load_bounds(cu_prefix, cu_q, cu_seg, r), max_q, max_prefix, total_q, total_prefix,
+                        total_segs, b);
 }
 
 // Visible packed-key intervals of local token i (0 <= i < n_q) of a request

@@ -128,6 +128,21 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// Tensor store shared -> global of one box (the tensor map's box shape and
+// swizzle), tracked by the thread's bulk-async group: commit with
+// bulk_commit() and wait with bulk_wait_read() before the shared memory is
+// reused or the CTA exits.  Coordinates must not be negative and the
+// innermost one times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int32_t c0, int32_t c1, int32_t c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed bulk store of this thread has read its shared memory
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // Plain bulk copy global -> shared (no tensor map): both addresses 16-byte
 // aligned, size a multiple of 16; completes `bytes` on the mbarrier.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
@@ -203,6 +218,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
         : "r"(taddr)
         : "memory");
 }
+
+// The same load left in flight: v is valid only after tmem_wait_ld32(v), which
+// waits for every TMEM load of the thread and names v as its output, so no
+// use of v moves above it.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, float (&v)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : D3D_R8(0), D3D_R8(8), D3D_R8(16), D3D_R8(24)
+        : "r"(taddr)
+        : "memory");
+}
+
+#define D3D_M8(i) "+f"(v[i + 0]), "+f"(v[i + 1]), "+f"(v[i + 2]), "+f"(v[i + 3]), "+f"(v[i + 4]), "+f"(v[i + 5]), \
+                  "+f"(v[i + 6]), "+f"(v[i + 7])
+__device__ __forceinline__ void tmem_wait_ld32(float (&v)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : D3D_M8(0), D3D_M8(8), D3D_M8(16), D3D_M8(24) : : "memory");
+}
+#undef D3D_M8
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
 {
@@ -341,6 +378,16 @@ __device__ __forceinline__ float2 dsmem_ld_f2(uint32_t caddr)
     return v;
 }
 
+__device__ __forceinline__ uint4 smem_ld_v4(uint32_t saddr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(saddr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void smem_st_v4(uint32_t saddr, uint4 v)
 {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
@@ -350,6 +397,22 @@ __device__ __forceinline__ void smem_st_v4(uint32_t saddr, uint4 v)
 __device__ __forceinline__ void smem_st_f2(uint32_t saddr, float2 v)
 {
     asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(saddr), "f"(v.x), "f"(v.y) : "memory");
+}
+
+// 128 consecutive 32-bit TMEM columns of this thread's lane as four 32-column
+// loads in flight together (each needs only 32 contiguous registers), one
+// wait, completed before returning.
+__device__ __forceinline__ void tmem_ld32x4(uint32_t taddr, float (&v)[128])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%129];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95}, [%130];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%131];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : D3D_R8(0), D3D_R8(8), D3D_R8(16), D3D_R8(24), D3D_R8(32), D3D_R8(40), D3D_R8(48), D3D_R8(56), D3D_R8(64), D3D_R8(72), D3D_R8(80), D3D_R8(88), D3D_R8(96), D3D_R8(104), D3D_R8(112), D3D_R8(120)
+        : "r"(taddr), "r"(taddr + 32u), "r"(taddr + 64u), "r"(taddr + 96u)
+        : "memory");
 }
 
 #undef D3D_R8

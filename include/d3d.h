@@ -140,6 +140,16 @@ int d3d_validate_segments(const d3d_segment_t *segs, const int32_t *cu_q, const 
  *               status word only: the key splits of a query tile combine
  *               their partial results through distributed shared memory of
  *               a thread-block cluster, not through global scratch)
+ *   max_ctas    0: the plan may use every SM.  n > 0: a budget of n SMs
+ *               (each CTA holds one), so that a kernel running beside the
+ *               attention keeps the others: the plan picks its kernel and key
+ *               split for a wave of at most n CTAs.  The launch never has
+ *               fewer CTAs than the unsplit plan (one per query-tile pair of
+ *               each request and KV head, R * Hkv * ceil(MT / 2), MT the
+ *               query tiles of a head group): a budget below that count is
+ *               exceeded (the CTAs then run in more than one wave when they
+ *               outnumber the free SMs).  Results do not depend on it.  Negative:
+ *               D3D_ERR_INVALID_ARG.
  *   flags       0, or D3D_ATTN_AFTER_INDEPENDENT: the launch may start while
  *               the kernel before it on the stream still runs (programmatic
  *               dependent launch) -- for the verification of the same round,
@@ -150,25 +160,30 @@ int d3d_validate_segments(const d3d_segment_t *segs, const int32_t *cu_q, const 
  * Device-side checks: offsets out of the totals' range or a segment table
  * that breaks the rules of d3d_validate_segments set D3D_ERR_DEVICE_INPUT
  * in the status word (the affected rows are written as zeros).
+ * The launch holds one or two 128-row query tiles per CTA (two halve the K/V
+ * bytes each SM receives per flop) and splits the keys of a tile (pair) over
+ * up to 8 CTAs of a cluster; the plan minimises the estimated time on the
+ * device's SMs (or max_ctas of them).
  * ======================================================================== */
 #define D3D_ATTN_AFTER_INDEPENDENT 1
 
 size_t d3d_packed_draft_attn_workspace_size(int R, int Hq, int Hkv, int d, int max_q, int max_prefix);
 
-/* Number of CTAs the d3d_packed_draft_attn launch for these sizes uses on the
- * current device; each holds one SM from its start to its end (they all fit
- * in one wave when the count is at most the SM count).  A caller that runs
+/* Number of CTAs the d3d_packed_draft_attn launch for these sizes (and this
+ * max_ctas) uses on the current device; each holds one SM from its start to
+ * its end (they all fit in one wave when the count is at most the SM count).  A caller that runs
  * another kernel beside the attention can give it the remaining SMs (see
  * d3d_spec_verify's sm_limit).  Returns the count, or a negative status for
  * arguments d3d_packed_draft_attn would reject (D3D_ERR_INVALID_ARG,
  * D3D_ERR_UNSUPPORTED); 0 when there is nothing to compute. */
-int d3d_packed_draft_attn_ctas(int R, int Hq, int Hkv, int d, int max_q, int max_prefix);
+int d3d_packed_draft_attn_ctas(int R, int Hq, int Hkv, int d, int max_q, int max_prefix, int max_ctas);
 
 int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_prefix, const void *k_packed,
                           const void *v_packed, const d3d_segment_t *segs, const int32_t *cu_prefix,
                           const int32_t *cu_q, const int32_t *cu_seg, int R, int Hq, int Hkv, int d,
                           int max_q, int max_prefix, int total_q, int total_prefix, int total_segs,
-                          float scale, void *out, void *ws, size_t ws_bytes, int flags, cudaStream_t stream);
+                          float scale, void *out, void *ws, size_t ws_bytes, int max_ctas, int flags,
+                          cudaStream_t stream);
 
 /*
  * Failure-detection hook (no counterpart on the pages).  mode 1 makes every

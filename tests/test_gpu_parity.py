@@ -334,8 +334,11 @@ def test_round_on_one_stream_overlapping(d3d, attention_first):
     ref_v = oracle_verify(v)
     ref_a = oracle.packed_attn(a, heads=(28, 32))
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    side = sms - d3d.d3d_packed_draft_attn_ctas(1, cfg["Hq"], cfg["Hkv"], cfg["d"], a["max_q"], a["max_prefix"])
-    assert side > 0
+    # the attention in one wave of at most 96 CTAs, the verification on the rest
+    budget = 96
+    side = sms - d3d.d3d_packed_draft_attn_ctas(1, cfg["Hq"], cfg["Hkv"], cfg["d"], a["max_q"], a["max_prefix"],
+                                                budget)
+    assert side >= sms - budget
     from gpu_util import bf16, f32, i32
     t = {k: bf16(a[k]) for k in ("q", "kp", "vp", "kn", "vn")}
     ix = {k: i32(a[k]) for k in ("segs", "cu_prefix", "cu_q", "cu_seg")}
@@ -358,7 +361,7 @@ def test_round_on_one_stream_overlapping(d3d, attention_first):
             def att():
                 d3d.d3d_packed_draft_attn(t["q"], t["kp"], t["vp"], t["kn"], t["vn"], ix["segs"], ix["cu_prefix"],
                                           ix["cu_q"], ix["cu_seg"], a["max_q"], a["max_prefix"], a["scale"], out, wsa,
-                                          after_independent=not attention_first)
+                                          after_independent=not attention_first, max_ctas=budget)
             if attention_first:
                 att()
                 ver()
@@ -432,10 +435,36 @@ def test_async_round_declines_key_splits(d3d):
 
 
 def test_attention_cta_count_matches_plan(d3d):
-    # one CTA per query tile and key split, all in one wave on this GPU
-    n = d3d.d3d_packed_draft_attn_ctas(1, 32, 8, 128, 384, 2048)
+    # one CTA per query tile (or tile pair) and key split, all in one wave on
+    # this GPU, and within the CTA budget when one is given; the unsplit
+    # two-tile plan (R * Hkv * ceil(MT / 2) = 1 * 8 * 6 CTAs, MT = 384 / 32
+    # query tiles) is the floor below which no budget goes
     sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = d3d.d3d_packed_draft_attn_ctas(1, 32, 8, 128, 384, 2048)
     assert 0 < n <= sms
+    floor = d3d.d3d_packed_draft_attn_ctas(1, 32, 8, 128, 384, 2048, 1)
+    assert floor >= 48
+    for budget in (24, 48, 96, 120):
+        assert 0 < d3d.d3d_packed_draft_attn_ctas(1, 32, 8, 128, 384, 2048, budget) <= max(budget, floor)
+
+
+@pytest.mark.parametrize("budget", [0, 120, 96, 48, 12])
+def test_attn_plans_under_cta_budgets(d3d, budget):
+    # the CTA budget changes the plan (one or two query tiles per CTA, the key
+    # split); every plan meets the oracle on the async8b layout (sampled heads)
+    a = W.attn_inputs(**W.CONFIGS["async8b"], seed=17)
+    from gpu_util import bf16, i32
+    t = {k: bf16(a[k]) for k in ("q", "kp", "vp", "kn", "vn")}
+    ix = {k: i32(a[k]) for k in ("segs", "cu_prefix", "cu_q", "cu_seg")}
+    out = torch.full_like(t["q"], float("nan"))
+    ws = d3d.new_workspace(d3d.d3d_packed_draft_attn_workspace_size(1, 32, 8, 128, a["max_q"], a["max_prefix"]))
+    d3d.d3d_packed_draft_attn(t["q"], t["kp"], t["vp"], t["kn"], t["vn"], ix["segs"], ix["cu_prefix"], ix["cu_q"],
+                              ix["cu_seg"], a["max_q"], a["max_prefix"], a["scale"], out, ws, max_ctas=budget)
+    torch.cuda.synchronize()
+    heads = [0, 13, 31]
+    got = out.float().cpu().numpy()
+    assert_attn_close(got[:, heads], _oracle_heads(a, heads)[:, heads], "budget %d" % budget)
+    assert d3d.d3d_workspace_status(ws) == 0
 
 
 # ------------------------------------------------------------------ greedy (temperature 0)

@@ -94,25 +94,27 @@ def test_invalid_arguments_rejected_on_host(d3d):
     assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 1 << 20, 0, -1)) == d3d.D3D_ERR_INVALID_ARG
     assert L.d3d_spec_verify(*args(1, 4, 10, 1.0, 1, fake, 1 << 20, 0, 3, None, fake)) == d3d.D3D_ERR_INVALID_ARG
 
-    def attn(R=1, Hq=32, Hkv=8, d=128, max_q=16, scale=0.1, ws=fake, wsb=1 << 30, flags=0):
+    def attn(R=1, Hq=32, Hkv=8, d=128, max_q=16, scale=0.1, ws=fake, wsb=1 << 30, flags=0, max_ctas=0):
         return L.d3d_packed_draft_attn(fake, fake, fake, fake, fake, fake, fake, fake, fake, R, Hq, Hkv, d, max_q,
-                                       64, 16, 64, 1, scale, fake, ws, wsb, flags, None)
+                                       64, 16, 64, 1, scale, fake, ws, wsb, max_ctas, flags, None)
     assert attn(flags=2) == d3d.D3D_ERR_INVALID_ARG
+    assert attn(max_ctas=-1) == d3d.D3D_ERR_INVALID_ARG
     assert attn(Hq=30, Hkv=8) == d3d.D3D_ERR_INVALID_ARG
     assert attn(d=96) == d3d.D3D_ERR_UNSUPPORTED
     assert attn(Hq=24, Hkv=8) == d3d.D3D_ERR_UNSUPPORTED  # G = 3 does not divide 128
     assert attn(max_q=8193) == d3d.D3D_ERR_UNSUPPORTED
     assert L.d3d_packed_draft_attn(ctypes.c_void_p(264), fake, fake, fake, fake, fake, fake, fake, fake, 1, 32, 8,
-                                   128, 16, 64, 16, 64, 1, 0.1, fake, fake, 1 << 30, 0, None) == d3d.D3D_ERR_INVALID_ARG
+                                   128, 16, 64, 16, 64, 1, 0.1, fake, fake, 1 << 30, 0, 0, None) == d3d.D3D_ERR_INVALID_ARG
     assert attn(scale=0.0) == d3d.D3D_ERR_INVALID_ARG
     assert attn(scale=float("inf")) == d3d.D3D_ERR_INVALID_ARG
     assert attn(ws=None) == d3d.D3D_ERR_WORKSPACE
     assert attn(R=0) == d3d.D3D_OK
     ctas = L.d3d_packed_draft_attn_ctas
-    assert ctas(1, 30, 8, 128, 16, 64) == d3d.D3D_ERR_INVALID_ARG
-    assert ctas(1, 32, 8, 96, 16, 64) == d3d.D3D_ERR_UNSUPPORTED
-    assert ctas(1, 24, 8, 128, 16, 64) == d3d.D3D_ERR_UNSUPPORTED
-    assert ctas(0, 32, 8, 128, 16, 64) == 0 and ctas(1, 32, 8, 128, 0, 64) == 0
+    assert ctas(1, 32, 8, 128, 16, 64, -1) == d3d.D3D_ERR_INVALID_ARG
+    assert ctas(1, 30, 8, 128, 16, 64, 0) == d3d.D3D_ERR_INVALID_ARG
+    assert ctas(1, 32, 8, 96, 16, 64, 0) == d3d.D3D_ERR_UNSUPPORTED
+    assert ctas(1, 24, 8, 128, 16, 64, 0) == d3d.D3D_ERR_UNSUPPORTED
+    assert ctas(0, 32, 8, 128, 16, 64, 0) == 0 and ctas(1, 32, 8, 128, 0, 64, 0) == 0
 
     # the fused round: missing calls, then each part's own argument checks
     assert L.d3d_async_round(None, None, None) == d3d.D3D_ERR_INVALID_ARG
@@ -250,3 +252,4 @@ def test_noalloc_limit_edge_in_workspace_sizes(d3d):
     # workspace of 211 requests at B = 16, V = 151936 but not of 212
     assert d3d.d3d_spec_verify_workspace_size(211, 16, 151936) <= 2 << 20
     assert d3d.d3d_spec_verify_workspace_size(212, 16, 151936) > 2 << 20
+
