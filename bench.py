@@ -59,7 +59,7 @@ CSRC = os.path.join(ROOT, "diffusion_drafted_speculative_gb300", "csrc")
 NCU_TRAFFIC = {
     ("async8b", "attn"): {"sources": ("attn.cu", "attn_common.cuh", "sm100_ptx.cuh", "d3d_common.cuh",
                                       "verify_body.cuh"),
-                          "sha": "7f3d645126d08223", "bytes": 13179648},
+                          "sha": "21be421b59f172a0", "bytes": 13180928},
     ("async8b", "verify"): {"sources": ("verify.cu", "verify_body.cuh", "sm100_ptx.cuh", "d3d_common.cuh"),
                             "sha": "802f314046cc7507", "bytes": 9547776},
     ("async8b", "greedy"): {"sources": ("verify.cu", "greedy_body.cuh", "verify_body.cuh", "sm100_ptx.cuh",
@@ -506,6 +506,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                   "round_attn_ctas": attn_ctas, "verify_side_sms": verify_sms, "round_launch": "fused" if fused_round
                   else args.round,
                   "verify_side_us": round(t_verify_side * 1e3, 3),
+                  "verify_launch": {"whole_device_slice_ctas": d3d.d3d_spec_verify_slice_ctas(R, B, V, cfg["logits"], 1.0, 0),
+                                    "side_slice_ctas": d3d.d3d_spec_verify_slice_ctas(R, B, V, cfg["logits"], 1.0,
+                                                                                      verify_sms),
+                                    "rule": "CTAs of the vocabulary-slice launch (0: the chunked launch)"},
                   "match_us": round(t_match * 1e3, 3),
                   "attn_query_tokens_per_s": round(wl["n_q"] * R / (t_attn * 1e-3), 1),
                   "verify_positions_per_s": round(wl["positions"] / (t_verify * 1e-3), 1),

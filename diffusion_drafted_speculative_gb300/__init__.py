@@ -18,7 +18,8 @@ import torch
 __all__ = [
     "D3DError", "lib", "d3d_status_string", "d3d_version", "d3d_validate_segments",
     "d3d_packed_draft_attn", "d3d_packed_draft_attn_workspace_size", "d3d_packed_draft_attn_ctas",
-    "d3d_spec_verify", "d3d_spec_verify_workspace_size", "d3d_spec_verify_noalloc", "d3d_async_round",
+    "d3d_spec_verify", "d3d_spec_verify_workspace_size", "d3d_spec_verify_slice_ctas", "d3d_spec_verify_noalloc",
+    "d3d_async_round",
     "AttnCall", "VerifyCall", "d3d_build_branches", "d3d_build_branches_workspace_size",
     "d3d_accept_probs", "d3d_accept_probs_workspace_size", "d3d_branch_match", "d3d_workspace_status", "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
     "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
@@ -55,6 +56,7 @@ EXPORTED = {
     "d3d_packed_draft_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                                    _F, _P, _P, _Z, _I, _I, _P]),
     "d3d_spec_verify_workspace_size": (_Z, [_I, _I, _I]),
+    "d3d_spec_verify_slice_ctas": (_I, [_I, _I, _I, _I, _F, _I, _Z]),
     "d3d_packed_draft_attn_ctas": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "d3d_spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I,
                              _P, _P, _Z, _I, _I, _P]),
@@ -166,6 +168,19 @@ def d3d_debug_inject_fault(mode: int) -> None:
 
 def d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix) -> int:
     return int(lib.d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix))
+
+
+def d3d_spec_verify_slice_ctas(R, B, V, logits_dtype, temperature, sm_limit: int = 0, ws_bytes=None) -> int:
+    """CTAs of the vocabulary-slice verification launch for these sizes (0: the
+    call takes the chunked or greedy launch); ws_bytes defaults to
+    d3d_spec_verify_workspace_size."""
+    if ws_bytes is None:
+        ws_bytes = lib.d3d_spec_verify_workspace_size(R, B, V)
+    n = int(lib.d3d_spec_verify_slice_ctas(R, B, V, int(logits_dtype), float(temperature), int(sm_limit),
+                                           int(ws_bytes)))
+    if n < 0:
+        _check("d3d_spec_verify_slice_ctas", n)
+    return n
 
 
 def d3d_packed_draft_attn_ctas(R, Hq, Hkv, d, max_q, max_prefix, max_ctas: int = 0) -> int:

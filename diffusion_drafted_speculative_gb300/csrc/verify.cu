@@ -6,6 +6,7 @@
 
 #include "greedy_body.cuh"
 #include "verify_body.cuh"
+#include "verify_slice.cuh"
 
 namespace d3d {
 namespace {
@@ -61,10 +62,89 @@ int launch_verify_nt(const VArgs &a_in, int sm_limit, int flags, cudaStream_t st
     return cuda_status(e);
 }
 
-// With an SM limit the CTAs are 512 threads, one per SM (the register file
-// holds one): a launch beside another kernel takes at most sm_limit SMs.
-template <typename T> int launch_verify(const VArgs &a, int sm_limit, int flags, cudaStream_t stream)
+constexpr int kSliceSmemMax = 219 * 1024;  // dynamic shared memory of a slice CTA (227 KB per CTA less its static arrays)
+
+// Slice width W (a multiple of kSliceGrain) and count nS when the request's
+// rows split over the SMs the launch may use with every row of a slice
+// resident in one CTA's shared memory, else false.  W is the smallest width
+// that gives each request at most its share of the SMs.
+inline int slice_width(int R, int V, int units)
 {
+    const int per = units / R;  // slices per request
+    if (per < 1)
+        return 0;
+    const long long w = ((long long)V + per - 1) / per;
+    return (int)((w + kSliceGrain - 1) / kSliceGrain * kSliceGrain);
+}
+
+// The workspace the slice launch can need: its finest slices (every unit a
+// launch may hold) give the most records.
+inline size_t slice_ws_bound(int R, int B, int V)
+{
+    const int W = slice_width(R, V, kSliceMaxUnits);
+    return W > 0 ? verify_layout(R, B, V, W).total : 0;
+}
+
+template <typename T>
+bool slice_plan(const VArgs &a, int sm_limit, size_t ws_bytes, int &W, int &nS, size_t &dyn)
+{
+    // rows and slices start on 16-byte boundaries (bulk copies)
+    if ((size_t)a.V * sizeof(T) % 16 != 0 || (reinterpret_cast<uintptr_t>(a.target) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(a.draft) & 15) != 0)
+        return false;
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    int units = (sm_limit > 0 && sm_limit < nsm) ? sm_limit : nsm;
+    if (units > kSliceMaxUnits)
+        units = kSliceMaxUnits;
+    W = slice_width(a.R, a.V, units);
+    if (W <= 0)
+        return false;
+    nS = (a.V + W - 1) / W;
+    dyn = SliceLayout<T>(a.B, W, nS).total;
+    if (dyn > (size_t)kSliceSmemMax || verify_layout(a.R, a.B, a.V, W).total > ws_bytes)
+        return false;
+    return set_max_dyn_smem<verify_slice_kernel<T>>(kSliceSmemMax) == cudaSuccess;
+}
+
+template <typename T>
+int launch_verify_slice(const VArgs &a, int W, int nS, size_t dyn, int flags, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.R * nS));
+    cfg.blockDim = dim3(kSliceThreads);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;  // the CTAs of a request wait on one another
+    attr[0].val.cooperative = 1;
+    unsigned na = 1;
+    if (flags & D3D_VERIFY_AFTER_INDEPENDENT) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cuda_status(cudaLaunchKernelEx(&cfg, verify_slice_kernel<T>, a, W, nS));
+}
+
+// The slice launch when the call's requests split over the SMs with their
+// slices resident in shared memory; otherwise the chunked kernel: with an SM
+// limit its CTAs are 512 threads, one per SM (the register file holds one),
+// so a launch beside another kernel takes at most sm_limit SMs.
+template <typename T>
+int launch_verify(const VArgs &a, int sm_limit, int flags, cudaStream_t stream, size_t ws_bytes)
+{
+    int W = 0, nS = 0;
+    size_t dyn = 0;
+    if (slice_plan<T>(a, sm_limit, ws_bytes, W, nS, dyn))
+        return launch_verify_slice<T>(a, W, nS, dyn, flags, stream);
+    cudaGetLastError();
     if (sm_limit > 0)
         return launch_verify_nt<T, kNTLimited>(a, sm_limit, flags, stream);
     return launch_verify_nt<T, kNTDevice>(a, 0, flags, stream);
@@ -79,8 +159,31 @@ size_t d3d_spec_verify_workspace_size(int R, int B, int V)
 {
     if (R < 0 || B < 2 || V < 1 || B > d3d::kMaxB || V > d3d::kMaxChunks * d3d::kVChunkMin)
         return 0;
-    // the smaller chunk has the most records: the workspace fits both launches
-    return d3d::verify_layout(R, B, V, d3d::kVChunkMin).total;
+    // the smaller chunk has the most records: the workspace fits both chunked
+    // launches; the slice launch needs at most slice_ws_bound
+    const size_t chunked = d3d::verify_layout(R, B, V, d3d::kVChunkMin).total;
+    const size_t sliced = d3d::slice_ws_bound(R, B, V);
+    return chunked > sliced ? chunked : sliced;
+}
+
+int d3d_spec_verify_slice_ctas(int R, int B, int V, int logits_dtype, float temperature, int sm_limit,
+                               size_t ws_bytes)
+{
+    if (R < 0 || B < 2 || B > d3d::kMaxB || V < 1 || V > d3d::kMaxChunks * d3d::kVChunkMin || sm_limit < 0 ||
+        !(temperature >= 0.f) || (logits_dtype != D3D_DTYPE_BF16 && logits_dtype != D3D_DTYPE_F32))
+        return D3D_ERR_INVALID_ARG;
+    if (R == 0 || temperature == 0.f)
+        return 0;  // nothing to launch, or the greedy launch
+    d3d::VArgs a{};
+    a.R = R, a.B = B, a.V = V;
+    static __align__(16) unsigned char probe[16];  // stands for 16-byte aligned rows
+    a.target = a.draft = probe;
+    int W = 0, nS = 0;
+    size_t dyn = 0;
+    const bool sliced = logits_dtype == D3D_DTYPE_BF16 ? d3d::slice_plan<uint16_t>(a, sm_limit, ws_bytes, W, nS, dyn)
+                                                       : d3d::slice_plan<float>(a, sm_limit, ws_bytes, W, nS, dyn);
+    cudaGetLastError();
+    return sliced ? R * nS : 0;
 }
 
 int d3d_spec_verify(const void *target_logits, const void *draft_logits, int logits_dtype,
@@ -105,8 +208,8 @@ int d3d_spec_verify(const void *target_logits, const void *draft_logits, int log
         return logits_dtype == D3D_DTYPE_BF16 ? d3d::launch_greedy<uint16_t>(a, sm_limit, flags, stream)
                                               : d3d::launch_greedy<float>(a, sm_limit, flags, stream);
     if (logits_dtype == D3D_DTYPE_BF16)
-        return d3d::launch_verify<uint16_t>(a, sm_limit, flags, stream);
-    return d3d::launch_verify<float>(a, sm_limit, flags, stream);
+        return d3d::launch_verify<uint16_t>(a, sm_limit, flags, stream, ws_bytes);
+    return d3d::launch_verify<float>(a, sm_limit, flags, stream, ws_bytes);
 }
 
 }  // extern "C"
@@ -192,6 +295,6 @@ extern "C" int d3d_spec_verify_noalloc(const void *target_logits, const void *dr
         return logits_dtype == D3D_DTYPE_BF16 ? d3d::launch_greedy<uint16_t>(a, 0, 0, stream)
                                               : d3d::launch_greedy<float>(a, 0, 0, stream);
     if (logits_dtype == D3D_DTYPE_BF16)
-        return d3d::launch_verify<uint16_t>(a, 0, 0, stream);
-    return d3d::launch_verify<float>(a, 0, 0, stream);
+        return d3d::launch_verify<uint16_t>(a, 0, 0, stream, d3d::kNoAllocScratchBytes);
+    return d3d::launch_verify<float>(a, 0, 0, stream, d3d::kNoAllocScratchBytes);
 }

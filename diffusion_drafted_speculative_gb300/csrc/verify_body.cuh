@@ -467,7 +467,7 @@ __device__ inline void load_request_inputs(int r, int B, const int32_t *__restri
 // uniforms.  With write_outputs the CTA also writes accept_len, num_tokens,
 // alpha/p/q and the accepted tokens.
 template <int NT>
-__device__ void select_request(int r, int B, int V, int nch, const Rec *__restrict__ rec,
+__device__ void select_request(int r, int B, int V, int nch, int chunk_w, const Rec *__restrict__ rec,
                                const int32_t *s_y, const float *s_u, bool write_outputs,
                                int32_t *__restrict__ accept_len, int32_t *__restrict__ out_tokens,
                                int32_t *__restrict__ num_tokens, float *__restrict__ alpha_out,
@@ -529,7 +529,7 @@ __device__ void select_request(int r, int B, int V, int nch, const Rec *__restri
                     if (write_outputs)
                         record_status(status, D3D_ERR_DEVICE_INPUT);
                 } else {
-                    const Rec t = rec_at(jj * nch + yv / VCfg<NT>::kChunk);
+                    const Rec t = rec_at(jj * nch + yv / chunk_w);
                     p = fast_exp2(t.xP - MP) / sp;
                     q = fast_exp2(t.xQ - MQ) / sq;
                     al = (p >= q) ? 1.f : p / q;
@@ -680,6 +680,110 @@ __device__ void scan_owner(const float (&w)[kVPer], int c0, float target, bool t
     }
     if ((takelast || cand == 0x7fffffff) && threadIdx.x == 0)
         *out_tok = s_lastpos;
+    __syncthreads();
+}
+
+// The phase-D decision of one request: which chunk holds the sample's
+// crossing and where.  From the request's chunk sums part2_r[cc] = (residual
+// mass, P mass), by warp 0 (every thread of the CTA calls it; the result is
+// in *dec after the final barrier): the total S of the residual (or of P when
+// the residual has no mass left in fp32, or for the bonus row), the target
+// u*S, the first chunk whose inclusive sum passes it and the target's offset
+// into that chunk.  Sums and the product are kept as fp32 pairs (df_add /
+// df_mul), so that magnitude-S quantities carry no 2^-24 S rounding; the
+// owner chunk then scans against an offset on its own scale.  When rounding
+// leaves the target at or past the end, the last chunk with mass owns it and
+// takes its last position with mass.
+struct Decision {
+    int kind;      // 0: residual max(0, P - Q); 1: P
+    int owner;     // chunk holding the crossing (-1: no mass anywhere)
+    int takelast;  // take the owner's last position with mass
+    float rem;     // target minus the masses of the chunks before the owner
+};
+
+template <int NT>
+__device__ void decide_request(const float2 *__restrict__ part2_r, int nch, int mode, float us, float2 *s_sums,
+                               Decision *dec)
+{
+    for (int cc = threadIdx.x; cc < nch; cc += NT)
+        s_sums[cc] = __ldcg(part2_r + cc);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int per = (nch + 31) >> 5;  // consecutive chunks per lane
+        const int c_lo = min(nch, lane * per), c_hi = min(nch, c_lo + per);
+        float rh = 0.f, rl = 0.f, ph = 0.f, pl = 0.f;  // this lane's residual and P masses
+        for (int cc = c_lo; cc < c_hi; ++cc) {
+            df_add(rh, rl, s_sums[cc].x, 0.f);
+            df_add(ph, pl, s_sums[cc].y, 0.f);
+        }
+        // inclusive scan over the lanes (chunk order) of both masses
+        float irh = rh, irl = rl, iph = ph, ipl = pl;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float a = __shfl_up_sync(kFull, irh, o), b = __shfl_up_sync(kFull, irl, o);
+            const float c2 = __shfl_up_sync(kFull, iph, o), d = __shfl_up_sync(kFull, ipl, o);
+            if (lane >= o) {
+                df_add(irh, irl, a, b);
+                df_add(iph, ipl, c2, d);
+            }
+        }
+        // residual unless it has no mass left in fp32 (then P at that row)
+        const float Srh = __shfl_sync(kFull, irh, 31);
+        const int kind = (mode == 0 && Srh > 0.f) ? 0 : 1;
+        const float inh = kind == 0 ? irh : iph, inl = kind == 0 ? irl : ipl;
+        const float Sh = __shfl_sync(kFull, inh, 31), Sl = __shfl_sync(kFull, inl, 31);
+        float th, tl;
+        df_mul(us, Sh, Sl, th, tl);
+        float exh = __shfl_up_sync(kFull, inh, 1), exl = __shfl_up_sync(kFull, inl, 1);
+        if (lane == 0)
+            exh = exl = 0.f;
+        auto mass = [&](int cc) { return kind == 0 ? s_sums[cc].x : s_sums[cc].y; };
+        // the first lane whose inclusive sum passes the target holds the crossing
+        const unsigned bal = __ballot_sync(kFull, c_lo < c_hi && df_gt(inh, inl, th, tl));
+        int owner = -1, takelast = 0;
+        float rem = 0.f;
+        if (bal) {
+            const int L = __ffs(bal) - 1;
+            if (lane == L) {
+                float runh = exh, runl = exl;
+                int last_mass = -1;
+                for (int cc = c_lo; cc < c_hi; ++cc) {
+                    float nh = runh, nl = runl;
+                    df_add(nh, nl, mass(cc), 0.f);
+                    if (mass(cc) > 0.f)
+                        last_mass = cc;
+                    if (df_gt(nh, nl, th, tl)) {
+                        owner = cc;
+                        break;
+                    }
+                    runh = nh, runl = nl;
+                }
+                if (owner < 0) {  // the two summation orders disagree in the last bits
+                    owner = last_mass;
+                    takelast = 1;
+                }
+                rem = (th - runh) + (tl - runl);
+            }
+            owner = __shfl_sync(kFull, owner, L);
+            takelast = __shfl_sync(kFull, takelast, L);
+            rem = __shfl_sync(kFull, rem, L);
+        } else {  // rounding left u*S at or past the end: last chunk with mass
+            takelast = 1;
+            int lastc = -1;
+            for (int cc = c_lo; cc < c_hi; ++cc)
+                if (mass(cc) > 0.f)
+                    lastc = cc;
+            const unsigned b2 = __ballot_sync(kFull, lastc >= 0);
+            owner = b2 ? __shfl_sync(kFull, lastc, 31 - __clz(b2)) : -1;
+        }
+        if (lane == 0) {
+            dec->kind = kind;
+            dec->owner = owner;
+            dec->takelast = takelast;
+            dec->rem = rem;
+        }
+    }
     __syncthreads();
 }
 
@@ -965,96 +1069,11 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
         }
     }
 
-    __shared__ int s_kind_used, s_owner, s_takelast;
-    __shared__ float s_rem;
-    // Phase D decision for request r from its chunk sums, by warp 0 (everyone
-    // reads the shared results after the call): the total S, the target u*S,
-    // the chunk holding the crossing and the target's offset into that chunk.
-    // Sums and the product are kept as fp32 pairs (df_add / df_mul), so that
-    // magnitude-S quantities carry no 2^-24 S rounding; the owner chunk then
-    // scans against an offset on its own scale.
+    __shared__ Decision s_dec;
+    // phase D decision for request r from its chunk sums (the records are no
+    // longer needed: their shared memory holds the sums)
     auto decide = [&](int r, const Sel &sel) {
-        float2 *s_sums = reinterpret_cast<float2 *>(s_dyn);  // the records are no longer needed
-        for (int cc = threadIdx.x; cc < nch; cc += NT)
-            s_sums[cc] = __ldcg(part2 + (size_t)r * nch + cc);
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            const int lane = threadIdx.x;
-            const int per = (nch + 31) >> 5;  // consecutive chunks per lane
-            const int c_lo = min(nch, lane * per), c_hi = min(nch, c_lo + per);
-            float rh = 0.f, rl = 0.f, ph = 0.f, pl = 0.f;  // this lane's residual and P masses
-            for (int cc = c_lo; cc < c_hi; ++cc) {
-                df_add(rh, rl, s_sums[cc].x, 0.f);
-                df_add(ph, pl, s_sums[cc].y, 0.f);
-            }
-            // inclusive scan over the lanes (chunk order) of both masses
-            float irh = rh, irl = rl, iph = ph, ipl = pl;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float a = __shfl_up_sync(kFull, irh, o), b = __shfl_up_sync(kFull, irl, o);
-                const float c2 = __shfl_up_sync(kFull, iph, o), d = __shfl_up_sync(kFull, ipl, o);
-                if (lane >= o) {
-                    df_add(irh, irl, a, b);
-                    df_add(iph, ipl, c2, d);
-                }
-            }
-            // residual unless it has no mass left in fp32 (then P at that row)
-            const float Srh = __shfl_sync(kFull, irh, 31);
-            const int kind = (sel.mode == 0 && Srh > 0.f) ? 0 : 1;
-            const float inh = kind == 0 ? irh : iph, inl = kind == 0 ? irl : ipl;
-            const float Sh = __shfl_sync(kFull, inh, 31), Sl = __shfl_sync(kFull, inl, 31);
-            float th, tl;
-            df_mul(s_us, Sh, Sl, th, tl);
-            float exh = __shfl_up_sync(kFull, inh, 1), exl = __shfl_up_sync(kFull, inl, 1);
-            if (lane == 0)
-                exh = exl = 0.f;
-            auto mass = [&](int cc) { return kind == 0 ? s_sums[cc].x : s_sums[cc].y; };
-            // the first lane whose inclusive sum passes the target holds the crossing
-            const unsigned bal = __ballot_sync(kFull, c_lo < c_hi && df_gt(inh, inl, th, tl));
-            int owner = -1, takelast = 0;
-            float rem = 0.f;
-            if (bal) {
-                const int L = __ffs(bal) - 1;
-                if (lane == L) {
-                    float runh = exh, runl = exl;
-                    int last_mass = -1;
-                    for (int cc = c_lo; cc < c_hi; ++cc) {
-                        float nh = runh, nl = runl;
-                        df_add(nh, nl, mass(cc), 0.f);
-                        if (mass(cc) > 0.f)
-                            last_mass = cc;
-                        if (df_gt(nh, nl, th, tl)) {
-                            owner = cc;
-                            break;
-                        }
-                        runh = nh, runl = nl;
-                    }
-                    if (owner < 0) {  // the two summation orders disagree in the last bits
-                        owner = last_mass;
-                        takelast = 1;
-                    }
-                    rem = (th - runh) + (tl - runl);
-                }
-                owner = __shfl_sync(kFull, owner, L);
-                takelast = __shfl_sync(kFull, takelast, L);
-                rem = __shfl_sync(kFull, rem, L);
-            } else {  // rounding left u*S at or past the end: last chunk with mass
-                takelast = 1;
-                int lastc = -1;
-                for (int cc = c_lo; cc < c_hi; ++cc)
-                    if (mass(cc) > 0.f)
-                        lastc = cc;
-                const unsigned b2 = __ballot_sync(kFull, lastc >= 0);
-                owner = b2 ? __shfl_sync(kFull, lastc, 31 - __clz(b2)) : -1;
-            }
-            if (lane == 0) {
-                s_kind_used = kind;
-                s_owner = owner;
-                s_takelast = takelast;
-                s_rem = rem;
-            }
-        }
-        __syncthreads();
+        decide_request<NT>(part2 + (size_t)r * nch, nch, sel.mode, s_us, reinterpret_cast<float2 *>(s_dyn), &s_dec);
     };
     // The match of request r once its sampled token is written (the writer is a
     // thread of this CTA, and a barrier separates the write from this read).
@@ -1092,7 +1111,7 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
         load_request_inputs<NT>(r, B, y, u_acc, u_s, s_y, s_u, &s_us);
         if (!wait_count(bar + kBarInts * r, B * nch, status))
             return;
-        select_request<NT>(r, B, V, nch, rec, s_y, s_u, j == 0 && chunk == 0, accept_len, out_tokens, num_tokens,
+        select_request<NT>(r, B, V, nch, C::kChunk, rec, s_y, s_u, j == 0 && chunk == 0, accept_len, out_tokens, num_tokens,
                        alpha_out, p_out, q_out, awl_out, status, sel, s_rec);
         if (j != sel.row) {
             passed_a(r, B * nch);  // counted once the CTA's work is done: off the critical path
@@ -1109,14 +1128,14 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
         if (!wait_count(bar + kBarInts * r + 2, nch, status))
             return;
         decide(r, sel);
-        if (s_owner == chunk) {
-            if (s_kind_used != sel.mode) {  // residual without mass in fp32: P at that row
+        if (s_dec.owner == chunk) {
+            if (s_dec.kind != sel.mode) {  // residual without mass in fp32: P at that row
                 float a1, a2;
                 kept_masses(1, eP, eQ, mtP, mtQ, sel, a1, a2);
             }
-            scan_owner<NT>(eQ, c0, s_rem, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
+            scan_owner<NT>(eQ, c0, s_dec.rem, s_dec.takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
             fused_match(r, sel.a);
-        } else if (s_owner < 0 && chunk == 0) {
+        } else if (s_dec.owner < 0 && chunk == 0) {
             // no mass anywhere: cannot happen for a finite softmax row
             if (threadIdx.x == 0) {
                 record_status(status, D3D_ERR_DEVICE_INPUT);
@@ -1141,7 +1160,7 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
         if (!wait_count(bar + kBarInts * r, B * nch, status))
             return;
         passed_a(r, nch);
-        select_request<NT>(r, B, V, nch, rec, s_y, s_u, chunk == 0, accept_len, out_tokens, num_tokens, alpha_out,
+        select_request<NT>(r, B, V, nch, C::kChunk, rec, s_y, s_u, chunk == 0, accept_len, out_tokens, num_tokens, alpha_out,
                        p_out, q_out, awl_out, status, sel, s_rec);
         const T *prow = target + ((size_t)r * B + sel.row) * V;
         const T *qrow = draft + ((size_t)r * (B - 1) + (sel.mode == 0 ? sel.row : 0)) * V;
@@ -1164,20 +1183,20 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
             return;
         // every phase-C item of r waited for r's phase A, so the records are complete
         if (!cd_same)
-            select_request<NT>(r, B, V, nch, rec, s_y, s_u, false, accept_len, out_tokens, num_tokens, alpha_out,
+            select_request<NT>(r, B, V, nch, C::kChunk, rec, s_y, s_u, false, accept_len, out_tokens, num_tokens, alpha_out,
                                p_out, q_out, awl_out, status, sel, s_rec);
         decide(r, sel);
-        if (s_owner == chunk) {
+        if (s_dec.owner == chunk) {
             const int c0 = chunk * C::kChunk, c1 = min(V, c0 + C::kChunk);
-            if (!cd_same || s_kind_used != sel.mode) {  // masses not kept (or the fallback kind)
+            if (!cd_same || s_dec.kind != sel.mode) {  // masses not kept (or the fallback kind)
                 const T *prow = target + ((size_t)r * B + sel.row) * V;
                 const T *qrow = draft + ((size_t)r * (B - 1) + (sel.mode == 0 ? sel.row : 0)) * V;
                 float a1, a2;
-                chunk_masses<T, NT>(prow, qrow, s_kind_used, c0, c1, c, sel, w, a1, a2);
+                chunk_masses<T, NT>(prow, qrow, s_dec.kind, c0, c1, c, sel, w, a1, a2);
             }
-            scan_owner<NT>(w, c0, s_rem, s_takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
+            scan_owner<NT>(w, c0, s_dec.rem, s_dec.takelast != 0, out_tokens + (size_t)r * B + sel.a, red);
             fused_match(r, sel.a);
-        } else if (s_owner < 0 && chunk == 0) {
+        } else if (s_dec.owner < 0 && chunk == 0) {
             if (threadIdx.x == 0) {
                 record_status(status, D3D_ERR_DEVICE_INPUT);
                 out_tokens[(size_t)r * B + sel.a] = 0;

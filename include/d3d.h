@@ -190,11 +190,12 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
  * later d3d_packed_draft_attn launch skip its first key-tile load, so the
  * consumer's bounded wait expires: the kernel records D3D_ERR_DEVICE_TIMEOUT
  * in the workspace status word, releases its resources and returns.  mode 2
- * makes every later d3d_spec_verify launch that streams bf16 rows through its
- * shared-memory ring (an sm_limit launch) skip the copies of CTA 0's first
- * item: that CTA's bounded wait expires, it records D3D_ERR_DEVICE_TIMEOUT,
- * waits out its other copies and leaves, and the request's other CTAs give
- * up their bounded waits.  The outputs of such a call are undefined and the
+ * makes every later d3d_spec_verify launch that copies logit rows into
+ * shared memory by bulk copies skip one copy of CTA 0: its first item's
+ * copies in the ring of an sm_limit launch over bf16 rows, or its first row
+ * in the vocabulary-slice launch.  That CTA's bounded wait expires, it
+ * records D3D_ERR_DEVICE_TIMEOUT, waits out its other copies and leaves, and
+ * the request's other CTAs give up their bounded waits.  The outputs of such a call are undefined and the
  * workspace must be re-initialised.  mode 0 (the default) restores normal
  * operation.  The setting is process-global and not thread-safe.
  */
@@ -289,6 +290,13 @@ int d3d_build_branches(const void *draft_logits, int logits_dtype, const int32_t
  *   out_tokens[r] = [y_0 .. y_{a-1}, t, -1, ...], num_tokens[r] = a + 1
  *   (the round's tau: accepted drafts plus the target's own token).
  *
+ * Launch shapes (results do not depend on them): when every request's rows
+ * split over the SMs the launch may use (sm_limit, else the device) with
+ * the 2B-1 rows of each vocabulary slice resident in one CTA's shared
+ * memory, each CTA holds one (request, slice) and reads its rows once;
+ * otherwise CTAs take (request, position, chunk) items and reload the
+ * sampled row.  Both wait on one another through the workspace.
+ *
  * Greedy verification, temperature == 0 ([D3D] "Experiments", [DScout]
  * "Experiments": the pages' results are greedy; the T -> 0 limit of the
  * rule above).  g_j = argmax_v target[r,j,v], ties to the lowest index;
@@ -322,7 +330,9 @@ int d3d_build_branches(const void *draft_logits, int logits_dtype, const int32_t
  *               "Background: asynchronous drafting and cache hits": each
  *               branch hypothesises an accepted prefix and its corrected
  *               token), so the match needs nothing from the drafting pass.
- *   ws          workspace, d3d_spec_verify_workspace_size() bytes
+ *   ws          workspace, d3d_spec_verify_workspace_size() bytes (enough
+ *               for every launch shape; a smaller one that still holds the
+ *               chunked launch's records makes the call take that shape)
  *   sm_limit    0: the kernel may use every SM.  n > 0: at most n CTAs, each
  *               holding a whole SM, so that a kernel running beside it (the
  *               drafting attention of the same round, launched as its
@@ -342,6 +352,15 @@ int d3d_build_branches(const void *draft_logits, int logits_dtype, const int32_t
 #define D3D_VERIFY_AFTER_INDEPENDENT 1
 
 size_t d3d_spec_verify_workspace_size(int R, int B, int V);
+
+/* Launch shape of d3d_spec_verify for these sizes on the current device,
+ * with 16-byte aligned logit pointers and a workspace of ws_bytes: the
+ * number of CTAs of the vocabulary-slice launch (R times the slices of a
+ * request; each holds one SM from its start to its end), or 0 when the call
+ * takes the chunked launch (or the greedy one, temperature == 0, or R == 0).
+ * D3D_ERR_INVALID_ARG for sizes d3d_spec_verify would reject. */
+int d3d_spec_verify_slice_ctas(int R, int B, int V, int logits_dtype, float temperature, int sm_limit,
+                               size_t ws_bytes);
 
 int d3d_spec_verify(const void *target_logits, const void *draft_logits, int logits_dtype,
                     const int32_t *draft_tokens, const float *u_accept, const float *u_sample, int R, int B,

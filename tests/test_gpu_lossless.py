@@ -66,3 +66,38 @@ def test_gpu_lossless_chi_square(d3d, T, dt, sm_limit):
     assert len(first) >= 1_000_000
     assert _chi2_p(first, P[0]) > 1e-4
     assert _chi2_p(second, P[1]) > 1e-4
+
+
+@pytest.mark.parametrize("dt", [W.DT_F32, W.DT_BF16])
+def test_gpu_lossless_chi_square_slice_launch(d3d, dt):
+    # the vocabulary-slice launch (38 requests of 4 slices of 64 entries over
+    # the whole device): >= 190,000 seeded trials; the sample's crossing falls
+    # in any of the four slices, so the decision across slices is exercised
+    V, B, R, T = 256, 3, 38, 1.0
+    assert d3d.d3d_spec_verify_slice_ctas(R, B, V, dt, T, 0) == 4 * R
+    rng = np.random.default_rng(78)
+    x = (rng.standard_normal((B, V)) * 1.5).astype(np.float32)
+    z = (x[: B - 1] + rng.standard_normal((B - 1, V))).astype(np.float32)
+    if dt == W.DT_BF16:
+        x, z = W.bf16_to_f32(W.bf16_bits(x)), W.bf16_to_f32(W.bf16_bits(z))
+    P = scipy.special.softmax(x.astype(np.float64) / T, axis=-1)
+    Q = scipy.special.softmax(z.astype(np.float64) / T, axis=-1)
+    tg = np.ascontiguousarray(np.broadcast_to(x, (R, B, V)))
+    dr = np.ascontiguousarray(np.broadcast_to(z, (R, B - 1, V)))
+    if dt == W.DT_BF16:
+        tg, dr = W.bf16_bits(tg), W.bf16_bits(dr)
+    first, second = [], []
+    ws = None
+    for call in range(5000):
+        r2 = np.random.default_rng(5000 + call)
+        y = np.stack([r2.choice(V, size=R, p=Q[j]) for j in range(B - 1)], axis=1).astype(np.int32)
+        u = W.uniform24(r2, (R, B))
+        v = dict(target=tg, draft=dr, dtype=dt, y=y, u_accept=np.ascontiguousarray(u[:, : B - 1]),
+                 u_sample=np.ascontiguousarray(u[:, B - 1]), R=R, B=B, V=V, temperature=T)
+        got, ws = run_verify(d3d, v, ws=ws, want_probs=False)
+        first.append(got["out_tokens"][:, 0])
+        second.append(got["out_tokens"][got["accept_len"] >= 1, 1])
+    first, second = np.concatenate(first), np.concatenate(second)
+    assert len(first) >= 190_000
+    assert _chi2_p(first, P[0]) > 1e-4
+    assert _chi2_p(second, P[1]) > 1e-4

@@ -286,6 +286,64 @@ def test_verify_sm_limit_same_results(d3d, sm_limit):
         assert d3d.d3d_workspace_status(ws2) == 0
 
 
+@pytest.mark.parametrize("cfg,over,sm_limit", [("async8b", {}, 0), ("async8b", {}, 56), ("async8b", dict(R=2), 0),
+                                              ("async8b", dict(R=4, B=4), 56), ("tiny", dict(R=38, V=256), 0),
+                                              ("long_block", {}, 0), ("async8b", dict(logits=W.DT_F32, V=32000), 0)])
+def test_verify_slice_launch_matches_oracle_and_chunked(d3d, cfg, over, sm_limit):
+    # one CTA per (request, vocabulary slice) with the slice's rows resident in
+    # shared memory; the same inputs under an SM limit of 8 (too few SMs for
+    # resident slices) take the chunked launch.  Both meet the oracle, and
+    # their probabilities agree to the last bits
+    v = W.verify_inputs(**dict(W.CONFIGS[cfg], **over), seed=71)
+    R, B, V, dt, T = v["R"], v["B"], v["V"], v["dtype"], v.get("temperature", 1.0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = d3d.d3d_spec_verify_slice_ctas(R, B, V, dt, T, sm_limit)
+    assert 0 < n <= (sm_limit or sms) and n % R == 0
+    got, ws = run_verify(d3d, v, sm_limit=sm_limit)
+    ref = oracle_verify(v)
+    compare_verify(got, ref, min_kept=0.75, what="%s slices %d" % (cfg, n))
+    assert d3d.d3d_workspace_status(ws) == 0
+    assert d3d.d3d_spec_verify_slice_ctas(R, B, V, dt, T, 8) == 0
+    chunked, _ = run_verify(d3d, v, sm_limit=8)
+    compare_verify(chunked, ref, min_kept=0.75, what="%s chunked" % cfg)
+    for k in ("alpha", "p", "q"):
+        np.testing.assert_allclose(got[k], chunked[k], rtol=1e-6, atol=1e-30, err_msg=k)
+
+
+def test_verify_slice_shapes(d3d):
+    # the slice launch needs 16-byte aligned rows and each slice's rows in one
+    # CTA's shared memory; otherwise (and at temperature 0) the chunked or
+    # greedy launch runs
+    bf, f = W.DT_BF16, W.DT_F32
+    assert d3d.d3d_spec_verify_slice_ctas(1, 16, 151936, bf, 1.0, 56) == 56
+    assert d3d.d3d_spec_verify_slice_ctas(1, 16, 151936, bf, 0.0, 56) == 0
+    assert d3d.d3d_spec_verify_slice_ctas(2, 16, 70001, bf, 1.0, 0) == 0    # rows not 16-byte aligned
+    assert d3d.d3d_spec_verify_slice_ctas(24, 16, 151936, bf, 1.0, 0) == 0  # slices too wide for shared memory
+    assert d3d.d3d_spec_verify_slice_ctas(0, 16, 151936, bf, 1.0, 0) == 0
+    small = d3d.d3d_spec_verify_workspace_size(1, 16, 151936) // 8
+    assert d3d.d3d_spec_verify_slice_ctas(1, 16, 151936, bf, 1.0, 0, ws_bytes=small) == 0  # too little workspace
+    assert d3d.d3d_spec_verify_slice_ctas(3, 5, 1000, f, 0.7, 0) > 0
+
+
+def test_verify_slice_wait_runs_out_reports_status_and_context_survives(d3d):
+    # failure detection without a GPU fault: in the slice launch CTA 0 never
+    # issues its first row's copy, its bounded wait runs out, it records the
+    # timeout, waits out its other copies and leaves; the other CTAs give up
+    # their bounded waits.  The next call, on a re-initialised workspace, is correct
+    v = W.verify_inputs(**W.CONFIGS["async8b"], seed=13)
+    assert d3d.d3d_spec_verify_slice_ctas(1, 16, 151936, W.DT_BF16, 1.0, 56) > 0
+    d3d.d3d_debug_inject_fault(2)
+    try:
+        _, ws = run_verify(d3d, v, sm_limit=56)
+    finally:
+        d3d.d3d_debug_inject_fault(0)
+    assert d3d.d3d_workspace_status(ws, clear=True) == d3d.D3D_ERR_DEVICE_TIMEOUT
+    d3d.d3d_workspace_init(ws)
+    got, _ = run_verify(d3d, v, ws=ws, sm_limit=56)
+    compare_verify(got, oracle_verify(v), min_kept=1.0, what="slices, after a timed-out call")
+    assert d3d.d3d_workspace_status(ws) == 0
+
+
 def _heads_hitting(ref, B, V, M, seed):
     """Branch heads for a verification batch: random heads of every length plus,
     for most requests, one copy of the oracle's verified tokens (a planted hit)

@@ -68,9 +68,11 @@ def _same(got, ref):
 
 def test_noalloc_matches_workspace_entry_point_twice(d3d):
     # call 1: the 16-request serving batch; call 2: another shape, dtype and
-    # temperature, so anything the first call left behind would show
+    # temperature, so anything the first call left behind would show; call 3:
+    # one request, which takes the vocabulary-slice launch
     calls = [W.verify_inputs(**W.CONFIGS["serve32b"], seed=21),
-             W.verify_inputs(R=64, B=5, V=12345, logits=W.DT_F32, seed=22, temperature=0.7)]
+             W.verify_inputs(R=64, B=5, V=12345, logits=W.DT_F32, seed=22, temperature=0.7),
+             W.verify_inputs(**W.CONFIGS["async8b"], seed=24)]
     for v in calls:
         ref, _ = run_verify(d3d, v)
         got = _noalloc_via_abi(d3d, v)
