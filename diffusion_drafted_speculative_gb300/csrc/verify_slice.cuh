@@ -168,29 +168,38 @@ __device__ __forceinline__ void verify_slice_body(const VArgs &a, int W, int nS)
     __shared__ Decision s_dec;
     __shared__ int s_cand, s_lastpos;
 
-    if (threadIdx.x == 0) {
+    // a kernel launched after this one as an independent programmatic
+    // dependent (the round's drafting attention) may start at once
+    if (threadIdx.x == 0)
         sm100::pdl_trigger();
-        for (int i = 0; i < nrows; ++i)
-            sm100::mbar_init(bars_s + 8u * (uint32_t)i, 1);
+    // ---- 1. the slice's rows into shared memory (rows are 16-byte aligned and
+    // the slice is a multiple of 16 bytes: checked by the host): thread i
+    // initialises row i's mbarrier and issues its bulk copy, before anything
+    // else, so that the copies are in flight while the request's inputs load
+    const uint32_t row_bytes = (uint32_t)n * (uint32_t)sizeof(T);
+    for (int i = threadIdx.x; i < nrows; i += kSliceThreads) {
+        const uint32_t b = bars_s + 8u * (uint32_t)i;
+        sm100::mbar_init(b, 1);
         sm100::fence_barrier_init();
+        if (a.fault == 2 && blockIdx.x == 0 && i == 0)
+            continue;  // injected fault: this row's copy never arrives
+        const T *src = (i < B) ? target + ((size_t)r * B + i) * V + v0
+                               : draft + ((size_t)r * (B - 1) + (i - B)) * V + v0;
+        sm100::mbar_arrive_expect_tx(b, row_bytes);
+        sm100::bulk_load(rows_s + (uint32_t)i * (uint32_t)W * (uint32_t)sizeof(T), src, row_bytes, b);
+    }
+    if (threadIdx.x == 0)
         s_abort = 0;
+    // the branch heads of the fused match go to L2 now (read once the token is known)
+    if (a.branch != nullptr) {
+        const int32_t *h = a.heads + (size_t)r * M * B;
+        for (int o = (int)threadIdx.x * 32; o < M * B; o += kSliceThreads * 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(h + o));
+        if (threadIdx.x == 0 && M > 0)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.head_len + (size_t)r * M));
     }
     load_request_inputs<kSliceThreads>(r, B, a.y, a.u_acc, a.u_s, s_y, s_u, &s_us);
     __syncthreads();
-    // ---- 1. the slice's rows into shared memory (rows are 16-byte aligned and
-    // the slice is a multiple of 16 bytes: checked by the host)
-    const uint32_t row_bytes = (uint32_t)n * (uint32_t)sizeof(T);
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < nrows; ++i) {
-            if (a.fault == 2 && blockIdx.x == 0 && i == 0)
-                continue;  // injected fault: this row's copy never arrives
-            const T *src = (i < B) ? target + ((size_t)r * B + i) * V + v0
-                                   : draft + ((size_t)r * (B - 1) + (i - B)) * V + v0;
-            const uint32_t b = bars_s + 8u * (uint32_t)i;
-            sm100::mbar_arrive_expect_tx(b, row_bytes);
-            sm100::bulk_load(rows_s + (uint32_t)i * (uint32_t)W * (uint32_t)sizeof(T), src, row_bytes, b);
-        }
-    }
     // bounded wait for row i (the whole warp); false when it or another wait ran out
     auto wait_row = [&](int i) -> bool {
         const uint32_t b = bars_s + 8u * (uint32_t)i;
