@@ -215,10 +215,15 @@ void d3d_debug_inject_fault(int mode);
  *   temperature > 0 (else D3D_ERR_INVALID_ARG)
  *   accept_prob [R, B-1] float32 output; survival [R, B-1] and tau [R]
  *               float32 outputs, each may be NULL
- *   ws          d3d_accept_probs_workspace_size() bytes
- * Two launches on the stream (the second a programmatic dependent of the
- * first); fp32 arithmetic, sums in a fixed order (results do not depend on
- * scheduling); a_j is clamped to 1.  2 <= B <= 257 (B > 257:
+ *   ws          d3d_accept_probs_workspace_size() bytes (enough for either
+ *               shape; a smaller one that still holds the two launches'
+ *               chunk records makes the call take that shape)
+ * When each request's rows split over the device's SMs with the 2(B-1) rows
+ * of a vocabulary slice resident in one CTA's shared memory: one cooperative
+ * launch, one CTA per (request, slice), the logits read once.  Otherwise two
+ * launches on the stream (the second a programmatic dependent of the first),
+ * the logits read twice.  fp32 arithmetic, sums in a fixed order (results do
+ * not depend on scheduling); a_j is clamped to 1.  2 <= B <= 257 (B > 257:
  * D3D_ERR_UNSUPPORTED).
  * ======================================================================== */
 size_t d3d_accept_probs_workspace_size(int R, int B, int V);

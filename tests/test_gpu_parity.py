@@ -759,6 +759,30 @@ def test_accept_probs_and_tau_match_oracle(d3d, cfg, over):
         np.testing.assert_array_equal(x, y)
 
 
+def test_accept_probs_slice_and_two_launch_shapes_agree(d3d):
+    # one request: the slice launch (rows read once) with the full workspace;
+    # a workspace that holds only the two launches' chunk records takes those
+    from gpu_util import bf16
+    v = W.verify_inputs(**W.CONFIGS["async8b"], seed=72)
+    R, B, V = v["R"], v["B"], v["V"]
+    tg, dr = bf16(v["target"]), bf16(v["draft"])
+    full = d3d.d3d_accept_probs_workspace_size(R, B, V)
+    res = []
+    for nbytes in (full, full // 8):
+        ws = d3d.new_workspace(nbytes)
+        a = torch.full((R, B - 1), float("nan"), device="cuda")
+        tau = torch.full((R,), float("nan"), device="cuda")
+        d3d.d3d_accept_probs(tg, dr, 1.0, a, ws, tau=tau)
+        torch.cuda.synchronize()
+        assert d3d.d3d_workspace_status(ws) == 0
+        res.append((a.cpu().numpy(), tau.cpu().numpy()))
+    ref = oracle.accept_probs(v)
+    for a, tau in res:
+        np.testing.assert_allclose(a, ref["accept_prob"], rtol=1e-4, atol=2e-6)
+        np.testing.assert_allclose(tau, ref["tau"], rtol=2e-4)
+    np.testing.assert_allclose(res[0][0], res[1][0], rtol=1e-5, atol=1e-7)
+
+
 def test_verify_workspace_reuse_and_many_requests(d3d):
     v = W.verify_inputs(R=4096, B=4, V=64, logits=W.DT_F32, seed=10)
     got1, ws = run_verify(d3d, v)
