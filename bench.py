@@ -59,12 +59,10 @@ CSRC = os.path.join(ROOT, "diffusion_drafted_speculative_gb300", "csrc")
 NCU_TRAFFIC = {
     ("async8b", "attn"): {"sources": ("attn.cu", "attn_common.cuh", "sm100_ptx.cuh", "d3d_common.cuh",
                                       "verify_body.cuh"),
-                          "sha": "21be421b59f172a0", "bytes": 13180928},
-    ("async8b", "verify"): {"sources": ("verify.cu", "verify_body.cuh", "sm100_ptx.cuh", "d3d_common.cuh"),
-                            "sha": "802f314046cc7507", "bytes": 9547776},
-    ("async8b", "greedy"): {"sources": ("verify.cu", "greedy_body.cuh", "verify_body.cuh", "sm100_ptx.cuh",
+                          "sha": "016c81580e70ad9a", "bytes": 13178880},
+    ("async8b", "verify"): {"sources": ("verify.cu", "verify_slice.cuh", "verify_body.cuh", "sm100_ptx.cuh",
                                         "d3d_common.cuh"),
-                            "sha": "e5969c79af57e049", "bytes": 4903168},
+                            "sha": "c0d20894a1c2335c", "bytes": 9490432},
 }
 
 

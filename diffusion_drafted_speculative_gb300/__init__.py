@@ -23,7 +23,7 @@ __all__ = [
     "AttnCall", "VerifyCall", "d3d_build_branches", "d3d_build_branches_workspace_size",
     "d3d_accept_probs", "d3d_accept_probs_workspace_size", "d3d_branch_match", "d3d_workspace_status", "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
     "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
-    "D3D_ERR_DEVICE_TIMEOUT", "D3D_ERR_DEVICE_INPUT", "D3D_DTYPE_F32", "D3D_DTYPE_BF16",
+    "D3D_ERR_DEVICE_TIMEOUT", "D3D_ERR_DEVICE_INPUT", "D3D_ERR_INTERNAL", "D3D_DTYPE_F32", "D3D_DTYPE_BF16",
     "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR", "D3D_ATTN_AFTER_INDEPENDENT", "D3D_VERIFY_AFTER_INDEPENDENT",
 ]
 
@@ -34,6 +34,7 @@ D3D_ERR_WORKSPACE = -3
 D3D_ERR_CUDA = -4
 D3D_ERR_DEVICE_TIMEOUT = -5
 D3D_ERR_DEVICE_INPUT = -6
+D3D_ERR_INTERNAL = -7
 D3D_DTYPE_F32 = 0
 D3D_DTYPE_BF16 = 1
 D3D_SEG_CAUSAL = 0
@@ -42,7 +43,9 @@ D3D_ATTN_AFTER_INDEPENDENT = 1
 D3D_VERIFY_AFTER_INDEPENDENT = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libd3d.so")
+# D3D_LIBRARY=debug selects the build with device-side internal index checks
+# (libd3d_debug.so, built beside libd3d.so; same entry points and results)
+LIB_PATH = os.path.join(_HERE, "libd3d_debug.so" if os.environ.get("D3D_LIBRARY") == "debug" else "libd3d.so")
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 # name -> (restype, argtypes): every symbol declared in include/d3d.h
@@ -81,8 +84,9 @@ class D3DError(RuntimeError):
 
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
-        raise ImportError("libd3d.so is not built (expected at %s); run "
-                          "`python diffusion_drafted_speculative_gb300/build.py` (or __graft_entry__.build())" % LIB_PATH)
+        raise ImportError("%s is not built (expected at %s); run "
+                          "`python diffusion_drafted_speculative_gb300/build.py` (or __graft_entry__.build())"
+                          % (os.path.basename(LIB_PATH), LIB_PATH))
     so = ctypes.CDLL(LIB_PATH)
     for name, (res, args) in EXPORTED.items():
         fn = getattr(so, name)

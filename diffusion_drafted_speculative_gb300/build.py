@@ -1,8 +1,10 @@
 """Build the C-ABI CUDA library ``libd3d.so`` in-tree for sm_103a (GB300).
 
 Each ``csrc/*.cu`` file is compiled by nvcc in parallel into ``_build/`` and
-linked into ``libd3d.so`` next to this file.  Rebuilds only when a source or
-header is newer than the library.  Run ``python
+linked into ``libd3d.so`` next to this file; ``debug=True`` builds
+``libd3d_debug.so`` the same way with the device-side internal index checks
+(``-DD3D_DEBUG_CHECKS``; objects in ``_build/debug/``).  Rebuilds only when a
+source or header is newer than the library.  Run ``python
 diffusion_drafted_speculative_gb300/build.py`` (this file imports nothing from
 the package, whose import needs the built library) or call :func:`build`.
 """
@@ -21,6 +23,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libd3d.so")
+LIB_DEBUG = os.path.join(HERE, "libd3d_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
@@ -42,23 +45,25 @@ def _inputs() -> list[str]:
     return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB):
+def stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile and link libd3d.so; returns its path."""
-    if not force and not stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None, debug: bool = False) -> str:
+    """Compile and link libd3d.so (libd3d_debug.so with debug=True); returns its path."""
+    lib = LIB_DEBUG if debug else LIB
+    if not force and not stale(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
-    extra = list(extra or [])
+    out_dir = os.path.join(BUILD, "debug") if debug else BUILD
+    os.makedirs(out_dir, exist_ok=True)
+    extra = list(extra or []) + (["-DD3D_DEBUG_CHECKS"] if debug else [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -71,15 +76,16 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".%d.tmp" % os.getpid()
+    tmp = lib + ".%d.tmp" % os.getpid()
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (res.stdout, res.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     v = "-v" in sys.argv
-    print(build(force="-f" in sys.argv, verbose=v, extra=["-Xptxas", "-v"] if v else None))
+    print(build(force="-f" in sys.argv, verbose=v, extra=["-Xptxas", "-v"] if v else None,
+                debug="--debug" in sys.argv))

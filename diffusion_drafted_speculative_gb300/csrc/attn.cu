@@ -459,7 +459,9 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
     // output row of staged row i of the query tile, or null beyond the request
     auto out_row = [&](int i) -> uint16_t * {
         const int tok = mt * p.TQ + i / p.G;
-        return tok < b.n_q ? p.out + ((size_t)(b.q0 + tok) * p.Hq + hk * p.G + (i % p.G)) * D : nullptr;
+        if (tok >= b.n_q || !dbg_ok(b.q0 + tok < p.total_q && hk * p.G + (i % p.G) < p.Hq, status))
+            return nullptr;
+        return p.out + ((size_t)(b.q0 + tok) * p.Hq + hk * p.G + (i % p.G)) * D;
     };
 
     if (warp == kTmaWarp) {
@@ -489,7 +491,11 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
                 return true;
             }
             bool pre;
-            const int row = tile_row(k, pre);
+            int row = tile_row(k, pre);
+            // debug build: the tile's first row lies in the request's prefix or
+            // packed rows (else the copy reads row 0 and the status says so)
+            if (!dbg_ok(pre ? (row >= b.p0 && row < b.p0 + b.L) : (row >= b.q0 && row < b.q0 + b.n_q), status))
+                row = 0;
             const CUtensorMap *m = is_k ? (pre ? tm_kp : tm_kn) : (pre ? tm_vp : tm_vn);
             const uint32_t dst = (is_k ? sK : sV) + s * Lay::kKBytes;
             if (leader) {
@@ -1227,7 +1233,9 @@ __device__ __forceinline__ void attn_pair_body(unsigned unit, const CUtensorMap 
     // output row of staged pair row i (tile i / 128), or null beyond the request
     auto out_row = [&](int i) -> uint16_t * {
         const int tok = (mt0 + (i >> 7)) * p.TQ + (i & 127) / p.G;
-        return tok < b.n_q ? p.out + ((size_t)(b.q0 + tok) * p.Hq + hk * p.G + ((i & 127) % p.G)) * D : nullptr;
+        if (tok >= b.n_q || !dbg_ok(b.q0 + tok < p.total_q && hk * p.G + ((i & 127) % p.G) < p.Hq, status))
+            return nullptr;
+        return p.out + ((size_t)(b.q0 + tok) * p.Hq + hk * p.G + ((i & 127) % p.G)) * D;
     };
 
 
@@ -1260,7 +1268,11 @@ __device__ __forceinline__ void attn_pair_body(unsigned unit, const CUtensorMap 
                 return true;
             }
             bool pre;
-            const int row = tile_row(k, pre);
+            int row = tile_row(k, pre);
+            // debug build: the tile's first row lies in the request's prefix or
+            // packed rows (else the copy reads row 0 and the status says so)
+            if (!dbg_ok(pre ? (row >= b.p0 && row < b.p0 + b.L) : (row >= b.q0 && row < b.q0 + b.n_q), status))
+                row = 0;
             const CUtensorMap *m = is_k ? (pre ? tm_kp : tm_kn) : (pre ? tm_vp : tm_vn);
             const uint32_t dst = (is_k ? sK : sV) + s * Lay::kKBytes;
             if (leader) {

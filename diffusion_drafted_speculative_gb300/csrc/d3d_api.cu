@@ -17,6 +17,7 @@ const char *d3d_status_string(int status)
     case D3D_ERR_CUDA: return "CUDA runtime error at enqueue time";
     case D3D_ERR_DEVICE_TIMEOUT: return "device: bounded wait expired";
     case D3D_ERR_DEVICE_INPUT: return "device: input data out of range";
+    case D3D_ERR_INTERNAL: return "device: internal index check failed (debug build)";
     default: return "unknown status";
     }
 }

@@ -28,6 +28,24 @@ __device__ inline void record_status(int32_t *status, int32_t code)
     atomicCAS(reinterpret_cast<int *>(status), D3D_OK, code);
 }
 
+// Internal index checks of the debug build (compiled with D3D_DEBUG_CHECKS):
+// a failed check records D3D_ERR_INTERNAL in the status word and returns
+// false, and the caller skips the access; it never traps.  In the normal
+// build the check is compiled out and returns true.
+#ifdef D3D_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+__device__ __forceinline__ bool dbg_ok(bool cond, int32_t *status)
+{
+    if (kDebugChecks && !cond) {
+        record_status(status, D3D_ERR_INTERNAL);
+        return false;
+    }
+    return true;
+}
+
 __device__ inline float bf16_bits_to_float(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
 // One logit as float (f32, or bf16 bits: exact), read through the read-only path.

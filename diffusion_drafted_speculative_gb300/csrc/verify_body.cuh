@@ -1056,7 +1056,7 @@ __device__ __forceinline__ void verify_body(unsigned vb, unsigned vgrid, const V
         }
         // the record and its signal after the barrier: the release's wait
         // overlaps the next item's loads and exponentials in the other warps
-        if (threadIdx.x == 0) {
+        if (threadIdx.x == 0 && dbg_ok(item < nA, reinterpret_cast<int32_t *>(ws))) {
             float4 *dst = reinterpret_cast<float4 *>(rec + item);
             dst[0] = make_float4(m1, z1, m2, z2);
             dst[1] = make_float4(xyP, xyQ, 0.f, 0.f);

@@ -234,7 +234,7 @@ __device__ __forceinline__ void verify_slice_body(const VArgs &a, int W, int nS)
             if (has_y)
                 xQ = SliceVec<T>::at(row_of(B + j), yv - v0) * c;
         }
-        if (lane == 0) {
+        if (lane == 0 && dbg_ok(r < a.R && s < nS && ((size_t)r * B + j) * nS + s < (size_t)a.R * B * nS, status)) {
             float4 *dst = reinterpret_cast<float4 *>(rec + ((size_t)r * B + j) * nS + s);
             dst[0] = make_float4(mP, zP, mQ, zQ);
             dst[1] = make_float4(xP, xQ, 0.f, 0.f);
@@ -375,9 +375,10 @@ __device__ __forceinline__ void verify_slice_body(const VArgs &a, int W, int nS)
             // rounding between the two summation orders: the run's last position with mass
             if (tok < 0)
                 tok = last >= 0 ? last : s_lastpos;
-            *out_tok = tok;
+            if (dbg_ok(tok >= v0 && tok < v1, status))
+                *out_tok = tok;
         }
-        if ((takelast || cand == 0x7fffffff) && threadIdx.x == 0)
+        if ((takelast || cand == 0x7fffffff) && threadIdx.x == 0 && dbg_ok(s_lastpos >= v0 && s_lastpos < v1, status))
             *out_tok = s_lastpos;
         __syncthreads();
         if (a.branch != nullptr && threadIdx.x < 32) {

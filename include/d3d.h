@@ -49,6 +49,8 @@ extern "C" {
 #define D3D_ERR_CUDA (-4)            /* a CUDA runtime call failed at enqueue time   */
 #define D3D_ERR_DEVICE_TIMEOUT (-5)  /* device status: a bounded wait expired        */
 #define D3D_ERR_DEVICE_INPUT (-6)    /* device status: device-side data out of range */
+#define D3D_ERR_INTERNAL (-7)        /* device status, debug build only: an internal
+                                        index check failed (the access was skipped)  */
 
 /* ---- enums -------------------------------------------------------------- */
 #define D3D_DTYPE_F32 0

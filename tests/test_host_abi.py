@@ -253,3 +253,18 @@ def test_noalloc_limit_edge_in_workspace_sizes(d3d):
     assert d3d.d3d_spec_verify_workspace_size(211, 16, 151936) <= 2 << 20
     assert d3d.d3d_spec_verify_workspace_size(212, 16, 151936) > 2 << 20
 
+
+
+def test_debug_build_exports_every_symbol(d3d):
+    # the build with device-side internal index checks has the same entry points
+    import __graft_entry__
+
+    path = __graft_entry__._build_module().build(debug=True)
+    assert os.path.basename(path) == "libd3d_debug.so"
+    so = ctypes.CDLL(path)
+    for name in _header_functions():
+        assert hasattr(so, name), name
+    fn = so.d3d_status_string
+    fn.restype = ctypes.c_char_p
+    fn.argtypes = [ctypes.c_int]
+    assert b"internal index check" in fn(d3d.D3D_ERR_INTERNAL)
