@@ -350,28 +350,9 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
     if (tid == 0)
         pdl_trigger();
 
-    // early exits are uniform over the CTAs of a cluster (same r and tile).
-    // Every exit first waits for a kernel this launch overlaps (programmatic
-    // dependent launch): the stream moves on only when both have finished.
-    ReqBounds b;
-    if (!request_bounds(p.cu_prefix, p.cu_q, p.cu_seg, r, p.max_q, p.max_prefix, p.total_q, p.total_prefix,
-                        p.total_segs, b)) {
-        if (tid == 0 && sp == 0)
-            record_status(status, D3D_ERR_DEVICE_INPUT);
-        pdl_wait();
-        return;
-    }
-    if (mt * p.TQ >= b.n_q) {
-        pdl_wait();
-        return;
-    }
-
-    // ---- this split's key list: prefix tiles [pb, pe), then (last split only) packed tiles
-    const int nP = (b.L + kBN - 1) / kBN;
-    const int pb = split_prefix_begin(sp, p.S, nP, p.PK);
-    const int pe = (sp == p.S - 1) ? nP : split_prefix_begin(sp + 1, p.S, nP, p.PK);
-    const int n_pre = pe - pb;
-    const bool last_split = sp == p.S - 1;
+    // the request's offsets: loaded now, checked once the setup below is done
+    // (the setup does not depend on them and hides their latency)
+    ReqRaw braw = load_bounds(p.cu_prefix, p.cu_q, p.cu_seg, r);
 
     // ---- shared memory carve-up (1024-byte aligned base for the swizzled tiles)
     const uint32_t raw = smem_u32(smem_raw);
@@ -424,6 +405,31 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+
+    // the offsets are used only from here on (the empty asm keeps the compiler
+    // from moving their first use, and so the wait for the loads, above the
+    // barrier).  Early exits are uniform over the CTAs of a cluster (same r
+    // and tile) and come before any copy or cluster barrier; every exit first
+    // waits for a kernel this launch overlaps (programmatic dependent launch):
+    // the stream moves on only when both have finished.
+    asm volatile("" : "+r"(braw.q0), "+r"(braw.q1), "+r"(braw.p0), "+r"(braw.p1), "+r"(braw.s0), "+r"(braw.s1));
+    ReqBounds b;
+    const bool bounds_ok = check_bounds(braw, p.max_q, p.max_prefix, p.total_q, p.total_prefix, p.total_segs, b);
+    if (!bounds_ok || mt * p.TQ >= b.n_q) {
+        if (!bounds_ok && tid == 0 && sp == 0)
+            record_status(status, D3D_ERR_DEVICE_INPUT);
+        if (warp == kMmaWarp)
+            tmem_dealloc(tmem, kTmemCols);
+        pdl_wait();
+        return;
+    }
+
+    // ---- this split's key list: prefix tiles [pb, pe), then (last split only) packed tiles
+    const int nP = (b.L + kBN - 1) / kBN;
+    const int pb = split_prefix_begin(sp, p.S, nP, p.PK);
+    const int pe = (sp == p.S - 1) ? nP : split_prefix_begin(sp + 1, p.S, nP, p.PK);
+    const int n_pre = pe - pb;
+    const bool last_split = sp == p.S - 1;
 
     // number of packed tiles of the query tile; waits for the mask on first use
     // (called by whole warps: the vote keeps the answer warp-uniform)
