@@ -121,7 +121,29 @@ struct AttnParams {
     int max_q, max_prefix, total_q, total_prefix, total_segs;
     float scale_log2;
     int fault;
+    // one request whose offsets the contract fixes (cu_*[0] = 0, cu_*[1] = the
+    // totals, within max_q / max_prefix): the kernel takes them from here and
+    // checks the device arrays against them in its epilogue
+    int one_request;
 };
+
+// The bounds of request r: for a single request the documented offsets
+// (known on the host), otherwise from the device arrays (ok = false when they
+// lie).  For a single request `ok` only says the host values are usable; the
+// arrays are compared with them later (one_request_matches).
+__device__ __forceinline__ bool kernel_bounds(const AttnParams &p, const ReqRaw &braw, ReqBounds &b)
+{
+    if (p.one_request) {
+        b.q0 = 0, b.n_q = p.total_q, b.p0 = 0, b.L = p.total_prefix, b.s0 = 0, b.s1 = p.total_segs;
+        return true;
+    }
+    return check_bounds(braw, p.max_q, p.max_prefix, p.total_q, p.total_prefix, p.total_segs, b);
+}
+__device__ __forceinline__ bool one_request_matches(const AttnParams &p, const ReqRaw &w)
+{
+    return w.q0 == 0 && w.q1 == p.total_q && w.p0 == 0 && w.p1 == p.total_prefix && w.s0 == 0 &&
+           w.s1 == p.total_segs;
+}
 
 __device__ __forceinline__ float ex2(float x)
 {
@@ -412,9 +434,10 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
     // and tile) and come before any copy or cluster barrier; every exit first
     // waits for a kernel this launch overlaps (programmatic dependent launch):
     // the stream moves on only when both have finished.
-    asm volatile("" : "+r"(braw.q0), "+r"(braw.q1), "+r"(braw.p0), "+r"(braw.p1), "+r"(braw.s0), "+r"(braw.s1));
+    if (!p.one_request)  // a single request's bounds come from the host: nothing to wait for here
+        asm volatile("" : "+r"(braw.q0), "+r"(braw.q1), "+r"(braw.p0), "+r"(braw.p1), "+r"(braw.s0), "+r"(braw.s1));
     ReqBounds b;
-    const bool bounds_ok = check_bounds(braw, p.max_q, p.max_prefix, p.total_q, p.total_prefix, p.total_segs, b);
+    const bool bounds_ok = kernel_bounds(p, braw, b);
     if (!bounds_ok || mt * p.TQ >= b.n_q) {
         if (!bounds_ok && tid == 0 && sp == 0)
             record_status(status, D3D_ERR_DEVICE_INPUT);
@@ -815,7 +838,11 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
         wait_drain(bar(B_DONE), 0, status);
         // (max, column-half sum, tiles done) of this thread's row; a negative sum
         // marks a void row (failed descriptor check or an abandoned wait)
-        s_ml[w * kBM + row] = make_float4(m_ref, (aborted || row_bad) ? -1.f : l, (float)n_done, 0.f);
+        // a single request whose device offsets disagree with the host's: every row is void
+        const bool bad_req = p.one_request && !one_request_matches(p, braw);
+        if (bad_req && tid == 0 && sp == 0)
+            record_status(status, D3D_ERR_DEVICE_INPUT);
+        s_ml[w * kBM + row] = make_float4(m_ref, (aborted || row_bad || bad_req) ? -1.f : l, (float)n_done, 0.f);
         tc_fence_before();
         asm volatile("bar.sync 2, %0;" ::"n"(kSoftmaxThreads) : "memory");
         tc_fence_after();
@@ -1186,9 +1213,10 @@ __device__ __forceinline__ void attn_pair_body(unsigned unit, const CUtensorMap 
     // from moving their first use, and so the wait for the loads, above the
     // barrier); early exits are uniform over the CTAs of a cluster (same r and
     // pair) and come before any copy or cluster barrier
-    asm volatile("" : "+r"(braw.q0), "+r"(braw.q1), "+r"(braw.p0), "+r"(braw.p1), "+r"(braw.s0), "+r"(braw.s1));
+    if (!p.one_request)  // a single request's bounds come from the host: nothing to wait for here
+        asm volatile("" : "+r"(braw.q0), "+r"(braw.q1), "+r"(braw.p0), "+r"(braw.p1), "+r"(braw.s0), "+r"(braw.s1));
     ReqBounds b;
-    const bool bounds_ok = check_bounds(braw, p.max_q, p.max_prefix, p.total_q, p.total_prefix, p.total_segs, b);
+    const bool bounds_ok = kernel_bounds(p, braw, b);
     if (!bounds_ok || mt0 * p.TQ >= b.n_q) {
         if (!bounds_ok && tid == 0 && sp == 0)
             record_status(status, D3D_ERR_DEVICE_INPUT);
@@ -1594,7 +1622,11 @@ __device__ __forceinline__ void attn_pair_body(unsigned unit, const CUtensorMap 
 
         // ---- epilogue: every MMA done; the thread owns its whole row
         wait_drain(bar(P_DONE), 0, status);
-        const bool void_row = aborted || row_bad;
+        // a single request whose device offsets disagree with the host's: every row is void
+        const bool bad_req = p.one_request && !one_request_matches(p, braw);
+        if (bad_req && tid == 0 && sp == 0)
+            record_status(status, D3D_ERR_DEVICE_INPUT);
+        const bool void_row = aborted || row_bad || bad_req;
         const float inv = (void_row || !(l > 0.f)) ? 0.f : 1.f / l;
         const bool have = n_done > 0;
         const int prow = t * kBM + row;
@@ -2009,6 +2041,7 @@ int attn_prepare(const void *q, const void *k_prefix, const void *v_prefix, cons
     prm.total_segs = total_segs;
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.fault = fault_mode();
+    prm.one_request = R == 1 && total_q <= max_q && total_prefix <= max_prefix;
     return D3D_OK;
 }
 

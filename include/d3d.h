@@ -125,9 +125,14 @@ int d3d_validate_segments(const d3d_segment_t *segs, const int32_t *cu_q, const 
  *   k_packed    [total_q, Hkv, d] bf16     keys/values of the packed tokens
  *   v_packed    [total_q, Hkv, d] bf16
  *   segs        [total_segs] d3d_segment_t (device)
- *   cu_prefix   [R+1] int32 (device) prefix row offsets, cu_prefix[R] = total_prefix
- *   cu_q        [R+1] int32 (device) packed row offsets, cu_q[R] = total_q
- *   cu_seg      [R+1] int32 (device) segment offsets, cu_seg[R] = total_segs
+ *   cu_prefix   [R+1] int32 (device) prefix row offsets, cu_prefix[0] = 0,
+ *               cu_prefix[R] = total_prefix
+ *   cu_q        [R+1] int32 (device) packed row offsets, cu_q[0] = 0, cu_q[R] = total_q
+ *   cu_seg      [R+1] int32 (device) segment offsets, cu_seg[0] = 0,
+ *               cu_seg[R] = total_segs.  With R == 1 these fix every offset,
+ *               so the kernel starts from the totals and checks the arrays
+ *               against them afterwards (a mismatch: D3D_ERR_DEVICE_INPUT in
+ *               the status word and a zero output)
  *   max_q, max_prefix  host upper bounds of any request's packed / prefix
  *               length (they size the grid; a request beyond them is a
  *               device input error); max_q <= 8192 (64 tiles of 128 rows,

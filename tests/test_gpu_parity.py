@@ -193,6 +193,25 @@ def test_attn_many_splits_and_bad_descriptor(d3d):
     assert_attn_close(got2[~rows], oracle.packed_attn(a)[~rows], "other rows")
 
 
+@pytest.mark.parametrize("Hq", [32, 64])
+def test_attn_single_request_offsets_checked(d3d, Hq):
+    # one request: the kernel takes its offsets from the totals (the contract
+    # fixes them) and checks the device arrays afterwards; 32 query heads run
+    # the one-tile kernel, 64 the two-tile one.  Offsets that disagree with
+    # the totals void the whole output and set the status
+    a = W.attn_inputs(R=1, L=1024, Hq=Hq, Hkv=8, d=128, B=16, C=12, F=2, layout="async", seed=9)
+    got, ws = run_attn(d3d, a)
+    heads = [0, 5, Hq - 1]
+    assert_attn_close(got[:, heads], _oracle_heads(a, heads)[:, heads], "single request")
+    assert d3d.d3d_workspace_status(ws) == 0
+    for key, val in (("cu_prefix", [0, int(a["cu_prefix"][1]) - 128]), ("cu_q", [0, int(a["cu_q"][1]) - 16]),
+                     ("cu_seg", [0, int(a["cu_seg"][1]) - 1])):
+        bad = dict(a, **{key: np.array(val, dtype=np.int32)})
+        got2, ws2 = run_attn(d3d, bad)
+        assert d3d.d3d_workspace_status(ws2, clear=True) == d3d.D3D_ERR_DEVICE_INPUT, key
+        assert (got2 == 0).all(), key
+
+
 # ------------------------------------------------------------------ verification
 @pytest.mark.parametrize("seed", range(3))
 def test_verify_tiny_config_batched(d3d, seed):
