@@ -21,28 +21,33 @@
 //              row max, a rescale of its part of O in TMEM only when the max
 //              grows by more than 2^8, the exponentials (arguments and sums in
 //              packed f32x2 arithmetic), its part of the row sum, and P as
-//              bf16 pairs written over the first half of the S buffer.
+//              bf16 pairs written over the first half of the S buffer.  Once
+//              at the start each thread also copies its half of its Q row into
+//              TMEM (bf16 pairs, the A operand of S), so the S MMAs read only
+//              K from shared memory.
 //   warp 4kWG  TMA producer: the Q tile once, then K and V tiles into 3- and
 //              2-deep rings (3-D tensor maps, 128-byte swizzle), in the order
 //              the tensor core consumes them.
-//   warp 4kWG+1  MMA issuer (one thread), owner of TMEM.  S(k) = Q K_k^T goes to
-//              TMEM buffer k % 2; once P(k) is written it issues O += P(k) V_k
+//   warp 4kWG+1  MMA issuer (one thread), owner of TMEM.  S(k) = Q K_k^T (Q from
+//              TMEM, K from shared memory) goes to TMEM buffer k % 2; once
+//              P(k) is written it issues O += P(k) V_k
 //              (P read from TMEM) and S(k+2) into the buffer P(k) came from.
 //              The tensor core thus computes PV(k-1) and S(k+1) while the
 //              softmax works on tile k; MMAs of one thread run in issue order,
 //              so S(k+2) never overwrites P(k) before PV(k) has read it.
-// TMEM: S buffers in columns [0, 128) and [128, 256), O in [256, 256 + D).
-// At the end the parts' row sums add up (every part keeps the same running
+// TMEM: S buffers in columns [0, 128) and [128, 256), O in [256, 256 + D),
+// Q in [256 + D, 256 + 3D/2).  At the end the parts' row sums add up (every part keeps the same running
 // max) and each thread normalises and stores its D/kWG columns of the row.
 //
 // With S > 1 splits the S CTAs of a query tile run as one thread-block
 // cluster.  Each CTA writes its combined partial (O divided by its row sum,
 // bf16) into its own shared memory, in the K ring that nothing reads any
 // more, with the rows' (max, sum).  After a cluster barrier every CTA
-// combines its share of the head-dim columns (8-column unit u goes to split
-// u mod S) from all splits through distributed shared memory, in a fixed
-// order; a second cluster barrier keeps every CTA resident until its shared
-// memory has been read.  No global scratch is used.
+// combines its share of the head-dim columns (split sp takes a contiguous
+// range of 8-column units) from all splits through distributed shared
+// memory, in a fixed order, and stores it; a second cluster barrier keeps
+// every CTA resident until its shared memory has been read.  No global
+// scratch is used.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -93,7 +98,8 @@ enum {
     B_OW = B_MX + 2,            // one completion per PV (O written)
     B_MASK = B_OW + 1,          // visibility mask complete (256 arrivals)
     B_DONE = B_MASK + 1,        // every MMA of the CTA complete
-    B_COUNT = B_DONE + 1
+    B_QT = B_DONE + 1,          // Q copied into TMEM (one arrival per softmax warp)
+    B_COUNT = B_QT + 1
 };
 
 template <int D> struct Layout {
@@ -407,6 +413,7 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
         mbar_init(bar(B_OW), 1);
         mbar_init(bar(B_MASK), kSoftmaxThreads);
         mbar_init(bar(B_DONE), 1);
+        mbar_init(bar(B_QT), kSoftmaxThreads / 32);
         *abort_flag = 0u;
         mask[0] = mask[1] = 0u;
         fence_barrier_init();
@@ -587,9 +594,8 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * kBlockBytes + (kk % 4) * 32;
-                    const uint64_t a = sdesc_sw128(sQ + off, 16, 1024);
                     const uint64_t bd = sdesc_sw128(sK + ks * Lay::kKBytes + off, 16, 1024);
-                    mma_bf16_ss(tS, a, bd, idS, kk > 0 ? 1u : 0u);
+                    mma_bf16_ts(tS, tmem + 2u * kBN + D + (uint32_t)(kk * 8), bd, idS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(B_SF + (k & 1)));
                 mma_commit(bar(B_KE + ks));
@@ -614,7 +620,7 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
             }
             __syncwarp();
         };
-        bool ok = wait_all(bar(B_Q), 0);
+        bool ok = wait_all(bar(B_QT), 0);
         for (int k = 0; ok && k < 2; ++k) {
             const int e = exists(k);
             ok = e >= 0;
@@ -702,6 +708,33 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
             }
         }
         mbar_arrive(bar(B_MASK));
+
+        // Q into TMEM as the A operand of S = Q K^T: this thread's row, its
+        // warpgroup's half of the head dimension, as bf16 pairs per column
+        {
+            const bool okq = wait_bar(bar(B_Q), 0, abort_flag, status);
+            if (__all_sync(0xffffffffu, okq)) {
+                constexpr int kChunks = D / 8 / kWG;  // 16-byte chunks of the row per thread
+                uint32_t qv[kChunks * 4];
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    const int gc = w * kChunks + c;
+                    const uint4 u = smem_ld_v4(sQ + (uint32_t)(gc / 8) * kBlockBytes + (uint32_t)row * 128u +
+                                               ((uint32_t)((gc % 8) ^ (row & 7)) << 4));
+                    qv[4 * c] = u.x, qv[4 * c + 1] = u.y, qv[4 * c + 2] = u.z, qv[4 * c + 3] = u.w;
+                }
+                const uint32_t tQ = tmem + lane_off + 2u * kBN + D + (uint32_t)(w * kChunks * 4);
+                if constexpr (kChunks * 4 == 32)
+                    tmem_st32u(tQ, qv);
+                else
+                    tmem_st16(tQ, qv);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(B_QT));
+        }
 
         float m_ref = -INFINITY, l = 0.f;  // l: this thread's column part of the row sum
         bool aborted = false;
