@@ -51,7 +51,7 @@ METRIC = "packed-draft query tokens/s + verified positions/s; % HBM/tensor roofl
 UNIT = "packed-draft query tokens/s"
 # our kernel launches per step: one fused round launch, or the attention and
 # the verification (with the branch match fused into its last phase)
-LAUNCHES = {"fused": 1, "split": 2, "split-attention-first": 2}
+LAUNCHES = {"fused": 1, "attention-first": 2, "verify-first": 2}
 CSRC = os.path.join(ROOT, "diffusion_drafted_speculative_gb300", "csrc")
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of this bench's workload, keyed by a hash of the sources the
@@ -100,9 +100,10 @@ def parse_args():
                     help="skip the long-block, serving-batch and C/F-sweep measurements")
     ap.add_argument("--no-layout-parts", action="store_true",
                     help="skip timing the attention on the target-verify and training layouts")
-    ap.add_argument("--round", choices=["split", "split-attention-first", "fused"], default="split",
-                    help="split: the verification, then the attention as its programmatic dependent; "
-                         "split-attention-first: the other way round; "
+    ap.add_argument("--round", choices=["attention-first", "verify-first", "fused"], default="attention-first",
+                    help="attention-first: the attention (set up while the round before ends), then the "
+                         "verification as its programmatic dependent; verify-first: the verification, then "
+                         "the attention as its programmatic dependent; "
                          "fused: both in one cooperative launch (d3d_async_round)")
     return ap.parse_args()
 
@@ -289,10 +290,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     side_sms = props.multi_processor_count - attn_ctas
     verify_sms = side_sms if 0 < attn_ctas and side_sms > 0 else 0
 
-    def attn(s, after_independent=False, max_ctas=0):
+    def attn(s, after_independent=False, max_ctas=0, after_dependent=False):
         d3d.d3d_packed_draft_attn(s["q"], s["kp"], s["vp"], s["kn"], s["vn"], s["segs"], s["cu_prefix"], s["cu_q"],
                                   s["cu_seg"], max_q, max_prefix, scale, s["out"], ws_a,
-                                  after_independent=after_independent, max_ctas=max_ctas)
+                                  after_independent=after_independent, max_ctas=max_ctas,
+                                  after_dependent=after_dependent)
 
     def verify(s, sm_limit=0, fused_match=False, after_independent=False):
         extra = dict(heads=s["heads"], head_len=s["head_len"], branch=s["branch"]) if fused_match else {}
@@ -357,15 +359,17 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     def step(s):
         # the asynchronous round: the packed drafting pass and the verification
         # of the current block are independent and run concurrently: the
-        # verification on the SMs the attention leaves, then the attention as
-        # its programmatic dependent (--round split-attention-first: the other
-        # way round; --round fused: both in one cooperative launch); the branch
-        # match runs inside the verification's last phase (it needs the
+        # attention, launched as a programmatic dependent of the round before
+        # (it sets up while that round ends and reads its inputs once it has
+        # finished), then the verification on the SMs the attention leaves as
+        # the attention's programmatic dependent (--round verify-first: the
+        # other way round; --round fused: both in one cooperative launch); the
+        # branch match runs inside the verification's last phase (it needs the
         # verified tokens and the round's branch heads only)
         if fused_round:
             d3d.d3d_async_round(*round_calls(s))
-        elif args.round == "split-attention-first":
-            attn(s, max_ctas=round_budget)
+        elif args.round == "attention-first":
+            attn(s, max_ctas=round_budget, after_dependent=verify_sms > 0)
             verify(s, verify_sms, fused_match=True, after_independent=verify_sms > 0)
         else:
             verify(s, verify_sms, fused_match=True)

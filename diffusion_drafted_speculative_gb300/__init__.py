@@ -24,7 +24,8 @@ __all__ = [
     "d3d_accept_probs", "d3d_accept_probs_workspace_size", "d3d_branch_match", "d3d_workspace_status", "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
     "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
     "D3D_ERR_DEVICE_TIMEOUT", "D3D_ERR_DEVICE_INPUT", "D3D_ERR_INTERNAL", "D3D_DTYPE_F32", "D3D_DTYPE_BF16",
-    "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR", "D3D_ATTN_AFTER_INDEPENDENT", "D3D_VERIFY_AFTER_INDEPENDENT",
+    "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR", "D3D_ATTN_AFTER_INDEPENDENT", "D3D_ATTN_AFTER_DEPENDENT",
+    "D3D_VERIFY_AFTER_INDEPENDENT",
 ]
 
 D3D_OK = 0
@@ -40,6 +41,7 @@ D3D_DTYPE_BF16 = 1
 D3D_SEG_CAUSAL = 0
 D3D_SEG_BIDIR = 1
 D3D_ATTN_AFTER_INDEPENDENT = 1
+D3D_ATTN_AFTER_DEPENDENT = 2
 D3D_VERIFY_AFTER_INDEPENDENT = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -220,13 +222,15 @@ def _attn_args(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q,
 
 def d3d_packed_draft_attn(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q, cu_seg,
                           max_q: int, max_prefix: int, scale: float, out, ws, after_independent: bool = False,
-                          stream=None, max_ctas: int = 0) -> None:
+                          stream=None, max_ctas: int = 0, after_dependent: bool = False) -> None:
     """Packed drafting attention; shapes as in include/d3d.h (bf16 tensors, int32 tables).
-    max_ctas > 0 bounds the launch to one wave of that many CTAs (SMs)."""
+    max_ctas > 0 bounds the launch to one wave of that many CTAs (SMs).  after_independent /
+    after_dependent set D3D_ATTN_AFTER_INDEPENDENT / D3D_ATTN_AFTER_DEPENDENT (not both)."""
     args = _attn_args(q, k_prefix, v_prefix, k_packed, v_packed, segs, cu_prefix, cu_q, cu_seg, max_q, max_prefix,
                       scale, out, ws)
-    rc = lib.d3d_packed_draft_attn(*args, int(max_ctas), D3D_ATTN_AFTER_INDEPENDENT if after_independent else 0,
-                                   _stream(stream))
+    flags = (D3D_ATTN_AFTER_INDEPENDENT if after_independent else 0) | \
+        (D3D_ATTN_AFTER_DEPENDENT if after_dependent else 0)
+    rc = lib.d3d_packed_draft_attn(*args, int(max_ctas), flags, _stream(stream))
     _check("d3d_packed_draft_attn", rc)
 
 

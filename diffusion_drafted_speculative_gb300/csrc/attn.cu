@@ -131,6 +131,9 @@ struct AttnParams {
     // totals, within max_q / max_prefix): the kernel takes them from here and
     // checks the device arrays against them in its epilogue
     int one_request;
+    // the launch may start before the kernel ahead of it has finished, whose
+    // output it may read: it waits for that kernel before its first read
+    int wait_first;
 };
 
 // The bounds of request r: for a single request the documented offsets
@@ -380,7 +383,11 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
 
     // the request's offsets: loaded now, checked once the setup below is done
     // (the setup does not depend on them and hides their latency)
-    ReqRaw braw = load_bounds(p.cu_prefix, p.cu_q, p.cu_seg, r);
+    // (after a kernel whose output this one may read, nothing is read before
+    // it has finished: the offsets load after the setup then)
+    ReqRaw braw{};
+    if (!p.wait_first)
+        braw = load_bounds(p.cu_prefix, p.cu_q, p.cu_seg, r);
 
     // ---- shared memory carve-up (1024-byte aligned base for the swizzled tiles)
     const uint32_t raw = smem_u32(smem_raw);
@@ -441,6 +448,10 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
     // and tile) and come before any copy or cluster barrier; every exit first
     // waits for a kernel this launch overlaps (programmatic dependent launch):
     // the stream moves on only when both have finished.
+    if (p.wait_first) {  // the kernel ahead has finished and its writes are visible after this
+        pdl_wait();
+        braw = load_bounds(p.cu_prefix, p.cu_q, p.cu_seg, r);
+    }
     if (!p.one_request)  // a single request's bounds come from the host: nothing to wait for here
         asm volatile("" : "+r"(braw.q0), "+r"(braw.q1), "+r"(braw.p0), "+r"(braw.p1), "+r"(braw.s0), "+r"(braw.s1));
     ReqBounds b;
@@ -1191,7 +1202,11 @@ __device__ __forceinline__ void attn_pair_body(unsigned unit, const CUtensorMap 
         pdl_trigger();
     // the request's offsets: loaded now, checked once the setup below is done
     // (the setup does not depend on them and hides their latency)
-    ReqRaw braw = load_bounds(p.cu_prefix, p.cu_q, p.cu_seg, r);
+    // (after a kernel whose output this one may read, nothing is read before
+    // it has finished: the offsets load after the setup then)
+    ReqRaw braw{};
+    if (!p.wait_first)
+        braw = load_bounds(p.cu_prefix, p.cu_q, p.cu_seg, r);
     const int mt0 = 2 * mp;  // first query tile of the pair
 
     // ---- shared memory carve-up (1024-byte aligned base for the swizzled tiles)
@@ -1246,6 +1261,10 @@ __device__ __forceinline__ void attn_pair_body(unsigned unit, const CUtensorMap 
     // from moving their first use, and so the wait for the loads, above the
     // barrier); early exits are uniform over the CTAs of a cluster (same r and
     // pair) and come before any copy or cluster barrier
+    if (p.wait_first) {  // the kernel ahead has finished and its writes are visible after this
+        pdl_wait();
+        braw = load_bounds(p.cu_prefix, p.cu_q, p.cu_seg, r);
+    }
     if (!p.one_request)  // a single request's bounds come from the host: nothing to wait for here
         asm volatile("" : "+r"(braw.q0), "+r"(braw.q1), "+r"(braw.p0), "+r"(braw.p1), "+r"(braw.s0), "+r"(braw.s1));
     ReqBounds b;
@@ -1987,7 +2006,7 @@ int launch_attn(const CUtensorMap (&maps)[6], const AttnParams &prm, long long u
         a[na].val.clusterDim.z = 1;
         ++na;
     }
-    if (flags & D3D_ATTN_AFTER_INDEPENDENT) {  // may start while the previous kernel runs
+    if (flags & (D3D_ATTN_AFTER_INDEPENDENT | D3D_ATTN_AFTER_DEPENDENT)) {  // may start while the previous kernel runs
         a[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         a[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
@@ -2075,6 +2094,7 @@ int attn_prepare(const void *q, const void *k_prefix, const void *v_prefix, cons
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.fault = fault_mode();
     prm.one_request = R == 1 && total_q <= max_q && total_prefix <= max_prefix;
+    prm.wait_first = 0;
     return D3D_OK;
 }
 
@@ -2161,7 +2181,8 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
                           int max_prefix, int total_q, int total_prefix, int total_segs, float scale, void *out,
                           void *ws, size_t ws_bytes, int max_ctas, int flags, cudaStream_t stream)
 {
-    if ((flags & ~D3D_ATTN_AFTER_INDEPENDENT) != 0)
+    if ((flags & ~(D3D_ATTN_AFTER_INDEPENDENT | D3D_ATTN_AFTER_DEPENDENT)) != 0 ||
+        (flags & D3D_ATTN_AFTER_INDEPENDENT && flags & D3D_ATTN_AFTER_DEPENDENT))
         return D3D_ERR_INVALID_ARG;
     CUtensorMap maps[6];
     d3d::AttnParams prm;
@@ -2171,6 +2192,7 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
                                      ws_bytes, maps, prm, pl, max_ctas);
     if (rc != D3D_OK)
         return rc == 1 ? D3D_OK : rc;
+    prm.wait_first = (flags & D3D_ATTN_AFTER_DEPENDENT) != 0;
     if (d == 64)
         return d3d::launch_attn<64>(maps, prm, pl.units, pl.pair, flags, stream);
     return d3d::launch_attn<128>(maps, prm, pl.units, pl.pair, flags, stream);

@@ -163,7 +163,13 @@ int d3d_validate_segments(const d3d_segment_t *segs, const int32_t *cu_q, const 
  *               launched first with an sm_limit, whose output the attention
  *               does not read.  The attention still finishes only after that
  *               kernel has finished, so later work on the stream sees both.
- *               Other bits: D3D_ERR_INVALID_ARG.
+ *               Or D3D_ATTN_AFTER_DEPENDENT: the launch may also start while
+ *               the kernel before it runs, but it waits for that kernel to
+ *               finish (and its writes to be visible) before it reads any
+ *               input; only its setup (barriers, TMEM, tensor-map prefetch)
+ *               overlaps -- for the next round's attention after this round's
+ *               kernels.  The two bits are exclusive.  Other bits:
+ *               D3D_ERR_INVALID_ARG.
  * Device-side checks: offsets out of the totals' range or a segment table
  * that breaks the rules of d3d_validate_segments set D3D_ERR_DEVICE_INPUT
  * in the status word (the affected rows are written as zeros).
@@ -173,6 +179,7 @@ int d3d_validate_segments(const d3d_segment_t *segs, const int32_t *cu_q, const 
  * device's SMs (or max_ctas of them).
  * ======================================================================== */
 #define D3D_ATTN_AFTER_INDEPENDENT 1
+#define D3D_ATTN_AFTER_DEPENDENT 2
 
 size_t d3d_packed_draft_attn_workspace_size(int R, int Hq, int Hkv, int d, int max_q, int max_prefix);
 
@@ -431,8 +438,10 @@ int d3d_spec_verify_noalloc(const void *target_logits, const void *draft_logits,
  * error codes are those of the two calls.  D3D_ERR_UNSUPPORTED when the
  * attention would split keys across CTAs or fill every SM, when a part has
  * nothing to compute, or for greedy verification (temperature 0): then make
- * the two calls (the verification with
- * an sm_limit, the attention with D3D_ATTN_AFTER_INDEPENDENT).
+ * the two calls on one stream: the attention (D3D_ATTN_AFTER_DEPENDENT when
+ * the kernel before it may write its inputs), then the verification with an
+ * sm_limit and D3D_VERIFY_AFTER_INDEPENDENT; or the verification with an
+ * sm_limit, then the attention with D3D_ATTN_AFTER_INDEPENDENT.
  * Field meanings are those of the arguments of the two calls.
  * ======================================================================== */
 typedef struct {

@@ -212,6 +212,46 @@ def test_attn_single_request_offsets_checked(d3d, Hq):
         assert (got2 == 0).all(), key
 
 
+@pytest.mark.parametrize("cfg", [W.CONFIGS["async8b"],  # one request, the one-tile kernel
+                                 dict(R=4, L=(100, 900), Hq=64, Hkv=8, d=128, B=16, C=12, F=2, layout="async")])
+def test_attn_after_dependent_reads_the_previous_output(d3d, cfg):
+    # D3D_ATTN_AFTER_DEPENDENT: the second attention takes the first one's
+    # output as its queries and may start while the first still runs (the
+    # first leaves SMs free); it must read those queries only once they are
+    # written: the chained result equals the one of two plain launches
+    from gpu_util import bf16, i32
+    a = W.attn_inputs(**cfg, seed=31)
+    t = {k: bf16(a[k]) for k in ("q", "kp", "vp", "kn", "vn")}
+    ix = {k: i32(a[k]) for k in ("segs", "cu_prefix", "cu_q", "cu_seg")}
+    ws = d3d.new_workspace(d3d.d3d_packed_draft_attn_workspace_size(a["R"], a["Hq"], a["Hkv"], a["d"], a["max_q"],
+                                                                    a["max_prefix"]))
+    budget = d3d.d3d_packed_draft_attn_ctas(a["R"], a["Hq"], a["Hkv"], a["d"], a["max_q"], a["max_prefix"], 0)
+    budget = max(1, min(budget, torch.cuda.get_device_properties(0).multi_processor_count // 2))
+
+    def att(q, out, dep):
+        d3d.d3d_packed_draft_attn(q, t["kp"], t["vp"], t["kn"], t["vn"], ix["segs"], ix["cu_prefix"], ix["cu_q"],
+                                  ix["cu_seg"], a["max_q"], a["max_prefix"], a["scale"], out, ws,
+                                  max_ctas=budget, after_dependent=dep)
+    mid = torch.full_like(t["q"], float("nan"))
+    att(t["q"], mid, False)
+    want = torch.full_like(t["q"], float("nan"))
+    att(mid.clone(), want, False)
+    torch.cuda.synchronize()
+    assert torch.isfinite(want.float()).all()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        for _ in range(4):
+            mid2 = torch.full_like(t["q"], float("nan"))
+            got = torch.full_like(t["q"], float("nan"))
+            att(t["q"], mid2, False)
+            att(mid2, got, True)
+            att(got, torch.empty_like(got), True)  # a third in the chain; its output is not checked
+            st.synchronize()
+            assert torch.equal(mid2, mid)
+            assert torch.equal(got, want)
+    assert d3d.d3d_workspace_status(ws) == 0
+
+
 # ------------------------------------------------------------------ verification
 @pytest.mark.parametrize("seed", range(3))
 def test_verify_tiny_config_batched(d3d, seed):
@@ -438,7 +478,8 @@ def test_round_on_one_stream_overlapping(d3d, attention_first):
             def att():
                 d3d.d3d_packed_draft_attn(t["q"], t["kp"], t["vp"], t["kn"], t["vn"], ix["segs"], ix["cu_prefix"],
                                           ix["cu_q"], ix["cu_seg"], a["max_q"], a["max_prefix"], a["scale"], out, wsa,
-                                          after_independent=not attention_first, max_ctas=budget)
+                                          after_independent=not attention_first, max_ctas=budget,
+                                          after_dependent=attention_first)
             if attention_first:
                 att()
                 ver()

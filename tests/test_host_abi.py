@@ -97,7 +97,8 @@ def test_invalid_arguments_rejected_on_host(d3d):
     def attn(R=1, Hq=32, Hkv=8, d=128, max_q=16, scale=0.1, ws=fake, wsb=1 << 30, flags=0, max_ctas=0):
         return L.d3d_packed_draft_attn(fake, fake, fake, fake, fake, fake, fake, fake, fake, R, Hq, Hkv, d, max_q,
                                        64, 16, 64, 1, scale, fake, ws, wsb, max_ctas, flags, None)
-    assert attn(flags=2) == d3d.D3D_ERR_INVALID_ARG
+    assert attn(flags=3) == d3d.D3D_ERR_INVALID_ARG  # the two placement bits are exclusive
+    assert attn(flags=4) == d3d.D3D_ERR_INVALID_ARG
     assert attn(max_ctas=-1) == d3d.D3D_ERR_INVALID_ARG
     assert attn(Hq=30, Hkv=8) == d3d.D3D_ERR_INVALID_ARG
     assert attn(d=96) == d3d.D3D_ERR_UNSUPPORTED
