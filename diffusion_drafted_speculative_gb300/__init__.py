@@ -21,7 +21,7 @@ __all__ = [
     "d3d_spec_verify", "d3d_spec_verify_workspace_size", "d3d_spec_verify_slice_ctas", "d3d_spec_verify_noalloc",
     "d3d_async_round",
     "AttnCall", "VerifyCall", "d3d_build_branches", "d3d_build_branches_workspace_size",
-    "d3d_accept_probs", "d3d_accept_probs_workspace_size", "d3d_branch_match", "d3d_workspace_status", "d3d_workspace_init", "d3d_debug_inject_fault", "new_workspace", "EXPORTED",
+    "d3d_accept_probs", "d3d_accept_probs_workspace_size", "d3d_branch_match", "d3d_workspace_status", "d3d_workspace_init", "d3d_debug_inject_fault", "d3d_debug_force_attn_kernel", "new_workspace", "EXPORTED",
     "D3D_OK", "D3D_ERR_INVALID_ARG", "D3D_ERR_UNSUPPORTED", "D3D_ERR_WORKSPACE", "D3D_ERR_CUDA",
     "D3D_ERR_DEVICE_TIMEOUT", "D3D_ERR_DEVICE_INPUT", "D3D_ERR_INTERNAL", "D3D_DTYPE_F32", "D3D_DTYPE_BF16",
     "D3D_SEG_CAUSAL", "D3D_SEG_BIDIR", "D3D_ATTN_AFTER_INDEPENDENT", "D3D_ATTN_AFTER_DEPENDENT",
@@ -67,6 +67,7 @@ EXPORTED = {
                              _P, _P, _Z, _I, _I, _P]),
     "d3d_branch_match": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "d3d_debug_inject_fault": (None, [_I]),
+    "d3d_debug_force_attn_kernel": (None, [_I]),
     "d3d_spec_verify_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P]),
     "d3d_async_round": (_I, [_P, _P, _P]),
     "d3d_build_branches_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
@@ -170,6 +171,12 @@ def d3d_validate_segments(segs: torch.Tensor, cu_q: torch.Tensor, cu_seg: torch.
 def d3d_debug_inject_fault(mode: int) -> None:
     """Failure-detection hook: 1 makes later attention launches time out on purpose, 0 restores."""
     lib.d3d_debug_inject_fault(int(mode))
+
+
+def d3d_debug_force_attn_kernel(kind: int) -> None:
+    """Restrict later attention plans to one kernel: 1 one tile per CTA, 2 two tiles per CTA, 3 CTA pairs
+    (where it applies); 0 restores the plan's own choice."""
+    lib.d3d_debug_force_attn_kernel(int(kind))
 
 
 def d3d_packed_draft_attn_workspace_size(R, Hq, Hkv, d, max_q, max_prefix) -> int:

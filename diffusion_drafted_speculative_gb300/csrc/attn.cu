@@ -74,6 +74,11 @@ constexpr int kWG = D3D_ATTN_WG;  // softmax warpgroups: each takes 1/kWG of eve
 constexpr int kPart = kBN / kWG;  // 32 keys per softmax thread and tile
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
+// a CTA pair's stages hold half tiles: deeper rings in the same room
+constexpr int kDuoKStages = 4;
+constexpr int kDuoVStages = 3;
+constexpr int kMaxKStages = kDuoKStages;
+constexpr int kMaxVStages = kDuoVStages;
 constexpr int kSoftmaxThreads = kWG * 128;
 constexpr int kTmaWarp = kWG * 4;
 constexpr int kMmaWarp = kTmaWarp + 1;
@@ -88,11 +93,11 @@ constexpr int kMaxSplits = 8;  // key splits of a query tile: one thread-block c
 // barrier indices
 enum {
     B_Q = 0,
-    B_KF = 1,                   // kKStages
-    B_KE = B_KF + kKStages,     // kKStages
-    B_VF = B_KE + kKStages,     // kVStages
-    B_VE = B_VF + kVStages,     // kVStages
-    B_SF = B_VE + kVStages,     // 2: S(k) in TMEM buffer k % 2
+    B_KF = 1,                   // K stages
+    B_KE = B_KF + kMaxKStages,  // K stages
+    B_VF = B_KE + kMaxKStages,  // V stages
+    B_VE = B_VF + kMaxVStages,  // V stages
+    B_SF = B_VE + kMaxVStages,  // 2: S(k) in TMEM buffer k % 2
     B_PR = B_SF + 2,            // 2: P(k) in TMEM buffer k % 2 (one arrival per softmax warp)
     B_MX = B_PR + 2,            // 2: both halves' row maxima of tile k published (one per softmax warp)
     B_OW = B_MX + 2,            // one completion per PV (O written)
@@ -102,14 +107,20 @@ enum {
     B_COUNT = B_QT + 1
 };
 
-template <int D> struct Layout {
+// kDuo: one CTA of a pair (attn_duo_kernel), whose K stages hold half of a
+// tile's keys and V stages half of its head-dim columns
+template <int D, bool kDuo = false> struct Layout {
+    static constexpr int kKS = kDuo ? kDuoKStages : kKStages;
+    static constexpr int kVS = kDuo ? kDuoVStages : kVStages;
     static constexpr uint32_t kQBytes = kBM * D * 2;
-    static constexpr uint32_t kKBytes = kBN * D * 2;
-    static constexpr uint32_t kVBytes = kBN * D * 2;
+    static constexpr uint32_t kKRows = kDuo ? kBN / 2 : kBN;  // keys of a K stage
+    static constexpr uint32_t kKBlock = kKRows * 128;         // one 64-column block of a K stage
+    static constexpr uint32_t kKBytes = kKRows * D * 2;
+    static constexpr uint32_t kVBytes = kBN * (kDuo ? D / 2 : D) * 2;
     static constexpr uint32_t q = 0;
     static constexpr uint32_t k = q + kQBytes;
-    static constexpr uint32_t v = k + kKStages * kKBytes;
-    static constexpr uint32_t bars = v + kVStages * kVBytes;
+    static constexpr uint32_t v = k + kKS * kKBytes;
+    static constexpr uint32_t bars = v + kVS * kVBytes;
     static constexpr uint32_t misc = bars + B_COUNT * 8;
     static constexpr uint32_t mx = misc + 64;  // [2 buffers][kWG][kBM] row maxima of a tile's column parts
     static constexpr uint32_t ml = q;  // per warpgroup and row: (max, sum, tiles done), over Q after the last MMA
@@ -357,13 +368,14 @@ __device__ __forceinline__ void cluster_merge(int sp, int w, uint32_t part, uint
 // The attention of work unit `unit` (see the top of this file).  Threads past
 // the kThreads roles (a fused round launch has more) only pass the CTA's
 // barriers.  The tensor maps live in the kernel's parameter space.
-template <int D>
+template <int D, bool kDuo>
 __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q, const CUtensorMap *tm_kp,
                                           const CUtensorMap *tm_vp, const CUtensorMap *tm_kn,
                                           const CUtensorMap *tm_vn, const CUtensorMap *tm_o,
                                           const AttnParams &p)
 {
-    using Lay = Layout<D>;
+    using Lay = Layout<D, kDuo>;
+    static_assert(!kDuo || D == 128, "a CTA pair splits the head dimension into two 64-column blocks");
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -376,6 +388,10 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
     const int hk = (int)(u % (unsigned)p.Hkv);
     const int r = (int)(u / (unsigned)p.Hkv);
     int32_t *status = reinterpret_cast<int32_t *>(p.ws);
+    // CTA pair (kDuo): query tiles mt = 2j (rank 0, which issues the MMAs)
+    // and 2j + 1 (rank 1) of one request and KV head, one key list
+    const uint32_t crank = kDuo ? cluster_ctarank() : 0u;
+    const uint32_t peer = crank ^ 1u;
     // a kernel launched after this one as an independent programmatic
     // dependent (the verification of the same round) may start now
     if (tid == 0)
@@ -404,23 +420,26 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
 
     if (tid == 0) {
         mbar_init(bar(B_Q), 1);
-        for (int i = 0; i < kKStages; ++i) {
+        for (int i = 0; i < Lay::kKS; ++i) {
             mbar_init(bar(B_KF + i), 1);
             mbar_init(bar(B_KE + i), 1);
         }
-        for (int i = 0; i < kVStages; ++i) {
+        for (int i = 0; i < Lay::kVS; ++i) {
             mbar_init(bar(B_VF + i), 1);
             mbar_init(bar(B_VE + i), 1);
         }
+        // a pair's MMA-issuing CTA counts both CTAs' softmax warps; both
+        // CTAs' masks count the first warpgroups' warps of both
+        constexpr uint32_t kIssuerArrivals = (kDuo ? 2 : 1) * kSoftmaxThreads / 32;
         for (int b2 = 0; b2 < 2; ++b2) {
             mbar_init(bar(B_SF + b2), 1);
-            mbar_init(bar(B_PR + b2), kSoftmaxThreads / 32);
+            mbar_init(bar(B_PR + b2), kIssuerArrivals);
             mbar_init(bar(B_MX + b2), kSoftmaxThreads / 32);
         }
         mbar_init(bar(B_OW), 1);
-        mbar_init(bar(B_MASK), kSoftmaxThreads);
+        mbar_init(bar(B_MASK), kDuo ? 2 * 4 : kSoftmaxThreads);
         mbar_init(bar(B_DONE), 1);
-        mbar_init(bar(B_QT), kSoftmaxThreads / 32);
+        mbar_init(bar(B_QT), kIssuerArrivals);
         *abort_flag = 0u;
         mask[0] = mask[1] = 0u;
         fence_barrier_init();
@@ -434,11 +453,20 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
         prefetch_tmap(tm_o);
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
-        tmem_relinquish();
+        if constexpr (kDuo) {
+            tmem_alloc_pair(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (kDuo) {  // both CTAs' barriers are initialised before either signals the other's
+        cluster_arrive();
+        cluster_wait();
+    }
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -456,11 +484,17 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
         asm volatile("" : "+r"(braw.q0), "+r"(braw.q1), "+r"(braw.p0), "+r"(braw.p1), "+r"(braw.s0), "+r"(braw.s1));
     ReqBounds b;
     const bool bounds_ok = kernel_bounds(p, braw, b);
-    if (!bounds_ok || mt * p.TQ >= b.n_q) {
-        if (!bounds_ok && tid == 0 && sp == 0)
+    // a pair leaves together: only when its first tile is past the request
+    // (the second CTA of a pair with one tile in the request has no valid row)
+    if (!bounds_ok || (kDuo ? (mt & ~1) : mt) * p.TQ >= b.n_q) {
+        if (!bounds_ok && tid == 0 && sp == 0 && crank == 0)
             record_status(status, D3D_ERR_DEVICE_INPUT);
-        if (warp == kMmaWarp)
-            tmem_dealloc(tmem, kTmemCols);
+        if (warp == kMmaWarp) {
+            if constexpr (kDuo)
+                tmem_dealloc_pair(tmem, kTmemCols);
+            else
+                tmem_dealloc(tmem, kTmemCols);
+        }
         pdl_wait();
         return;
     }
@@ -478,7 +512,9 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
     uint32_t mk0 = 0, mk1 = 0;
     auto npk = [&]() -> int {
         if (npk_cache < 0) {
-            if (!__all_sync(0xffffffffu, wait_bar(bar(B_MASK), 0, abort_flag, status)))
+            const bool okm = kDuo ? wait_bar_cluster(bar(B_MASK), 0, abort_flag, status)
+                                  : wait_bar(bar(B_MASK), 0, abort_flag, status);
+            if (!__all_sync(0xffffffffu, okm))
                 return -1;
             mk0 = *(volatile uint32_t *)&mask[0];
             mk1 = *(volatile uint32_t *)&mask[1];
@@ -527,7 +563,7 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
         }
         __syncwarp();
         auto issue = [&](int k, bool is_k) -> bool {
-            const int ns = is_k ? kKStages : kVStages;
+            const int ns = is_k ? Lay::kKS : Lay::kVS;
             const int s = k % ns;
             const int empty = is_k ? B_KE : B_VE, full = is_k ? B_KF : B_VF;
             if (k >= ns && !__all_sync(0xffffffffu, wait_bar(bar(empty + s), ((k - ns) / ns) & 1, abort_flag, status)))
@@ -544,11 +580,26 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
             if (!dbg_ok(pre ? (row >= b.p0 && row < b.p0 + b.L) : (row >= b.q0 && row < b.q0 + b.n_q), status))
                 row = 0;
             const CUtensorMap *m = is_k ? (pre ? tm_kp : tm_kn) : (pre ? tm_vp : tm_vn);
-            const uint32_t dst = (is_k ? sK : sV) + s * Lay::kKBytes;
+            const uint32_t dst = is_k ? sK + s * Lay::kKBytes : sV + s * Lay::kVBytes;
             if (leader) {
-                mbar_arrive_expect_tx(bar(full + s), Lay::kKBytes);
-                for (int cb = 0; cb < D / 64; ++cb)
-                    tma_load_3d(dst + cb * kBlockBytes, m, bar(full + s), cb * 64, hk, row);
+                if constexpr (kDuo) {
+                    // this CTA's half (keys [64 crank, +64) of K, head-dim columns
+                    // [64 crank, +64) of V), counted on the issuing CTA's barrier,
+                    // which expects both halves
+                    const uint32_t fb = dsmem_addr(bar(full + s), 0u);
+                    if (crank == 0)
+                        mbar_arrive_expect_tx(bar(full + s), 2u * (is_k ? Lay::kKBytes : Lay::kVBytes));
+                    if (is_k) {
+                        for (int cb = 0; cb < D / 64; ++cb)
+                            tma_load_3d_pair(dst + cb * Lay::kKBlock, m, fb, cb * 64, hk, row + (int)crank * (kBN / 2));
+                    } else {
+                        tma_load_3d_pair(dst, m, fb, (int)crank * 64, hk, row);
+                    }
+                } else {
+                    mbar_arrive_expect_tx(bar(full + s), Lay::kKBytes);
+                    for (int cb = 0; cb < D / 64; ++cb)
+                        tma_load_3d(dst + cb * kBlockBytes, m, bar(full + s), cb * 64, hk, row);
+                }
             }
             __syncwarp();
             return true;
@@ -575,47 +626,70 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
         // last phase of each stage (tiles s, s + ns, ... of the n handled)
         auto issued = [](int n, int s, int ns) { return n > s ? (n - 1 - s) / ns + 1 : 0; };
         wait_drain(bar(B_Q), 0, status);
-        for (int s = 0; s < kKStages; ++s) {
-            const int c = issued(nk, s, kKStages) - ((s == 0 && skipped0) ? 1 : 0);
+        // (a pair's K/V copies are counted on the issuing CTA's barriers: it
+        // drains both halves, and the other CTA stays until the cluster
+        // barrier at the end)
+        for (int s = 0; crank == 0 && s < Lay::kKS; ++s) {
+            const int c = issued(nk, s, Lay::kKS) - ((s == 0 && skipped0) ? 1 : 0);
             if (c > 0)
                 wait_drain(bar(B_KF + s), (c - 1) & 1, status);
         }
-        for (int s = 0; s < kVStages; ++s) {
-            const int c = issued(nv, s, kVStages);
+        for (int s = 0; crank == 0 && s < Lay::kVS; ++s) {
+            const int c = issued(nv, s, Lay::kVS);
             if (c > 0)
                 wait_drain(bar(B_VF + s), (c - 1) & 1, status);
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp && crank == 0) {
         // =================== MMA issuer ===================
         // The whole warp runs the loop and waits (warp-uniform control flow,
         // so the descriptors stay warp-uniform); one elected lane issues the
-        // MMAs and their commits.
+        // MMAs and their commits.  A pair's MMAs span both CTAs (M = 256: each
+        // CTA's 128 rows of Q, P, S and O in its own TMEM) and read K and V
+        // from both CTAs' halves; their commits arrive on both CTAs' barriers.
         const bool leader = elect_one();
-        constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
-        constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 0, 1);
+        constexpr uint32_t kM = kDuo ? 2 * kBM : kBM;
+        constexpr uint32_t idS = idesc_bf16_f32(kM, kBN, 0, 0);
+        constexpr uint32_t idO = idesc_bf16_f32(kM, D, 0, 1);
         auto wait_all = [&](uint32_t bar_addr, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, wait_bar(bar_addr, parity, abort_flag, status));
         };
+        // a barrier both CTAs' softmax warps arrive on (TMEM hand-offs: the
+        // tcgen05 fences order them)
+        auto wait_all_pair = [&](uint32_t bar_addr, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, wait_bar(bar_addr, parity, abort_flag, status));
+        };
+        auto mma_ts = [&](uint32_t d_tmem, uint32_t a_tmem, uint64_t bd, uint32_t idesc, uint32_t acc) {
+            if constexpr (kDuo)
+                mma_bf16_ts_pair(d_tmem, a_tmem, bd, idesc, acc);
+            else
+                mma_bf16_ts(d_tmem, a_tmem, bd, idesc, acc);
+        };
+        auto commit = [&](uint32_t b_addr) {
+            if constexpr (kDuo)
+                mma_commit_pair(b_addr);
+            else
+                mma_commit(b_addr);
+        };
         // S(k) = Q K_k^T into TMEM buffer k % 2, then release the K stage
         auto issue_s = [&](int k) {
-            const int ks = k % kKStages;
+            const int ks = k % Lay::kKS;
             const uint32_t tS = tmem + (uint32_t)(k & 1) * kBN;
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * kBlockBytes + (kk % 4) * 32;
+                    const uint32_t off = (kk / 4) * Lay::kKBlock + (kk % 4) * 32;
                     const uint64_t bd = sdesc_sw128(sK + ks * Lay::kKBytes + off, 16, 1024);
-                    mma_bf16_ts(tS, tmem + 2u * kBN + D + (uint32_t)(kk * 8), bd, idS, kk > 0 ? 1u : 0u);
+                    mma_ts(tS, tmem + 2u * kBN + D + (uint32_t)(kk * 8), bd, idS, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(B_SF + (k & 1)));
-                mma_commit(bar(B_KE + ks));
+                commit(bar(B_SF + (k & 1)));
+                commit(bar(B_KE + ks));
             }
             __syncwarp();
         };
         // O += P(k) V_k with P read from buffer k % 2, then release the V stage
         auto issue_pv = [&](int k) {
-            const int vs = k % kVStages;
+            const int vs = k % Lay::kVS;
             const uint32_t tP = tmem + (uint32_t)(k & 1) * kBN, tO = tmem + 2u * kBN;
             if (leader) {
 #pragma unroll
@@ -624,19 +698,19 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
                     // MN-major: 16 keys = two 8-row groups = 2048 bytes, the next 64
                     // head-dim columns are 16 KB further
                     const uint64_t bd = sdesc_sw128(sV + vs * Lay::kVBytes + kk * 2048, kBlockBytes, 1024);
-                    mma_bf16_ts(tO, tP + kk * 8, bd, idO, (k > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tO, tP + kk * 8, bd, idO, (k > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(B_OW));
-                mma_commit(bar(B_VE + vs));
+                commit(bar(B_OW));
+                commit(bar(B_VE + vs));
             }
             __syncwarp();
         };
-        bool ok = wait_all(bar(B_QT), 0);
+        bool ok = wait_all_pair(bar(B_QT), 0);
         for (int k = 0; ok && k < 2; ++k) {
             const int e = exists(k);
             ok = e >= 0;
             if (e == 1) {
-                ok = wait_all(bar(B_KF + k % kKStages), (k / kKStages) & 1);
+                ok = wait_all(bar(B_KF + k % Lay::kKS), (k / Lay::kKS) & 1);
                 if (ok) {
                     tc_fence_after();
                     issue_s(k);
@@ -654,8 +728,8 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
                 ok = e >= 0;
                 break;
             }
-            ok = wait_all(bar(B_VF + k % kVStages), (k / kVStages) & 1) &&
-                 wait_all(bar(B_PR + (k & 1)), (k >> 1) & 1);
+            ok = wait_all(bar(B_VF + k % Lay::kVS), (k / Lay::kVS) & 1) &&
+                 wait_all_pair(bar(B_PR + (k & 1)), (k >> 1) & 1);
             if (!ok)
                 break;
             tc_fence_after();
@@ -663,7 +737,7 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
             const int e2 = exists(k + 2);
             ok = e2 >= 0;
             if (e2 == 1) {
-                ok = wait_all(bar(B_KF + (k + 2) % kKStages), ((k + 2) / kKStages) & 1);
+                ok = wait_all(bar(B_KF + (k + 2) % Lay::kKS), ((k + 2) / Lay::kKS) & 1);
                 if (ok)
                     issue_s(k + 2);
             }
@@ -671,7 +745,7 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
         // every MMA is complete when B_DONE fires: O final, and the Q and K/V
         // buffers free; TMEM is released only after it
         if (leader)
-            mma_commit(bar(B_DONE));
+            commit(bar(B_DONE));
         __syncwarp();
         wait_drain(bar(B_DONE), 0, status);
         __syncwarp();
@@ -702,6 +776,7 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
             seg_lo = 0;
             seg_hi = n_seg;
         }
+        uint32_t mw0 = 0u, mw1 = 0u;  // (pair) packed tiles this thread's row sees
         if (row_valid && last_split) {
             if (!row_visibility(seg_base, seg_lo, seg_hi, b.n_q, token, vis)) {
                 row_bad = true;
@@ -711,14 +786,43 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
                 auto mark = [&](int lo, int hi) {
                     if (lo >= hi)
                         return;
-                    for (int k = lo / kBN; k <= (hi - 1) / kBN && k < kMaxPackedTiles; ++k)
-                        atomicOr(&mask[k >> 5], 1u << (k & 31));
+                    for (int k = lo / kBN; k <= (hi - 1) / kBN && k < kMaxPackedTiles; ++k) {
+                        if constexpr (kDuo) {
+                            if (k < 32)
+                                mw0 |= 1u << k;
+                            else
+                                mw1 |= 1u << (k - 32);
+                        } else
+                            atomicOr(&mask[k >> 5], 1u << (k & 31));
+                    }
                 };
                 mark(vis.own_lo, vis.own_hi);
                 mark(vis.par_lo, vis.par_hi);
             }
         }
-        mbar_arrive(bar(B_MASK));
+        if constexpr (kDuo) {
+            // the pair's key list covers the rows of both tiles: each first-
+            // warpgroup warp ors its rows' tiles into both CTAs' masks, then
+            // arrives on both CTAs' mask barriers
+            if (w == 0) {
+                mw0 = __reduce_or_sync(0xffffffffu, mw0);
+                mw1 = __reduce_or_sync(0xffffffffu, mw1);
+                if (lane == 0) {
+                    if (mw0 != 0u) {
+                        atomicOr(&mask[0], mw0);
+                        red_or_cluster(dsmem_addr(smem_u32(&mask[0]), peer), mw0);
+                    }
+                    if (mw1 != 0u) {
+                        atomicOr(&mask[1], mw1);
+                        red_or_cluster(dsmem_addr(smem_u32(&mask[1]), peer), mw1);
+                    }
+                    mbar_arrive(bar(B_MASK));
+                    mbar_arrive_cluster(dsmem_addr(bar(B_MASK), peer));
+                }
+            }
+        } else {
+            mbar_arrive(bar(B_MASK));
+        }
 
         // Q into TMEM as the A operand of S = Q K^T: this thread's row, its
         // warpgroup's half of the head dimension, as bf16 pairs per column
@@ -743,8 +847,12 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(bar(B_QT));
+            if (lane == 0) {
+                if (kDuo && crank != 0)
+                    mbar_arrive_remote(dsmem_addr(bar(B_QT), 0u));
+                else
+                    mbar_arrive(bar(B_QT));
+            }
         }
 
         float m_ref = -INFINITY, l = 0.f;  // l: this thread's column part of the row sum
@@ -873,8 +981,12 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(bar(B_PR + bf));
+            if (lane == 0) {
+                if (kDuo && crank != 0)
+                    mbar_arrive_remote(dsmem_addr(bar(B_PR + bf), 0u));
+                else
+                    mbar_arrive(bar(B_PR + bf));
+            }
             n_done = k + 1;
         }
 
@@ -950,7 +1062,13 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
     // ---- every role is done (all waits are bounded, copies and MMAs drained)
     tc_fence_before();
     __syncthreads();
-    if (p.S > 1) {
+    if constexpr (kDuo) {
+        // neither CTA of a pair leaves (or frees TMEM) while the other's
+        // MMAs or copies may still use it
+        cluster_arrive();
+        cluster_wait();
+    }
+    if (!kDuo && p.S > 1) {
         // split combine across the cluster: every thread of every CTA passes
         // both cluster barriers exactly once
         cluster_arrive();
@@ -990,7 +1108,10 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
     // release TMEM
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        if constexpr (kDuo)
+            tmem_dealloc_pair(tmem, kTmemCols);
+        else
+            tmem_dealloc(tmem, kTmemCols);
     }
     pdl_wait();
 }
@@ -1002,7 +1123,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_vn, const __grid_constant__ CUtensorMap tm_o,
                    const AttnParams p)
 {
-    attn_body<D>(blockIdx.x, &tm_q, &tm_kp, &tm_vp, &tm_kn, &tm_vn, &tm_o, p);
+    attn_body<D, false>(blockIdx.x, &tm_q, &tm_kp, &tm_vp, &tm_kn, &tm_vn, &tm_o, p);
+}
+
+// CTA pairs: launched in clusters of two, one query tile per CTA, the MMAs of
+// both tiles issued by the even CTA over both SMs (the K maps' boxes hold 64
+// keys: each CTA loads half of every K tile and half of every V tile's
+// head-dim columns).
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_duo_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
+                    const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kn,
+                    const __grid_constant__ CUtensorMap tm_vn, const __grid_constant__ CUtensorMap tm_o,
+                    const AttnParams p)
+{
+    attn_body<D, true>(blockIdx.x, &tm_q, &tm_kp, &tm_vp, &tm_kn, &tm_vn, &tm_o, p);
 }
 
 // One launch for the asynchronous round ([D3D] "Background: asynchronous
@@ -1019,7 +1154,7 @@ __global__ void __launch_bounds__(kNTLimited, 1)
                    const AttnParams p, const VArgs va, int n_attn)
 {
     if (blockIdx.x < (unsigned)n_attn)
-        attn_body<D>(blockIdx.x, &tm_q, &tm_kp, &tm_vp, &tm_kn, &tm_vn, &tm_o, p);
+        attn_body<D, false>(blockIdx.x, &tm_q, &tm_kp, &tm_vp, &tm_kn, &tm_vn, &tm_o, p);
     else
         verify_body<T, kNTLimited>(blockIdx.x - (unsigned)n_attn, gridDim.x - (unsigned)n_attn, va);
 }
@@ -1804,9 +1939,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
+// Kernel the plan is restricted to (d3d_debug_force_attn_kernel): 0 any,
+// 1 one tile per CTA, 2 two tiles per CTA, 3 CTA pairs.
+inline int &forced_attn_kernel()
+{
+    static int kind = 0;
+    return kind;
+}
+
 struct AttnPlan {
     int G, TQ, MT, S, PK;
     bool pair;  // two query tiles per CTA (attn_pair_kernel); MT then counts tile pairs
+    bool duo;   // one query tile per CTA, CTA pairs sharing MMAs (attn_duo_kernel); MT then even, S = 1
     long long units;
 };
 
@@ -1824,6 +1968,52 @@ int num_sms()
 template <int D> cudaError_t set_smem_attr()
 {
     return set_max_dyn_smem<attn_tc_kernel<D>>((int)Layout<D>::alloc);
+}
+
+// The CTA-pair kernel (head dim 128 only): its shared-memory attribute and the
+// CTAs resident at once in clusters of two (one CTA per SM), cached per
+// device; 0 when the query fails or the kernel does not apply.
+template <int D> int duo_capacity()
+{
+    if constexpr (D != 128) {
+        return 0;
+    } else {
+        constexpr int kDev = 64;
+        static std::mutex mu;
+        static int cache[kDev];
+        static bool have[kDev];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDev) {
+            cudaGetLastError();
+            return 0;
+        }
+        std::lock_guard<std::mutex> lock(mu);
+        if (!have[dev]) {
+            int n = 0;
+            if (set_max_dyn_smem<attn_duo_kernel<D>>((int)Layout<D, true>::alloc) == cudaSuccess) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(128u);
+                cfg.blockDim = dim3(kThreads);
+                cfg.dynamicSmemBytes = Layout<D, true>::alloc;
+                cudaLaunchAttribute a[1];
+                a[0].id = cudaLaunchAttributeClusterDimension;
+                a[0].val.clusterDim.x = 2;
+                a[0].val.clusterDim.y = 1;
+                a[0].val.clusterDim.z = 1;
+                cfg.attrs = a;
+                cfg.numAttrs = 1;
+                if (cudaOccupancyMaxActiveClusters(&n, attn_duo_kernel<D>, &cfg) != cudaSuccess) {
+                    cudaGetLastError();
+                    n = 0;
+                }
+            } else {
+                cudaGetLastError();
+            }
+            cache[dev] = 2 * n;
+            have[dev] = true;
+        }
+        return cache[dev];
+    }
 }
 
 // CTAs of the attention kernel resident at once when launched in clusters of
@@ -1912,9 +2102,10 @@ template <int D> int cluster_capacity(int S, bool pair = false)
 // cluster's combine (waiting for the slowest split, the exchange, the
 // stores).  max_ctas > 0 caps the CTAs of one wave (the SMs left to a kernel
 // running beside the attention).
-template <int D> AttnPlan make_plan(int R, int Hq, int Hkv, int max_q, int max_prefix, int max_ctas = 0)
+template <int D>
+AttnPlan make_plan(int R, int Hq, int Hkv, int max_q, int max_prefix, int max_ctas = 0, bool allow_duo = true)
 {
-    constexpr double kTileCost1 = 1.0, kTileCost2 = 1.75, kFixed = 5.0, kCombine = 3.5;
+    constexpr double kTileCost1 = 1.0, kTileCost2 = 1.75, kTileCostDuo = 0.8, kFixed = 5.0, kCombine = 3.5;
     AttnPlan pl{};
     pl.G = Hq / Hkv;
     pl.TQ = kBM / pl.G;
@@ -1928,8 +2119,17 @@ template <int D> AttnPlan make_plan(int R, int Hq, int Hkv, int max_q, int max_p
     pl.MT = MT;
     pl.S = 1;
     pl.pair = false;
+    pl.duo = false;
+    // a forced kernel that does not apply here leaves the choice to the plan
+    int force = forced_attn_kernel();
+    if (force == 2 && (MT < 2 || set_pair_smem_attr<D>() != cudaSuccess))
+        force = 0;
+    if (force == 3 && (!allow_duo || duo_capacity<D>() < 2))
+        force = 0;
     for (int pair = 0; pair < 2; ++pair) {
         if (pair && (MT < 2 || set_pair_smem_attr<D>() != cudaSuccess))
+            continue;
+        if ((force == 1 && pair) || (force == 2 && !pair) || force == 3)
             continue;
         const int units_m = pair ? (MT + 1) / 2 : MT;
         const long long base = (long long)R * Hkv * units_m;
@@ -1947,6 +2147,25 @@ template <int D> AttnPlan make_plan(int R, int Hq, int Hkv, int max_q, int max_p
                 pl.S = S;
                 pl.pair = pair != 0;
                 pl.MT = units_m;
+            }
+        }
+    }
+    // CTA pairs: every query tile in its own CTA (tiles rounded up to pairs),
+    // no key splits; each SM receives half of every K/V tile
+    if (allow_duo && (force == 0 || force == 3)) {
+        const int MT2 = (MT + 1) / 2 * 2;
+        int cap = duo_capacity<D>();
+        if (cap > budget)
+            cap = budget / 2 * 2;
+        if (cap >= 2) {
+            const double waves = (double)(((long long)R * Hkv * MT2 + cap - 1) / cap);
+            const double cost = waves * (tiles * kTileCostDuo + kFixed);
+            if (cost < best - 1e-9 || force == 3) {
+                best = cost;
+                pl.S = 1;
+                pl.pair = false;
+                pl.duo = true;
+                pl.MT = MT2;
             }
         }
     }
@@ -1987,21 +2206,25 @@ bool make_map(CUtensorMap *m, const void *ptr, int d, int heads, long long rows,
 }
 
 template <int D>
-int launch_attn(const CUtensorMap (&maps)[6], const AttnParams &prm, long long units, bool pair, int flags,
+int launch_attn(const CUtensorMap (&maps)[6], const AttnParams &prm, long long units, bool pair, bool duo, int flags,
                 cudaStream_t stream)
 {
-    if ((pair ? set_pair_smem_attr<D>() : set_smem_attr<D>()) != cudaSuccess)
+    if (duo) {
+        if (D != 128 || duo_capacity<D>() < 2 || units % 2 != 0)
+            return D3D_ERR_INTERNAL;
+    } else if ((pair ? set_pair_smem_attr<D>() : set_smem_attr<D>()) != cudaSuccess) {
         return D3D_ERR_CUDA;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)units);
     cfg.blockDim = dim3(pair ? kPairThreads : kThreads);
-    cfg.dynamicSmemBytes = pair ? PairLayout<D>::alloc : Layout<D>::alloc;
+    cfg.dynamicSmemBytes = pair ? PairLayout<D>::alloc : duo ? Layout<128, true>::alloc : Layout<D>::alloc;
     cfg.stream = stream;
     cudaLaunchAttribute a[2];
     unsigned na = 0;
-    if (prm.S > 1) {  // the splits of one query tile form a cluster (consecutive CTAs)
+    if (prm.S > 1 || duo) {  // the splits of one query tile, or a CTA pair, form a cluster (consecutive CTAs)
         a[na].id = cudaLaunchAttributeClusterDimension;
-        a[na].val.clusterDim.x = (unsigned)prm.S;
+        a[na].val.clusterDim.x = duo ? 2u : (unsigned)prm.S;
         a[na].val.clusterDim.y = 1;
         a[na].val.clusterDim.z = 1;
         ++na;
@@ -2016,6 +2239,11 @@ int launch_attn(const CUtensorMap (&maps)[6], const AttnParams &prm, long long u
     if (pair)
         return cuda_status(
             cudaLaunchKernelEx(&cfg, attn_pair_kernel<D>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], prm));
+    if constexpr (D == 128) {
+        if (duo)
+            return cuda_status(
+                cudaLaunchKernelEx(&cfg, attn_duo_kernel<D>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], prm));
+    }
     return cuda_status(cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], prm));
 }
 
@@ -2050,8 +2278,8 @@ int attn_prepare(const void *q, const void *k_prefix, const void *v_prefix, cons
         return D3D_ERR_WORKSPACE;
     if (max_ctas < 0)
         return D3D_ERR_INVALID_ARG;
-    pl = d == 64 ? make_plan<64>(R, Hq, Hkv, max_q, max_prefix, max_ctas)
-                 : make_plan<128>(R, Hq, Hkv, max_q, max_prefix, max_ctas);
+    pl = d == 64 ? make_plan<64>(R, Hq, Hkv, max_q, max_prefix, max_ctas, !one_tile)
+                 : make_plan<128>(R, Hq, Hkv, max_q, max_prefix, max_ctas, !one_tile);
     if (one_tile && pl.pair) {  // the fused round launch holds the one-tile kernel only
         pl.pair = false;
         pl.S = 1;
@@ -2062,11 +2290,13 @@ int attn_prepare(const void *q, const void *k_prefix, const void *v_prefix, cons
         return D3D_ERR_UNSUPPORTED;
     // the output map has the query map's shape: a query tile's output box is
     // stored from the shared-memory staging in the same swizzled layout
-    if (!make_map(&maps[0], q, d, Hq, total_q, pl.G, pl.TQ) || !make_map(&maps[3], k_packed, d, Hkv, total_q, 1, kBN) ||
+    // (a CTA pair loads half of every K tile's keys per CTA)
+    const int k_box = pl.duo ? kBN / 2 : kBN;
+    if (!make_map(&maps[0], q, d, Hq, total_q, pl.G, pl.TQ) || !make_map(&maps[3], k_packed, d, Hkv, total_q, 1, k_box) ||
         !make_map(&maps[4], v_packed, d, Hkv, total_q, 1, kBN) || !make_map(&maps[5], out, d, Hq, total_q, pl.G, pl.TQ))
         return D3D_ERR_CUDA;
     if (total_prefix > 0) {
-        if (!make_map(&maps[1], k_prefix, d, Hkv, total_prefix, 1, kBN) ||
+        if (!make_map(&maps[1], k_prefix, d, Hkv, total_prefix, 1, k_box) ||
             !make_map(&maps[2], v_prefix, d, Hkv, total_prefix, 1, kBN))
             return D3D_ERR_CUDA;
     } else {  // no prefix rows anywhere: the prefix maps are never used
@@ -2175,6 +2405,12 @@ int d3d_packed_draft_attn_ctas(int R, int Hq, int Hkv, int d, int max_q, int max
 
 void d3d_debug_inject_fault(int mode) { d3d::fault_mode() = mode; }
 
+void d3d_debug_force_attn_kernel(int kind)
+{
+    if (kind >= 0 && kind <= 3)
+        d3d::forced_attn_kernel() = kind;
+}
+
 int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_prefix, const void *k_packed,
                           const void *v_packed, const d3d_segment_t *segs, const int32_t *cu_prefix,
                           const int32_t *cu_q, const int32_t *cu_seg, int R, int Hq, int Hkv, int d, int max_q,
@@ -2194,8 +2430,8 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
         return rc == 1 ? D3D_OK : rc;
     prm.wait_first = (flags & D3D_ATTN_AFTER_DEPENDENT) != 0;
     if (d == 64)
-        return d3d::launch_attn<64>(maps, prm, pl.units, pl.pair, flags, stream);
-    return d3d::launch_attn<128>(maps, prm, pl.units, pl.pair, flags, stream);
+        return d3d::launch_attn<64>(maps, prm, pl.units, pl.pair, pl.duo, flags, stream);
+    return d3d::launch_attn<128>(maps, prm, pl.units, pl.pair, pl.duo, flags, stream);
 }
 
 int d3d_async_round(const d3d_attn_call_t *a, const d3d_verify_call_t *v, cudaStream_t stream)

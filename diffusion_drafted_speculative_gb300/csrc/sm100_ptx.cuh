@@ -451,6 +451,131 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// ---- CTA pairs (cta_group::2) ------------------------------------------------
+// Two CTAs of a cluster (ranks 2j, 2j + 1) share one MMA: the even CTA issues
+// it, each CTA holds half of the M rows (A and D in its own TMEM or shared
+// memory at the same address) and half of the N columns of B in its shared
+// memory; both tensor cores read both halves of B.  Every tcgen05 instruction
+// of a kernel that uses these takes the pair form.
+
+// Allocation of ncols TMEM columns at the same address in both CTAs: one warp
+// of each CTA executes it (the two warps take part in one allocation).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc] over the pair: M = 2 x 128 rows (each
+// CTA's A and D lanes), B's N columns split in halves between the CTAs.
+__device__ __forceinline__ void mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the barrier at offset `bar` in both CTAs of the pair when
+// every tcgen05 operation issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
+// TMA tiled load into this CTA's shared memory whose completion (bytes) is
+// counted on a barrier of either CTA of the pair (bar_cluster: an address in
+// the cluster window, dsmem_addr).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap, uint32_t bar_cluster, int32_t c0,
+                                                 int32_t c1, int32_t c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
+        "%5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// Arrival on a barrier of another CTA of the cluster (address from
+// dsmem_addr), ordering this thread's earlier writes at cluster scope (for
+// data read with plain loads after the wait: wait_bar_cluster).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+// Arrival on a barrier of another CTA of the cluster with the default
+// (CTA-scope) release: a hand-off of TMEM data ordered by the tcgen05 fences
+// around it (tcgen05.fence::before_thread_sync here, ::after_thread_sync at
+// the waiting thread).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster)
+{
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+// try_wait whose acquire covers arrivals from other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// wait_bar for a barrier that CTAs of the cluster arrive on (see wait_bar).
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                                 int32_t *status)
+{
+    if (mbar_try_wait_cluster(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity))
+            return true;
+        if (*abort_flag)
+            return false;
+        if (global_ns() - t0 > kWaitTimeoutNs) {
+            *abort_flag = 1u;
+            record_status(status, D3D_ERR_DEVICE_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Bitwise or into a 32-bit word of a CTA of the cluster.
+__device__ __forceinline__ void red_or_cluster(uint32_t addr_cluster, uint32_t v)
+{
+    asm volatile("red.relaxed.cluster.shared::cluster.or.b32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
 // ---- descriptors -----------------------------------------------------------
 // Shared-memory matrix descriptor, 128-byte swizzle (SW128), sm_100 format:
 // start address >> 4 in bits 0-13, leading byte offset >> 4 in bits 16-29,

@@ -215,6 +215,19 @@ int d3d_packed_draft_attn(const void *q, const void *k_prefix, const void *v_pre
  */
 void d3d_debug_inject_fault(int mode);
 
+/*
+ * Kernel selection hook for tests and measurements (no counterpart on the
+ * pages).  d3d_packed_draft_attn and d3d_packed_draft_attn_ctas plan their
+ * launch among three kernels of equal results: 1 one query tile per CTA
+ * (with key splits), 2 two query tiles per CTA (with key splits), 3 CTA
+ * pairs sharing their MMAs (one tile per CTA, head_dim 128 only, no key
+ * splits).  kind 1..3 restricts later plans to that kernel where it applies
+ * (elsewhere the plan chooses as usual); 0 (the default) lets the plan
+ * choose.  Other values: ignored.  The setting is process-global and not
+ * thread-safe.
+ */
+void d3d_debug_force_attn_kernel(int kind);
+
 /* ========================================================================
  * Acceptance probabilities and expected acceptance length.
  *

@@ -193,6 +193,79 @@ def test_attn_many_splits_and_bad_descriptor(d3d):
     assert_attn_close(got2[~rows], oracle.packed_attn(a)[~rows], "other rows")
 
 
+# ------------------------------------------------------------------ each attention kernel
+KERNELS = {1: "one tile per CTA", 2: "two tiles per CTA", 3: "CTA pairs"}
+
+
+@pytest.fixture
+def force_kernel(d3d):
+    yield d3d.d3d_debug_force_attn_kernel
+    d3d.d3d_debug_force_attn_kernel(0)
+
+
+def _ragged_with_empty_request():
+    segs = W.async_segments(8, 3, 2)
+    a = W.attn_inputs(R=3, L=(0, 400), Hq=8, Hkv=2, d=128, seed=5, segs=segs)
+    n = int(segs[:, 1].sum())
+    keep_q = np.r_[0:n, 2 * n:3 * n]
+    a["q"], a["kn"], a["vn"] = a["q"][keep_q], a["kn"][keep_q], a["vn"][keep_q]
+    a["segs"] = np.concatenate([segs, segs]).astype(np.int32)
+    a["cu_q"] = np.array([0, n, n, 2 * n], np.int32)
+    a["cu_seg"] = np.array([0, len(segs), len(segs), 2 * len(segs)], np.int32)
+    return a
+
+
+def _kernel_case(case):
+    if case == "async8b":  # the benchmark shape: 12 query tiles per KV head
+        return W.attn_inputs(**W.CONFIGS["async8b"], seed=3), [0, 13, 31]
+    if case == "odd_tiles":  # 3 query tiles per request and KV head: a pair with one tile past the request
+        return W.attn_inputs(R=2, L=(100, 700), Hq=32, Hkv=8, d=128, B=16, C=4, F=1, layout="async", seed=4), \
+            [0, 7, 30]
+    if case == "empty_request":
+        return _ragged_with_empty_request(), list(range(8))
+    if case == "g8":  # 8 query heads per KV head, 16 tokens per tile, ragged prefix tail
+        return W.attn_inputs(R=1, L=1000, Hq=16, Hkv=2, d=128, B=16, C=2, F=2, layout="async", seed=6), [0, 9, 15]
+    if case == "peaky":  # large logits: the running max grows by more than 2^8 between tiles
+        return W.attn_inputs(R=1, L=700, Hq=4, Hkv=2, d=128, B=16, C=3, F=2, layout="async", seed=4,
+                             k_scale=4.0), [0, 1, 2, 3]
+    raise ValueError(case)
+
+
+@pytest.mark.parametrize("kind", sorted(KERNELS))
+@pytest.mark.parametrize("case", ["async8b", "odd_tiles", "empty_request", "g8", "peaky"])
+def test_attn_each_kernel(d3d, force_kernel, kind, case):
+    # every kernel the plan may pick gives the oracle's result on the same
+    # inputs; the CTA-pair kernel rounds each request's query tiles up to
+    # pairs, so its CTA count is even
+    a, heads = _kernel_case(case)
+    force_kernel(kind)
+    n = d3d.d3d_packed_draft_attn_ctas(a["R"], a["Hq"], a["Hkv"], a["d"], a["max_q"], a["max_prefix"], 0)
+    if kind == 3:
+        TQ = 128 // (a["Hq"] // a["Hkv"])
+        MT = (a["max_q"] + TQ - 1) // TQ
+        assert n == a["R"] * a["Hkv"] * ((MT + 1) // 2 * 2), "CTA pairs not planned"
+    got, ws = run_attn(d3d, a)
+    assert d3d.d3d_workspace_status(ws) == 0
+    assert_attn_close(got[:, heads], _oracle_heads(a, heads)[:, heads], "%s, %s" % (case, KERNELS[kind]))
+
+
+def test_attn_pair_kernel_wait_runs_out(d3d, force_kernel):
+    # the failure-injection path on the CTA-pair kernel: both CTAs of every
+    # pair skip their first key-tile half, the issuing CTA's bounded wait
+    # runs out and both give up theirs; the next call is correct
+    a = W.attn_inputs(R=1, L=256, Hq=4, Hkv=1, d=128, B=16, C=3, F=2, layout="async", seed=9)
+    force_kernel(3)
+    d3d.d3d_debug_inject_fault(1)
+    try:
+        _, ws = run_attn(d3d, a)
+    finally:
+        d3d.d3d_debug_inject_fault(0)
+    assert d3d.d3d_workspace_status(ws, clear=True) == d3d.D3D_ERR_DEVICE_TIMEOUT
+    got, ws2 = run_attn(d3d, a)
+    assert_attn_close(got, oracle.packed_attn(a), "after a timed-out call")
+    assert d3d.d3d_workspace_status(ws2) == 0
+
+
 @pytest.mark.parametrize("Hq", [32, 64])
 def test_attn_single_request_offsets_checked(d3d, Hq):
     # one request: the kernel takes its offsets from the totals (the contract
