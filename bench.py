@@ -59,10 +59,10 @@ CSRC = os.path.join(ROOT, "diffusion_drafted_speculative_gb300", "csrc")
 NCU_TRAFFIC = {
     ("async8b", "attn"): {"sources": ("attn.cu", "attn_common.cuh", "sm100_ptx.cuh", "d3d_common.cuh",
                                       "verify_body.cuh"),
-                          "sha": "016c81580e70ad9a", "bytes": 13178880},
+                          "sha": "cd95b5fbbaed7f42", "bytes": 13178368},
     ("async8b", "verify"): {"sources": ("verify.cu", "verify_slice.cuh", "verify_body.cuh", "sm100_ptx.cuh",
                                         "d3d_common.cuh"),
-                            "sha": "c0d20894a1c2335c", "bytes": 9490432},
+                            "sha": "ce99d02e41d2ef67", "bytes": 9490176},
 }
 
 

@@ -2105,7 +2105,7 @@ template <int D> int cluster_capacity(int S, bool pair = false)
 template <int D>
 AttnPlan make_plan(int R, int Hq, int Hkv, int max_q, int max_prefix, int max_ctas = 0, bool allow_duo = true)
 {
-    constexpr double kTileCost1 = 1.0, kTileCost2 = 1.75, kTileCostDuo = 0.8, kFixed = 5.0, kCombine = 3.5;
+    constexpr double kTileCost1 = 1.0, kTileCost2 = 1.75, kFixed = 5.0, kCombine = 3.5;
     AttnPlan pl{};
     pl.G = Hq / Hkv;
     pl.TQ = kBM / pl.G;
@@ -2151,8 +2151,12 @@ AttnPlan make_plan(int R, int Hq, int Hkv, int max_q, int max_prefix, int max_ct
         }
     }
     // CTA pairs: every query tile in its own CTA (tiles rounded up to pairs),
-    // no key splits; each SM receives half of every K/V tile
-    if (allow_duo && (force == 0 || force == 3)) {
+    // no key splits; each SM receives half of every K/V tile.  Measured on
+    // GB300 slower than the one-tile kernel on every workload here (its MMAs
+    // wait for the slower CTA's softmax of each tile, and it cannot split
+    // keys), so the plan takes it only when d3d_debug_force_attn_kernel asks.
+    constexpr double kTileCostDuo = 1.1;
+    if (allow_duo && force == 3) {
         const int MT2 = (MT + 1) / 2 * 2;
         int cap = duo_capacity<D>();
         if (cap > budget)
