@@ -1017,17 +1017,28 @@ __device__ __forceinline__ void attn_body(unsigned unit, const CUtensorMap *tm_q
         // this thread's part of the head dimension: columns [w*D/kWG, (w+1)*D/kWG),
         // staged in the V ring (free once every MMA is done) and stored below
         const uint32_t part = Xchg<D>::part(sK);
-#pragma unroll
-        for (int q = 0; q < D / kWG / 8; ++q) {
-            float x0[8];
-            if (have) {
-                tmem_ld8(tO + (uint32_t)(w * (D / kWG) + q * 8), x0);
+        // the thread's D/kWG columns of O in one TMEM load (one wait)
+        constexpr int kCols = D / kWG;
+        float xo[kCols];
+        if (have) {
+            const uint32_t t0 = tO + (uint32_t)(w * kCols);
+            if constexpr (kCols == 64) {
+                tmem_ld64(t0, xo);
+            } else if constexpr (kCols == 32) {
+                tmem_ld32(t0, xo);
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    x0[e] = 0.f;
+                for (int q = 0; q < kCols / 8; ++q)
+                    tmem_ld8(t0 + (uint32_t)(q * 8), *reinterpret_cast<float(*)[8]>(xo + 8 * q));
             }
-            const uint4 v = pack8(x0, inv);
+        } else {
+#pragma unroll
+            for (int e = 0; e < kCols; ++e)
+                xo[e] = 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < kCols / 8; ++q) {
+            const uint4 v = pack8(xo + 8 * q, inv);
             const int unit = w * (D / kWG / 8) + q;
             if (p.S == 1) {
                 smem_st_v4(stage_addr(sV, row, unit), v);
