@@ -71,7 +71,7 @@ constexpr int kBN = 128;  // keys per KV tile
 #endif
 static_assert(D3D_ATTN_WG == 2 || D3D_ATTN_WG == 4, "two or four softmax warpgroups");
 constexpr int kWG = D3D_ATTN_WG;  // softmax warpgroups: each takes 1/kWG of every key tile's columns
-constexpr int kPart = kBN / kWG;  // 32 keys per softmax thread and tile
+constexpr int kPart = kBN / kWG;  // keys per softmax thread and tile (64 with two warpgroups)
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 // a CTA pair's stages hold half tiles: deeper rings in the same room
