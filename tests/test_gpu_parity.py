@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_util import (NEAR_TIE, SAMPLE_BAND, assert_attn_close, compare_verify, oracle_verify, run_attn,
+from gpu_util import (NEAR_TIE, PROB_RTOL, SAMPLE_BAND, assert_attn_close, compare_verify, oracle_verify, run_attn,
                       run_match, run_verify)
 
 pytestmark = pytest.mark.gpu
@@ -885,9 +885,11 @@ def test_accept_probs_and_tau_match_oracle(d3d, cfg, over):
         torch.cuda.synchronize()
         outs.append((a.cpu().numpy(), sv.cpu().numpy(), tau.cpu().numpy()))
     a, sv, tau = outs[0]
-    np.testing.assert_allclose(a, ref["accept_prob"], rtol=1e-4, atol=2e-6)
-    np.testing.assert_allclose(sv, ref["survival"], rtol=5e-4, atol=2e-6)
-    np.testing.assert_allclose(tau, ref["tau"], rtol=2e-4)
+    # the probabilities' relative tolerance (1e-5) for all three; measured on
+    # GB300 over these cases and seeds 70-72: a 2.3e-7, S(k) 1.7e-6, tau 4.4e-7
+    np.testing.assert_allclose(a, ref["accept_prob"], rtol=PROB_RTOL, atol=0)
+    np.testing.assert_allclose(sv, ref["survival"], rtol=PROB_RTOL, atol=0)
+    np.testing.assert_allclose(tau, ref["tau"], rtol=PROB_RTOL)
     for x, y in zip(outs[0], outs[1]):
         np.testing.assert_array_equal(x, y)
 
@@ -911,8 +913,8 @@ def test_accept_probs_slice_and_two_launch_shapes_agree(d3d):
         res.append((a.cpu().numpy(), tau.cpu().numpy()))
     ref = oracle.accept_probs(v)
     for a, tau in res:
-        np.testing.assert_allclose(a, ref["accept_prob"], rtol=1e-4, atol=2e-6)
-        np.testing.assert_allclose(tau, ref["tau"], rtol=2e-4)
+        np.testing.assert_allclose(a, ref["accept_prob"], rtol=PROB_RTOL, atol=0)
+        np.testing.assert_allclose(tau, ref["tau"], rtol=PROB_RTOL)
     np.testing.assert_allclose(res[0][0], res[1][0], rtol=1e-5, atol=1e-7)
 
 
