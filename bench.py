@@ -542,6 +542,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         line["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload)
+        line["parity"] = workload_parity(torch, sets, cfg, rank, verify)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -880,6 +881,48 @@ class OracleRound:
         o.branch_match(dict(verified=r["out_tokens"], verified_len=r["num_tokens"], heads=self.hb["heads"],
                             head_len=self.hb["head_len"]))
         return time.perf_counter() - t0
+
+
+# The parity tests' near-tie rule: a draw whose |u_j - alpha_j| at the
+# deciding test is below NEAR_TIE, or whose u*S lies within SAMPLE_BAND * S of
+# a step of the oracle's CDF, is counted but not compared.
+NEAR_TIE = 1e-5
+SAMPLE_BAND = 1e-6
+
+
+def workload_parity(torch, sets, cfg, rank, verify) -> dict:
+    """The verification of every input set of the run (the step's call, fresh
+    outputs) against the oracle in fp64: accepted lengths, token counts and
+    tokens compared draw by draw outside the near-tie bands, which are
+    counted and reported."""
+    import oracle
+
+    compared = ex_a = ex_s = mismatched = 0
+    for i, s in enumerate(sets):
+        s2 = dict(s)
+        for k in ("accept_len", "out_tokens", "num_tokens", "branch"):
+            s2[k] = torch.empty_like(s[k])
+        verify(s2, 0, fused_match=True)
+        torch.cuda.synchronize()
+        v = W.verify_inputs(**cfg, seed=rank_seed(rank, i))
+        try:
+            ref = oracle.spec_verify_par(v)
+        except RuntimeError:
+            ref = oracle.spec_verify(v)
+        tie_a = ref["margin_accept"] < NEAR_TIE
+        tie_s = ~tie_a & (ref["margin_sample"] < SAMPLE_BAND)
+        keep = ~tie_a & ~tie_s
+        got = {k: s2[k].cpu().numpy() for k in ("accept_len", "num_tokens", "out_tokens")}
+        for r in np.nonzero(keep)[0]:
+            if any(not np.array_equal(got[k][r], ref[k][r]) for k in got):
+                mismatched += 1
+        compared += int(keep.sum())
+        ex_a += int(tie_a.sum())
+        ex_s += int(tie_s.sum())
+    return {"kind": "oracle (fp64), every input set of the run", "draws": compared + ex_a + ex_s,
+            "compared": compared, "mismatched": mismatched, "excluded_near_alpha": ex_a,
+            "excluded_sample_band": ex_s, "rule": "|u - alpha| < %g at the deciding test; u*S within %g*S of a CDF step"
+            % (NEAR_TIE, SAMPLE_BAND)}
 
 
 def cpu_baseline(wl_name: str) -> dict:
