@@ -170,7 +170,7 @@ __device__ void write_request(const BArgs &a, int r, const int32_t *s_y, const i
 }
 
 template <typename T, int kF>
-__global__ void __launch_bounds__(kBThreads) branch_build_kernel(const BArgs a)
+__global__ void __launch_bounds__(kBThreads, 2) branch_build_kernel(const BArgs a)
 {
     __shared__ float s_v[kBThreads / 32 + 1];
     __shared__ int s_i[kBThreads / 32 + 1];
@@ -201,6 +201,16 @@ __global__ void __launch_bounds__(kBThreads) branch_build_kernel(const BArgs a)
         }
         return;
     }
+    // the outputs the request's last CTA writes, touched now (their address
+    // translations are then at hand when the last CTA stores to them)
+    if (threadIdx.x < 6) {
+        const int o = (int)threadIdx.x;
+        const void *ptr = o == 0 ? (const void *)a.anchors : o == 1 ? (const void *)a.heads
+                        : o == 2 ? (const void *)a.head_len : o == 3 ? (const void *)a.segs
+                        : o == 4 ? (const void *)a.cu_q : (const void *)a.cu_seg;
+        if (ptr != nullptr)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+    }
     for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
         const int c = (int)(it % nch);
         const long long rp = it / nch;  // request * P + position
@@ -218,17 +228,27 @@ __global__ void __launch_bounds__(kBThreads) branch_build_kernel(const BArgs a)
 #pragma unroll
         for (int t = 0; t < kF; ++t)
             bv[t] = -INFINITY, bi[t] = INT_MAX;
-        if (vec) {  // 16-byte loads of 8 entries (V % 8 == 0, aligned rows)
+        if (vec) {  // 16-byte loads of 8 entries (V % 8 == 0, aligned rows), all in flight before the compares
+            float x[kBPer / 8][8];
 #pragma unroll
             for (int g = 0; g < kBPer / 8; ++g) {
                 const int v = v0 + g * (8 * kBThreads) + 8 * (int)threadIdx.x;
                 if (v < v1) {
-                    float x[8];
-                    load_logits8(row + v, x);
+                    load_logits8(row + v, x[g]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        x[g][e] = -INFINITY;
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < kBPer / 8; ++g) {
+                const int v = v0 + g * (8 * kBThreads) + 8 * (int)threadIdx.x;
+                if (v < v1) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         if (v + e != yv)
-                            keep_best<kF>(bv, bi, x[e], v + e);
+                            keep_best<kF>(bv, bi, x[g][e], v + e);
                 }
             }
         } else {
@@ -255,48 +275,65 @@ __global__ void __launch_bounds__(kBThreads) branch_build_kernel(const BArgs a)
         for (int j = threadIdx.x; j < B - 1; j += kBThreads)  // in flight while the lists merge
             s_y[j] = __ldg(a.y + (long long)r * (B - 1) + j);
         constexpr int kCache = 8;  // list entries each lane holds (rows of up to 256 entries)
-        for (int pp = w; pp < P; pp += kBThreads / 32) {
-            const float2 *lst = rec + ((long long)r * P + pp) * nch * F;
-            const int n = nch * F;
-            const bool cached = n <= 32 * kCache;
-            float cv[kCache];
-            int ci[kCache];
+        constexpr int kW = kBThreads / 32;
+        const int n = nch * F;
+        const bool cached = n <= 32 * kCache;
+        // warp w merges rows w, w + kW, w + 2 kW, ... in that order, the lists
+        // of two rows loaded together (one L2 round trip for both)
+        for (int pp0 = w; pp0 < P; pp0 += 2 * kW) {
+            float cvv[2][kCache];
+            int civ[2][kCache];
 #pragma unroll
-            for (int t = 0; t < kCache; ++t) {  // one pass over the row's lists
-                const int k = lane + 32 * t;
-                const float2 e = (cached && k < n) ? __ldcg(lst + k) : make_float2(-INFINITY, __int_as_float(INT_MAX));
-                cv[t] = e.x, ci[t] = __float_as_int(e.y);
+            for (int h = 0; h < 2; ++h) {
+                const int pp = pp0 + h * kW;
+                const float2 *lst = rec + ((long long)r * P + pp) * nch * F;
+#pragma unroll
+                for (int t = 0; t < kCache; ++t) {  // one pass over the row's lists
+                    const int k = lane + 32 * t;
+                    const float2 e = (cached && pp < P && k < n) ? __ldcg(lst + k)
+                                                                 : make_float2(-INFINITY, __int_as_float(INT_MAX));
+                    cvv[h][t] = e.x, civ[h][t] = __float_as_int(e.y);
+                }
             }
-            for (int f = 0; f < F; ++f) {
-                float v = -INFINITY;
-                int i = INT_MAX;
-                if (cached) {
 #pragma unroll
-                    for (int t = 0; t < kCache; ++t)
-                        if (ahead(cv[t], ci[t], v, i))
-                            v = cv[t], i = ci[t];
-                } else {  // long rows: read the lists again, skipping the pairs already taken
-                    for (int k = lane; k < n; k += 32) {
-                        const float2 e = __ldcg(lst + k);
-                        const int ei = __float_as_int(e.y);
-                        bool used = false;
-                        for (int t = 0; t < f; ++t)
-                            used = used || s_anc[pp * F + t] == ei;
-                        if (!used && ahead(e.x, ei, v, i))
-                            v = e.x, i = ei;
+            for (int h = 0; h < 2; ++h) {
+                const int pp = pp0 + h * kW;
+                if (pp >= P)
+                    break;
+                const float2 *lst = rec + ((long long)r * P + pp) * nch * F;
+                float(&cv)[kCache] = cvv[h];
+                int(&ci)[kCache] = civ[h];
+                for (int f = 0; f < F; ++f) {
+                    float v = -INFINITY;
+                    int i = INT_MAX;
+                    if (cached) {
+#pragma unroll
+                        for (int t = 0; t < kCache; ++t)
+                            if (ahead(cv[t], ci[t], v, i))
+                                v = cv[t], i = ci[t];
+                    } else {  // long rows: read the lists again, skipping the pairs already taken
+                        for (int k = lane; k < n; k += 32) {
+                            const float2 e = __ldcg(lst + k);
+                            const int ei = __float_as_int(e.y);
+                            bool used = false;
+                            for (int t = 0; t < f; ++t)
+                                used = used || s_anc[pp * F + t] == ei;
+                            if (!used && ahead(e.x, ei, v, i))
+                                v = e.x, i = ei;
+                        }
                     }
-                }
-                warp_best(v, i);
-                i = __shfl_sync(0xffffffffu, i, 0);
-                if (lane == 0)
-                    s_anc[pp * F + f] = i;
-                if (cached) {  // the winner leaves its lane's cache (indices are distinct)
+                    warp_best(v, i);
+                    i = __shfl_sync(0xffffffffu, i, 0);
+                    if (lane == 0)
+                        s_anc[pp * F + f] = i;
+                    if (cached) {  // the winner leaves its lane's cache (indices are distinct)
 #pragma unroll
-                    for (int t = 0; t < kCache; ++t)
-                        if (ci[t] == i)
-                            cv[t] = -INFINITY, ci[t] = INT_MAX;
+                        for (int t = 0; t < kCache; ++t)
+                            if (ci[t] == i)
+                                cv[t] = -INFINITY, ci[t] = INT_MAX;
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
         }
         __syncthreads();
