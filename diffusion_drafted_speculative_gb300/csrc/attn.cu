@@ -48,6 +48,15 @@
 // memory, in a fixed order, and stores it; a second cluster barrier keeps
 // every CTA resident until its shared memory has been read.  No global
 // scratch is used.
+//
+// The same body, instantiated with kDuo, is the CTA-pair kernel
+// (attn_duo_kernel): query tiles 2j and 2j+1 run as a cluster of two whose
+// even CTA issues cta_group::2 MMAs for both (each CTA's 128 rows in its own
+// TMEM, half of every K and V tile in each CTA's shared memory); the odd
+// CTA's softmax warps arrive on the even CTA's barriers and the MMA commits
+// arrive on both.  It is selected only through d3d_debug_force_attn_kernel
+// (measured slower than the one-tile kernel on every workload here).
+// The two-tile kernel (two query tiles per CTA) follows the one-tile body.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
