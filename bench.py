@@ -59,7 +59,7 @@ CSRC = os.path.join(ROOT, "diffusion_drafted_speculative_gb300", "csrc")
 NCU_TRAFFIC = {
     ("async8b", "attn"): {"sources": ("attn.cu", "attn_common.cuh", "sm100_ptx.cuh", "d3d_common.cuh",
                                       "verify_body.cuh"),
-                          "sha": "4f54b568b681905f", "bytes": 13178368},
+                          "sha": "f4e3d13cd7896800", "bytes": 13178368},
     ("async8b", "verify"): {"sources": ("verify.cu", "verify_slice.cuh", "verify_body.cuh", "sm100_ptx.cuh",
                                         "d3d_common.cuh"),
                             "sha": "ce99d02e41d2ef67", "bytes": 9490176},
