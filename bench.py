@@ -63,6 +63,13 @@ NCU_TRAFFIC = {
     ("async8b", "verify"): {"sources": ("verify.cu", "verify_slice.cuh", "verify_body.cuh", "sm100_ptx.cuh",
                                         "d3d_common.cuh"),
                             "sha": "ce99d02e41d2ef67", "bytes": 9490176},
+    ("async8b", "greedy"): {"sources": ("verify.cu", "greedy_body.cuh", "verify_body.cuh", "verify_slice.cuh",
+                                        "sm100_ptx.cuh", "d3d_common.cuh"),
+                            "sha": "81498f57f4483e7e", "bytes": 4903936},
+    ("async8b", "branches"): {"sources": ("branches.cu", "sm100_ptx.cuh", "d3d_common.cuh"),
+                              "sha": "1db77ce822f14171", "bytes": 3425536},
+    ("async8b", "accept"): {"sources": ("accept.cu", "sm100_ptx.cuh", "d3d_common.cuh"),
+                            "sha": "9d59b7469b95e2b9", "bytes": 9162112},
 }
 
 
@@ -74,6 +81,13 @@ def sources_sha(names) -> str:
         with open(os.path.join(CSRC, n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def hbm_part(nbytes: float, ms: float, peak: float, traffic) -> dict:
+    """HBM roofline entry of a part timed alone: algorithmic bytes over its time."""
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+            "bytes": nbytes, "traffic": traffic}
 
 
 def ncu_traffic(wl_name: str, part: str):
@@ -128,8 +142,13 @@ def workload(name: str) -> dict:
     attn_bytes = 2.0 * R * (2 * L_mean * Hkv * d + 2 * n_q * Hq * d + 2 * n_q * Hkv * d)
     verify_bytes = 2.0 * R * ((2 * B - 1) * V + 2 * V)
     greedy_bytes = 2.0 * R * B * V  # greedy verification reads the target logits only
+    # branch construction reads draft rows 0..C-2; the acceptance
+    # probabilities read target and draft rows 0..B-2 (bf16)
+    branch_bytes = 2.0 * R * max(cfg.get("C", 1) - 1, 0) * V
+    accept_bytes = 2.0 * R * 2 * (B - 1) * V
     return dict(cfg=cfg, segs=segs, n_q=n_q, R=R, flops=flops, attn_bytes=attn_bytes, verify_bytes=verify_bytes,
-                greedy_bytes=greedy_bytes, positions=R * B, vis_packed=vis_packed)
+                greedy_bytes=greedy_bytes, branch_bytes=branch_bytes, accept_bytes=accept_bytes, positions=R * B,
+                vis_packed=vis_packed)
 
 
 def workload_label(name: str) -> str:
@@ -533,7 +552,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                   "other_workloads": other,
                   "greedy_hbm": {"achieved": round(greedy_gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
                                  "frac": round(greedy_gbs / peaks["hbm"], 4), "bytes": wl["greedy_bytes"],
-                                 "traffic": ncu_traffic(args.workload, "greedy")}},
+                                 "traffic": ncu_traffic(args.workload, "greedy")},
+                  "branches_hbm": hbm_part(wl["branch_bytes"], t_branches, peaks["hbm"],
+                                           ncu_traffic(args.workload, "branches")),
+                  "accept_hbm": hbm_part(wl["accept_bytes"], t_accept, peaks["hbm"],
+                                         ncu_traffic(args.workload, "accept"))},
         "roofline": roof,
         "gpu_launches": args.steps * LAUNCHES["fused" if fused_round else args.round],
         "clocks": clk, "wall_s_timed_region": round(wall, 4),
